@@ -1,0 +1,128 @@
+/*
+ * gdr_bwd.h -- C ABI of the GB300 chunked gated delta rule backward (libgdrbwd.so).
+ *
+ * The operation: backward pass of chunked Gated DeltaNet, the call that returns the six gradients
+ * dq, dk, dv, dg, db and dh0 in one pass ("FlashQLA backward explained", gtnt.cn/news/163832,
+ * section 1, step 3).  Per (sequence, value head) the forward it differentiates is
+ *
+ *     S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T ,   S in R^{V x K}
+ *     o_t = scale * S_t q_t
+ *
+ * with the loss L = sum_t <o_t, dO_t> + <S_T, dht>.  With the per-channel (KDA) gate, exp(g_t) becomes
+ * diag(exp(g_t)) acting on the K index of S, and g is given per key channel (MindSpeed-Ops
+ * chunk_kda_bwd.md, input table: g [B, T, H, K] fp32 "gate log values").
+ *
+ * Entry conventions ("FlashQLA backward explained", section 1, "three entry conventions"): dh0 is
+ * accumulated and returned in fp32; dht is optional and absent means zero.  Unlike that library, this
+ * API takes the RAW per-token log-gate g (not its chunk-local cumulative sum) and returns dg with
+ * respect to the raw gate; the chunk cumsum and the closing reverse cumsum happen inside.
+ *
+ * Tensor layouts (all row-major, last axis contiguous, every base pointer 16-byte aligned):
+ *   q, k      [B, T, Hk, K]     qkv_dtype
+ *   v, dO     [B, T, Hv, V]     qkv_dtype
+ *   beta      [B, T, Hv]        beta_dtype
+ *   g         [B, T, Hv]        fp32 (gate_per_channel = 0)   or  [B, T, Hv, K] fp32 (= 1)
+ *   h0, dht   [N, Hv, V, K]     fp32, S[v][k] ordering; N = B (dense) or num_seqs (varlen)
+ *   dq, dk    [B, T, Hk, K]     dqdk_dtype
+ *   dv        [B, T, Hv, V]     dv_dtype
+ *   dbeta     [B, T, Hv]        fp32
+ *   dg        same shape as g   fp32
+ *   dh0       [N, Hv, V, K]     fp32
+ * Varlen (MindSpeed-Ops chunk_kda_bwd.md, input table: cu_seqlens [N+1], chunk_indices [NT, 2]):
+ * B must be 1, T is the packed total and cu_seqlens (int32, device) holds N+1 non-decreasing token
+ * offsets with cu_seqlens[0] = 0 and cu_seqlens[N] = T.  Chunks never cross a sequence boundary.
+ * GQA: value head hv reads key head hv / (Hv / Hk); dq and dk are summed over the Hv / Hk value heads
+ * of each key head.
+ *
+ * Ownership: every tensor pointer is a device pointer owned by the caller.  The plan is a host object
+ * owned by the library (create/destroy).  The workspace is device memory owned by the caller, at
+ * least gdr_bwd_workspace_bytes() bytes, 256-byte aligned; the library never allocates device memory.
+ *
+ * Errors: every call returns a gdr_status and never aborts or throws.  Arguments are checked on the
+ * host before anything is launched; a failed check returns GDR_ERR_INVALID_ARG (or
+ * GDR_ERR_UNSUPPORTED for a valid but unimplemented combination) and launches nothing.  Kernels
+ * report device-side problems (malformed cu_seqlens, an expired bounded wait) in a status word in the
+ * workspace, which gdr_bwd_get_status() reads.
+ */
+#ifndef GDR_BWD_H_
+#define GDR_BWD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDR_OK = 0,
+    GDR_ERR_INVALID_ARG = 1, /* bad shape, dtype, null required pointer, misalignment */
+    GDR_ERR_UNSUPPORTED = 2, /* valid request outside what this build implements */
+    GDR_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
+    GDR_ERR_OOM = 4,         /* host allocation of the plan failed */
+    GDR_ERR_TIMEOUT = 5,     /* a device-side bounded wait expired (read by gdr_bwd_get_status) */
+    GDR_ERR_DEVICE = 6       /* a kernel flagged malformed device input, e.g. cu_seqlens */
+} gdr_status;
+
+typedef enum { GDR_F32 = 0, GDR_BF16 = 1, GDR_F16 = 2 } gdr_dtype;
+
+/* Problem description.  Sizes: K, V in [1, 128]; BT in {16, 32, 64}; Hv a multiple of Hk. */
+typedef struct {
+    int B, T, Hk, Hv, K, V, BT;
+    int num_seqs;          /* 0: dense [B, T, ...]; > 0: varlen with B == 1 and cu_seqlens[num_seqs + 1] */
+    int gate_per_channel;  /* 0: g [B, T, Hv]; 1: KDA gate g [B, T, Hv, K] */
+    float scale;           /* output scale; <= 0 selects 1 / sqrt(K) */
+    gdr_dtype qkv_dtype;   /* storage type of q, k, v and dO */
+    gdr_dtype beta_dtype;  /* storage type of beta */
+    gdr_dtype dqdk_dtype;  /* storage type of dq and dk */
+    gdr_dtype dv_dtype;    /* storage type of dv */
+    int has_h0, has_dht;   /* whether h0 / dht are given (absent means zero) */
+} gdr_bwd_desc;
+
+/* Device pointers for one call.  h0, dht and cu_seqlens may be NULL when the descriptor says they
+ * are absent.  dh0 may be NULL (not returned). */
+typedef struct {
+    const void *q, *k, *v, *beta, *g, *h0, *dO, *dht;
+    const int32_t *cu_seqlens;
+    void *dq, *dk, *dv, *dbeta, *dg, *dh0;
+} gdr_bwd_args;
+
+typedef struct gdr_bwd_plan gdr_bwd_plan;
+
+/* Validate a descriptor and build a plan (host only; no device memory, no CUDA call).
+ * Returns GDR_ERR_INVALID_ARG for bad sizes, GDR_ERR_OOM if the host allocation fails. */
+gdr_status gdr_bwd_create(const gdr_bwd_desc *desc, gdr_bwd_plan **out);
+
+/* Bytes of device workspace that gdr_bwd_run needs for this plan (0 for a NULL plan). */
+size_t gdr_bwd_workspace_bytes(const gdr_bwd_plan *plan);
+
+/* Queue the whole backward on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ * Asynchronous: it never synchronises.  Outputs are fully overwritten.  The workspace must not be
+ * used by another call that may run concurrently. */
+gdr_status gdr_bwd_run(gdr_bwd_plan *plan, const gdr_bwd_args *args, void *workspace, size_t ws_bytes,
+                       void *stream);
+
+/* Synchronise `stream` and read the device status word that the last run on this workspace left:
+ * GDR_OK, GDR_ERR_TIMEOUT or GDR_ERR_DEVICE.  Also clears the word. */
+gdr_status gdr_bwd_get_status(gdr_bwd_plan *plan, void *workspace, void *stream);
+
+/* Free the plan (NULL is accepted). */
+void gdr_bwd_destroy(gdr_bwd_plan *plan);
+
+/* Varlen chunk bookkeeping on the device (MindSpeed-Ops chunk_kda_bwd.md, input table: chunk_indices
+ * [NT, 2] with NT = ceil(T / chunk_size)).  For the N sequences of cu_seqlens (device int32 [N+1]),
+ * writes chunk_offsets[s] = number of chunks before sequence s (chunk_offsets[N] = total), and
+ * chunk_indices[n] = (s, c) for the n-th chunk, sequence-major then chunk ascending; entries from the
+ * total up to max_chunks - 1 are set to (-1, -1).  max_chunks must be at least the total, e.g.
+ * T / BT + N.  Returns GDR_ERR_INVALID_ARG for null pointers, N < 1 or BT < 1; launches one kernel. */
+gdr_status gdr_chunk_indices(const int32_t *cu_seqlens, int num_seqs, int BT, int max_chunks,
+                             int32_t *chunk_indices, int32_t *chunk_offsets, void *stream);
+
+/* Static description of a status code. */
+const char *gdr_status_string(gdr_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_BWD_H_ */
