@@ -1,0 +1,278 @@
+// api.cu -- the C ABI of libgdrbwd.so: argument checks, workspace layout and the launch sequence
+//   K0 chunk bookkeeping (varlen) -> K1 WY prep -> K2 state recompute -> K3 state-gradient scan
+//   -> K4 per-chunk gradients -> K5 gate reverse cumsum + GQA reduction
+// all queued on the caller's stream.  No device memory is allocated here.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/gdr_bwd.h"
+#include "gdr_common.cuh"
+#include "gdr_kernels.h"
+
+using namespace gdr;
+
+struct gdr_bwd_plan {
+    gdr_bwd_desc d;
+    int G, N, dense, nts, max_chunks, bv;
+    long long tokens;  // B * T
+    // workspace byte offsets
+    size_t o_status, o_cidx, o_coff, o_gam, o_T, o_Aqk, o_W, o_U, o_Kt, o_Qg, o_h, o_dh, o_Vn, o_dVn, o_dgam, o_dqh,
+        o_dkh, total;
+};
+
+namespace {
+
+constexpr int kNumSMs = 152;
+
+bool valid_dtype(int d) { return d == GDR_F32 || d == GDR_BF16 || d == GDR_F16; }
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+void layout(gdr_bwd_plan &p) {
+    const gdr_bwd_desc &d = p.d;
+    size_t units = (size_t)p.max_chunks * d.Hv;
+    size_t gw = d.gate_per_channel ? DT : 1;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes);
+        return o;
+    };
+    p.o_status = take(256);
+    p.o_cidx = take(sizeof(int32_t) * 2 * (size_t)p.max_chunks);
+    p.o_coff = take(sizeof(int32_t) * ((size_t)p.N + 1));
+    p.o_gam = take(sizeof(float) * units * CT * gw);
+    p.o_T = take(sizeof(__half) * units * CT * CT);
+    p.o_Aqk = take(sizeof(__half) * units * CT * CT);
+    p.o_W = take(sizeof(__half) * units * CT * DT);
+    p.o_U = take(sizeof(__half) * units * CT * DT);
+    p.o_Kt = take(sizeof(__half) * units * CT * DT);
+    p.o_Qg = take(sizeof(__half) * units * CT * DT);
+    p.o_h = take(sizeof(__half) * units * DT * DT);
+    p.o_dh = take(sizeof(__half) * units * DT * DT);
+    p.o_Vn = take(sizeof(__half) * units * CT * DT);
+    p.o_dVn = take(sizeof(__half) * units * CT * DT);
+    p.o_dgam = take(sizeof(float) * units * CT * gw);
+    size_t per_head = p.G > 1 ? sizeof(float) * (size_t)p.tokens * d.Hv * d.K : 0;
+    p.o_dqh = take(per_head);
+    p.o_dkh = take(per_head);
+    p.total = off;
+}
+
+bool aligned(const void *ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+int choose_bv(const gdr_bwd_plan &p) {
+    const char *env = getenv("GDR_SCAN_BV");
+    if (env) {
+        int v = atoi(env);
+        if (v == 8 || v == 16 || v == 32) return v;
+    }
+    long long units = (long long)p.N * p.d.Hv;
+    if (units * (DT / 32) >= 2 * kNumSMs) return 32;
+    if (units * (DT / 16) >= 2 * kNumSMs) return 16;
+    return 8;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdr_status_string(gdr_status s) {
+    switch (s) {
+        case GDR_OK: return "ok";
+        case GDR_ERR_INVALID_ARG: return "invalid argument";
+        case GDR_ERR_UNSUPPORTED: return "unsupported configuration";
+        case GDR_ERR_CUDA: return "CUDA error";
+        case GDR_ERR_OOM: return "out of host memory";
+        case GDR_ERR_TIMEOUT: return "device wait timed out";
+        case GDR_ERR_DEVICE: return "device reported malformed input";
+    }
+    return "unknown status";
+}
+
+gdr_status gdr_bwd_create(const gdr_bwd_desc *desc, gdr_bwd_plan **out) {
+    if (!desc || !out) return GDR_ERR_INVALID_ARG;
+    *out = nullptr;
+    const gdr_bwd_desc &d = *desc;
+    if (d.B < 1 || d.T < 0 || d.Hk < 1 || d.Hv < 1 || d.Hv % d.Hk != 0) return GDR_ERR_INVALID_ARG;
+    if (d.K < 8 || d.K > DT || d.K % 8 || d.V < 8 || d.V > DT || d.V % 8) return GDR_ERR_INVALID_ARG;
+    if (d.BT != 16 && d.BT != 32 && d.BT != 64) return GDR_ERR_INVALID_ARG;
+    if (d.num_seqs < 0 || (d.num_seqs > 0 && d.B != 1)) return GDR_ERR_INVALID_ARG;
+    if (d.gate_per_channel != 0 && d.gate_per_channel != 1) return GDR_ERR_INVALID_ARG;
+    if (!valid_dtype(d.qkv_dtype) || !valid_dtype(d.beta_dtype) || !valid_dtype(d.dqdk_dtype) ||
+        !valid_dtype(d.dv_dtype))
+        return GDR_ERR_INVALID_ARG;
+    if (d.has_h0 != 0 && d.has_h0 != 1) return GDR_ERR_INVALID_ARG;
+    if (d.has_dht != 0 && d.has_dht != 1) return GDR_ERR_INVALID_ARG;
+    long long tokens = (long long)d.B * d.T;
+    if (tokens > (1LL << 30) || (long long)tokens * d.Hv * DT > (1LL << 40)) return GDR_ERR_UNSUPPORTED;
+    gdr_bwd_plan *p = new (std::nothrow) gdr_bwd_plan();
+    if (!p) return GDR_ERR_OOM;
+    p->d = d;
+    if (!(p->d.scale > 0.f)) p->d.scale = 1.0f / sqrtf((float)d.K);
+    p->G = d.Hv / d.Hk;
+    p->dense = d.num_seqs == 0;
+    p->N = p->dense ? d.B : d.num_seqs;
+    p->nts = (d.T + d.BT - 1) / d.BT;
+    p->tokens = tokens;
+    long long mc = p->dense ? (long long)d.B * p->nts : (long long)d.T / d.BT + d.num_seqs;
+    if (mc > (1LL << 30)) {
+        delete p;
+        return GDR_ERR_UNSUPPORTED;
+    }
+    p->max_chunks = (int)mc;
+    p->bv = choose_bv(*p);
+    layout(*p);
+    *out = p;
+    return GDR_OK;
+}
+
+size_t gdr_bwd_workspace_bytes(const gdr_bwd_plan *plan) { return plan ? plan->total : 0; }
+
+void gdr_bwd_destroy(gdr_bwd_plan *plan) { delete plan; }
+
+static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *workspace, size_t ws_bytes, void *stream_,
+                           void *const *events) {
+    if (!plan || !a) return GDR_ERR_INVALID_ARG;
+    const gdr_bwd_desc &d = plan->d;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (!a->q || !a->k || !a->v || !a->beta || !a->g || !a->dO) return GDR_ERR_INVALID_ARG;
+    if (!a->dq || !a->dk || !a->dv || !a->dbeta || !a->dg) return GDR_ERR_INVALID_ARG;
+    if ((d.has_h0 && !a->h0) || (d.has_dht && !a->dht)) return GDR_ERR_INVALID_ARG;
+    if (!plan->dense && !a->cu_seqlens) return GDR_ERR_INVALID_ARG;
+    const void *vec[] = {a->q, a->k, a->v, a->dO, a->dq, a->dk, a->dv};
+    for (const void *ptr : vec)
+        if (!aligned(ptr, 16)) return GDR_ERR_INVALID_ARG;
+    const void *nat[] = {a->beta, a->g, a->dbeta, a->dg, a->h0, a->dht, a->dh0, a->cu_seqlens};
+    for (const void *ptr : nat)
+        if (ptr && !aligned(ptr, 4)) return GDR_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < plan->total) return GDR_ERR_INVALID_ARG;
+
+    char *ws = reinterpret_cast<char *>(workspace);
+    Params P;
+    memset(&P, 0, sizeof(P));
+    P.B = d.B;
+    P.T = d.T;
+    P.Hk = d.Hk;
+    P.Hv = d.Hv;
+    P.K = d.K;
+    P.V = d.V;
+    P.BT = d.BT;
+    P.G = plan->G;
+    P.N = plan->N;
+    P.per_channel = d.gate_per_channel;
+    P.dense = plan->dense;
+    P.max_chunks = plan->max_chunks;
+    P.nts = plan->nts;
+    P.scale = d.scale;
+    P.qkv_dtype = d.qkv_dtype;
+    P.beta_dtype = d.beta_dtype;
+    P.dqdk_dtype = d.dqdk_dtype;
+    P.dv_dtype = d.dv_dtype;
+    P.q = a->q;
+    P.k = a->k;
+    P.v = a->v;
+    P.beta = a->beta;
+    P.dO = a->dO;
+    P.g = reinterpret_cast<const float *>(a->g);
+    P.h0 = d.has_h0 ? reinterpret_cast<const float *>(a->h0) : nullptr;
+    P.dht = d.has_dht ? reinterpret_cast<const float *>(a->dht) : nullptr;
+    P.cu = plan->dense ? nullptr : a->cu_seqlens;
+    P.dq = a->dq;
+    P.dk = a->dk;
+    P.dv = a->dv;
+    P.dbeta = reinterpret_cast<float *>(a->dbeta);
+    P.dg = reinterpret_cast<float *>(a->dg);
+    P.dh0 = reinterpret_cast<float *>(a->dh0);
+    P.status = reinterpret_cast<int *>(ws + plan->o_status);
+    P.chunk_idx = reinterpret_cast<int32_t *>(ws + plan->o_cidx);
+    P.chunk_off = reinterpret_cast<int32_t *>(ws + plan->o_coff);
+    P.gam = reinterpret_cast<float *>(ws + plan->o_gam);
+    P.Tm = reinterpret_cast<__half *>(ws + plan->o_T);
+    P.Aqk = reinterpret_cast<__half *>(ws + plan->o_Aqk);
+    P.W = reinterpret_cast<__half *>(ws + plan->o_W);
+    P.U = reinterpret_cast<__half *>(ws + plan->o_U);
+    P.Kt = reinterpret_cast<__half *>(ws + plan->o_Kt);
+    P.Qg = reinterpret_cast<__half *>(ws + plan->o_Qg);
+    P.h = reinterpret_cast<__half *>(ws + plan->o_h);
+    P.dh = reinterpret_cast<__half *>(ws + plan->o_dh);
+    P.Vn = reinterpret_cast<__half *>(ws + plan->o_Vn);
+    P.dVn = reinterpret_cast<__half *>(ws + plan->o_dVn);
+    P.dgam = reinterpret_cast<float *>(ws + plan->o_dgam);
+    P.dq_h = plan->G > 1 ? reinterpret_cast<float *>(ws + plan->o_dqh) : nullptr;
+    P.dk_h = plan->G > 1 ? reinterpret_cast<float *>(ws + plan->o_dkh) : nullptr;
+
+    auto mark = [&](int i) -> bool {
+        return !events || cudaEventRecord((cudaEvent_t)events[i], stream) == cudaSuccess;
+    };
+    if (cudaMemsetAsync(P.status, 0, sizeof(int), stream) != cudaSuccess) return GDR_ERR_CUDA;
+    if (!mark(0)) return GDR_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (!plan->dense) {
+        e = launch_k0(a->cu_seqlens, plan->N, d.BT, plan->max_chunks, d.T, P.chunk_idx, P.chunk_off, P.status, stream);
+        if (e != cudaSuccess) return GDR_ERR_CUDA;
+    }
+    if (!mark(1)) return GDR_ERR_CUDA;
+    const bool any_chunks = plan->max_chunks > 0;
+    if (any_chunks && (e = launch_k1(P, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    if (!mark(2)) return GDR_ERR_CUDA;
+    if (any_chunks && (e = launch_k2(P, plan->bv, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    if (!mark(3)) return GDR_ERR_CUDA;
+    if ((e = launch_k3(P, plan->bv, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    if (!mark(4)) return GDR_ERR_CUDA;
+    if (any_chunks && (e = launch_k4(P, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    if (!mark(5)) return GDR_ERR_CUDA;
+    if (any_chunks && (e = launch_k5(P, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    if (!mark(6)) return GDR_ERR_CUDA;
+    return GDR_OK;
+}
+
+gdr_status gdr_bwd_run(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *workspace, size_t ws_bytes, void *stream) {
+    return run_impl(plan, a, workspace, ws_bytes, stream, nullptr);
+}
+
+gdr_status gdr_bwd_run_profiled(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *workspace, size_t ws_bytes,
+                                void *stream, void *const *events) {
+    if (!events) return GDR_ERR_INVALID_ARG;
+    for (int i = 0; i <= GDR_BWD_NUM_STAGES; ++i)
+        if (!events[i]) return GDR_ERR_INVALID_ARG;
+    return run_impl(plan, a, workspace, ws_bytes, stream, events);
+}
+
+int gdr_bwd_launch_count(const gdr_bwd_plan *plan) {
+    if (!plan) return 0;
+    int n = plan->dense ? 0 : 1;  // K0
+    n += 1;                       // K3 always runs (it also writes dh0)
+    if (plan->max_chunks > 0) n += 4;
+    return n;
+}
+
+gdr_status gdr_bwd_get_status(gdr_bwd_plan *plan, void *workspace, void *stream_) {
+    if (!plan || !workspace) return GDR_ERR_INVALID_ARG;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    int word = 0;
+    int *dev = reinterpret_cast<int *>(reinterpret_cast<char *>(workspace) + plan->o_status);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GDR_ERR_CUDA;
+    if (cudaMemcpy(&word, dev, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GDR_ERR_CUDA;
+    if (cudaMemset(dev, 0, sizeof(int)) != cudaSuccess) return GDR_ERR_CUDA;
+    if (word & ST_TIMEOUT) return GDR_ERR_TIMEOUT;
+    if (word & ST_BAD_SEQLENS) return GDR_ERR_DEVICE;
+    return GDR_OK;
+}
+
+gdr_status gdr_chunk_indices(const int32_t *cu_seqlens, int num_seqs, int BT, int max_chunks, int32_t *chunk_indices,
+                             int32_t *chunk_offsets, void *stream) {
+    if (!cu_seqlens || !chunk_indices || !chunk_offsets || num_seqs < 1 || BT < 1 || max_chunks < 0)
+        return GDR_ERR_INVALID_ARG;
+    if (launch_k0(cu_seqlens, num_seqs, BT, max_chunks, -1, chunk_indices, chunk_offsets, nullptr,
+                  (cudaStream_t)stream) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    return GDR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,309 @@
+// gdr_common.cuh -- device-side building blocks shared by the backward kernels.
+//
+// Tile geometry: every chunk is handled as a CT x DT tile (CT = 64 tokens, DT = 128 features).  A chunk
+// shorter than CT (the ragged tail of a sequence, or BT < 64) and K or V smaller than DT are zero-padded;
+// the padding is exact for this recurrence (a zero key row adds nothing to any state, a zero feature
+// column stays zero), so one tile shape serves every size the API accepts.
+//
+// Arithmetic: tensor-core operands are fp16 with fp32 accumulation; the states, gate math, cumulative
+// sums and every reduction stay in fp32.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace gdr {
+
+constexpr int CT = 64;        // tokens per chunk tile
+constexpr int DT = 128;       // features per tile (K and V padded to this)
+constexpr int PADH = 8;       // fp16 row padding in shared memory (keeps ldmatrix rows on distinct banks)
+constexpr int LDD = DT + PADH;  // pitch (halves) of a [*][DT] shared tile
+constexpr int LDC = CT + PADH;  // pitch (halves) of a [*][CT] shared tile
+
+// Device status bits (OR-ed into the workspace status word).
+constexpr int ST_BAD_SEQLENS = 1;
+constexpr int ST_TIMEOUT = 2;
+
+enum DType { F32 = 0, BF16 = 1, F16 = 2 };
+
+// Everything a kernel needs, passed by value.
+struct Params {
+    // sizes
+    int B, T, Hk, Hv, K, V, BT, G, N, per_channel, dense, max_chunks, nts;  // nts: chunks per dense seq
+    float scale;
+    int qkv_dtype, beta_dtype, dqdk_dtype, dv_dtype;
+    // inputs
+    const void *q, *k, *v, *beta, *dO;
+    const float *g, *h0, *dht;
+    const int32_t *cu;
+    // outputs
+    void *dq, *dk, *dv;
+    float *dbeta, *dg, *dh0;
+    // workspace
+    int *status;
+    int32_t *chunk_idx;  // [max_chunks][2]
+    int32_t *chunk_off;  // [N + 1]
+    float *gam;          // [u][CT] or [u][CT][DT]  chunk-local cumulative gate
+    __half *Tm;          // [u][CT][CT]   (I + A_kk)^-1
+    __half *Aqk;         // [u][CT][CT]   M (.) Q K^T   (causal, decayed; unscaled)
+    __half *W, *U;       // [u][CT][DT]
+    __half *Kt;          // [u][CT][DT]   K (.) exp(gamma_C - gamma)
+    __half *Qg;          // [u][CT][DT]   Q (.) exp(gamma)
+    __half *h, *dh;      // [u][DT][DT]   state entering / adjoint leaving each chunk, [v][k]
+    __half *Vn, *dVn;    // [u][CT][DT]
+    float *dgam;         // [u][CT] or [u][CT][DT]
+    float *dq_h, *dk_h;  // [T][Hv][K] per value head (GQA only)
+};
+
+// ---------------------------------------------------------------- sequence / chunk bookkeeping
+struct ChunkInfo {
+    int s, c, tok0, len;
+};
+
+__device__ __forceinline__ void seq_range(const Params &P, int s, int &bos, int &eos) {
+    if (P.dense) {
+        bos = s * P.T;
+        eos = bos + P.T;
+    } else {
+        bos = P.cu[s];
+        eos = P.cu[s + 1];
+    }
+}
+
+// Chunk n of the global, sequence-major list.  Returns false for entries past the total.
+__device__ __forceinline__ bool chunk_info(const Params &P, int n, ChunkInfo &ci) {
+    int s, c;
+    if (P.dense) {
+        s = n / P.nts;
+        c = n - s * P.nts;
+        if (s >= P.N) return false;
+    } else {
+        s = P.chunk_idx[2 * n];
+        c = P.chunk_idx[2 * n + 1];
+        if (s < 0) return false;
+    }
+    int bos, eos;
+    seq_range(P, s, bos, eos);
+    ci.s = s;
+    ci.c = c;
+    ci.tok0 = bos + c * P.BT;
+    int len = eos - ci.tok0;
+    ci.len = len < P.BT ? len : P.BT;
+    return ci.len > 0;
+}
+
+__device__ __forceinline__ int seq_chunk_base(const Params &P, int s) {
+    return P.dense ? s * P.nts : P.chunk_off[s];
+}
+
+// ---------------------------------------------------------------- element conversion
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+
+// Load 8 consecutive elements (16- or 32-byte aligned) as floats.
+__device__ __forceinline__ void load8(const float *p, float (&o)[8]) {
+    float4 a = *reinterpret_cast<const float4 *>(p);
+    float4 b = *reinterpret_cast<const float4 *>(p + 4);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&o)[8]) {
+    uint4 r = *reinterpret_cast<const uint4 *>(p);
+    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __bfloat1622float2(h2[i]);
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void load8(const __half *p, float (&o)[8]) {
+    uint4 r = *reinterpret_cast<const uint4 *>(p);
+    const __half2 *h2 = reinterpret_cast<const __half2 *>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __half22float2(h2[i]);
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8_half(const float (&x)[8]) {
+    uint4 r;
+    __half2 *h2 = reinterpret_cast<__half2 *>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h2[i] = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+    return r;
+}
+
+__device__ __forceinline__ float load_scalar(const void *p, size_t i, int dt) {
+    if (dt == F32) return reinterpret_cast<const float *>(p)[i];
+    if (dt == BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
+    return __half2float(reinterpret_cast<const __half *>(p)[i]);
+}
+
+__device__ __forceinline__ void store_scalar(void *p, size_t i, float x, int dt) {
+    if (dt == F32) reinterpret_cast<float *>(p)[i] = x;
+    else if (dt == BF16) reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
+    else reinterpret_cast<__half *>(p)[i] = __float2half_rn(x);
+}
+
+// Stage a [rows][ncols] block of a strided input (row r at src + r * stride) into a shared fp16 tile
+// [CT][LDD], multiplying row r by rowmul (nullable).  Rows >= rows and columns >= ncols become zero.
+// ncols must be a multiple of 8 or the full row is loaded element-wise.
+template <typename Tin>
+__device__ __forceinline__ void stage_rows_f16(__half *dst, const Tin *src, size_t stride, int rows, int ncols,
+                                               const float *rowmul, float mul, int tid, int nthr) {
+    for (int e = tid; e < CT * (DT / 8); e += nthr) {
+        int r = e / (DT / 8), c8 = (e % (DT / 8)) * 8;
+        float x[8];
+        if (r < rows && c8 + 8 <= ncols) {
+            load8(src + (size_t)r * stride + c8, x);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                x[j] = (r < rows && c8 + j < ncols) ? to_f32(src[(size_t)r * stride + c8 + j]) : 0.f;
+        }
+        float m = mul * (rowmul ? rowmul[r] : 1.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] *= m;
+        *reinterpret_cast<uint4 *>(dst + r * LDD + c8) = pack8_half(x);
+    }
+}
+
+// ---------------------------------------------------------------- tensor-core fragments (mma.sync)
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[2], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One warp accumulates a (16*MT) x (8*NT) tile: acc += A[m0.., 0:kdim] * B[0:kdim, n0..].
+//   AT = false: A(m, k) = A[m * lda + k]  (row-major M x K)
+//   AT = true : A(m, k) = A[k * lda + m]  (stored transposed, K x M)
+//   BT = false: B(k, n) = B[k * ldb + n]  (row-major K x N)
+//   BT = true : B(k, n) = B[n * ldb + k]  (stored transposed, N x K)
+// kdim is a multiple of 16.
+template <int MT, int NT, bool AT, bool BT>
+__device__ __forceinline__ void warp_mma(float (&acc)[MT][NT][4], const __half *A, int lda, const __half *B, int ldb,
+                                         int m0, int n0, int kdim) {
+    const int lane = threadIdx.x & 31;
+    const int r8 = lane & 7, mat = lane >> 3;
+    for (int k0 = 0; k0 < kdim; k0 += 16) {
+        uint32_t a[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            int mb = m0 + mt * 16;
+            if (!AT) {
+                const __half *p = A + (size_t)(mb + (lane & 15)) * lda + k0 + (lane >> 4) * 8;
+                ldsm_x4(a[mt], p);
+            } else {
+                const __half *p = A + (size_t)(k0 + r8 + (mat >> 1) * 8) * lda + mb + (mat & 1) * 8;
+                ldsm_x4_t(a[mt], p);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt + 1 < NT; nt += 2) {
+            int nb = n0 + nt * 8;
+            uint32_t b[4];
+            if (BT) {
+                const __half *p = B + (size_t)(nb + r8 + (mat >> 1) * 8) * ldb + k0 + (mat & 1) * 8;
+                ldsm_x4(b, p);
+            } else {
+                const __half *p = B + (size_t)(k0 + r8 + (mat & 1) * 8) * ldb + nb + (mat >> 1) * 8;
+                ldsm_x4_t(b, p);
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                mma16816(acc[mt][nt], a[mt], b[0], b[1]);
+                mma16816(acc[mt][nt + 1], a[mt], b[2], b[3]);
+            }
+        }
+        if (NT & 1) {
+            constexpr int nt = NT - 1;
+            int nb = n0 + nt * 8;
+            int m2 = (lane >> 3) & 1;
+            uint32_t b[2];
+            if (BT) {
+                const __half *p = B + (size_t)(nb + r8) * ldb + k0 + m2 * 8;
+                ldsm_x2(b, p);
+            } else {
+                const __half *p = B + (size_t)(k0 + r8 + m2 * 8) * ldb + nb;
+                ldsm_x2_t(b, p);
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][nt], a[mt], b[0], b[1]);
+        }
+    }
+}
+
+template <int MT, int NT>
+__device__ __forceinline__ void zero_acc(float (&acc)[MT][NT][4]) {
+#pragma unroll
+    for (int i = 0; i < MT; ++i)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
+}
+
+// Row / column of accumulator element e of tile (mt, nt) for the calling lane.
+__device__ __forceinline__ int acc_row(int m0, int mt, int e) {
+    return m0 + mt * 16 + ((threadIdx.x & 31) >> 2) + ((e >> 1) << 3);
+}
+__device__ __forceinline__ int acc_col(int n0, int nt, int e) {
+    return n0 + nt * 8 + ((threadIdx.x & 3) << 1) + (e & 1);
+}
+
+// ---------------------------------------------------------------- async copies
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// Copy a dense [rows][cols] fp16 block (cols multiple of 8) from global into a padded shared tile.
+__device__ __forceinline__ void cp_block_f16(__half *dst, int ldd, const __half *src, int rows, int cols, int tid,
+                                             int nthr) {
+    const int per_row = cols / 8;
+    for (int e = tid; e < rows * per_row; e += nthr) {
+        int r = e / per_row, c8 = (e % per_row) * 8;
+        cp_async16(dst + r * ldd + c8, src + (size_t)r * cols + c8);
+    }
+}
+
+__device__ __forceinline__ void flag_status(int *status, int bits) { atomicOr(status, bits); }
+
+}  // namespace gdr

@@ -1,0 +1,25 @@
+// gdr_kernels.h -- host-side launchers of the backward kernels (internal to libgdrbwd.so).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdr {
+
+struct Params;
+
+// K0: varlen chunk bookkeeping (one block).  expect_total_tokens < 0 skips the cu[N] == T check.
+cudaError_t launch_k0(const int32_t *cu, int N, int BT, int max_chunks, int expect_total_tokens, int32_t *chunk_idx,
+                      int32_t *chunk_off, int *status, cudaStream_t stream);
+// K1: chunk-local WY preparation (gate cumsum, A_kk inverse, W, U, decayed copies of K and Q).
+cudaError_t launch_k1(const Params &P, cudaStream_t stream);
+// K2: forward state recompute (fused_gdr_h), serial over chunks, tiled over V.
+cudaError_t launch_k2(const Params &P, int bv, cudaStream_t stream);
+// K3: reverse state-gradient scan, serial over chunks, tiled over V.
+cudaError_t launch_k3(const Params &P, int bv, cudaStream_t stream);
+// K4: per-chunk gradients dq, dk, dv, dbeta and the cumulative-gate gradient.
+cudaError_t launch_k4(const Params &P, cudaStream_t stream);
+// K5: reverse cumsum of the gate gradient and GQA reduction of dq / dk.
+cudaError_t launch_k5(const Params &P, cudaStream_t stream);
+
+}  // namespace gdr

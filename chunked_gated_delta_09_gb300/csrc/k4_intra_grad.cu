@@ -1,0 +1,446 @@
+// k4_intra_grad.cu -- per-chunk gradients (one CTA per chunk x value head).
+//
+// Given the state entering the chunk S_0 = h_n, the adjoint of the state leaving it dS_next = dh_n,
+// V_new, dV_new and T from the two scans and the WY preparation, this kernel produces the chunk's dq,
+// dk, dv, dbeta and the gradient of the chunk-local cumulative gate.  It follows the WY-gradient stage
+// of MindSpeed-Ops chunk_kda_bwd.md ("implementation principle": the inter-chunk products
+// dq = dO h^T, dk = v_new dh^T, dw = -(dv h^T), then the WY corrections with g, beta and A, and the
+// gradient through the triangular inverse dA = -A (dA_pre A) of the dA post kernels).  With
+// D = scale dO, M[r, j] = exp(gamma_r - gamma_j) [j <= r], L the strict part of M, K~ = K (.) exp(gamma_C - gamma):
+//   P      = (D V_new^T) (.) M
+//   dq     = diag(Gamma) D S_0 + P K
+//   dk     = P^T Q + K~-rowscale (V_new dS_next) + diag(beta Gamma) T^T dW + E K + E^T K
+//   dW     = -dV_new S_0,   dT = dW (diag(beta Gamma) K)^T + dV_new (diag(beta) V)^T
+//   dv     = diag(beta) T^T dV_new
+//   dA     = strict_lower(-T^T dT T^T),   E = diag(beta) (L (.) dA)
+//   dbeta  = rowsum(T^T dW (.) Gamma K) + rowsum(T^T dV_new (.) V) + rowsum(dA (.) L (.) K K^T)
+//   dgamma = q (.) dq - k (.) (P^T Q + K~ term) + k (.) (W term + E K - E^T K), plus, on the last row,
+//            Gamma_C <S_0, dS_next> + sum_j k_j (.) (K~ term)_j
+// (for the scalar gate the dgamma row is summed over channels).  The per-channel (KDA) gate turns each
+// decayed C x C product into a per-channel sum that the owner of each output element evaluates directly.
+#include "gdr_common.cuh"
+#include "gdr_kernels.h"
+
+namespace gdr {
+
+constexpr int K4_THREADS = 256;
+
+struct K4Smem {
+    __half Qs[CT * LDD], Ks[CT * LDD], Vs[CT * LDD], Ds[CT * LDD], Vns[CT * LDD], dVns[CT * LDD];
+    __half Hs[DT * LDD], dHs[DT * LDD];
+    __half Ts[CT * LDC], Pms[CT * LDC];
+    float gam[CT];
+    float beta[CT];
+    float dbeta[CT];
+    float dgrow[CT];
+    float lastrow[DT];
+};
+
+// Store 32 accumulator elements (C x K tile of this warp) as an output gradient row block.
+__device__ __forceinline__ void store_ck(const float (&a)[1][8][4], int m0, int n0, int len, int ncols, void *base,
+                                         size_t row_stride, int dt) {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+            if (r < len && c < ncols) store_scalar(base, (size_t)r * row_stride + c, a[0][nt][e], dt);
+        }
+}
+
+template <typename Tin, bool PC>
+__global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    K4Smem &S = *reinterpret_cast<K4Smem *>(smem_raw);
+    float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K4Smem));  // [CT][DT] per-channel only
+    // buffers reused once their first owner is done
+    __half *dWs = S.Ds;     // dW          after dq
+    __half *KGb = S.Qs;     // beta Gamma K (per-channel) after dk_O
+    __half *dTs = S.Pms;    // dT          after dk_O
+    __half *Xs = S.Vns;     // dT T^T      after dk_SC   (pitch LDC)
+    __half *Es = S.Pms;     // E           after X
+
+    if (*P.status & ST_BAD_SEQLENS) return;
+    const int n = blockIdx.x, hv = blockIdx.y, hk = hv / P.G;
+    ChunkInfo ci;
+    if (!chunk_info(P, n, ci)) return;
+    const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+    const size_t u = (size_t)n * P.Hv + hv;
+    const int len = ci.len;
+
+    // ---- stage everything
+    cp_block_f16(S.Hs, LDD, P.h + u * DT * DT, DT, DT, tid, K4_THREADS);
+    cp_block_f16(S.dHs, LDD, P.dh + u * DT * DT, DT, DT, tid, K4_THREADS);
+    cp_block_f16(S.Vns, LDD, P.Vn + u * CT * DT, CT, DT, tid, K4_THREADS);
+    cp_block_f16(S.dVns, LDD, P.dVn + u * CT * DT, CT, DT, tid, K4_THREADS);
+    cp_block_f16(S.Ts, LDC, P.Tm + u * CT * CT, CT, CT, tid, K4_THREADS);
+    cp_async_commit();
+    const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
+    const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
+    const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
+    const Tin *dop = reinterpret_cast<const Tin *>(P.dO) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
+    stage_rows_f16(S.Ks, kp, (size_t)P.Hk * P.K, len, P.K, nullptr, 1.f, tid, K4_THREADS);
+    stage_rows_f16(S.Qs, qp, (size_t)P.Hk * P.K, len, P.K, nullptr, 1.f, tid, K4_THREADS);
+    stage_rows_f16(S.Vs, vp, (size_t)P.Hv * P.V, len, P.V, nullptr, 1.f, tid, K4_THREADS);
+    stage_rows_f16(S.Ds, dop, (size_t)P.Hv * P.V, len, P.V, nullptr, P.scale, tid, K4_THREADS);
+    if (tid < CT) {
+        S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
+        S.dbeta[tid] = 0.f;
+        S.dgrow[tid] = 0.f;
+        if (!PC) S.gam[tid] = P.gam[u * CT + tid];
+    }
+    if (tid < DT) S.lastrow[tid] = 0.f;
+    if (PC)
+        for (int e = tid; e < CT * DT; e += K4_THREADS) gamK[e] = P.gam[u * CT * DT + e];
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // C x K tiling: warp w owns rows m0 .. m0+15 and columns n0 .. n0+63
+    const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 64;
+    // C x C tiling: rows cm0 .. cm0+15, columns cn0 .. cn0+31
+    const int cm0 = (wid & 3) * 16, cn0 = (wid >> 2) * 32;
+    auto G_ = [&](int r, int c) -> float { return PC ? gamK[r * DT + c] : S.gam[r]; };
+    const int rl = len - 1;
+
+    // ---- S1: P = (D V_new^T) (.) causal mask (.) [scalar: decay]
+    {
+        float g1[1][4][4];
+        zero_acc(g1);
+        warp_mma<1, 4, false, true>(g1, S.Ds, LDD, S.Vns, LDD, cm0, cn0, DT);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
+                float x = 0.f;
+                if (j <= r) x = PC ? g1[0][nt][e] : g1[0][nt][e] * expf(S.gam[r] - S.gam[j]);
+                S.Pms[r * LDC + j] = __float2half_rn(x);
+            }
+    }
+    __syncthreads();
+
+    float dgam[1][8][4];  // per-element gate-gradient contributions (rows x channels of this warp's tile)
+    float dk[1][8][4];
+    zero_acc(dgam);
+    // ---- S2: dq = Gamma (.) (D S_0) + P K   [per-channel: decayed sum per element]
+    {
+        float dq[1][8][4];
+        zero_acc(dq);
+        warp_mma<1, 8, false, false>(dq, S.Ds, LDD, S.Hs, LDD, m0, n0, DT);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dq[0][nt][e] *= expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e)));
+        if (!PC) {
+            warp_mma<1, 8, false, false>(dq, S.Pms, LDC, S.Ks, LDD, m0, n0, CT);
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                    float gr = gamK[r * DT + c], s = 0.f;
+                    for (int j = 0; j <= r; ++j)
+                        s += __half2float(S.Pms[r * LDC + j]) * __half2float(S.Ks[j * LDD + c]) * expf(gr - gamK[j * DT + c]);
+                    dq[0][nt][e] += s;
+                }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                dgam[0][nt][e] += __half2float(S.Qs[r * LDD + c]) * dq[0][nt][e];
+            }
+        if (P.G == 1)
+            store_ck(dq, m0, n0, len, P.K, reinterpret_cast<char *>(P.dq) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
+                     (P.dqdk_dtype == F32 ? 4 : 2), (size_t)P.Hk * P.K, P.dqdk_dtype);
+        else
+            store_ck(dq, m0, n0, len, P.K, P.dq_h + ((size_t)ci.tok0 * P.Hv + hv) * P.K, (size_t)P.Hv * P.K, F32);
+    }
+    // ---- S3: dk_O = P^T Q
+    {
+        zero_acc(dk);
+        if (!PC) {
+            warp_mma<1, 8, true, false>(dk, S.Pms, LDC, S.Qs, LDD, m0, n0, CT);
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int j = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                    float gj = gamK[j * DT + c], s = 0.f;
+                    for (int r = j; r < CT; ++r)
+                        s += __half2float(S.Pms[r * LDC + j]) * __half2float(S.Qs[r * LDD + c]) * expf(gamK[r * DT + c] - gj);
+                    dk[0][nt][e] = s;
+                }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                dgam[0][nt][e] -= __half2float(S.Ks[r * LDD + c]) * dk[0][nt][e];
+            }
+    }
+    __syncthreads();  // Ds, Pms, Qs free
+
+    // ---- S4: dk_SC = exp(gamma_C - gamma) (.) (V_new dS_next); last-row gate terms
+    {
+        float t[1][8][4];
+        zero_acc(t);
+        warp_mma<1, 8, false, false>(t, S.Vns, LDD, S.dHs, LDD, m0, n0, DT);
+        float part = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                float x = t[0][nt][e] * expf(G_(rl, c) - G_(r, c));
+                float kx = __half2float(S.Ks[r * LDD + c]) * x;
+                dk[0][nt][e] += x;
+                dgam[0][nt][e] -= kx;
+                if (PC) atomicAdd(&S.lastrow[c], kx);
+                else part += kx;
+            }
+        if (!PC) {
+            float s = part;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) atomicAdd(&S.lastrow[0], s);
+        }
+        // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate)
+        for (int c = tid; c < DT; c += K4_THREADS) {
+            float s = 0.f;
+            for (int v = 0; v < DT; ++v) s += __half2float(S.Hs[v * LDD + c]) * __half2float(S.dHs[v * LDD + c]);
+            s *= expf(G_(rl, c));
+            if (PC) atomicAdd(&S.lastrow[c], s);
+            else atomicAdd(&S.lastrow[0], s);
+        }
+    }
+    // ---- S5: dW = -dV_new S_0  -> dWs (fp16);  per-channel: beta Gamma K -> KGb
+    {
+        float t[1][8][4];
+        zero_acc(t);
+        warp_mma<1, 8, false, false>(t, S.dVns, LDD, S.Hs, LDD, m0, n0, DT);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                *reinterpret_cast<__half2 *>(dWs + r * LDD + c) = __floats2half2_rn(-t[0][nt][e], -t[0][nt][e + 1]);
+            }
+        if (PC) {
+            for (int e = tid; e < CT * DT; e += K4_THREADS) {
+                int r = e / DT, c = e % DT;
+                KGb[r * LDD + c] = __float2half_rn(S.beta[r] * expf(gamK[e]) * __half2float(S.Ks[r * LDD + c]));
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- S6: dT = dW (beta Gamma K)^T + dV_new (beta V)^T  -> dTs (fp16)
+    {
+        float a[1][4][4], b[1][4][4];
+        zero_acc(a);
+        zero_acc(b);
+        warp_mma<1, 4, false, true>(a, dWs, LDD, PC ? KGb : S.Ks, LDD, cm0, cn0, DT);
+        warp_mma<1, 4, false, true>(b, S.dVns, LDD, S.Vs, LDD, cm0, cn0, DT);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
+                float x = (PC ? a[0][nt][e] : a[0][nt][e] * S.beta[j] * expf(S.gam[j])) + b[0][nt][e] * S.beta[j];
+                dTs[r * LDC + j] = __float2half_rn(x);
+            }
+    }
+    // ---- S7: T^T dW -> dk_W, dbeta, dgamma
+    float rowb[2] = {0.f, 0.f};  // dbeta partials for rows m0 + lane/4 and +8
+    {
+        float t[1][8][4];
+        zero_acc(t);
+        warp_mma<1, 8, true, false>(t, S.Ts, LDC, dWs, LDD, m0, n0, CT);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                float Gm = expf(G_(r, c));
+                float kv = __half2float(S.Ks[r * LDD + c]);
+                float x = S.beta[r] * Gm * t[0][nt][e];
+                dk[0][nt][e] += x;
+                dgam[0][nt][e] += kv * x;
+                rowb[e >> 1] += t[0][nt][e] * kv * Gm;
+            }
+    }
+    // ---- S8: T^T dV_new -> dv, dbeta
+    {
+        float t[1][8][4];
+        zero_acc(t);
+        warp_mma<1, 8, true, false>(t, S.Ts, LDC, S.dVns, LDD, m0, n0, CT);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                rowb[e >> 1] += t[0][nt][e] * __half2float(S.Vs[r * LDD + c]);
+                t[0][nt][e] *= S.beta[r];
+            }
+        store_ck(t, m0, n0, len, P.V, reinterpret_cast<char *>(P.dv) + ((size_t)ci.tok0 * P.Hv + hv) * P.V *
+                 (P.dv_dtype == F32 ? 4 : 2), (size_t)P.Hv * P.V, P.dv_dtype);
+    }
+    __syncthreads();  // dTs complete; Vns free
+
+    // ---- S9: X = dT T^T -> Xs (fp16)
+    {
+        float x[1][4][4];
+        zero_acc(x);
+        warp_mma<1, 4, false, true>(x, dTs, LDC, S.Ts, LDC, cm0, cn0, CT);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
+                *reinterpret_cast<__half2 *>(Xs + r * LDC + j) = __floats2half2_rn(x[0][nt][e], x[0][nt][e + 1]);
+            }
+    }
+    __syncthreads();
+    // ---- S10: dA = strict_lower(-T^T X); dbeta from A; E = beta (.) L (.) dA -> Es
+    {
+        float da[1][4][4], kk[1][4][4];
+        zero_acc(da);
+        warp_mma<1, 4, true, false>(da, S.Ts, LDC, Xs, LDC, cm0, cn0, CT);
+        if (!PC) {
+            zero_acc(kk);
+            warp_mma<1, 4, false, true>(kk, S.Ks, LDD, S.Ks, LDD, cm0, cn0, DT);
+        }
+        float rb[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int i = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
+                float dA = j < i ? -da[0][nt][e] : 0.f;
+                float L = 1.f, kkd = 0.f;
+                if (j < i) {
+                    if (!PC) {
+                        L = expf(S.gam[i] - S.gam[j]);
+                        kkd = L * kk[0][nt][e];
+                    } else {
+                        for (int c = 0; c < DT; ++c)
+                            kkd += __half2float(S.Ks[i * LDD + c]) * __half2float(S.Ks[j * LDD + c]) *
+                                   expf(gamK[i * DT + c] - gamK[j * DT + c]);
+                    }
+                }
+                rb[e >> 1] += dA * kkd;
+                Es[i * LDC + j] = __float2half_rn(S.beta[i] * (PC ? 1.f : L) * dA);
+            }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float s = rb[h];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if ((lane & 3) == 0) atomicAdd(&S.dbeta[cm0 + (lane >> 2) + 8 * h], s);
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float s = rowb[h];
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        if ((lane & 3) == 0) atomicAdd(&S.dbeta[m0 + (lane >> 2) + 8 * h], s);
+    }
+    __syncthreads();
+    // ---- S11: dk_Ar = E K (+), dk_Ac = E^T K (-)
+    {
+        float a[1][8][4], b[1][8][4];
+        zero_acc(a);
+        zero_acc(b);
+        if (!PC) {
+            warp_mma<1, 8, false, false>(a, Es, LDC, S.Ks, LDD, m0, n0, CT);
+            warp_mma<1, 8, true, false>(b, Es, LDC, S.Ks, LDD, m0, n0, CT);
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                    float gr = gamK[r * DT + c], sa = 0.f, sb = 0.f;
+                    for (int j = 0; j < r; ++j)
+                        sa += __half2float(Es[r * LDC + j]) * __half2float(S.Ks[j * LDD + c]) * expf(gr - gamK[j * DT + c]);
+                    for (int i = r + 1; i < CT; ++i)
+                        sb += __half2float(Es[i * LDC + r]) * __half2float(S.Ks[i * LDD + c]) * expf(gamK[i * DT + c] - gr);
+                    a[0][nt][e] = sa;
+                    b[0][nt][e] = sb;
+                }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                float kv = __half2float(S.Ks[r * LDD + c]);
+                dk[0][nt][e] += a[0][nt][e] + b[0][nt][e];
+                dgam[0][nt][e] += kv * (a[0][nt][e] - b[0][nt][e]);
+            }
+    }
+    // ---- dk out
+    if (P.G == 1)
+        store_ck(dk, m0, n0, len, P.K, reinterpret_cast<char *>(P.dk) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
+                 (P.dqdk_dtype == F32 ? 4 : 2), (size_t)P.Hk * P.K, P.dqdk_dtype);
+    else
+        store_ck(dk, m0, n0, len, P.K, P.dk_h + ((size_t)ci.tok0 * P.Hv + hv) * P.K, (size_t)P.Hv * P.K, F32);
+
+    // ---- gate gradient of the cumulative gate
+    if (!PC) {
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) rs[e >> 1] += dgam[0][nt][e];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float s = rs[h];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if ((lane & 3) == 0) atomicAdd(&S.dgrow[m0 + (lane >> 2) + 8 * h], s);
+        }
+        __syncthreads();
+        if (tid < CT) {
+            float x = S.dgrow[tid] + (tid == rl ? S.lastrow[0] : 0.f);
+            P.dgam[u * CT + tid] = tid < len ? x : 0.f;
+            if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = S.dbeta[tid];
+        }
+    } else {
+        __syncthreads();
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                float x = dgam[0][nt][e] + (r == rl ? S.lastrow[c] : 0.f);
+                P.dgam[(u * CT + r) * DT + c] = r < len ? x : 0.f;
+            }
+        if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = S.dbeta[tid];
+    }
+}
+
+template <typename Tin, bool PC>
+static cudaError_t launch_k4_t(const Params &P, cudaStream_t stream) {
+    size_t smem = sizeof(K4Smem) + (PC ? sizeof(float) * CT * DT : 0);
+    cudaError_t e = cudaFuncSetAttribute(k4_intra_grad<Tin, PC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(P.max_chunks, P.Hv);
+    k4_intra_grad<Tin, PC><<<grid, K4_THREADS, smem, stream>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_k4(const Params &P, cudaStream_t stream) {
+    if (P.qkv_dtype == F32) return P.per_channel ? launch_k4_t<float, true>(P, stream) : launch_k4_t<float, false>(P, stream);
+    if (P.qkv_dtype == BF16)
+        return P.per_channel ? launch_k4_t<__nv_bfloat16, true>(P, stream) : launch_k4_t<__nv_bfloat16, false>(P, stream);
+    return P.per_channel ? launch_k4_t<__half, true>(P, stream) : launch_k4_t<__half, false>(P, stream);
+}
+
+}  // namespace gdr

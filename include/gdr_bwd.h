@@ -17,7 +17,8 @@
  * API takes the RAW per-token log-gate g (not its chunk-local cumulative sum) and returns dg with
  * respect to the raw gate; the chunk cumsum and the closing reverse cumsum happen inside.
  *
- * Tensor layouts (all row-major, last axis contiguous, every base pointer 16-byte aligned):
+ * Tensor layouts (all row-major, last axis contiguous; q, k, v, dO, dq, dk, dv 16-byte aligned, the
+ * others 4-byte aligned):
  *   q, k      [B, T, Hk, K]     qkv_dtype
  *   v, dO     [B, T, Hv, V]     qkv_dtype
  *   beta      [B, T, Hv]        beta_dtype
@@ -66,7 +67,8 @@ typedef enum {
 
 typedef enum { GDR_F32 = 0, GDR_BF16 = 1, GDR_F16 = 2 } gdr_dtype;
 
-/* Problem description.  Sizes: K, V in [1, 128]; BT in {16, 32, 64}; Hv a multiple of Hk. */
+/* Problem description.  Sizes: K and V multiples of 8 in [8, 128]; BT in {16, 32, 64}; Hv a multiple
+ * of Hk; B * T at most 2^30 tokens. */
 typedef struct {
     int B, T, Hk, Hv, K, V, BT;
     int num_seqs;          /* 0: dense [B, T, ...]; > 0: varlen with B == 1 and cu_seqlens[num_seqs + 1] */
@@ -101,6 +103,21 @@ size_t gdr_bwd_workspace_bytes(const gdr_bwd_plan *plan);
  * used by another call that may run concurrently. */
 gdr_status gdr_bwd_run(gdr_bwd_plan *plan, const gdr_bwd_args *args, void *workspace, size_t ws_bytes,
                        void *stream);
+
+/* Number of stages and the kernels behind them: 0 varlen chunk bookkeeping, 1 WY preparation,
+ * 2 forward state recompute, 3 state-gradient scan, 4 per-chunk gradients, 5 gate reverse cumsum and
+ * GQA reduction. */
+#define GDR_BWD_NUM_STAGES 6
+
+/* Same as gdr_bwd_run, and records events[0] before the first stage and events[i + 1] after stage i
+ * (events: GDR_BWD_NUM_STAGES + 1 cudaEvent_t handles created by the caller, all on `stream`'s device).
+ * A stage that has nothing to do (stage 0 for dense input) records its event right after the previous
+ * one.  Used to time each kernel on the stream it runs on.  NULL events -> GDR_ERR_INVALID_ARG. */
+gdr_status gdr_bwd_run_profiled(gdr_bwd_plan *plan, const gdr_bwd_args *args, void *workspace, size_t ws_bytes,
+                                void *stream, void *const *events);
+
+/* Number of kernel launches one gdr_bwd_run of this plan queues (0 for a NULL plan). */
+int gdr_bwd_launch_count(const gdr_bwd_plan *plan);
 
 /* Synchronise `stream` and read the device status word that the last run on this workspace left:
  * GDR_OK, GDR_ERR_TIMEOUT or GDR_ERR_DEVICE.  Also clears the word. */

@@ -1,0 +1,71 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path, run the oracle, compare."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+import oracle
+from chunked_gated_delta_09_gb300 import ops
+
+# relative L2 bars: 2e-2 for bf16 / fp16 outputs, 5e-3 for fp32 outputs
+TOL = {torch.float32: 5e-3, torch.bfloat16: 2e-2, torch.float16: 2e-2}
+
+
+def out_dtypes(prob):
+    return dict(dq=prob.dqdk_dtype, dk=prob.dqdk_dtype, dv=prob.dv_dtype, dbeta=torch.float32,
+                dg=torch.float32, dh0=torch.float32)
+
+
+def run_gpu(prob, plan=None, device="cuda"):
+    plan = plan or ops.plan_for(prob)
+    d = ops.problem_to_device(prob, device)
+    out = plan.alloc_outputs(device)
+    ws = plan.alloc_workspace(device)
+    plan.run(out=out, workspace=ws, **d)
+    st = plan.get_status(ws)
+    assert st == 0, f"device status {st}"
+    torch.cuda.synchronize()
+    return {k: v.float().cpu().to(torch.float64).numpy() for k, v in out.items()}
+
+
+def rel_l2(got, ref):
+    nr = np.linalg.norm(ref)
+    diff = np.linalg.norm(got - ref)
+    return diff / nr if nr > 0 else diff
+
+
+def compare(prob, got, ref, keys=None, slices=None):
+    """Return {name: (rel_l2, tol)} and assert every output is within its tolerance."""
+    res = {}
+    for name, dt in out_dtypes(prob).items():
+        if keys is not None and name not in keys:
+            continue
+        g, r = got[name], ref[name]
+        if slices and name in slices:
+            g = g[slices[name]]
+        assert g.shape == r.shape, (name, g.shape, r.shape)
+        assert np.all(np.isfinite(g)), f"{name} has non-finite values"
+        e = rel_l2(g, r)
+        res[name] = (e, TOL[dt])
+    bad = {k: v for k, v in res.items() if not v[0] <= v[1]}
+    assert not bad, f"{prob.name}: outside tolerance {bad} (all: {res})"
+    return res
+
+
+def head_subset(prob, hks):
+    """The same problem restricted to key heads `hks` and the value heads that read them."""
+    G = prob.Hv // prob.Hk
+    hvs = [hk * G + j for hk in hks for j in range(G)]
+    sub = dataclasses.replace(
+        prob, name=prob.name + f"[hk{hks}]", Hk=len(hks), Hv=len(hvs),
+        q=prob.q[:, :, hks].contiguous(), k=prob.k[:, :, hks].contiguous(), v=prob.v[:, :, hvs].contiguous(),
+        beta=prob.beta[:, :, hvs].contiguous(), g=prob.g[:, :, hvs].contiguous(),
+        dO=prob.dO[:, :, hvs].contiguous(),
+        h0=None if prob.h0 is None else prob.h0[:, hvs].contiguous(),
+        dht=None if prob.dht is None else prob.dht[:, hvs].contiguous())
+    slices = dict(dq=(slice(None), slice(None), hks), dk=(slice(None), slice(None), hks),
+                  dv=(slice(None), slice(None), hvs), dbeta=(slice(None), slice(None), hvs),
+                  dg=(slice(None), slice(None), hvs), dh0=(slice(None), hvs))
+    return sub, slices
