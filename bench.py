@@ -44,7 +44,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="gdn_t32k_bf16")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=8192)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=32768)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
 
@@ -208,7 +208,7 @@ def run_reference(args):
         return
     import oracle
     nthr = oracle.max_threads()
-    tokens = 2048
+    tokens = 8192
     sample = cpu_sample(args.workload, tokens, min(16, nthr))
     for _ in range(args.warmup):
         time_oracle(sample)

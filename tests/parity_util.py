@@ -2,6 +2,8 @@
 from __future__ import annotations
 
 import dataclasses
+import json
+import os
 
 import numpy as np
 import torch
@@ -49,6 +51,10 @@ def compare(prob, got, ref, keys=None, slices=None):
         assert np.all(np.isfinite(g)), f"{name} has non-finite values"
         e = rel_l2(g, r)
         res[name] = (e, TOL[dt])
+    log = os.environ.get("GDR_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"case": prob.name, **{k: v[0] for k, v in res.items()}}) + "\n")
     bad = {k: v for k, v in res.items() if not v[0] <= v[1]}
     assert not bad, f"{prob.name}: outside tolerance {bad} (all: {res})"
     return res
