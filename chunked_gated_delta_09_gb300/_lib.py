@@ -13,8 +13,9 @@ GDR_F32, GDR_BF16, GDR_F16 = 0, 1, 2
 
 # every function the header declares
 EXPORTS = ("gdr_bwd_create", "gdr_bwd_workspace_bytes", "gdr_bwd_run", "gdr_bwd_run_profiled",
-           "gdr_bwd_launch_count", "gdr_bwd_get_status", "gdr_bwd_destroy", "gdr_chunk_indices",
-           "gdr_status_string")
+           "gdr_bwd_launch_count", "gdr_bwd_get_status", "gdr_bwd_run_noalloc", "gdr_bwd_destroy",
+           "gdr_chunk_indices", "gdr_status_string")
+NOALLOC_MAX_WORKSPACE = 64 << 20
 NUM_STAGES = 6
 STAGE_NAMES = ("k0_chunk_indices", "k1_wy_prep", "k2_fused_gdr_h", "k3_dh_scan", "k4_intra_grad", "k5_dg_reduce")
 
@@ -63,6 +64,8 @@ def load(path: str | None = None):
         lib.gdr_bwd_run_profiled.restype = ci
         lib.gdr_bwd_launch_count.argtypes = [vp]
         lib.gdr_bwd_launch_count.restype = ci
+        lib.gdr_bwd_run_noalloc.argtypes = [vp, ctypes.POINTER(GdrBwdArgs), vp]
+        lib.gdr_bwd_run_noalloc.restype = ci
         lib.gdr_bwd_get_status.argtypes = [vp, vp, vp]
         lib.gdr_bwd_get_status.restype = ci
         lib.gdr_bwd_destroy.argtypes = [vp]

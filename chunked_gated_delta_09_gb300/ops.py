@@ -93,6 +93,17 @@ class GdrBwdPlan:
         if st != _lib.GDR_OK:
             raise GdrError(st, "gdr_bwd_run_profiled")
 
+    def run_noalloc(self, *, q, k, v, beta, g, dO, h0=None, dht=None, cu_seqlens=None, out: dict, stream=None):
+        """Queue gdr_bwd_run_noalloc: the same backward with the library's own static scratch array
+        instead of a workspace (plans up to NOALLOC_MAX_WORKSPACE bytes of workspace)."""
+        args = GdrBwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), beta=_ptr(beta), g=_ptr(g), h0=_ptr(h0), dO=_ptr(dO),
+                          dht=_ptr(dht), cu_seqlens=_ptr(cu_seqlens), dq=_ptr(out["dq"]), dk=_ptr(out["dk"]),
+                          dv=_ptr(out["dv"]), dbeta=_ptr(out["dbeta"]), dg=_ptr(out["dg"]),
+                          dh0=_ptr(out.get("dh0")))
+        st = self.lib.gdr_bwd_run_noalloc(self.handle, ctypes.byref(args), _stream_ptr(stream))
+        if st != _lib.GDR_OK:
+            raise GdrError(st, "gdr_bwd_run_noalloc")
+
     @property
     def launch_count(self) -> int:
         return int(self.lib.gdr_bwd_launch_count(self.handle))

@@ -123,6 +123,19 @@ int gdr_bwd_launch_count(const gdr_bwd_plan *plan);
  * GDR_OK, GDR_ERR_TIMEOUT or GDR_ERR_DEVICE.  Also clears the word. */
 gdr_status gdr_bwd_get_status(gdr_bwd_plan *plan, void *workspace, void *stream);
 
+/* No counterpart on the pages.  The whole backward without a caller-provided workspace, for callers
+ * that cannot allocate device memory when they need it (a plugin that may only use the tensors it is
+ * given, a fixed device-memory budget, a loop that cannot afford cudaMalloc's implicit synchronisation).
+ * Its scratch memory is one file-scope __device__ array of GDR_BWD_NOALLOC_MAX_WORKSPACE bytes, which
+ * every GPU that loads the library holds until the process exits.  It allocates nothing and calls no
+ * allocating routine.  Plans whose gdr_bwd_workspace_bytes() exceeds the maximum are rejected with
+ * GDR_ERR_UNSUPPORTED before anything is launched.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that first call before any
+ * stream capture starts.  All calls share the array: calls that overlap on the GPU race, and the
+ * device status word of these calls cannot be read with gdr_bwd_get_status. */
+#define GDR_BWD_NOALLOC_MAX_WORKSPACE (64u << 20)
+gdr_status gdr_bwd_run_noalloc(gdr_bwd_plan *plan, const gdr_bwd_args *args, void *stream);
+
 /* Free the plan (NULL is accepted). */
 void gdr_bwd_destroy(gdr_bwd_plan *plan);
 
