@@ -69,14 +69,18 @@ __global__ void __launch_bounds__(K2_THREADS) k2_fused_gdr_h(const Params P, int
         int len = eos - (bos + c * P.BT);
         len = len < P.BT ? len : P.BT;
         if (PC) {
-            for (int e = tid; e < DT; e += K2_THREADS) gC[buf * DT + e] = P.gam[(u * CT + len - 1) * DT + e];
+            for (int e = tid; e < DT / 4; e += K2_THREADS)
+                cp_async16(gC + buf * DT + 4 * e, P.gam + (u * CT + len - 1) * DT + 4 * e);
         } else if (tid == 0) {
-            gC[buf * DT] = P.gam[u * CT + len - 1];
+            cp_async4(gC + buf * DT, P.gam + u * CT + len - 1);
         }
         cp_async_commit();
     };
 
-    if (nc > 0) issue(0, 0);
+    if (nc > 0) {
+        issue(0, 0);
+        cp_async_wait<0>();
+    }
     for (int c = 0; c < nc; ++c) {
         const int buf = c & 1;
         const size_t u = (size_t)(base + c) * P.Hv + hv;
@@ -87,8 +91,7 @@ __global__ void __launch_bounds__(K2_THREADS) k2_fused_gdr_h(const Params P, int
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) Sts[acc_row(m0, mt, e) * LDB + acc_col(0, nt, e)] = __float2half_rn(acc[mt][nt][e]);
-        cp_async_wait<0>();
-        __syncthreads();
+        __syncthreads();  // chunk c's operands (waited for at the end of the previous step) and S^T visible
         if (c + 1 < nc) issue(c + 1, buf ^ 1);
         // h_n[v][k] for this V slice (coalesced along k)
         {
@@ -127,6 +130,7 @@ __global__ void __launch_bounds__(K2_THREADS) k2_fused_gdr_h(const Params P, int
                 for (int nt = 0; nt < NT; ++nt) acc[mt][nt][e] *= G;
             }
         warp_mma<2, NT, true, false>(acc, Kts + buf * CT * LDD, LDD, Vns, LDB, m0, 0, CT);
+        if (c + 1 < nc) cp_async_wait<0>();  // chunk c+1's operands landed (this thread's copies)
     }
 }
 

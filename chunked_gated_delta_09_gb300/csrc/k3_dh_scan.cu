@@ -25,8 +25,8 @@ template <typename Tin, int BV, bool PC>
 __global__ void __launch_bounds__(K3_THREADS) k3_dh_scan(const Params P, int nvt) {
     constexpr int LDB = ScanLd3<BV>::value;
     constexpr int NT = BV / 8;
-    constexpr int DV8 = CT * (BV / 8);                  // 8-element vectors in one D slice
-    constexpr int DREG = (DV8 + K3_THREADS - 1) / K3_THREADS;
+    constexpr int EPC = 16 / sizeof(Tin);              // input elements per 16-byte copy
+    constexpr int DCH = CT * (BV / EPC);                // 16-byte copies per raw dO slice
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __half *Ws = reinterpret_cast<__half *>(smem_raw);  // [2][CT][LDD]
     __half *Kts = Ws + 2 * CT * LDD;                    // [2][CT][LDD]
@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(K3_THREADS) k3_dh_scan(const Params P, int nvt
     __half *dSts = Ds + 2 * CT * LDB;                   // [DT][LDB]
     __half *dVs = dSts + DT * LDB;                      // [CT][LDB]   -dV_new slice
     float *gC = reinterpret_cast<float *>(dVs + CT * LDB);  // [2][DT]
+    Tin *Draw = reinterpret_cast<Tin *>(gC + 2 * DT);        // [2][CT][BV] raw dO slice
 
     if (*P.status & ST_BAD_SEQLENS) return;
     const int vt = blockIdx.x % nvt, hv = (blockIdx.x / nvt) % P.Hv, s = blockIdx.x / (nvt * P.Hv);
@@ -61,37 +62,28 @@ __global__ void __launch_bounds__(K3_THREADS) k3_dh_scan(const Params P, int nvt
                 acc[mt][nt][e] = x;
             }
 
-    // D slice prefetch through registers (it needs a dtype conversion, so no cp.async)
-    float dreg[DREG][8];
-    auto load_d = [&](int c) {
+    // raw dO slice: one 16-byte copy per (row, EPC columns); rows past the chunk or columns past V zero-fill
+    auto issue_d = [&](int c, int buf) {
         int tok0 = bos + c * P.BT;
         int len = eos - tok0;
         len = len < P.BT ? len : P.BT;
-#pragma unroll
-        for (int i = 0; i < DREG; ++i) {
-            int e = tid + i * K3_THREADS;
-            int r = e / (BV / 8), c8 = (e % (BV / 8)) * 8;
-            bool ok = e < DV8 && r < len;
-            if (ok && v0 + c8 + 8 <= P.V) {
-                load8(dOp + ((size_t)(tok0 + r) * P.Hv + hv) * P.V + v0 + c8, dreg[i]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    dreg[i][j] = (ok && v0 + c8 + j < P.V) ? to_f32(dOp[((size_t)(tok0 + r) * P.Hv + hv) * P.V + v0 + c8 + j]) : 0.f;
-            }
+        for (int e = tid; e < DCH; e += K3_THREADS) {
+            int r = e / (BV / EPC), cc = (e % (BV / EPC)) * EPC;
+            bool ok = r < len && v0 + cc + EPC <= P.V;
+            const Tin *src = ok ? dOp + ((size_t)(tok0 + r) * P.Hv + hv) * P.V + v0 + cc : dOp;
+            cp_async16_zfill(Draw + (buf * CT + r) * BV + cc, src, ok ? 16 : 0);
         }
     };
-    auto store_d = [&](int buf) {
+    // scale and convert the copies this thread made (visible to it after its own wait)
+    auto convert_d = [&](int buf) {
+        for (int e = tid; e < DCH; e += K3_THREADS) {
+            int r = e / (BV / EPC), cc = (e % (BV / EPC)) * EPC;
+            const Tin *src = Draw + (buf * CT + r) * BV + cc;
+            __half *dst = Ds + buf * CT * LDB + r * LDB + cc;
 #pragma unroll
-        for (int i = 0; i < DREG; ++i) {
-            int e = tid + i * K3_THREADS;
-            if (e < DV8) {
-                int r = e / (BV / 8), c8 = (e % (BV / 8)) * 8;
-                float x[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) x[j] = dreg[i][j] * P.scale;
-                *reinterpret_cast<uint4 *>(Ds + buf * CT * LDB + r * LDB + c8) = pack8_half(x);
-            }
+            for (int j = 0; j < EPC; j += 2)
+                *reinterpret_cast<__half2 *>(dst + j) =
+                    __floats2half2_rn(to_f32(src[j]) * P.scale, to_f32(src[j + 1]) * P.scale);
         }
     };
     auto issue = [&](int c, int buf) {
@@ -103,17 +95,19 @@ __global__ void __launch_bounds__(K3_THREADS) k3_dh_scan(const Params P, int nvt
         int len = eos - (bos + c * P.BT);
         len = len < P.BT ? len : P.BT;
         if (PC) {
-            for (int e = tid; e < DT; e += K3_THREADS) gC[buf * DT + e] = P.gam[(u * CT + len - 1) * DT + e];
+            for (int e = tid; e < DT / 4; e += K3_THREADS)
+                cp_async16(gC + buf * DT + 4 * e, P.gam + (u * CT + len - 1) * DT + 4 * e);
         } else if (tid == 0) {
-            gC[buf * DT] = P.gam[u * CT + len - 1];
+            cp_async4(gC + buf * DT, P.gam + u * CT + len - 1);
         }
+        issue_d(c, buf);
         cp_async_commit();
     };
 
     if (nc > 0) {
-        load_d(nc - 1);
-        store_d((nc - 1) & 1);
         issue(nc - 1, (nc - 1) & 1);
+        cp_async_wait<0>();
+        convert_d((nc - 1) & 1);
     }
     for (int c = nc - 1; c >= 0; --c) {
         const int buf = c & 1;
@@ -125,12 +119,8 @@ __global__ void __launch_bounds__(K3_THREADS) k3_dh_scan(const Params P, int nvt
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     dSts[acc_row(m0, mt, e) * LDB + acc_col(0, nt, e)] = __float2half_rn(acc[mt][nt][e]);
-        cp_async_wait<0>();
-        __syncthreads();
-        if (c > 0) {
-            issue(c - 1, buf ^ 1);
-            load_d(c - 1);
-        }
+        __syncthreads();  // chunk c's operands (waited for and converted at the end of the previous step)
+        if (c > 0) issue(c - 1, buf ^ 1);
         {
             __half *dhg = P.dh + u * DT * DT;
             for (int e = tid; e < BV * DT; e += K3_THREADS) {
@@ -167,7 +157,10 @@ __global__ void __launch_bounds__(K3_THREADS) k3_dh_scan(const Params P, int nvt
             }
         warp_mma<2, NT, true, false>(acc, Qgs + buf * CT * LDD, LDD, Ds + buf * CT * LDB, LDB, m0, 0, CT);
         warp_mma<2, NT, true, false>(acc, Ws + buf * CT * LDD, LDD, dVs, LDB, m0, 0, CT);
-        if (c > 0) store_d(buf ^ 1);
+        if (c > 0) {
+            cp_async_wait<0>();
+            convert_d(buf ^ 1);
+        }
     }
     if (P.dh0) {
 #pragma unroll
@@ -186,7 +179,7 @@ template <typename Tin, int BV, bool PC>
 static cudaError_t launch_k3_t(const Params &P, cudaStream_t stream) {
     constexpr int LDB = ScanLd3<BV>::value;
     size_t smem = sizeof(__half) * (6 * CT * LDD + 2 * CT * LDC + 2 * CT * LDB + DT * LDB + CT * LDB) +
-                  sizeof(float) * 2 * DT;
+                  sizeof(float) * 2 * DT + sizeof(Tin) * 2 * CT * BV;
     cudaError_t e = cudaFuncSetAttribute(k3_dh_scan<Tin, BV, PC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int nvt = DT / BV;
