@@ -19,10 +19,12 @@ using namespace gdr;
 struct gdr_bwd_plan {
     gdr_bwd_desc d;
     int G, N, dense, nts, max_chunks, bv;
+    int k4_tc;  // per-chunk gradients on tcgen05 (scalar gate); the per-channel gate uses the mma.sync kernel
+    int scan_tc, NS, Lseg;  // tensor-core segment-parallel scans and their segmentation
     long long tokens;  // B * T
     // workspace byte offsets
     size_t o_status, o_cidx, o_coff, o_gam, o_T, o_Aqk, o_W, o_U, o_Kt, o_Qg, o_h, o_dh, o_Vn, o_dVn, o_dgam, o_dqh,
-        o_dkh, total;
+        o_dkh, o_seg, total;
 };
 
 namespace {
@@ -61,6 +63,8 @@ void layout(gdr_bwd_plan &p) {
     size_t per_head = p.G > 1 ? sizeof(float) * (size_t)p.tokens * d.Hv * d.K : 0;
     p.o_dqh = take(per_head);
     p.o_dkh = take(per_head);
+    size_t seg_units = p.NS > 1 ? (size_t)p.N * d.Hv * p.NS : 0;
+    p.o_seg = take(5 * sizeof(float) * seg_units * DT * DT);
     p.total = off;
 }
 
@@ -128,6 +132,24 @@ gdr_status gdr_bwd_create(const gdr_bwd_desc *desc, gdr_bwd_plan **out) {
     }
     p->max_chunks = (int)mc;
     p->bv = choose_bv(*p);
+    {
+        // segments: enough (sequence x head x segment) CTAs to give every SM one, at least 4 chunks each
+        const char *ls = getenv("GDR_SCAN_LEGACY");
+        p->scan_tc = !(ls && atoi(ls) != 0);
+        long long units = (long long)p->N * d.Hv;
+        long long maxnc = p->dense ? p->nts : ((long long)d.T + d.BT - 1) / d.BT;
+        long long ns = units > 0 ? kNumSMs / units : 1;
+        ns = ns < (maxnc + 3) / 4 ? ns : (maxnc + 3) / 4;
+        const char *env = getenv("GDR_NSEG");
+        if (env && atoi(env) > 0) ns = atoi(env);
+        if (ns < 1 || !p->scan_tc) ns = 1;
+        p->NS = (int)ns;
+        p->Lseg = maxnc > 0 ? (int)((maxnc + ns - 1) / ns) : 1;
+    }
+    // per-chunk gradients: the mma.sync kernel is currently the faster one; GDR_K4_TC=1 selects the
+    // tcgen05 kernel (scalar gate only)
+    const char *k4tc = getenv("GDR_K4_TC");
+    p->k4_tc = !d.gate_per_channel && k4tc && atoi(k4tc) != 0;
     layout(*p);
     *out = p;
     return GDR_OK;
@@ -207,6 +229,17 @@ static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *work
     P.dgam = reinterpret_cast<float *>(ws + plan->o_dgam);
     P.dq_h = plan->G > 1 ? reinterpret_cast<float *>(ws + plan->o_dqh) : nullptr;
     P.dk_h = plan->G > 1 ? reinterpret_cast<float *>(ws + plan->o_dkh) : nullptr;
+    P.NS = plan->NS;
+    P.Lseg = plan->Lseg;
+    if (plan->NS > 1) {
+        size_t one = (size_t)plan->N * d.Hv * plan->NS * DT * DT;
+        float *seg = reinterpret_cast<float *>(ws + plan->o_seg);
+        P.segE = seg;
+        P.segPhi = seg + one;
+        P.segF = seg + 2 * one;
+        P.segSin = seg + 3 * one;
+        P.segdS = seg + 4 * one;
+    }
 
     auto mark = [&](int i) -> bool {
         return !events || cudaEventRecord((cudaEvent_t)events[i], stream) == cudaSuccess;
@@ -222,11 +255,28 @@ static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *work
     const bool any_chunks = plan->max_chunks > 0;
     if (any_chunks && (e = launch_k1(P, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     if (!mark(2)) return GDR_ERR_CUDA;
-    if (any_chunks && (e = launch_k2(P, plan->bv, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    if (plan->scan_tc) {
+        if (any_chunks && plan->NS > 1) {
+            if ((e = launch_k2_scan(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+            if ((e = launch_k23_combine(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+        }
+        if (any_chunks && (e = launch_k2_scan(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    } else if (any_chunks && (e = launch_k2(P, plan->bv, stream)) != cudaSuccess) {
+        return GDR_ERR_CUDA;
+    }
     if (!mark(3)) return GDR_ERR_CUDA;
-    if ((e = launch_k3(P, plan->bv, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    if (plan->scan_tc) {
+        if (any_chunks && plan->NS > 1) {
+            if ((e = launch_k3_scan(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+            if ((e = launch_k23_combine(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+        }
+        if ((e = launch_k3_scan(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    } else if ((e = launch_k3(P, plan->bv, stream)) != cudaSuccess) {
+        return GDR_ERR_CUDA;
+    }
     if (!mark(4)) return GDR_ERR_CUDA;
-    if (any_chunks && (e = launch_k4(P, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    if (any_chunks && (e = (plan->k4_tc ? launch_k4_tc(P, stream) : launch_k4(P, stream))) != cudaSuccess)
+        return GDR_ERR_CUDA;
     if (!mark(5)) return GDR_ERR_CUDA;
     if (any_chunks && (e = launch_k5(P, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     if (!mark(6)) return GDR_ERR_CUDA;
@@ -248,8 +298,9 @@ gdr_status gdr_bwd_run_profiled(gdr_bwd_plan *plan, const gdr_bwd_args *a, void 
 int gdr_bwd_launch_count(const gdr_bwd_plan *plan) {
     if (!plan) return 0;
     int n = plan->dense ? 0 : 1;  // K0
-    n += 1;                       // K3 always runs (it also writes dh0)
-    if (plan->max_chunks > 0) n += 4;
+    n += 1;                       // the final state-gradient scan always runs (it also writes dh0)
+    if (plan->max_chunks > 0) n += 4;  // K1, forward scan, K4, K5
+    if (plan->max_chunks > 0 && plan->scan_tc && plan->NS > 1) n += 4;  // local scans and combines
     return n;
 }
 

@@ -54,6 +54,11 @@ struct Params {
     __half *Vn, *dVn;    // [u][CT][DT]
     float *dgam;         // [u][CT] or [u][CT][DT]
     float *dq_h, *dk_h;  // [T][Hv][K] per value head (GQA only)
+    // segment-parallel scans: NS segments of Lseg chunks per sequence; per (sequence, head, segment)
+    // fp32 [DT][DT] summaries: local end state E, transition product Phi, local start gradient F,
+    // exact entry state Sin and exact exit gradient dS
+    int NS, Lseg;
+    float *segE, *segPhi, *segF, *segSin, *segdS;
 };
 
 // ---------------------------------------------------------------- sequence / chunk bookkeeping

@@ -17,8 +17,15 @@ cudaError_t launch_k1(const Params &P, cudaStream_t stream);
 cudaError_t launch_k2(const Params &P, int bv, cudaStream_t stream);
 // K3: reverse state-gradient scan, serial over chunks, tiled over V.
 cudaError_t launch_k3(const Params &P, int bv, cudaStream_t stream);
+// Segment-parallel scans on the tensor cores: local (zero-start) pass or final (exact-start) pass.
+cudaError_t launch_k2_scan(const Params &P, bool local, cudaStream_t stream);
+cudaError_t launch_k3_scan(const Params &P, bool local, cudaStream_t stream);
+// Exact fp32 combination of segment summaries (forward entry states / backward exit gradients).
+cudaError_t launch_k23_combine(const Params &P, bool fwd, cudaStream_t stream);
 // K4: per-chunk gradients dq, dk, dv, dbeta and the cumulative-gate gradient.
 cudaError_t launch_k4(const Params &P, cudaStream_t stream);
+// K4 on the 5th-generation tensor cores (scalar gate only).
+cudaError_t launch_k4_tc(const Params &P, cudaStream_t stream);
 // K5: reverse cumsum of the gate gradient and GQA reduction of dq / dk.
 cudaError_t launch_k5(const Params &P, cudaStream_t stream);
 

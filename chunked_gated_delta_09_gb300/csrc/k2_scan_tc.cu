@@ -1,0 +1,251 @@
+// k2_scan_tc.cu -- forward state recompute on the 5th-generation tensor cores, segment-parallel.
+//
+// Per chunk the state update is linear in the state ("FlashQLA backward explained", section 1, step 2:
+// fused_gdr_h rebuilds the chunk states h):
+//     V_new = U - W S^T,      S <- Gamma_C S + V_new^T K~        (K~ = K (.) exp(gamma_C - gamma))
+// i.e. S <- S M_n + U^T K~ with the transition M_n = Gamma_C I - W^T K~ (K x K).  A sequence is cut into
+// segments of Lseg chunks so that sequences x heads x segments CTAs fill the GPU:
+//   local pass (LOCAL = true): every segment runs from a zero state (-> E_s) and, alongside, the rows
+//     of the transition product Phi_s = prod M_n run from the identity (the same update without U);
+//   combine (k23_combine.cu): S_entry(s+1) = S_entry(s) Phi_s + E_s, exactly, in fp32;
+//   final pass (LOCAL = false): every segment runs from its exact entry state and writes h_n and V_new.
+// This is the state-passing correction that the page's context-parallel path applies across devices
+// (section 3: partition states corrected with an all-gather), done inside one GPU.
+//
+// One CTA holds the whole 128 x 128 fp32 state (and Phi) in tensor memory; each step issues two MMA
+// groups: V_new^T = S W^T (M = 128 state rows, N = 64 tokens) and S += V_new^T K~ (N = 128).
+#include "gdr_common.cuh"
+#include "gdr_kernels.h"
+#include "tc_util.cuh"
+
+namespace gdr {
+
+constexpr int SC_THREADS = 256;
+constexpr uint32_t SC_WAIT_LIMIT = 1u << 24;
+
+template <bool LOCAL>
+struct __align__(1024) FwdSmem {
+    unsigned char W[2][CT * DT * 2], Kt[2][CT * DT * 2], U[2][CT * DT * 2];
+    unsigned char Sa[DT * DT * 2];                 // state rows as fp16 (A operand)
+    unsigned char Vna[DT * CT * 2];                // V_new^T [v][c] (A operand)
+    unsigned char Pa[LOCAL ? DT * DT * 2 : 16];    // transition rows as fp16
+    unsigned char Vpa[LOCAL ? DT * CT * 2 : 16];   // -(W Phi^T)^T
+    float gC[2][DT];
+    uint64_t bar;
+    uint32_t tslot;
+};
+
+// cp.async a row-major fp16 block [CT][DT] into a core-matrix tile; conflict-free lane map.
+__device__ __forceinline__ void cp_tile_ct_dt(unsigned char *tile, const __half *src, int tid) {
+    const int wid = tid >> 5, lane = tid & 31;
+#pragma unroll
+    for (int i = 0; i < (CT * DT / 8) / SC_THREADS; ++i) {
+        int it = wid + (SC_THREADS / 32) * i;  // 0 .. 31
+        int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
+        cp_async16(tile + tc::tile_off(r, c8, DT), src + (size_t)r * DT + c8);
+    }
+}
+
+template <bool PC, bool LOCAL>
+__global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    FwdSmem<LOCAL> &S = *reinterpret_cast<FwdSmem<LOCAL> *>(smem_raw);
+    if (*P.status & ST_BAD_SEQLENS) return;
+    const int NS = P.NS;
+    const int seg = blockIdx.x % NS, hv = (blockIdx.x / NS) % P.Hv, s = blockIdx.x / (NS * P.Hv);
+    int bos, eos;
+    seq_range(P, s, bos, eos);
+    const int nc = (eos - bos + P.BT - 1) / P.BT;
+    const int c_lo = seg * P.Lseg, c_hi = min(nc, c_lo + P.Lseg);
+    if (c_lo >= c_hi && !(seg == 0 && !LOCAL)) return;  // empty segment (segment 0 of an empty sequence has no work either)
+    if (c_lo >= c_hi) return;
+    const int base = seq_chunk_base(P, s);
+    const size_t su = ((size_t)s * P.Hv + hv) * NS + seg;
+    const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+    const int q = wid & 3, half = wid >> 2;
+    const int row = 32 * q + lane;  // state row (v) / transition row (k') owned in the epilogues
+
+    if (wid == 0) tc::tmem_alloc(&S.tslot, LOCAL ? 512 : 256);
+    if (tid == 0) {
+        tc::mbar_init(&S.bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    auto issue = [&](int c, int buf) {
+        const size_t u = (size_t)(base + c) * P.Hv + hv;
+        cp_tile_ct_dt(S.W[buf], P.W + u * CT * DT, tid);
+        cp_tile_ct_dt(S.Kt[buf], P.Kt + u * CT * DT, tid);
+        cp_tile_ct_dt(S.U[buf], P.U + u * CT * DT, tid);
+        int len = eos - (bos + c * P.BT);
+        len = len < P.BT ? len : P.BT;
+        if (PC) {
+            if (tid < DT / 4) cp_async16(&S.gC[buf][4 * tid], P.gam + (u * CT + len - 1) * DT + 4 * tid);
+        } else if (tid == 0) {
+            cp_async4(&S.gC[buf][0], P.gam + u * CT + len - 1);
+        }
+        cp_async_commit();
+    };
+    issue(c_lo, 0);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = S.tslot;
+    constexpr int T_S = 0, T_P = 128, T_VN = LOCAL ? 256 : 128, T_VP = 320;
+
+    // ---- initial state: zero (local pass) or the exact entry state (final pass); transition = I
+    {
+        const float *src = nullptr;
+        if (!LOCAL) src = NS > 1 ? P.segSin + su * DT * DT : (P.h0 ? P.h0 + ((size_t)s * P.Hv + hv) * P.V * P.K : nullptr);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                int col = 64 * half + 32 * h + t;
+                float x = 0.f;
+                if (src) {
+                    if (NS > 1) x = src[(size_t)row * DT + col];
+                    else if (row < P.V && col < P.K) x = src[(size_t)row * P.K + col];
+                }
+                v[t] = x;
+            }
+            tc::st32(tc::taddr(tm, T_S + 64 * half + 32 * h), v);
+            if (LOCAL) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t) v[t] = (64 * half + 32 * h + t == row) ? 1.f : 0.f;
+                tc::st32(tc::taddr(tm, T_P + 64 * half + 32 * h), v);
+            }
+        }
+        tc::wait_st();
+    }
+    const uint32_t sSa = smem_u32(S.Sa), sVna = smem_u32(S.Vna), sPa = smem_u32(S.Pa), sVpa = smem_u32(S.Vpa);
+    uint32_t parity = 0;
+    bool lost = false;
+    auto mma_done = [&]() {
+        if (tid == 0) tc::commit(&S.bar);
+        bool ok = tc::mbar_wait(&S.bar, parity, SC_WAIT_LIMIT);
+        parity ^= 1u;
+        lost = __syncthreads_or(!ok) != 0;
+        tc::fence_after();
+    };
+    cp_async_wait<0>();
+
+    for (int c = c_lo; c < c_hi && !lost; ++c) {
+        const int buf = (c - c_lo) & 1;
+        const size_t u = (size_t)(base + c) * P.Hv + hv;
+        tc::fence_smem_to_async();
+        tc::fence_before();
+        __syncthreads();  // chunk c's operands landed everywhere; previous MMAs finished
+        tc::fence_after();
+        // epilogue 0: state rows -> fp16 operand (+ h_n), then scale by Gamma_C in place
+#pragma unroll
+        for (int m = 0; m < (LOCAL ? 2 : 1); ++m) {
+            const int tcol = m ? T_P : T_S;
+            unsigned char *tile = m ? S.Pa : S.Sa;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c0 = 64 * half + 32 * h;
+                float v[32];
+                tc::ld32(tc::taddr(tm, tcol + c0), v);
+#pragma unroll
+                for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(tile, row, c0 + j8, DT, v + j8);
+                if (!LOCAL) {
+                    uint4 pk[4];
+                    __half2 *h2 = reinterpret_cast<__half2 *>(pk);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) h2[t] = __floats2half2_rn(v[2 * t], v[2 * t + 1]);
+                    uint4 *dst = reinterpret_cast<uint4 *>(P.h + u * DT * DT + (size_t)row * DT + c0);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) dst[t] = pk[t];
+                }
+#pragma unroll
+                for (int t = 0; t < 32; ++t) v[t] *= expf(PC ? S.gC[buf][c0 + t] : S.gC[buf][0]);
+                tc::st32(tc::taddr(tm, tcol + c0), v);
+            }
+        }
+        tc::wait_st();
+        tc::fence_smem_to_async();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        if (c + 1 < c_hi) issue(c + 1, buf ^ 1);
+        // MMA 1: V_new^T (pre) = S W^T   [and  (W Phi^T)^T]
+        if (tid == 0) {
+            tc::gemm(tm + T_VN, sSa, DT, false, smem_u32(S.W[buf]), DT, false, 128, 64, DT, false);
+            if (LOCAL) tc::gemm(tm + T_VP, sPa, DT, false, smem_u32(S.W[buf]), DT, false, 128, 64, DT, false);
+        }
+        mma_done();
+        if (lost) break;
+        // epilogue 1: V_new^T = U^T - S W^T  (transition rows: -(Phi W^T)) -> fp16 operand (+ V_new)
+        {
+            const int c0 = 32 * half;
+            float v[32];
+            tc::ld32(tc::taddr(tm, T_VN + c0), v);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) v[t] = tc::ld_tile(S.U[buf], c0 + t, row, DT) - v[t];
+#pragma unroll
+            for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.Vna, row, c0 + j8, CT, v + j8);
+            if (!LOCAL) {
+                __half *vg = P.Vn + u * CT * DT;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) vg[(size_t)(c0 + t) * DT + row] = __float2half_rn(v[t]);
+            }
+            if (LOCAL) {
+                tc::ld32(tc::taddr(tm, T_VP + c0), v);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) v[t] = -v[t];
+#pragma unroll
+                for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.Vpa, row, c0 + j8, CT, v + j8);
+            }
+        }
+        tc::fence_smem_to_async();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        // MMA 2: S += V_new^T K~   [Phi += (-(W Phi^T))^T K~]
+        if (tid == 0) {
+            tc::gemm(tm + T_S, sVna, CT, false, smem_u32(S.Kt[buf]), DT, true, 128, 128, CT, true);
+            if (LOCAL) tc::gemm(tm + T_P, sVpa, CT, false, smem_u32(S.Kt[buf]), DT, true, 128, 128, CT, true);
+        }
+        mma_done();
+        cp_async_wait<0>();
+    }
+    // ---- local pass: segment summaries E_s (state) and Phi_s (transition rows), fp32
+    if (LOCAL && !lost) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            float *dst = (m ? P.segPhi : P.segE) + su * DT * DT + (size_t)row * DT;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c0 = 64 * half + 32 * h;
+                float v[32];
+                tc::ld32(tc::taddr(tm, (m ? T_P : T_S) + c0), v);
+#pragma unroll
+                for (int t = 0; t < 32; t += 4)
+                    *reinterpret_cast<float4 *>(dst + c0 + t) = make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]);
+            }
+        }
+    }
+    if (lost && tid == 0) flag_status(P.status, ST_TIMEOUT);
+    tc::fence_before();
+    __syncthreads();
+    if (wid == 0) {
+        tc::fence_after();
+        tc::tmem_dealloc(tm, LOCAL ? 512 : 256);
+    }
+}
+
+template <bool PC, bool LOCAL>
+static cudaError_t launch_fwd_t(const Params &P, cudaStream_t stream) {
+    size_t smem = sizeof(FwdSmem<LOCAL>);
+    cudaError_t e = cudaFuncSetAttribute(k2_scan_tc<PC, LOCAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k2_scan_tc<PC, LOCAL><<<P.N * P.Hv * P.NS, SC_THREADS, smem, stream>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_k2_scan(const Params &P, bool local, cudaStream_t stream) {
+    if (local) return P.per_channel ? launch_fwd_t<true, true>(P, stream) : launch_fwd_t<false, true>(P, stream);
+    return P.per_channel ? launch_fwd_t<true, false>(P, stream) : launch_fwd_t<false, false>(P, stream);
+}
+
+}  // namespace gdr

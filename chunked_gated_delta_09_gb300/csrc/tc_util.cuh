@@ -1,0 +1,173 @@
+// tc_util.cuh -- 5th-generation tensor core (tcgen05) helpers: tensor memory, shared-memory operand
+// descriptors, MMA issue/commit, bounded mbarrier waits and tensor-memory loads.
+//
+// Operand tiles live in shared memory in the canonical no-swizzle "core matrix" layout: a tile of R rows
+// and C columns (fp16) is split into 8 x 8 core matrices of 128 contiguous bytes, row-major inside
+// (16 bytes per row); core matrix (r/8, c/8) sits at (r/8) * (C/8) * 128 + (c/8) * 128.  The same tile
+// serves as an MMA operand in two ways:
+//   K-major view : operand rows = tile rows, reduction = tile columns
+//                  LBO = 128 (next core matrix along the reduction), SBO = (C/8) * 128
+//   MN-major view: operand rows = tile columns, reduction = tile rows (the transposed matrix)
+//                  LBO = (C/8) * 128, SBO = 128
+// i.e. for both majors LBO is the byte stride between core matrices adjacent along the reduction
+// dimension and SBO the stride along M/N.  One MMA consumes 16 reduction elements.
+#pragma once
+
+#include <stdint.h>
+
+#include "gdr_common.cuh"
+
+namespace gdr {
+namespace tc {
+
+__device__ __forceinline__ uint32_t tile_off(int r, int c, int C) {
+    return (uint32_t)((r >> 3) * (C >> 3) * 128 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
+}
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version for this architecture; no swizzle
+    return d;
+}
+
+// Descriptor of reduction step kk (16 elements) of a tile used in K-major / MN-major view.
+__device__ __forceinline__ uint64_t desc_k(uint32_t tile, int C, int kk) {
+    return smem_desc(tile + kk * 256, 128, (C >> 3) * 128);
+}
+__device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int C, int kk) {
+    return smem_desc(tile + kk * 2 * (C >> 3) * 128, (C >> 3) * 128, 128);
+}
+
+// Instruction descriptor: fp16 A and B, fp32 accumulator, M x N, operand majors.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// D[M x N] (+)= A[M x Kr] B[N x Kr]^T over Kr / 16 MMAs; a_mn / b_mn select the operand views.
+__device__ __forceinline__ void gemm(uint32_t d_tmem, uint32_t a_tile, int a_C, bool a_mn, uint32_t b_tile, int b_C,
+                                     bool b_mn, int M, int N, int Kr, bool accumulate) {
+    const uint32_t id = idesc_f16(M, N, a_mn, b_mn);
+    for (int kk = 0; kk < Kr / 16; ++kk) {
+        uint64_t a = a_mn ? desc_mn(a_tile, a_C, kk) : desc_k(a_tile, a_C, kk);
+        uint64_t b = b_mn ? desc_mn(b_tile, b_C, kk) : desc_k(b_tile, b_C, kk);
+        mma(d_tmem, a, b, id, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+__device__ __forceinline__ void commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+        smem_u32(bar)));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+// Wait for the mbarrier phase with the given parity; gives up after `limit` polls and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
+    uint32_t done = 0;
+    for (uint32_t it = 0; it < limit; ++it) {
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity));
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+// Make this thread's generic-proxy shared-memory writes visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_smem_to_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+// Allocation by one full warp; the column base is written to *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(slot)),
+                 "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(base), "r"(ncols));
+}
+
+// 32 consecutive columns of this warp's 32 lanes (lane quarter of the warp) -> 32 registers per thread.
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 registers per thread -> 32 consecutive columns of this warp's 32 lanes.
+__device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])));
+}
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+// Tensor-memory address of (lane quarter of this warp, column).
+__device__ __forceinline__ uint32_t taddr(uint32_t base, int col) {
+    return base + ((uint32_t)((threadIdx.x >> 5) & 3) * 32u << 16) + (uint32_t)col;
+}
+
+// Lane l of the warp returns the sum over the warp of v[l] (v is consumed).
+__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            float send = up ? v[i] : v[i + s];
+            float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+// Write 8 fp32 values as one 16-byte row segment of core matrix (r/8, c0/8) of a tile (c0 % 8 == 0).
+__device__ __forceinline__ void st_tile8(unsigned char *tile, int r, int c0, int C, const float *x) {
+    uint4 p;
+    __half2 *h2 = reinterpret_cast<__half2 *>(&p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h2[i] = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+    *reinterpret_cast<uint4 *>(tile + tile_off(r, c0, C)) = p;
+}
+
+__device__ __forceinline__ float ld_tile(const unsigned char *tile, int r, int c, int C) {
+    return __half2float(*reinterpret_cast<const __half *>(tile + tile_off(r, c, C)));
+}
+
+}  // namespace tc
+}  // namespace gdr

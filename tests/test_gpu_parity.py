@@ -69,3 +69,14 @@ def test_workload_sampled_heads(name, hks):
     got = run_gpu(prob)
     sub, slices = head_subset(prob, hks)
     compare(prob, got, oracle.problem_backward(sub), slices=slices)
+
+
+@pytest.mark.parametrize("nseg", [1, 2, 3, 7])
+@pytest.mark.parametrize("per_channel", [False, True], ids=["scalar", "kda"])
+def test_segment_parallel_scan_matches_oracle(nseg, per_channel, monkeypatch):
+    """The scans split each sequence into segments and combine exactly; any segment count gives the
+    oracle's gradients (varlen sequences of different lengths, some shorter than a segment)."""
+    monkeypatch.setenv("GDR_NSEG", str(nseg))
+    prob = make_problem(f"nseg{nseg}", B=1, Hk=1, Hv=2, K=64, V=64, per_channel=per_channel,
+                        seq_lens=[700, 64, 130, 1], seed=88)
+    compare(prob, run_gpu(prob), oracle.problem_backward(prob))
