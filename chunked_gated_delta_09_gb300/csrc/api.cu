@@ -18,12 +18,12 @@ using namespace gdr;
 
 struct gdr_bwd_plan {
     gdr_bwd_desc d;
-    int G, N, dense, nts, max_chunks, bv;
+    int G, N, dense, nts, max_chunks;
     int k4_tc;  // per-chunk gradients on tcgen05 (scalar gate); the per-channel gate uses the mma.sync kernel
-    int scan_tc, NS, Lseg;  // tensor-core segment-parallel scans and their segmentation
+    int NS, Lseg;  // segment-parallel scans: segments per sequence and chunks per segment
     long long tokens;  // B * T
     // workspace byte offsets
-    size_t o_status, o_cidx, o_coff, o_gam, o_T, o_Aqk, o_W, o_U, o_Kt, o_Qg, o_h, o_dh, o_Vn, o_dVn, o_dgam, o_dqh,
+    size_t o_status, o_cidx, o_coff, o_gam, o_T, o_Aqk, o_W, o_U, o_Kt, o_Qg, o_Dt, o_h, o_dh, o_Vn, o_dVn, o_dgam, o_dqh,
         o_dkh, o_seg, total;
 };
 
@@ -55,6 +55,7 @@ void layout(gdr_bwd_plan &p) {
     p.o_U = take(sizeof(__half) * units * CT * DT);
     p.o_Kt = take(sizeof(__half) * units * CT * DT);
     p.o_Qg = take(sizeof(__half) * units * CT * DT);
+    p.o_Dt = take(sizeof(__half) * units * CT * DT);
     p.o_h = take(sizeof(__half) * units * DT * DT);
     p.o_dh = take(sizeof(__half) * units * DT * DT);
     p.o_Vn = take(sizeof(__half) * units * CT * DT);
@@ -64,24 +65,11 @@ void layout(gdr_bwd_plan &p) {
     p.o_dqh = take(per_head);
     p.o_dkh = take(per_head);
     size_t seg_units = p.NS > 1 ? (size_t)p.N * d.Hv * p.NS : 0;
-    p.o_seg = take(5 * sizeof(float) * seg_units * DT * DT);
+    p.o_seg = take(6 * sizeof(float) * seg_units * DT * DT);
     p.total = off;
 }
 
 bool aligned(const void *ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
-
-int choose_bv(const gdr_bwd_plan &p) {
-    const char *env = getenv("GDR_SCAN_BV");
-    if (env) {
-        int v = atoi(env);
-        if (v == 8 || v == 16 || v == 32) return v;
-    }
-    // Measured on the T=32768, H=16 workload: BV=16 beats 8 (fewer redundant operand loads per chunk)
-    // and 32 (more parallel CTAs); 32 only pays when there are many independent sequence x head units.
-    long long units = (long long)p.N * p.d.Hv;
-    if (units * (DT / 32) >= 4 * kNumSMs) return 32;
-    return 16;
-}
 
 }  // namespace
 
@@ -131,18 +119,15 @@ gdr_status gdr_bwd_create(const gdr_bwd_desc *desc, gdr_bwd_plan **out) {
         return GDR_ERR_UNSUPPORTED;
     }
     p->max_chunks = (int)mc;
-    p->bv = choose_bv(*p);
     {
         // segments: enough (sequence x head x segment) CTAs to give every SM one, at least 4 chunks each
-        const char *ls = getenv("GDR_SCAN_LEGACY");
-        p->scan_tc = !(ls && atoi(ls) != 0);
         long long units = (long long)p->N * d.Hv;
         long long maxnc = p->dense ? p->nts : ((long long)d.T + d.BT - 1) / d.BT;
         long long ns = units > 0 ? kNumSMs / units : 1;
         ns = ns < (maxnc + 3) / 4 ? ns : (maxnc + 3) / 4;
         const char *env = getenv("GDR_NSEG");
         if (env && atoi(env) > 0) ns = atoi(env);
-        if (ns < 1 || !p->scan_tc) ns = 1;
+        if (ns < 1) ns = 1;
         p->NS = (int)ns;
         p->Lseg = maxnc > 0 ? (int)((maxnc + ns - 1) / ns) : 1;
     }
@@ -222,6 +207,7 @@ static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *work
     P.U = reinterpret_cast<__half *>(ws + plan->o_U);
     P.Kt = reinterpret_cast<__half *>(ws + plan->o_Kt);
     P.Qg = reinterpret_cast<__half *>(ws + plan->o_Qg);
+    P.Dt = reinterpret_cast<__half *>(ws + plan->o_Dt);
     P.h = reinterpret_cast<__half *>(ws + plan->o_h);
     P.dh = reinterpret_cast<__half *>(ws + plan->o_dh);
     P.Vn = reinterpret_cast<__half *>(ws + plan->o_Vn);
@@ -236,9 +222,10 @@ static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *work
         float *seg = reinterpret_cast<float *>(ws + plan->o_seg);
         P.segE = seg;
         P.segPhi = seg + one;
-        P.segF = seg + 2 * one;
-        P.segSin = seg + 3 * one;
-        P.segdS = seg + 4 * one;
+        P.segPhiT = seg + 2 * one;
+        P.segF = seg + 3 * one;
+        P.segSin = seg + 4 * one;
+        P.segdS = seg + 5 * one;
     }
 
     auto mark = [&](int i) -> bool {
@@ -255,25 +242,17 @@ static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *work
     const bool any_chunks = plan->max_chunks > 0;
     if (any_chunks && (e = launch_k1(P, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     if (!mark(2)) return GDR_ERR_CUDA;
-    if (plan->scan_tc) {
-        if (any_chunks && plan->NS > 1) {
-            if ((e = launch_k2_scan(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
-            if ((e = launch_k23_combine(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
-        }
-        if (any_chunks && (e = launch_k2_scan(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
-    } else if (any_chunks && (e = launch_k2(P, plan->bv, stream)) != cudaSuccess) {
-        return GDR_ERR_CUDA;
+    if (any_chunks && plan->NS > 1) {
+        if ((e = launch_k2_scan(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+        if ((e = launch_k23_combine(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     }
+    if (any_chunks && (e = launch_k2_scan(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     if (!mark(3)) return GDR_ERR_CUDA;
-    if (plan->scan_tc) {
-        if (any_chunks && plan->NS > 1) {
-            if ((e = launch_k3_scan(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
-            if ((e = launch_k23_combine(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
-        }
-        if ((e = launch_k3_scan(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
-    } else if ((e = launch_k3(P, plan->bv, stream)) != cudaSuccess) {
-        return GDR_ERR_CUDA;
+    if (any_chunks && plan->NS > 1) {
+        if ((e = launch_k3_scan(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+        if ((e = launch_k23_combine(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     }
+    if ((e = launch_k3_scan(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     if (!mark(4)) return GDR_ERR_CUDA;
     if (any_chunks && (e = (plan->k4_tc ? launch_k4_tc(P, stream) : launch_k4(P, stream))) != cudaSuccess)
         return GDR_ERR_CUDA;
@@ -300,7 +279,7 @@ int gdr_bwd_launch_count(const gdr_bwd_plan *plan) {
     int n = plan->dense ? 0 : 1;  // K0
     n += 1;                       // the final state-gradient scan always runs (it also writes dh0)
     if (plan->max_chunks > 0) n += 4;  // K1, forward scan, K4, K5
-    if (plan->max_chunks > 0 && plan->scan_tc && plan->NS > 1) n += 4;  // local scans and combines
+    if (plan->max_chunks > 0 && plan->NS > 1) n += 4;  // local scans and combines
     return n;
 }
 

@@ -44,21 +44,26 @@ struct Params {
     int *status;
     int32_t *chunk_idx;  // [max_chunks][2]
     int32_t *chunk_off;  // [N + 1]
-    float *gam;          // [u][CT] or [u][CT][DT]  chunk-local cumulative gate
-    __half *Tm;          // [u][CT][CT]   (I + A_kk)^-1
-    __half *Aqk;         // [u][CT][CT]   M (.) Q K^T   (causal, decayed; unscaled)
-    __half *W, *U;       // [u][CT][DT]
-    __half *Kt;          // [u][CT][DT]   K (.) exp(gamma_C - gamma)
-    __half *Qg;          // [u][CT][DT]   Q (.) exp(gamma)
-    __half *h, *dh;      // [u][DT][DT]   state entering / adjoint leaving each chunk, [v][k]
-    __half *Vn, *dVn;    // [u][CT][DT]
+    // Per chunk x value head unit u = n Hv + hv.  fp16 matrices are stored as core-matrix tiles
+    // ("tile [R][C]": see ctile_off), each moved whole by bulk copies.
+    float *gam;          // [u][CT] or [u][CT][DT]  chunk-local cumulative gate (fp32)
+    __half *Tm;          // tile [r][i]   64 x 64    (I + A_kk)^-1
+    __half *Aqk;         // tile [r][j]   64 x 64    M (.) Q K^T (causal, decayed, unscaled)
+    __half *W, *U;       // tile [c][k] / [c][v]     64 x 128
+    __half *Kt;          // tile [c][k]   64 x 128   K (.) exp(gamma_C - gamma)
+    __half *Qg;          // tile [r][k]   64 x 128   Q (.) exp(gamma)
+    __half *Dt;          // tile [r][v]   64 x 128   scale * dO
+    __half *h, *dh;      // tile [v][k]   128 x 128  state entering / adjoint leaving the chunk
+    __half *Vn;          // tile [v][c]   128 x 64   V_new^T
+    __half *dVn;         // tile [v][c]   128 x 64   -dV_new^T
     float *dgam;         // [u][CT] or [u][CT][DT]
     float *dq_h, *dk_h;  // [T][Hv][K] per value head (GQA only)
     // segment-parallel scans: NS segments of Lseg chunks per sequence; per (sequence, head, segment)
-    // fp32 [DT][DT] summaries: local end state E, transition product Phi, local start gradient F,
+    // fp32 [DT][DT] summaries: local end state E, transition product Phi (and its transpose), local
+    // start gradient F,
     // exact entry state Sin and exact exit gradient dS
     int NS, Lseg;
-    float *segE, *segPhi, *segF, *segSin, *segdS;
+    float *segE, *segPhi, *segPhiT, *segF, *segSin, *segdS;
 };
 
 // ---------------------------------------------------------------- sequence / chunk bookkeeping
@@ -269,6 +274,102 @@ __device__ __forceinline__ void warp_mma(float (&acc)[MT][NT][4], const __half *
             for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][nt], a[mt], b[0], b[1]);
         }
     }
+}
+
+// Byte offset of element (r, c) in a core-matrix tile with C columns: 8 x 8 blocks of 128 contiguous
+// bytes, block (r/8, c/8) at (r/8) (C/8) 128 + (c/8) 128 (the layout the tensor-core descriptors read).
+__device__ __forceinline__ uint32_t ctile_off(int r, int c, int C) {
+    return (uint32_t)((r >> 3) * (C >> 3) * 128 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
+}
+__device__ __forceinline__ float ctile_get(const unsigned char *t, int r, int c, int C) {
+    return __half2float(*reinterpret_cast<const __half *>(t + ctile_off(r, c, C)));
+}
+__device__ __forceinline__ void ctile_set(unsigned char *t, int r, int c, int C, float x) {
+    *reinterpret_cast<__half *>(t + ctile_off(r, c, C)) = __float2half_rn(x);
+}
+
+// warp_mma on core-matrix tiles (each 8 x 8 ldmatrix block is one contiguous core matrix):
+//   A(m, k) = tile element (m, k) of a tile with A_C columns (AT = false) or (k, m) (AT = true);
+//   B(k, n) = tile element (k, n) (BT = false) or (n, k) (BT = true).
+template <int MT, int NT, bool AT, bool BT>
+__device__ __forceinline__ void warp_mma_ct(float (&acc)[MT][NT][4], const unsigned char *A, int A_C,
+                                            const unsigned char *B, int B_C, int m0, int n0, int kdim) {
+    const int lane = threadIdx.x & 31;
+    const int r8 = lane & 7, mat = lane >> 3;
+    for (int k0 = 0; k0 < kdim; k0 += 16) {
+        uint32_t a[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            int mb = m0 + mt * 16;
+            if (!AT) ldsm_x4(a[mt], A + ctile_off(mb + (lane & 15), k0 + (lane >> 4) * 8, A_C));
+            else ldsm_x4_t(a[mt], A + ctile_off(k0 + r8 + (mat >> 1) * 8, mb + (mat & 1) * 8, A_C));
+        }
+#pragma unroll
+        for (int nt = 0; nt + 1 < NT; nt += 2) {
+            int nb = n0 + nt * 8;
+            uint32_t b[4];
+            if (BT) ldsm_x4(b, B + ctile_off(nb + r8 + (mat >> 1) * 8, k0 + (mat & 1) * 8, B_C));
+            else ldsm_x4_t(b, B + ctile_off(k0 + r8 + (mat & 1) * 8, nb + (mat >> 1) * 8, B_C));
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                mma16816(acc[mt][nt], a[mt], b[0], b[1]);
+                mma16816(acc[mt][nt + 1], a[mt], b[2], b[3]);
+            }
+        }
+        if (NT & 1) {
+            constexpr int nt = NT - 1;
+            int nb = n0 + nt * 8;
+            int m2 = (lane >> 3) & 1;
+            uint32_t b[2];
+            if (BT) ldsm_x2(b, B + ctile_off(nb + r8, k0 + m2 * 8, B_C));
+            else ldsm_x2_t(b, B + ctile_off(k0 + r8 + m2 * 8, nb, B_C));
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][nt], a[mt], b[0], b[1]);
+        }
+    }
+}
+
+// Convert two strided [rows][cols] input blocks into fp16 [CT][DT] core-matrix tiles (rows >= nrows or
+// columns >= ncols become zero), multiplying by m0 / m1, with every global load of the thread issued
+// before the first conversion.  Work item `it` of warp w covers rows 8 (it / 4) .. +7 and 16-byte
+// columns 4 (it % 4) .. +3: the 8 lanes of each 16-byte store phase write the 8 rows of one core matrix
+// (distinct banks), and each row reads 64 contiguous bytes from global memory.
+template <typename Tin, int NTHR>
+__device__ __forceinline__ void stage_ct_pair(unsigned char *t0, const Tin *s0, size_t st0, int nc0, float m0,
+                                              unsigned char *t1, const Tin *s1, size_t st1, int nc1, float m1,
+                                              int nrows, int tid) {
+    constexpr int PER = CT * (DT / 8) / NTHR;  // 8-element chunks per thread per tile
+    static_assert(PER * NTHR == CT * (DT / 8), "thread count must divide the tile");
+    const int wid = tid >> 5, lane = tid & 31;
+    float x[2][PER][8];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        const Tin *src = w ? s1 : s0;
+        const size_t st = w ? st1 : st0;
+        const int nc = w ? nc1 : nc0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            int it = wid + (NTHR / 32) * i;
+            int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
+            if (r < nrows && c8 + 8 <= nc) {
+                load8(src + (size_t)r * st + c8, x[w][i]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[w][i][j] = 0.f;
+            }
+        }
+    }
+#pragma unroll
+    for (int w = 0; w < 2; ++w)
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            int it = wid + (NTHR / 32) * i;
+            int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
+            const float m = w ? m1 : m0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[w][i][j] *= m;
+            *reinterpret_cast<uint4 *>((w ? t1 : t0) + ctile_off(r, c8, DT)) = pack8_half(x[w][i]);
+        }
 }
 
 template <int MT, int NT>

@@ -13,11 +13,8 @@ cudaError_t launch_k0(const int32_t *cu, int N, int BT, int max_chunks, int expe
                       int32_t *chunk_off, int *status, cudaStream_t stream);
 // K1: chunk-local WY preparation (gate cumsum, A_kk inverse, W, U, decayed copies of K and Q).
 cudaError_t launch_k1(const Params &P, cudaStream_t stream);
-// K2: forward state recompute (fused_gdr_h), serial over chunks, tiled over V.
-cudaError_t launch_k2(const Params &P, int bv, cudaStream_t stream);
-// K3: reverse state-gradient scan, serial over chunks, tiled over V.
-cudaError_t launch_k3(const Params &P, int bv, cudaStream_t stream);
-// Segment-parallel scans on the tensor cores: local (zero-start) pass or final (exact-start) pass.
+// K2 / K3: forward state recompute (fused_gdr_h) and reverse state-gradient scan, segment-parallel on
+// the tensor cores: local (zero-start) pass or final (exact-start) pass.
 cudaError_t launch_k2_scan(const Params &P, bool local, cudaStream_t stream);
 cudaError_t launch_k3_scan(const Params &P, bool local, cudaStream_t stream);
 // Exact fp32 combination of segment summaries (forward entry states / backward exit gradients).

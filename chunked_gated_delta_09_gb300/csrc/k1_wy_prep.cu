@@ -7,19 +7,24 @@
 // and its triangular inverse T = (I + A_kk)^{-1}, the "intra-chunk triangular matrix" A [B, T, H, BT] of
 // MindSpeed-Ops chunk_kda_bwd.md (input table), by blocked forward substitution in shared memory.  It
 // then writes the WY factors W = T diag(beta Gamma) K and U = T diag(beta) V, the decayed attention
-// matrix Aqk = M (.) Q K^T (M[i, j] = exp(gamma_i - gamma_j), j <= i), and the decayed copies
-// K (.) exp(gamma_C - gamma) and Q (.) exp(gamma) that the two scans use.
+// matrix Aqk = M (.) Q K^T (M[i, j] = exp(gamma_i - gamma_j), j <= i), the decayed copies
+// K~ = K (.) exp(gamma_C - gamma) and Q~ = Q (.) exp(gamma) that the two scans use, and D = scale dO.
 // Per-channel gate: each exp(gamma_a - gamma_b) is taken per key channel inside the K contraction.
+//
+// Every matrix output is built in shared memory in the core-matrix tile layout that the tensor-core
+// kernels read, and leaves with one bulk copy per tile.
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
+#include "tc_util.cuh"
 
 namespace gdr {
 
 constexpr int K1_THREADS = 256;
 
-struct K1Smem {
-    __half Ks[CT * LDD], Qs[CT * LDD], Vs[CT * LDD], KB[CT * LDD], VB[CT * LDD];
-    __half Th[CT * LDC];
+struct __align__(1024) K1Smem {
+    unsigned char Ks[CT * DT * 2], Qs[CT * DT * 2], Vs[CT * DT * 2];  // Qs later holds beta Gamma K, Vs beta V
+    unsigned char oKt[CT * DT * 2], oQg[CT * DT * 2], oD[CT * DT * 2], oW[CT * DT * 2], oU[CT * DT * 2];
+    unsigned char oT[CT * CT * 2], oAqk[CT * CT * 2];
     float A32[CT][CT + 1];
     float T32[CT][CT + 1];
     float X32[3][16][17];
@@ -28,8 +33,8 @@ struct K1Smem {
 };
 
 template <typename Tin, bool PC>
-__global__ void __launch_bounds__(K1_THREADS) k1_wy_prep(const Params P) {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
+__global__ void __launch_bounds__(K1_THREADS, 1) k1_wy_prep(const Params P) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     K1Smem &S = *reinterpret_cast<K1Smem *>(smem_raw);
     float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K1Smem));  // [CT][DT], per-channel only
 
@@ -40,6 +45,16 @@ __global__ void __launch_bounds__(K1_THREADS) k1_wy_prep(const Params P) {
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
     const size_t u = (size_t)n * P.Hv + hv;
     const int len = ci.len;
+
+    // ---- stage q, k (key head) and v, scale * dO (value head) as fp16 tiles (all loads in flight first)
+    const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
+    const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
+    const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
+    const Tin *dop = reinterpret_cast<const Tin *>(P.dO) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
+    stage_ct_pair<Tin, K1_THREADS>(S.Ks, kp, (size_t)P.Hk * P.K, P.K, 1.f, S.Qs, qp, (size_t)P.Hk * P.K, P.K, 1.f, len,
+                                   tid);
+    stage_ct_pair<Tin, K1_THREADS>(S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, S.oD, dop, (size_t)P.Hv * P.V, P.V, P.scale,
+                                   len, tid);
 
     // ---- beta, gate cumsum
     if (tid < CT) S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
@@ -72,25 +87,17 @@ __global__ void __launch_bounds__(K1_THREADS) k1_wy_prep(const Params P) {
             }
         }
     }
-    // ---- stage q, k (key head) and v (value head) as fp16
-    const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
-    const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
-    const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    stage_rows_f16(S.Ks, kp, (size_t)P.Hk * P.K, len, P.K, nullptr, 1.f, tid, K1_THREADS);
-    stage_rows_f16(S.Qs, qp, (size_t)P.Hk * P.K, len, P.K, nullptr, 1.f, tid, K1_THREADS);
-    stage_rows_f16(S.Vs, vp, (size_t)P.Hv * P.V, len, P.V, nullptr, 1.f, tid, K1_THREADS);
     for (int e = tid; e < CT * (CT + 1); e += K1_THREADS) (&S.T32[0][0])[e] = 0.f;
     __syncthreads();
 
-    __half *Aqk_g = P.Aqk + u * CT * CT;
-    // ---- A_kk (fp32, shared) and Aqk (fp16, global)
+    // ---- A_kk (fp32, shared) and Aqk (fp16 tile)
     if (!PC) {
         const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 32;
         float kk[1][4][4], qk[1][4][4];
         zero_acc(kk);
         zero_acc(qk);
-        warp_mma<1, 4, false, true>(kk, S.Ks, LDD, S.Ks, LDD, m0, n0, DT);
-        warp_mma<1, 4, false, true>(qk, S.Qs, LDD, S.Ks, LDD, m0, n0, DT);
+        warp_mma_ct<1, 4, false, true>(kk, S.Ks, DT, S.Ks, DT, m0, n0, DT);
+        warp_mma_ct<1, 4, false, true>(qk, S.Qs, DT, S.Ks, DT, m0, n0, DT);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -98,7 +105,7 @@ __global__ void __launch_bounds__(K1_THREADS) k1_wy_prep(const Params P) {
                 int i = acc_row(m0, 0, e), j = acc_col(n0, nt, e);
                 float d = expf(S.gam[i] - S.gam[j]);
                 S.A32[i][j] = j < i ? S.beta[i] * d * kk[0][nt][e] : 0.f;
-                Aqk_g[i * CT + j] = __float2half_rn(j <= i ? d * qk[0][nt][e] : 0.f);
+                ctile_set(S.oAqk, i, j, CT, j <= i ? d * qk[0][nt][e] : 0.f);
             }
     } else {
         for (int e = tid; e < CT * CT; e += K1_THREADS) {
@@ -107,16 +114,52 @@ __global__ void __launch_bounds__(K1_THREADS) k1_wy_prep(const Params P) {
             if (j <= i && i < len) {
                 for (int c = 0; c < DT; ++c) {
                     float d = expf(gamK[i * DT + c] - gamK[j * DT + c]);
-                    float kj = __half2float(S.Ks[j * LDD + c]);
-                    akk += __half2float(S.Ks[i * LDD + c]) * kj * d;
-                    aqk += __half2float(S.Qs[i * LDD + c]) * kj * d;
+                    float kj = ctile_get(S.Ks, j, c, DT);
+                    akk += ctile_get(S.Ks, i, c, DT) * kj * d;
+                    aqk += ctile_get(S.Qs, i, c, DT) * kj * d;
                 }
             }
             S.A32[i][j] = j < i ? S.beta[i] * akk : 0.f;
-            Aqk_g[i * CT + j] = __float2half_rn(j <= i ? aqk : 0.f);
+            ctile_set(S.oAqk, i, j, CT, j <= i ? aqk : 0.f);
         }
     }
     __syncthreads();
+
+    // ---- decayed copies of K and Q; W and U operands (beta Gamma K over Q's tile, beta V in place)
+    {
+        const float gC = PC ? 0.f : S.gam[len - 1];
+        for (int e = tid; e < CT * DT / 8; e += K1_THREADS) {
+            // 8 consecutive columns of one row (one 16-byte core-matrix row segment)
+            int i = e / (DT / 8), c8 = (e % (DT / 8)) * 8;
+            uint32_t off = ctile_off(i, c8, DT);
+            float kx[8], qx[8], vx[8], o1[8], o2[8], o3[8], o4[8];
+            const __half2 *k2 = reinterpret_cast<const __half2 *>(S.Ks + off);
+            const __half2 *q2 = reinterpret_cast<const __half2 *>(S.Qs + off);
+            const __half2 *v2 = reinterpret_cast<const __half2 *>(S.Vs + off);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                float2 a = __half22float2(k2[t]), b = __half22float2(q2[t]), c = __half22float2(v2[t]);
+                kx[2 * t] = a.x; kx[2 * t + 1] = a.y;
+                qx[2 * t] = b.x; qx[2 * t + 1] = b.y;
+                vx[2 * t] = c.x; vx[2 * t + 1] = c.y;
+            }
+            const float bi = S.beta[i];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                float gi = PC ? gamK[i * DT + c8 + t] : S.gam[i];
+                float gc = PC ? gamK[(len - 1) * DT + c8 + t] : gC;
+                float Gi = expf(gi);
+                o1[t] = kx[t] * expf(gc - gi);  // K~
+                o2[t] = qx[t] * Gi;             // Q~
+                o3[t] = bi * Gi * kx[t];        // beta Gamma K
+                o4[t] = bi * vx[t];             // beta V
+            }
+            tc::st_tile8(S.oKt, i, c8, DT, o1);
+            tc::st_tile8(S.oQg, i, c8, DT, o2);
+            tc::st_tile8(S.Qs, i, c8, DT, o3);
+            tc::st_tile8(S.Vs, i, c8, DT, o4);
+        }
+    }
 
     // ---- T = (I + A_kk)^-1: diagonal 16x16 blocks by per-column forward substitution
     if (wid < 4 && lane < 16) {
@@ -150,28 +193,12 @@ __global__ void __launch_bounds__(K1_THREADS) k1_wy_prep(const Params P) {
         }
         __syncthreads();
     }
-
-    // ---- operands for W and U, decayed copies of K and Q, T in fp16
-    __half *Kt_g = P.Kt + u * CT * DT, *Qg_g = P.Qg + u * CT * DT;
-    const float gC = PC ? 0.f : S.gam[len - 1];
-    for (int e = tid; e < CT * DT; e += K1_THREADS) {
-        int i = e / DT, c = e % DT;
-        float gi = PC ? gamK[i * DT + c] : S.gam[i];
-        float gc = PC ? gamK[(len - 1) * DT + c] : gC;
-        float kv = __half2float(S.Ks[i * LDD + c]);
-        float qv = __half2float(S.Qs[i * LDD + c]);
-        float Gi = expf(gi);
-        S.KB[i * LDD + c] = __float2half_rn(S.beta[i] * Gi * kv);
-        S.VB[i * LDD + c] = __float2half_rn(S.beta[i] * __half2float(S.Vs[i * LDD + c]));
-        Kt_g[e] = __float2half_rn(kv * expf(gc - gi));
-        Qg_g[e] = __float2half_rn(qv * Gi);
-    }
-    __half *T_g = P.Tm + u * CT * CT;
-    for (int e = tid; e < CT * CT; e += K1_THREADS) {
-        int i = e / CT, j = e % CT;
-        __half t = __float2half_rn(S.T32[i][j]);
-        S.Th[i * LDC + j] = t;
-        T_g[e] = t;
+    for (int e = tid; e < CT * CT / 8; e += K1_THREADS) {
+        int i = e / (CT / 8), j8 = (e % (CT / 8)) * 8;
+        float x[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] = S.T32[i][j8 + t];
+        tc::st_tile8(S.oT, i, j8, CT, x);
     }
     __syncthreads();
 
@@ -179,25 +206,34 @@ __global__ void __launch_bounds__(K1_THREADS) k1_wy_prep(const Params P) {
     {
         const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 64;
         float acc[1][8][4];
-        __half *W_g = P.W + u * CT * DT, *U_g = P.U + u * CT * DT;
-        zero_acc(acc);
-        warp_mma<1, 8, false, false>(acc, S.Th, LDC, S.KB, LDD, m0, n0, CT);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int w = 0; w < 2; ++w) {
+            zero_acc(acc);
+            warp_mma_ct<1, 8, false, false>(acc, S.oT, CT, w ? S.Vs : S.Qs, DT, m0, n0, CT);
+            unsigned char *dst = w ? S.oU : S.oW;
 #pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-                int i = acc_row(m0, 0, e), j = acc_col(n0, nt, e);
-                *reinterpret_cast<__half2 *>(W_g + i * DT + j) = __floats2half2_rn(acc[0][nt][e], acc[0][nt][e + 1]);
-            }
-        zero_acc(acc);
-        warp_mma<1, 8, false, false>(acc, S.Th, LDC, S.VB, LDD, m0, n0, CT);
+            for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-                int i = acc_row(m0, 0, e), j = acc_col(n0, nt, e);
-                *reinterpret_cast<__half2 *>(U_g + i * DT + j) = __floats2half2_rn(acc[0][nt][e], acc[0][nt][e + 1]);
-            }
+                for (int e = 0; e < 4; e += 2) {
+                    int i = acc_row(m0, 0, e), j = acc_col(n0, nt, e);
+                    *reinterpret_cast<__half2 *>(dst + ctile_off(i, j, DT)) =
+                        __floats2half2_rn(acc[0][nt][e], acc[0][nt][e + 1]);
+                }
+        }
+    }
+    // ---- bulk stores of every tile
+    tc::fence_smem_to_async();
+    __syncthreads();
+    if (tid == 0) {
+        tc::bulk_s2g(P.Tm + u * CT * CT, S.oT, CT * CT * 2);
+        tc::bulk_s2g(P.Aqk + u * CT * CT, S.oAqk, CT * CT * 2);
+        tc::bulk_s2g(P.W + u * CT * DT, S.oW, CT * DT * 2);
+        tc::bulk_s2g(P.U + u * CT * DT, S.oU, CT * DT * 2);
+        tc::bulk_s2g(P.Kt + u * CT * DT, S.oKt, CT * DT * 2);
+        tc::bulk_s2g(P.Qg + u * CT * DT, S.oQg, CT * DT * 2);
+        tc::bulk_s2g(P.Dt + u * CT * DT, S.oD, CT * DT * 2);
+        tc::bulk_commit();
+        tc::bulk_wait();
     }
 }
 

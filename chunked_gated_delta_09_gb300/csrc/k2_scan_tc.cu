@@ -13,7 +13,8 @@
 // (section 3: partition states corrected with an all-gather), done inside one GPU.
 //
 // One CTA holds the whole 128 x 128 fp32 state (and Phi) in tensor memory; each step issues two MMA
-// groups: V_new^T = S W^T (M = 128 state rows, N = 64 tokens) and S += V_new^T K~ (N = 128).
+// groups: V_new^T = S W^T (M = 128 state rows, N = 64 tokens) and S += V_new^T K~ (N = 128).  Operand
+// tiles arrive by bulk copy one chunk ahead; h_n and V_new^T leave by bulk copy from the operand tiles.
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
 #include "tc_util.cuh"
@@ -26,25 +27,14 @@ constexpr uint32_t SC_WAIT_LIMIT = 1u << 24;
 template <bool LOCAL>
 struct __align__(1024) FwdSmem {
     unsigned char W[2][CT * DT * 2], Kt[2][CT * DT * 2], U[2][CT * DT * 2];
-    unsigned char Sa[DT * DT * 2];                 // state rows as fp16 (A operand)
-    unsigned char Vna[DT * CT * 2];                // V_new^T [v][c] (A operand)
-    unsigned char Pa[LOCAL ? DT * DT * 2 : 16];    // transition rows as fp16
-    unsigned char Vpa[LOCAL ? DT * CT * 2 : 16];   // -(W Phi^T)^T
-    float gC[2][DT];
-    uint64_t bar;
+    unsigned char Sa[DT * DT * 2];                // state rows as fp16 (A operand; h_n)
+    unsigned char Vna[DT * CT * 2];               // V_new^T [v][c] (A operand)
+    unsigned char Pa[LOCAL ? DT * DT * 2 : 16];   // transition rows as fp16
+    unsigned char Vpa[LOCAL ? DT * CT * 2 : 16];  // -(Phi W^T)
+    float gam[2][DT];                             // gate row block of the chunk (scalar: first CT used)
+    uint64_t bar, lbar[2];
     uint32_t tslot;
 };
-
-// cp.async a row-major fp16 block [CT][DT] into a core-matrix tile; conflict-free lane map.
-__device__ __forceinline__ void cp_tile_ct_dt(unsigned char *tile, const __half *src, int tid) {
-    const int wid = tid >> 5, lane = tid & 31;
-#pragma unroll
-    for (int i = 0; i < (CT * DT / 8) / SC_THREADS; ++i) {
-        int it = wid + (SC_THREADS / 32) * i;  // 0 .. 31
-        int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
-        cp_async16(tile + tc::tile_off(r, c8, DT), src + (size_t)r * DT + c8);
-    }
-}
 
 template <bool PC, bool LOCAL>
 __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
@@ -57,8 +47,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
     seq_range(P, s, bos, eos);
     const int nc = (eos - bos + P.BT - 1) / P.BT;
     const int c_lo = seg * P.Lseg, c_hi = min(nc, c_lo + P.Lseg);
-    if (c_lo >= c_hi && !(seg == 0 && !LOCAL)) return;  // empty segment (segment 0 of an empty sequence has no work either)
-    if (c_lo >= c_hi) return;
+    if (c_lo >= c_hi) return;  // segment without chunks
     const int base = seq_chunk_base(P, s);
     const size_t su = ((size_t)s * P.Hv + hv) * NS + seg;
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
@@ -68,26 +57,29 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
     if (wid == 0) tc::tmem_alloc(&S.tslot, LOCAL ? 512 : 256);
     if (tid == 0) {
         tc::mbar_init(&S.bar, 1);
+        tc::mbar_init(&S.lbar[0], 1);
+        tc::mbar_init(&S.lbar[1], 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
+    auto chunk_len = [&](int c) {
+        int len = eos - (bos + c * P.BT);
+        return len < P.BT ? len : P.BT;
+    };
+    // one thread: bulk-load chunk c's operand tiles and gate row into buffer `buf`
     auto issue = [&](int c, int buf) {
         const size_t u = (size_t)(base + c) * P.Hv + hv;
-        cp_tile_ct_dt(S.W[buf], P.W + u * CT * DT, tid);
-        cp_tile_ct_dt(S.Kt[buf], P.Kt + u * CT * DT, tid);
-        cp_tile_ct_dt(S.U[buf], P.U + u * CT * DT, tid);
-        int len = eos - (bos + c * P.BT);
-        len = len < P.BT ? len : P.BT;
-        if (PC) {
-            if (tid < DT / 4) cp_async16(&S.gC[buf][4 * tid], P.gam + (u * CT + len - 1) * DT + 4 * tid);
-        } else if (tid == 0) {
-            cp_async4(&S.gC[buf][0], P.gam + u * CT + len - 1);
-        }
-        cp_async_commit();
+        const uint32_t gbytes = PC ? DT * 4 : CT * 4;
+        const float *gsrc = PC ? P.gam + (u * CT + chunk_len(c) - 1) * DT : P.gam + u * CT;
+        tc::mbar_expect_tx(&S.lbar[buf], 3 * CT * DT * 2 + gbytes);
+        tc::bulk_g2s(S.W[buf], P.W + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
+        tc::bulk_g2s(S.Kt[buf], P.Kt + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
+        tc::bulk_g2s(S.U[buf], P.U + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
+        tc::bulk_g2s(S.gam[buf], gsrc, gbytes, &S.lbar[buf]);
     };
-    issue(c_lo, 0);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    if (tid == 0) issue(c_lo, 0);
     const uint32_t tm = S.tslot;
     constexpr int T_S = 0, T_P = 128, T_VN = LOCAL ? 256 : 128, T_VP = 320;
 
@@ -118,7 +110,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
         tc::wait_st();
     }
     const uint32_t sSa = smem_u32(S.Sa), sVna = smem_u32(S.Vna), sPa = smem_u32(S.Pa), sVpa = smem_u32(S.Vpa);
-    uint32_t parity = 0;
+    uint32_t parity = 0, lpar0 = 0, lpar1 = 0;
     bool lost = false;
     auto mma_done = [&]() {
         if (tid == 0) tc::commit(&S.bar);
@@ -127,16 +119,22 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
         lost = __syncthreads_or(!ok) != 0;
         tc::fence_after();
     };
-    cp_async_wait<0>();
 
     for (int c = c_lo; c < c_hi && !lost; ++c) {
         const int buf = (c - c_lo) & 1;
         const size_t u = (size_t)(base + c) * P.Hv + hv;
-        tc::fence_smem_to_async();
+        // chunk c's tiles landed; the previous step's bulk stores no longer read Sa / Vna
+        bool ok = tc::mbar_wait(&S.lbar[buf], buf ? lpar1 : lpar0, SC_WAIT_LIMIT);
+        if (buf) lpar1 ^= 1u;
+        else lpar0 ^= 1u;
+        if (!LOCAL && tid == 0) tc::bulk_wait_read();
         tc::fence_before();
-        __syncthreads();  // chunk c's operands landed everywhere; previous MMAs finished
+        lost = __syncthreads_or(!ok) != 0;
         tc::fence_after();
-        // epilogue 0: state rows -> fp16 operand (+ h_n), then scale by Gamma_C in place
+        if (lost) break;
+        if (c + 1 < c_hi && tid == 0) issue(c + 1, buf ^ 1);
+        const float gl = PC ? 0.f : S.gam[buf][chunk_len(c) - 1];
+        // epilogue 0: state rows -> fp16 operand (= h_n), then scale by Gamma_C in place
 #pragma unroll
         for (int m = 0; m < (LOCAL ? 2 : 1); ++m) {
             const int tcol = m ? T_P : T_S;
@@ -148,17 +146,14 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
                 tc::ld32(tc::taddr(tm, tcol + c0), v);
 #pragma unroll
                 for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(tile, row, c0 + j8, DT, v + j8);
-                if (!LOCAL) {
-                    uint4 pk[4];
-                    __half2 *h2 = reinterpret_cast<__half2 *>(pk);
+                if (PC) {
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) h2[t] = __floats2half2_rn(v[2 * t], v[2 * t + 1]);
-                    uint4 *dst = reinterpret_cast<uint4 *>(P.h + u * DT * DT + (size_t)row * DT + c0);
+                    for (int t = 0; t < 32; ++t) v[t] *= expf(S.gam[buf][c0 + t]);
+                } else {
+                    const float G = expf(gl);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) dst[t] = pk[t];
+                    for (int t = 0; t < 32; ++t) v[t] *= G;
                 }
-#pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] *= expf(PC ? S.gC[buf][c0 + t] : S.gC[buf][0]);
                 tc::st32(tc::taddr(tm, tcol + c0), v);
             }
         }
@@ -167,15 +162,15 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
-        if (c + 1 < c_hi) issue(c + 1, buf ^ 1);
-        // MMA 1: V_new^T (pre) = S W^T   [and  (W Phi^T)^T]
+        // MMA 1: V_new^T (pre) = S W^T   [and  Phi W^T];  h_n leaves by bulk copy
         if (tid == 0) {
             tc::gemm(tm + T_VN, sSa, DT, false, smem_u32(S.W[buf]), DT, false, 128, 64, DT, false);
             if (LOCAL) tc::gemm(tm + T_VP, sPa, DT, false, smem_u32(S.W[buf]), DT, false, 128, 64, DT, false);
+            if (!LOCAL) tc::bulk_s2g(P.h + u * DT * DT, S.Sa, DT * DT * 2);
         }
         mma_done();
         if (lost) break;
-        // epilogue 1: V_new^T = U^T - S W^T  (transition rows: -(Phi W^T)) -> fp16 operand (+ V_new)
+        // epilogue 1: V_new^T = U^T - S W^T  (transition rows: -(Phi W^T)) -> fp16 operand
         {
             const int c0 = 32 * half;
             float v[32];
@@ -184,11 +179,6 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
             for (int t = 0; t < 32; ++t) v[t] = tc::ld_tile(S.U[buf], c0 + t, row, DT) - v[t];
 #pragma unroll
             for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.Vna, row, c0 + j8, CT, v + j8);
-            if (!LOCAL) {
-                __half *vg = P.Vn + u * CT * DT;
-#pragma unroll
-                for (int t = 0; t < 32; ++t) vg[(size_t)(c0 + t) * DT + row] = __float2half_rn(v[t]);
-            }
             if (LOCAL) {
                 tc::ld32(tc::taddr(tm, T_VP + c0), v);
 #pragma unroll
@@ -201,15 +191,18 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
-        // MMA 2: S += V_new^T K~   [Phi += (-(W Phi^T))^T K~]
+        // MMA 2: S += V_new^T K~   [Phi += (-(Phi W^T)) K~];  V_new^T leaves by bulk copy
         if (tid == 0) {
             tc::gemm(tm + T_S, sVna, CT, false, smem_u32(S.Kt[buf]), DT, true, 128, 128, CT, true);
             if (LOCAL) tc::gemm(tm + T_P, sVpa, CT, false, smem_u32(S.Kt[buf]), DT, true, 128, 128, CT, true);
+            if (!LOCAL) {
+                tc::bulk_s2g(P.Vn + u * DT * CT, S.Vna, DT * CT * 2);
+                tc::bulk_commit();
+            }
         }
         mma_done();
-        cp_async_wait<0>();
     }
-    // ---- local pass: segment summaries E_s (state) and Phi_s (transition rows), fp32
+    // ---- local pass: segment summaries E_s (state), Phi_s and Phi_s^T (transition rows), fp32
     if (LOCAL && !lost) {
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
@@ -222,10 +215,16 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
 #pragma unroll
                 for (int t = 0; t < 32; t += 4)
                     *reinterpret_cast<float4 *>(dst + c0 + t) = make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]);
+                if (m) {  // Phi^T, so that the backward combine also reads rows
+                    float *dT = P.segPhiT + su * DT * DT + row;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) dT[(size_t)(c0 + t) * DT] = v[t];
+                }
             }
         }
     }
     if (lost && tid == 0) flag_status(P.status, ST_TIMEOUT);
+    if (tid == 0) tc::bulk_wait();
     tc::fence_before();
     __syncthreads();
     if (wid == 0) {

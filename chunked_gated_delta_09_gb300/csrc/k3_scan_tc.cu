@@ -9,8 +9,9 @@
 //     at its start);
 //   combine (k23_combine.cu): dS_exit(s-1) = dS_exit(s) Phi_s^T + F_s, exactly, in fp32;
 //   final pass (LOCAL = false): every segment runs from its exact exit gradient and writes dh_n and
-//     dV_new; segment 0 also writes dh0.
-// One CTA holds the 128 x 128 fp32 dS in tensor memory; each step issues two MMA groups.
+//     -dV_new^T; segment 0 also writes dh0.
+// One CTA holds the 128 x 128 fp32 dS in tensor memory; each step issues two MMA groups.  Operand tiles
+// arrive by bulk copy one chunk ahead; dh_n and -dV_new^T leave by bulk copy from the operand tiles.
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
 #include "tc_util.cuh"
@@ -20,30 +21,19 @@ namespace gdr {
 constexpr int SB_THREADS = 256;
 constexpr uint32_t SB_WAIT_LIMIT = 1u << 24;
 
-template <typename Tin>
 struct __align__(1024) BwdSmem {
     unsigned char Aq[2][CT * CT * 2], D[2][CT * DT * 2], Kt[2][CT * DT * 2], Qg[2][CT * DT * 2], W[2][CT * DT * 2];
-    unsigned char dSa[DT * DT * 2];  // dS rows as fp16 (A operand)
+    unsigned char dSa[DT * DT * 2];  // dS rows as fp16 (A operand; dh_n)
     unsigned char dVa[DT * CT * 2];  // -dV_new^T [v][c] (A operand)
-    Tin Draw[CT * DT];               // raw dO slice of the next chunk
-    float gC[2][DT];
-    uint64_t bar;
+    float gam[2][DT];
+    uint64_t bar, lbar[2];
     uint32_t tslot;
 };
 
-__device__ __forceinline__ void cp_tile_sb(unsigned char *tile, const __half *src, int cols, int tid) {
-    const int wid = tid >> 5, lane = tid & 31;
-    const int cpr = cols / 8;  // 16-byte chunks per row
-    for (int it = wid; it < (CT / 8) * (cpr / 4); it += SB_THREADS / 32) {
-        int r = 8 * (it / (cpr / 4)) + (lane & 7), c8 = 8 * (4 * (it % (cpr / 4)) + (lane >> 3));
-        cp_async16(tile + tc::tile_off(r, c8, cols), src + (size_t)r * cols + c8);
-    }
-}
-
-template <typename Tin, bool PC, bool LOCAL>
+template <bool PC, bool LOCAL>
 __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    BwdSmem<Tin> &S = *reinterpret_cast<BwdSmem<Tin> *>(smem_raw);
+    BwdSmem &S = *reinterpret_cast<BwdSmem *>(smem_raw);
     if (*P.status & ST_BAD_SEQLENS) return;
     const int NS = P.NS;
     const int seg = blockIdx.x % NS, hv = (blockIdx.x / NS) % P.Hv, s = blockIdx.x / (NS * P.Hv);
@@ -66,61 +56,34 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
         return;
     }
     const int base = seq_chunk_base(P, s);
-    const Tin *dOp = reinterpret_cast<const Tin *>(P.dO);
-    constexpr int EPC = 16 / sizeof(Tin);  // input elements per 16-byte copy
 
     if (wid == 0) tc::tmem_alloc(&S.tslot, 256);
     if (tid == 0) {
         tc::mbar_init(&S.bar, 1);
+        tc::mbar_init(&S.lbar[0], 1);
+        tc::mbar_init(&S.lbar[1], 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
-    // raw dO slice of chunk c: rows past the chunk and columns past V zero-fill.  Each thread later
-    // converts exactly the copies it issued (lane % 8 -> row inside a core matrix).
-    auto for_my_d = [&](auto &&fn) {
-#pragma unroll
-        for (int i = 0; i < (CT * DT / 8) / SB_THREADS; ++i) {
-            int it = wid + (SB_THREADS / 32) * i;
-            int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
-            fn(r, c8);
-        }
+    auto chunk_len = [&](int c) {
+        int len = eos - (bos + c * P.BT);
+        return len < P.BT ? len : P.BT;
     };
     auto issue = [&](int c, int buf) {
         const size_t u = (size_t)(base + c) * P.Hv + hv;
-        cp_tile_sb(S.Aq[buf], P.Aqk + u * CT * CT, CT, tid);
-        cp_tile_sb(S.Kt[buf], P.Kt + u * CT * DT, DT, tid);
-        cp_tile_sb(S.Qg[buf], P.Qg + u * CT * DT, DT, tid);
-        cp_tile_sb(S.W[buf], P.W + u * CT * DT, DT, tid);
-        const int tok0 = bos + c * P.BT;
-        int len = eos - tok0;
-        len = len < P.BT ? len : P.BT;
-        for_my_d([&](int r, int c8) {
-#pragma unroll
-            for (int h = 0; h < 8 / EPC; ++h) {
-                int cc = c8 + h * EPC;
-                bool ok = r < len && cc + EPC <= P.V;
-                const Tin *src = ok ? dOp + ((size_t)(tok0 + r) * P.Hv + hv) * P.V + cc : dOp;
-                cp_async16_zfill(S.Draw + r * DT + cc, src, ok ? 16 : 0);
-            }
-        });
-        if (PC) {
-            if (tid < DT / 4) cp_async16(&S.gC[buf][4 * tid], P.gam + (u * CT + len - 1) * DT + 4 * tid);
-        } else if (tid == 0) {
-            cp_async4(&S.gC[buf][0], P.gam + u * CT + len - 1);
-        }
-        cp_async_commit();
+        const uint32_t gbytes = PC ? DT * 4 : CT * 4;
+        const float *gsrc = PC ? P.gam + (u * CT + chunk_len(c) - 1) * DT : P.gam + u * CT;
+        tc::mbar_expect_tx(&S.lbar[buf], CT * CT * 2 + 4 * CT * DT * 2 + gbytes);
+        tc::bulk_g2s(S.Aq[buf], P.Aqk + u * CT * CT, CT * CT * 2, &S.lbar[buf]);
+        tc::bulk_g2s(S.D[buf], P.Dt + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
+        tc::bulk_g2s(S.Kt[buf], P.Kt + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
+        tc::bulk_g2s(S.Qg[buf], P.Qg + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
+        tc::bulk_g2s(S.W[buf], P.W + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
+        tc::bulk_g2s(S.gam[buf], gsrc, gbytes, &S.lbar[buf]);
     };
-    auto convert_d = [&](int buf) {
-        for_my_d([&](int r, int c8) {
-            float x[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) x[j] = to_f32(S.Draw[r * DT + c8 + j]) * P.scale;
-            tc::st_tile8(S.D[buf], r, c8, DT, x);
-        });
-    };
-    issue(c_hi - 1, (c_hi - 1 - c_lo) & 1);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    if (tid == 0) issue(c_hi - 1, (c_hi - 1 - c_lo) & 1);
     const uint32_t tm = S.tslot;
     constexpr int T_S = 0, T_DV = 128;
     {
@@ -144,7 +107,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
         tc::wait_st();
     }
     const uint32_t sdSa = smem_u32(S.dSa), sdVa = smem_u32(S.dVa);
-    uint32_t parity = 0;
+    uint32_t parity = 0, lpar0 = 0, lpar1 = 0;
     bool lost = false;
     auto mma_done = [&]() {
         if (tid == 0) tc::commit(&S.bar);
@@ -153,17 +116,21 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
         lost = __syncthreads_or(!ok) != 0;
         tc::fence_after();
     };
-    cp_async_wait<0>();
-    convert_d((c_hi - 1 - c_lo) & 1);
 
     for (int c = c_hi - 1; c >= c_lo && !lost; --c) {
         const int buf = (c - c_lo) & 1;
         const size_t u = (size_t)(base + c) * P.Hv + hv;
-        tc::fence_smem_to_async();
+        bool ok = tc::mbar_wait(&S.lbar[buf], buf ? lpar1 : lpar0, SB_WAIT_LIMIT);
+        if (buf) lpar1 ^= 1u;
+        else lpar0 ^= 1u;
+        if (!LOCAL && tid == 0) tc::bulk_wait_read();
         tc::fence_before();
-        __syncthreads();  // chunk c's operands (and its converted D) visible; previous MMAs finished
+        lost = __syncthreads_or(!ok) != 0;
         tc::fence_after();
-        // epilogue 0: dS rows -> fp16 operand (+ dh_n), then scale by Gamma_C in place
+        if (lost) break;
+        if (c > c_lo && tid == 0) issue(c - 1, buf ^ 1);
+        const float gl = PC ? 0.f : S.gam[buf][chunk_len(c) - 1];
+        // epilogue 0: dS rows -> fp16 operand (= dh_n), then scale by Gamma_C in place
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int c0 = 64 * half + 32 * h;
@@ -171,17 +138,14 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
             tc::ld32(tc::taddr(tm, T_S + c0), v);
 #pragma unroll
             for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.dSa, row, c0 + j8, DT, v + j8);
-            if (!LOCAL) {
-                uint4 pk[4];
-                __half2 *h2 = reinterpret_cast<__half2 *>(pk);
+            if (PC) {
 #pragma unroll
-                for (int t = 0; t < 16; ++t) h2[t] = __floats2half2_rn(v[2 * t], v[2 * t + 1]);
-                uint4 *dst = reinterpret_cast<uint4 *>(P.dh + u * DT * DT + (size_t)row * DT + c0);
+                for (int t = 0; t < 32; ++t) v[t] *= expf(S.gam[buf][c0 + t]);
+            } else {
+                const float G = expf(gl);
 #pragma unroll
-                for (int t = 0; t < 4; ++t) dst[t] = pk[t];
+                for (int t = 0; t < 32; ++t) v[t] *= G;
             }
-#pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] *= expf(PC ? S.gC[buf][c0 + t] : S.gC[buf][0]);
             tc::st32(tc::taddr(tm, T_S + c0), v);
         }
         tc::wait_st();
@@ -189,24 +153,19 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
-        if (c > c_lo) issue(c - 1, buf ^ 1);
-        // MMA 1: dV_new^T = D^T Aqk + dS K~^T
+        // MMA 1: dV_new^T = D^T Aqk + dS K~^T;  dh_n leaves by bulk copy
         if (tid == 0) {
             tc::gemm(tm + T_DV, smem_u32(S.D[buf]), DT, true, smem_u32(S.Aq[buf]), CT, true, 128, 64, CT, false);
             tc::gemm(tm + T_DV, sdSa, DT, false, smem_u32(S.Kt[buf]), DT, false, 128, 64, DT, true);
+            if (!LOCAL) tc::bulk_s2g(P.dh + u * DT * DT, S.dSa, DT * DT * 2);
         }
         mma_done();
         if (lost) break;
-        // epilogue 1: dV_new (+ global), -dV_new^T -> fp16 operand
+        // epilogue 1: -dV_new^T -> fp16 operand
         {
             const int c0 = 32 * half;
             float v[32];
             tc::ld32(tc::taddr(tm, T_DV + c0), v);
-            if (!LOCAL) {
-                __half *dg = P.dVn + u * CT * DT;
-#pragma unroll
-                for (int t = 0; t < 32; ++t) dg[(size_t)(c0 + t) * DT + row] = __float2half_rn(v[t]);
-            }
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] = -v[t];
 #pragma unroll
@@ -216,18 +175,17 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
-        // MMA 2: dS += D^T Q~ - dV_new^T W
+        // MMA 2: dS += D^T Q~ - dV_new^T W;  -dV_new^T leaves by bulk copy
         if (tid == 0) {
             tc::gemm(tm + T_S, smem_u32(S.D[buf]), DT, true, smem_u32(S.Qg[buf]), DT, true, 128, 128, CT, true);
             tc::gemm(tm + T_S, sdVa, CT, false, smem_u32(S.W[buf]), DT, true, 128, 128, CT, true);
+            if (!LOCAL) {
+                tc::bulk_s2g(P.dVn + u * DT * CT, S.dVa, DT * CT * 2);
+                tc::bulk_commit();
+            }
         }
         mma_done();
-        if (c > c_lo) {
-            cp_async_wait<0>();
-            convert_d(buf ^ 1);
-        }
     }
-    cp_async_wait<0>();
     // ---- local pass: F_s; final pass of segment 0: dh0
     if (!lost && (LOCAL || (seg == 0 && P.dh0))) {
 #pragma unroll
@@ -249,6 +207,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
         }
     }
     if (lost && tid == 0) flag_status(P.status, ST_TIMEOUT);
+    if (tid == 0) tc::bulk_wait();
     tc::fence_before();
     __syncthreads();
     if (wid == 0) {
@@ -257,25 +216,18 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
     }
 }
 
-template <typename Tin, bool PC, bool LOCAL>
+template <bool PC, bool LOCAL>
 static cudaError_t launch_bwd_t(const Params &P, cudaStream_t stream) {
-    size_t smem = sizeof(BwdSmem<Tin>);
-    cudaError_t e = cudaFuncSetAttribute(k3_scan_tc<Tin, PC, LOCAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    size_t smem = sizeof(BwdSmem);
+    cudaError_t e = cudaFuncSetAttribute(k3_scan_tc<PC, LOCAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k3_scan_tc<Tin, PC, LOCAL><<<P.N * P.Hv * P.NS, SB_THREADS, smem, stream>>>(P);
+    k3_scan_tc<PC, LOCAL><<<P.N * P.Hv * P.NS, SB_THREADS, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
-template <typename Tin>
-static cudaError_t launch_bwd_d(const Params &P, bool local, cudaStream_t stream) {
-    if (local) return P.per_channel ? launch_bwd_t<Tin, true, true>(P, stream) : launch_bwd_t<Tin, false, true>(P, stream);
-    return P.per_channel ? launch_bwd_t<Tin, true, false>(P, stream) : launch_bwd_t<Tin, false, false>(P, stream);
-}
-
 cudaError_t launch_k3_scan(const Params &P, bool local, cudaStream_t stream) {
-    if (P.qkv_dtype == F32) return launch_bwd_d<float>(P, local, stream);
-    if (P.qkv_dtype == BF16) return launch_bwd_d<__nv_bfloat16>(P, local, stream);
-    return launch_bwd_d<__half>(P, local, stream);
+    if (local) return P.per_channel ? launch_bwd_t<true, true>(P, stream) : launch_bwd_t<false, true>(P, stream);
+    return P.per_channel ? launch_bwd_t<true, false>(P, stream) : launch_bwd_t<false, false>(P, stream);
 }
 
 }  // namespace gdr

@@ -1,4 +1,4 @@
-// k4_intra_grad.cu -- per-chunk gradients (one CTA per chunk x value head).
+// k4_intra_grad.cu -- per-chunk gradients with warp-level tensor-core MMAs (one CTA per chunk x head).
 //
 // Given the state entering the chunk S_0 = h_n, the adjoint of the state leaving it dS_next = dh_n,
 // V_new, dV_new and T from the two scans and the WY preparation, this kernel produces the chunk's dq,
@@ -17,23 +17,31 @@
 //   dgamma = q (.) dq - k (.) (P^T Q + K~ term) + k (.) (W term + E K - E^T K), plus, on the last row,
 //            Gamma_C <S_0, dS_next> + sum_j k_j (.) (K~ term)_j
 // (for the scalar gate the dgamma row is summed over channels).  The per-channel (KDA) gate turns each
-// decayed C x C product into a per-channel sum that the owner of each output element evaluates directly.
+// decayed C x C product into a per-channel sum that the owner of each output element evaluates directly;
+// this kernel serves that gate (the scalar gate runs on k4_intra_grad_tc.cu).
+//
+// All operands live in shared memory as core-matrix tiles (ctile_off); the workspace tiles arrive by
+// bulk copy.  The workspace holds V_new^T and -dV_new^T (tiles [v][c]).
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
+#include "tc_util.cuh"
 
 namespace gdr {
 
 constexpr int K4_THREADS = 256;
+constexpr uint32_t K4_WAIT_LIMIT = 1u << 24;
 
-struct K4Smem {
-    __half Qs[CT * LDD], Ks[CT * LDD], Vs[CT * LDD], Ds[CT * LDD], Vns[CT * LDD], dVns[CT * LDD];
-    __half Hs[DT * LDD], dHs[DT * LDD];
-    __half Ts[CT * LDC], Pms[CT * LDC];
+struct __align__(1024) K4Smem {
+    unsigned char Qs[CT * DT * 2], Ks[CT * DT * 2], Vs[CT * DT * 2], Ds[CT * DT * 2];
+    unsigned char VnT[DT * CT * 2], NdVT[DT * CT * 2];  // V_new^T, -dV_new^T  [v][c]
+    unsigned char Hs[DT * DT * 2], dHs[DT * DT * 2];    // [v][k]
+    unsigned char Ts[CT * CT * 2], Pms[CT * CT * 2];
     float gam[CT];
     float beta[CT];
     float dbeta[CT];
     float dgrow[CT];
     float lastrow[DT];
+    uint64_t lbar;
 };
 
 // Store 32 accumulator elements (C x K tile of this warp) as an output gradient row block.
@@ -50,15 +58,15 @@ __device__ __forceinline__ void store_ck(const float (&a)[1][8][4], int m0, int 
 
 template <typename Tin, bool PC>
 __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     K4Smem &S = *reinterpret_cast<K4Smem *>(smem_raw);
     float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K4Smem));  // [CT][DT] per-channel only
     // buffers reused once their first owner is done
-    __half *dWs = S.Ds;     // dW          after dq
-    __half *KGb = S.Qs;     // beta Gamma K (per-channel) after dk_O
-    __half *dTs = S.Pms;    // dT          after dk_O
-    __half *Xs = S.Vns;     // dT T^T      after dk_SC   (pitch LDC)
-    __half *Es = S.Pms;     // E           after X
+    unsigned char *dWs = S.Ds;     // dW [r][k]          after dq
+    unsigned char *KGb = S.Qs;     // beta Gamma K       after dk_O (per-channel)
+    unsigned char *dTs = S.Pms;    // dT                 after dk_O
+    unsigned char *Xs = S.VnT;     // dT T^T (C x C)     after dk_SC
+    unsigned char *Es = S.Pms;     // E                  after X
 
     if (*P.status & ST_BAD_SEQLENS) return;
     const int n = blockIdx.x, hv = blockIdx.y, hk = hv / P.G;
@@ -68,21 +76,25 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     const size_t u = (size_t)n * P.Hv + hv;
     const int len = ci.len;
 
-    // ---- stage everything
-    cp_block_f16(S.Hs, LDD, P.h + u * DT * DT, DT, DT, tid, K4_THREADS);
-    cp_block_f16(S.dHs, LDD, P.dh + u * DT * DT, DT, DT, tid, K4_THREADS);
-    cp_block_f16(S.Vns, LDD, P.Vn + u * CT * DT, CT, DT, tid, K4_THREADS);
-    cp_block_f16(S.dVns, LDD, P.dVn + u * CT * DT, CT, DT, tid, K4_THREADS);
-    cp_block_f16(S.Ts, LDC, P.Tm + u * CT * CT, CT, CT, tid, K4_THREADS);
-    cp_async_commit();
+    // ---- stage everything: workspace tiles by bulk copy, inputs converted to fp16 tiles
+    if (tid == 0) {
+        tc::mbar_init(&S.lbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        tc::mbar_expect_tx(&S.lbar, 2 * DT * DT * 2 + 2 * DT * CT * 2 + CT * CT * 2 + CT * DT * 2);
+        tc::bulk_g2s(S.Hs, P.h + u * DT * DT, DT * DT * 2, &S.lbar);
+        tc::bulk_g2s(S.dHs, P.dh + u * DT * DT, DT * DT * 2, &S.lbar);
+        tc::bulk_g2s(S.VnT, P.Vn + u * DT * CT, DT * CT * 2, &S.lbar);
+        tc::bulk_g2s(S.NdVT, P.dVn + u * DT * CT, DT * CT * 2, &S.lbar);
+        tc::bulk_g2s(S.Ts, P.Tm + u * CT * CT, CT * CT * 2, &S.lbar);
+        tc::bulk_g2s(S.Ds, P.Dt + u * CT * DT, CT * DT * 2, &S.lbar);
+    }
     const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    const Tin *dop = reinterpret_cast<const Tin *>(P.dO) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    stage_rows_f16(S.Ks, kp, (size_t)P.Hk * P.K, len, P.K, nullptr, 1.f, tid, K4_THREADS);
-    stage_rows_f16(S.Qs, qp, (size_t)P.Hk * P.K, len, P.K, nullptr, 1.f, tid, K4_THREADS);
-    stage_rows_f16(S.Vs, vp, (size_t)P.Hv * P.V, len, P.V, nullptr, 1.f, tid, K4_THREADS);
-    stage_rows_f16(S.Ds, dop, (size_t)P.Hv * P.V, len, P.V, nullptr, P.scale, tid, K4_THREADS);
+    stage_ct_pair<Tin, K4_THREADS>(S.Ks, kp, (size_t)P.Hk * P.K, P.K, 1.f, S.Qs, qp, (size_t)P.Hk * P.K, P.K, 1.f, len,
+                                   tid);
+    stage_ct_pair<Tin, K4_THREADS>(S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, len,
+                                   tid);
     if (tid < CT) {
         S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
         S.dbeta[tid] = 0.f;
@@ -92,21 +104,26 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     if (tid < DT) S.lastrow[tid] = 0.f;
     if (PC)
         for (int e = tid; e < CT * DT; e += K4_THREADS) gamK[e] = P.gam[u * CT * DT + e];
-    cp_async_wait<0>();
-    __syncthreads();
+    __syncthreads();  // barrier initialised
+    const bool loaded = tc::mbar_wait(&S.lbar, 0, K4_WAIT_LIMIT);
+    if (__syncthreads_or(!loaded)) {
+        if (tid == 0) flag_status(P.status, ST_TIMEOUT);
+        return;
+    }
 
     // C x K tiling: warp w owns rows m0 .. m0+15 and columns n0 .. n0+63
     const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 64;
     // C x C tiling: rows cm0 .. cm0+15, columns cn0 .. cn0+31
     const int cm0 = (wid & 3) * 16, cn0 = (wid >> 2) * 32;
     auto G_ = [&](int r, int c) -> float { return PC ? gamK[r * DT + c] : S.gam[r]; };
+    auto Kv = [&](int r, int c) -> float { return ctile_get(S.Ks, r, c, DT); };
     const int rl = len - 1;
 
     // ---- S1: P = (D V_new^T) (.) causal mask (.) [scalar: decay]
     {
         float g1[1][4][4];
         zero_acc(g1);
-        warp_mma<1, 4, false, true>(g1, S.Ds, LDD, S.Vns, LDD, cm0, cn0, DT);
+        warp_mma_ct<1, 4, false, false>(g1, S.Ds, DT, S.VnT, CT, cm0, cn0, DT);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -114,7 +131,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
                 float x = 0.f;
                 if (j <= r) x = PC ? g1[0][nt][e] : g1[0][nt][e] * expf(S.gam[r] - S.gam[j]);
-                S.Pms[r * LDC + j] = __float2half_rn(x);
+                ctile_set(S.Pms, r, j, CT, x);
             }
     }
     __syncthreads();
@@ -126,13 +143,13 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     {
         float dq[1][8][4];
         zero_acc(dq);
-        warp_mma<1, 8, false, false>(dq, S.Ds, LDD, S.Hs, LDD, m0, n0, DT);
+        warp_mma_ct<1, 8, false, false>(dq, S.Ds, DT, S.Hs, DT, m0, n0, DT);
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) dq[0][nt][e] *= expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e)));
         if (!PC) {
-            warp_mma<1, 8, false, false>(dq, S.Pms, LDC, S.Ks, LDD, m0, n0, CT);
+            warp_mma_ct<1, 8, false, false>(dq, S.Pms, CT, S.Ks, DT, m0, n0, CT);
         } else {
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
@@ -141,7 +158,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                     float gr = gamK[r * DT + c], s = 0.f;
                     for (int j = 0; j <= r; ++j)
-                        s += __half2float(S.Pms[r * LDC + j]) * __half2float(S.Ks[j * LDD + c]) * expf(gr - gamK[j * DT + c]);
+                        s += ctile_get(S.Pms, r, j, CT) * Kv(j, c) * expf(gr - gamK[j * DT + c]);
                     dq[0][nt][e] += s;
                 }
         }
@@ -150,7 +167,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                dgam[0][nt][e] += __half2float(S.Qs[r * LDD + c]) * dq[0][nt][e];
+                dgam[0][nt][e] += ctile_get(S.Qs, r, c, DT) * dq[0][nt][e];
             }
         if (P.G == 1)
             store_ck(dq, m0, n0, len, P.K, reinterpret_cast<char *>(P.dq) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
@@ -162,7 +179,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     {
         zero_acc(dk);
         if (!PC) {
-            warp_mma<1, 8, true, false>(dk, S.Pms, LDC, S.Qs, LDD, m0, n0, CT);
+            warp_mma_ct<1, 8, true, false>(dk, S.Pms, CT, S.Qs, DT, m0, n0, CT);
         } else {
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
@@ -171,7 +188,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                     int j = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                     float gj = gamK[j * DT + c], s = 0.f;
                     for (int r = j; r < CT; ++r)
-                        s += __half2float(S.Pms[r * LDC + j]) * __half2float(S.Qs[r * LDD + c]) * expf(gamK[r * DT + c] - gj);
+                        s += ctile_get(S.Pms, r, j, CT) * ctile_get(S.Qs, r, c, DT) * expf(gamK[r * DT + c] - gj);
                     dk[0][nt][e] = s;
                 }
         }
@@ -180,7 +197,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                dgam[0][nt][e] -= __half2float(S.Ks[r * LDD + c]) * dk[0][nt][e];
+                dgam[0][nt][e] -= Kv(r, c) * dk[0][nt][e];
             }
     }
     __syncthreads();  // Ds, Pms, Qs free
@@ -189,7 +206,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     {
         float t[1][8][4];
         zero_acc(t);
-        warp_mma<1, 8, false, false>(t, S.Vns, LDD, S.dHs, LDD, m0, n0, DT);
+        warp_mma_ct<1, 8, true, false>(t, S.VnT, CT, S.dHs, DT, m0, n0, DT);
         float part = 0.f;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
@@ -197,7 +214,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                 float x = t[0][nt][e] * expf(G_(rl, c) - G_(r, c));
-                float kx = __half2float(S.Ks[r * LDD + c]) * x;
+                float kx = Kv(r, c) * x;
                 dk[0][nt][e] += x;
                 dgam[0][nt][e] -= kx;
                 if (PC) atomicAdd(&S.lastrow[c], kx);
@@ -212,47 +229,47 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate)
         for (int c = tid; c < DT; c += K4_THREADS) {
             float s = 0.f;
-            for (int v = 0; v < DT; ++v) s += __half2float(S.Hs[v * LDD + c]) * __half2float(S.dHs[v * LDD + c]);
+            for (int v = 0; v < DT; ++v) s += ctile_get(S.Hs, v, c, DT) * ctile_get(S.dHs, v, c, DT);
             s *= expf(G_(rl, c));
             if (PC) atomicAdd(&S.lastrow[c], s);
             else atomicAdd(&S.lastrow[0], s);
         }
     }
-    // ---- S5: dW = -dV_new S_0  -> dWs (fp16);  per-channel: beta Gamma K -> KGb
+    // ---- S5: dW = -dV_new S_0 (the stored tile is -dV_new^T)  -> dWs;  per-channel: beta Gamma K -> KGb
     {
         float t[1][8][4];
         zero_acc(t);
-        warp_mma<1, 8, false, false>(t, S.dVns, LDD, S.Hs, LDD, m0, n0, DT);
+        warp_mma_ct<1, 8, true, false>(t, S.NdVT, CT, S.Hs, DT, m0, n0, DT);
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; e += 2) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                *reinterpret_cast<__half2 *>(dWs + r * LDD + c) = __floats2half2_rn(-t[0][nt][e], -t[0][nt][e + 1]);
+                *reinterpret_cast<__half2 *>(dWs + ctile_off(r, c, DT)) = __floats2half2_rn(t[0][nt][e], t[0][nt][e + 1]);
             }
         if (PC) {
             for (int e = tid; e < CT * DT; e += K4_THREADS) {
                 int r = e / DT, c = e % DT;
-                KGb[r * LDD + c] = __float2half_rn(S.beta[r] * expf(gamK[e]) * __half2float(S.Ks[r * LDD + c]));
+                ctile_set(KGb, r, c, DT, S.beta[r] * expf(gamK[e]) * Kv(r, c));
             }
         }
     }
     __syncthreads();
 
-    // ---- S6: dT = dW (beta Gamma K)^T + dV_new (beta V)^T  -> dTs (fp16)
+    // ---- S6: dT = dW (beta Gamma K)^T + dV_new (beta V)^T  -> dTs
     {
         float a[1][4][4], b[1][4][4];
         zero_acc(a);
         zero_acc(b);
-        warp_mma<1, 4, false, true>(a, dWs, LDD, PC ? KGb : S.Ks, LDD, cm0, cn0, DT);
-        warp_mma<1, 4, false, true>(b, S.dVns, LDD, S.Vs, LDD, cm0, cn0, DT);
+        warp_mma_ct<1, 4, false, true>(a, dWs, DT, PC ? KGb : S.Ks, DT, cm0, cn0, DT);
+        warp_mma_ct<1, 4, true, true>(b, S.NdVT, CT, S.Vs, DT, cm0, cn0, DT);  // = -(dV_new V^T)
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
-                float x = (PC ? a[0][nt][e] : a[0][nt][e] * S.beta[j] * expf(S.gam[j])) + b[0][nt][e] * S.beta[j];
-                dTs[r * LDC + j] = __float2half_rn(x);
+                float x = (PC ? a[0][nt][e] : a[0][nt][e] * S.beta[j] * expf(S.gam[j])) - b[0][nt][e] * S.beta[j];
+                ctile_set(dTs, r, j, CT, x);
             }
     }
     // ---- S7: T^T dW -> dk_W, dbeta, dgamma
@@ -260,49 +277,50 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     {
         float t[1][8][4];
         zero_acc(t);
-        warp_mma<1, 8, true, false>(t, S.Ts, LDC, dWs, LDD, m0, n0, CT);
+        warp_mma_ct<1, 8, true, false>(t, S.Ts, CT, dWs, DT, m0, n0, CT);
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                 float Gm = expf(G_(r, c));
-                float kv = __half2float(S.Ks[r * LDD + c]);
+                float kv = Kv(r, c);
                 float x = S.beta[r] * Gm * t[0][nt][e];
                 dk[0][nt][e] += x;
                 dgam[0][nt][e] += kv * x;
                 rowb[e >> 1] += t[0][nt][e] * kv * Gm;
             }
     }
-    // ---- S8: T^T dV_new -> dv, dbeta
+    // ---- S8: T^T dV_new -> dv, dbeta  (negated tile: product is -T^T dV_new)
     {
         float t[1][8][4];
         zero_acc(t);
-        warp_mma<1, 8, true, false>(t, S.Ts, LDC, S.dVns, LDD, m0, n0, CT);
+        warp_mma_ct<1, 8, true, true>(t, S.Ts, CT, S.NdVT, CT, m0, n0, CT);
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                rowb[e >> 1] += t[0][nt][e] * __half2float(S.Vs[r * LDD + c]);
-                t[0][nt][e] *= S.beta[r];
+                float x = -t[0][nt][e];
+                rowb[e >> 1] += x * ctile_get(S.Vs, r, c, DT);
+                t[0][nt][e] = S.beta[r] * x;
             }
         store_ck(t, m0, n0, len, P.V, reinterpret_cast<char *>(P.dv) + ((size_t)ci.tok0 * P.Hv + hv) * P.V *
                  (P.dv_dtype == F32 ? 4 : 2), (size_t)P.Hv * P.V, P.dv_dtype);
     }
-    __syncthreads();  // dTs complete; Vns free
+    __syncthreads();  // dTs complete; VnT free
 
-    // ---- S9: X = dT T^T -> Xs (fp16)
+    // ---- S9: X = dT T^T -> Xs
     {
         float x[1][4][4];
         zero_acc(x);
-        warp_mma<1, 4, false, true>(x, dTs, LDC, S.Ts, LDC, cm0, cn0, CT);
+        warp_mma_ct<1, 4, false, true>(x, dTs, CT, S.Ts, CT, cm0, cn0, CT);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; e += 2) {
                 int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
-                *reinterpret_cast<__half2 *>(Xs + r * LDC + j) = __floats2half2_rn(x[0][nt][e], x[0][nt][e + 1]);
+                *reinterpret_cast<__half2 *>(Xs + ctile_off(r, j, CT)) = __floats2half2_rn(x[0][nt][e], x[0][nt][e + 1]);
             }
     }
     __syncthreads();
@@ -310,10 +328,10 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     {
         float da[1][4][4], kk[1][4][4];
         zero_acc(da);
-        warp_mma<1, 4, true, false>(da, S.Ts, LDC, Xs, LDC, cm0, cn0, CT);
+        warp_mma_ct<1, 4, true, false>(da, S.Ts, CT, Xs, CT, cm0, cn0, CT);
         if (!PC) {
             zero_acc(kk);
-            warp_mma<1, 4, false, true>(kk, S.Ks, LDD, S.Ks, LDD, cm0, cn0, DT);
+            warp_mma_ct<1, 4, false, true>(kk, S.Ks, DT, S.Ks, DT, cm0, cn0, DT);
         }
         float rb[2] = {0.f, 0.f};
 #pragma unroll
@@ -329,12 +347,11 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                         kkd = L * kk[0][nt][e];
                     } else {
                         for (int c = 0; c < DT; ++c)
-                            kkd += __half2float(S.Ks[i * LDD + c]) * __half2float(S.Ks[j * LDD + c]) *
-                                   expf(gamK[i * DT + c] - gamK[j * DT + c]);
+                            kkd += Kv(i, c) * Kv(j, c) * expf(gamK[i * DT + c] - gamK[j * DT + c]);
                     }
                 }
                 rb[e >> 1] += dA * kkd;
-                Es[i * LDC + j] = __float2half_rn(S.beta[i] * (PC ? 1.f : L) * dA);
+                ctile_set(Es, i, j, CT, S.beta[i] * (PC ? 1.f : L) * dA);
             }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -358,8 +375,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         zero_acc(a);
         zero_acc(b);
         if (!PC) {
-            warp_mma<1, 8, false, false>(a, Es, LDC, S.Ks, LDD, m0, n0, CT);
-            warp_mma<1, 8, true, false>(b, Es, LDC, S.Ks, LDD, m0, n0, CT);
+            warp_mma_ct<1, 8, false, false>(a, Es, CT, S.Ks, DT, m0, n0, CT);
+            warp_mma_ct<1, 8, true, false>(b, Es, CT, S.Ks, DT, m0, n0, CT);
         } else {
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
@@ -368,9 +385,9 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                     float gr = gamK[r * DT + c], sa = 0.f, sb = 0.f;
                     for (int j = 0; j < r; ++j)
-                        sa += __half2float(Es[r * LDC + j]) * __half2float(S.Ks[j * LDD + c]) * expf(gr - gamK[j * DT + c]);
+                        sa += ctile_get(Es, r, j, CT) * Kv(j, c) * expf(gr - gamK[j * DT + c]);
                     for (int i = r + 1; i < CT; ++i)
-                        sb += __half2float(Es[i * LDC + r]) * __half2float(S.Ks[i * LDD + c]) * expf(gamK[i * DT + c] - gr);
+                        sb += ctile_get(Es, i, r, CT) * Kv(i, c) * expf(gamK[i * DT + c] - gr);
                     a[0][nt][e] = sa;
                     b[0][nt][e] = sb;
                 }
@@ -380,7 +397,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                float kv = __half2float(S.Ks[r * LDD + c]);
+                float kv = Kv(r, c);
                 dk[0][nt][e] += a[0][nt][e] + b[0][nt][e];
                 dgam[0][nt][e] += kv * (a[0][nt][e] - b[0][nt][e]);
             }

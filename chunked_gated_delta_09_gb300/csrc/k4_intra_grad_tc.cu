@@ -30,8 +30,9 @@ constexpr int R_DQA = 0, R_DKO = 128, R_TDW = 192, C_DT1 = 320;
 constexpr int C_X = 0, C_DA = 64, R_DKAR = 128, R_DKAC = 192;
 
 struct __align__(1024) K4TSmem {
-    unsigned char Q[CT * DT * 2], K[CT * DT * 2], V[CT * DT * 2], D[CT * DT * 2], Vn[CT * DT * 2], dVn[CT * DT * 2];
-    unsigned char H[DT * DT * 2], dH[DT * DT * 2];  // [v][k] tiles: S_0 and dS_next
+    unsigned char Q[CT * DT * 2], K[CT * DT * 2], V[CT * DT * 2], D[CT * DT * 2];
+    unsigned char Vn[DT * CT * 2], dVn[DT * CT * 2];  // V_new^T and -dV_new^T, tiles [v][c]
+    unsigned char H[DT * DT * 2], dH[DT * DT * 2];    // [v][k] tiles: S_0 and dS_next
     unsigned char T[CT * CT * 2];
     unsigned char Pm[CT * CT * 2];   // P, later X
     unsigned char dWT[DT * CT * 2];  // dW^T [k][r]
@@ -40,60 +41,9 @@ struct __align__(1024) K4TSmem {
     // partial sums in fixed slots, added in a fixed order at the end (run-to-run reproducible):
     // dbeta: 4 lane quarters x (TdU, TdW) + 2 column halves x (A term); dgrow: 4 quarters; lastrow: 8 warps
     float db_tdu[4][CT], db_tdw[4][CT], db_a[2][CT], dg_q[4][CT], last_w[8];
-    uint64_t bar;
+    uint64_t bar, lbar;
     uint32_t tslot;
 };
-
-// cp.async a row-major fp16 block [rows][cols] into a core-matrix tile.
-__device__ __forceinline__ void stage_ws_tile(unsigned char *tile, const __half *src, int rows, int cols, int tid) {
-    const int per_row = cols / 8;
-    for (int e = tid; e < rows * per_row; e += K4T_THREADS) {
-        int r = e / per_row, c8 = (e % per_row) * 8;
-        cp_async16(tile + tc::tile_off(r, c8, cols), src + (size_t)r * cols + c8);
-    }
-}
-
-// Convert two strided input blocks into [CT][DT] core-matrix tiles (rows >= nrows or columns >= ncols
-// become zero), with every global load of the thread issued before the first conversion.  Work item
-// `it` of warp w covers rows 8 (it / 4) .. +7 and 16-byte columns 4 (it % 4) .. +3: the 8 lanes of each
-// store phase write the 8 rows of one core matrix (distinct banks), and each row reads 64 contiguous
-// bytes from global memory.
-template <typename Tin>
-__device__ __forceinline__ void stage_in_pair(unsigned char *t0, const Tin *s0, size_t st0, int nc0, float m0,
-                                              unsigned char *t1, const Tin *s1, size_t st1, int nc1, float m1, int nrows,
-                                              int tid) {
-    constexpr int PER = CT * (DT / 8) / K4T_THREADS;  // 8-element chunks per thread per tile
-    const int wid = tid >> 5, lane = tid & 31;
-    float x[2][PER][8];
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-        const Tin *src = w ? s1 : s0;
-        const size_t st = w ? st1 : st0;
-        const int nc = w ? nc1 : nc0;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            int it = wid + (K4T_THREADS / 32) * i;
-            int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
-            if (r < nrows && c8 + 8 <= nc) {
-                load8(src + (size_t)r * st + c8, x[w][i]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) x[w][i][j] = 0.f;
-            }
-        }
-    }
-#pragma unroll
-    for (int w = 0; w < 2; ++w)
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            int it = wid + (K4T_THREADS / 32) * i;
-            int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
-            const float m = w ? m1 : m0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) x[w][i][j] *= m;
-            tc::st_tile8(w ? t1 : t0, r, c8, DT, x[w][i]);
-        }
-}
 
 template <typename Tin>
 __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params P) {
@@ -110,27 +60,29 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     if (wid == 0) tc::tmem_alloc(&S.tslot, K4T_TMEM_COLS);
     if (tid == 0) {
         tc::mbar_init(&S.bar, 1);
+        tc::mbar_init(&S.lbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        // ---- workspace tiles by bulk copy
+        tc::mbar_expect_tx(&S.lbar, 2 * DT * DT * 2 + 2 * DT * CT * 2 + CT * CT * 2 + CT * DT * 2);
+        tc::bulk_g2s(S.H, P.h + u * DT * DT, DT * DT * 2, &S.lbar);
+        tc::bulk_g2s(S.dH, P.dh + u * DT * DT, DT * DT * 2, &S.lbar);
+        tc::bulk_g2s(S.Vn, P.Vn + u * DT * CT, DT * CT * 2, &S.lbar);
+        tc::bulk_g2s(S.dVn, P.dVn + u * DT * CT, DT * CT * 2, &S.lbar);
+        tc::bulk_g2s(S.T, P.Tm + u * CT * CT, CT * CT * 2, &S.lbar);
+        tc::bulk_g2s(S.D, P.Dt + u * CT * DT, CT * DT * 2, &S.lbar);
     }
-
-    // ---- stage operands: workspace tiles asynchronously, inputs with conversion
-    stage_ws_tile(S.H, P.h + u * DT * DT, DT, DT, tid);
-    stage_ws_tile(S.dH, P.dh + u * DT * DT, DT, DT, tid);
-    stage_ws_tile(S.Vn, P.Vn + u * CT * DT, CT, DT, tid);
-    stage_ws_tile(S.dVn, P.dVn + u * CT * DT, CT, DT, tid);
-    stage_ws_tile(S.T, P.Tm + u * CT * CT, CT, CT, tid);
-    cp_async_commit();
     if (tid < CT) {
         S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
         S.gam[tid] = P.gam[u * CT + tid];
         S.db_a[0][tid] = 0.f;
         S.db_a[1][tid] = 0.f;
     }
-    cp_async_wait<0>();
-    tc::fence_smem_to_async();
     tc::fence_before();
-    __syncthreads();
+    __syncthreads();  // barrier initialisation and the tensor-memory address visible
     tc::fence_after();
+    // thread 0 waits for the bulk loads and starts the tile-only MMAs; everyone else converts inputs
+    // meanwhile (the barrier after the conversion orders their later reads after that wait)
+    const bool loaded = tid == 0 ? tc::mbar_wait(&S.lbar, 0, K4T_WAIT_LIMIT) : true;
     const uint32_t tm = S.tslot;
     const uint32_t sQ = smem_u32(S.Q), sK = smem_u32(S.K), sV = smem_u32(S.V), sD = smem_u32(S.D);
     const uint32_t sVn = smem_u32(S.Vn), sdVn = smem_u32(S.dVn), sH = smem_u32(S.H), sdH = smem_u32(S.dH);
@@ -138,17 +90,18 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     unsigned char *Xs = S.Pm, *Es = S.dT;
     const uint32_t sX = sPm, sE = sdT;
     // phase 1, part 1: products of workspace tiles only, overlapping the input conversion below
-    if (tid == 0) {
-        tc::gemm(tm + R_DKSC, sdH, DT, true, sVn, DT, false, 128, 64, DT, false);
-        tc::gemm(tm + R_DWT, sH, DT, true, sdVn, DT, false, 128, 64, DT, false);
-        tc::gemm(tm + R_TDU, sdVn, DT, true, sT, CT, true, 128, 64, CT, false);
+    if (tid == 0 && loaded) {
+        tc::gemm(tm + R_DKSC, sdH, DT, true, sVn, CT, true, 128, 64, DT, false);
+        tc::gemm(tm + R_DWT, sH, DT, true, sdVn, CT, true, 128, 64, DT, false);
+        tc::gemm(tm + R_TDU, sdVn, CT, false, sT, CT, true, 128, 64, CT, false);
     }
     const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    const Tin *dop = reinterpret_cast<const Tin *>(P.dO) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    stage_in_pair(S.K, kp, (size_t)P.Hk * P.K, P.K, 1.f, S.Q, qp, (size_t)P.Hk * P.K, P.K, 1.f, len, tid);
-    stage_in_pair(S.V, vp, (size_t)P.Hv * P.V, P.V, 1.f, S.D, dop, (size_t)P.Hv * P.V, P.V, P.scale, len, tid);
+    stage_ct_pair<Tin, K4T_THREADS>(S.K, kp, (size_t)P.Hk * P.K, P.K, 1.f, S.Q, qp, (size_t)P.Hk * P.K, P.K, 1.f, len,
+                                    tid);
+    stage_ct_pair<Tin, K4T_THREADS>(S.V, vp, (size_t)P.Hv * P.V, P.V, 1.f, S.V, vp, (size_t)P.Hv * P.V, P.V, 1.f, len,
+                                    tid);
     if (tid < CT) {
         S.G[tid] = expf(S.gam[tid]);
         S.GC[tid] = expf(S.gam[rl] - S.gam[tid]);
@@ -158,14 +111,14 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     __syncthreads();
     tc::fence_after();
     uint32_t parity = 0;
-    bool lost = false;
+    bool lost = __syncthreads_or(!loaded) != 0;
 
     // Each phase: one thread issues, everyone waits (bounded) and agrees on the outcome.
     auto finish_phase = [&]() {
         if (tid == 0) tc::commit(&S.bar);
         bool ok = tc::mbar_wait(&S.bar, parity, K4T_WAIT_LIMIT);
         parity ^= 1u;
-        lost = __syncthreads_or(!ok) != 0;
+        lost = __syncthreads_or(!ok || lost) != 0;
         tc::fence_after();
     };
     auto publish_tiles = [&]() {  // make epilogue-written tiles visible to the next phase's MMAs
@@ -186,10 +139,10 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     for (int t = 0; t < 32; ++t) kreg[t] = tc::ld_tile(S.K, c0 + t, k, DT);
 
     // ---------------- phase 1, part 2 (needs the converted inputs)
-    if (tid == 0) {
-        tc::gemm(tm + C_G1, sD, DT, false, sVn, DT, false, 64, 64, DT, false);
+    if (tid == 0 && !lost) {
+        tc::gemm(tm + C_G1, sD, DT, false, sVn, CT, true, 64, 64, DT, false);
         tc::gemm(tm + R_DQI, sH, DT, true, sD, DT, false, 128, 64, DT, false);
-        tc::gemm(tm + C_DT2, sdVn, DT, false, sV, DT, false, 64, 64, DT, false);
+        tc::gemm(tm + C_DT2, sdVn, CT, true, sV, DT, false, 64, 64, DT, false);
         tc::gemm(tm + C_KK, sK, DT, false, sK, DT, false, 64, 64, DT, false);
     }
     finish_phase();
@@ -210,15 +163,10 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                 tc::st_tile8(S.Pm, r64, c0 + j8, CT, x);
             }
         }
-        // dW^T -> dWT tile (negated)
+        // dW^T -> dWT tile (the stored dV tile is negated, so the product already is dW^T)
         tc::ld32(tc::taddr(tm, R_DWT + c0), g);
 #pragma unroll
-        for (int j8 = 0; j8 < 32; j8 += 8) {
-            float x[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) x[t] = -g[j8 + t];
-            tc::st_tile8(S.dWT, k, c0 + j8, CT, x);
-        }
+        for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.dWT, k, c0 + j8, CT, g + j8);
         // dk_SC = exp(gamma_C - gamma_j) (V_new dS)_j
         tc::ld32(tc::taddr(tm, R_DKSC + c0), g);
 #pragma unroll
@@ -231,6 +179,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         }
         // TdU^T -> dv (coalesced over the feature index), dbeta += rowsum(TdU (.) V)
         tc::ld32(tc::taddr(tm, R_TDU + c0), g);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) g[t] = -g[t];  // negated dV tile
         {
             float db[32];
 #pragma unroll
@@ -300,7 +250,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     int j = c0 + j8 + t;
-                    x[t] = S.beta[j] * (S.G[j] * a[j8 + t] + b[j8 + t]);
+                    x[t] = S.beta[j] * (S.G[j] * a[j8 + t] - b[j8 + t]);  // dT2 came negated
                 }
                 tc::st_tile8(S.dT, r64, c0 + j8, CT, x);
             }
