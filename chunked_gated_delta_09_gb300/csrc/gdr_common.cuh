@@ -372,6 +372,42 @@ __device__ __forceinline__ void stage_ct_pair(unsigned char *t0, const Tin *s0, 
         }
 }
 
+// Single-block version of stage_ct_pair.
+template <typename Tin, int NTHR>
+__device__ __forceinline__ void stage_ct_one(unsigned char *t0, const Tin *s0, size_t st0, int nc0, float m0, int nrows,
+                                             int tid) {
+    constexpr int PER = CT * (DT / 8) / NTHR;
+    const int wid = tid >> 5, lane = tid & 31;
+    float x[PER][8];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        int it = wid + (NTHR / 32) * i;
+        int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
+        if (r < nrows && c8 + 8 <= nc0) {
+            load8(s0 + (size_t)r * st0 + c8, x[i]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        int it = wid + (NTHR / 32) * i;
+        int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[i][j] *= m0;
+        *reinterpret_cast<uint4 *>(t0 + ctile_off(r, c8, DT)) = pack8_half(x[i]);
+    }
+}
+
+// Store two adjacent values (columns c, c+1) of an output row in the output dtype.
+__device__ __forceinline__ void store_pair(void *p, size_t i, float a, float b, int dt) {
+    if (dt == F32) *reinterpret_cast<float2 *>(reinterpret_cast<float *>(p) + i) = make_float2(a, b);
+    else if (dt == BF16)
+        *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(p) + i) = __floats2bfloat162_rn(a, b);
+    else *reinterpret_cast<__half2 *>(reinterpret_cast<__half *>(p) + i) = __floats2half2_rn(a, b);
+}
+
 template <int MT, int NT>
 __device__ __forceinline__ void zero_acc(float (&acc)[MT][NT][4]) {
 #pragma unroll

@@ -11,8 +11,9 @@
 // K~ = K (.) exp(gamma_C - gamma) and Q~ = Q (.) exp(gamma) that the two scans use, and D = scale dO.
 // Per-channel gate: each exp(gamma_a - gamma_b) is taken per key channel inside the K contraction.
 //
-// Every matrix output is built in shared memory in the core-matrix tile layout that the tensor-core
-// kernels read, and leaves with one bulk copy per tile.
+// Every matrix output is written in the core-matrix tile layout that the tensor-core kernels read:
+// element-wise outputs straight from registers (8 lanes write one contiguous 128-byte core matrix),
+// matrix products through shared memory and one bulk copy per tile.
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
 #include "tc_util.cuh"
@@ -22,8 +23,8 @@ namespace gdr {
 constexpr int K1_THREADS = 256;
 
 struct __align__(1024) K1Smem {
-    unsigned char Ks[CT * DT * 2], Qs[CT * DT * 2], Vs[CT * DT * 2];  // Qs later holds beta Gamma K, Vs beta V
-    unsigned char oKt[CT * DT * 2], oQg[CT * DT * 2], oD[CT * DT * 2], oW[CT * DT * 2], oU[CT * DT * 2];
+    // Ks later holds W, Qs holds beta Gamma K then U, Vs holds beta V
+    unsigned char Ks[CT * DT * 2], Qs[CT * DT * 2], Vs[CT * DT * 2];
     unsigned char oT[CT * CT * 2], oAqk[CT * CT * 2];
     float A32[CT][CT + 1];
     float T32[CT][CT + 1];
@@ -32,8 +33,36 @@ struct __align__(1024) K1Smem {
     float beta[CT];
 };
 
+// Convert a strided [rows][cols] input block to an fp16 [CT][DT] tile written straight to global memory.
+template <typename Tin>
+__device__ __forceinline__ void stage_ct_global(__half *dst, const Tin *src, size_t stride, int ncols, float mul,
+                                                int nrows, int tid) {
+    constexpr int PER = CT * (DT / 8) / K1_THREADS;
+    const int wid = tid >> 5, lane = tid & 31;
+    float x[PER][8];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        int it = wid + (K1_THREADS / 32) * i;
+        int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
+        if (r < nrows && c8 + 8 <= ncols) {
+            load8(src + (size_t)r * stride + c8, x[i]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        int it = wid + (K1_THREADS / 32) * i;
+        int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[i][j] *= mul;
+        *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(dst) + ctile_off(r, c8, DT)) = pack8_half(x[i]);
+    }
+}
+
 template <typename Tin, bool PC>
-__global__ void __launch_bounds__(K1_THREADS, 1) k1_wy_prep(const Params P) {
+__global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Params P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     K1Smem &S = *reinterpret_cast<K1Smem *>(smem_raw);
     float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K1Smem));  // [CT][DT], per-channel only
@@ -53,8 +82,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_wy_prep(const Params P) {
     const Tin *dop = reinterpret_cast<const Tin *>(P.dO) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
     stage_ct_pair<Tin, K1_THREADS>(S.Ks, kp, (size_t)P.Hk * P.K, P.K, 1.f, S.Qs, qp, (size_t)P.Hk * P.K, P.K, 1.f, len,
                                    tid);
-    stage_ct_pair<Tin, K1_THREADS>(S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, S.oD, dop, (size_t)P.Hv * P.V, P.V, P.scale,
-                                   len, tid);
+    stage_ct_one<Tin, K1_THREADS>(S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, len, tid);
+    stage_ct_global(P.Dt + u * CT * DT, dop, (size_t)P.Hv * P.V, P.V, P.scale, len, tid);
 
     // ---- beta, gate cumsum
     if (tid < CT) S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
@@ -125,13 +154,15 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_wy_prep(const Params P) {
     }
     __syncthreads();
 
-    // ---- decayed copies of K and Q; W and U operands (beta Gamma K over Q's tile, beta V in place)
+    // ---- decayed copies of K and Q (to global); W and U operands (beta Gamma K over Q's tile, beta V)
     {
         const float gC = PC ? 0.f : S.gam[len - 1];
+        unsigned char *Ktg = reinterpret_cast<unsigned char *>(P.Kt + u * CT * DT);
+        unsigned char *Qgg = reinterpret_cast<unsigned char *>(P.Qg + u * CT * DT);
         for (int e = tid; e < CT * DT / 8; e += K1_THREADS) {
-            // 8 consecutive columns of one row (one 16-byte core-matrix row segment)
-            int i = e / (DT / 8), c8 = (e % (DT / 8)) * 8;
-            uint32_t off = ctile_off(i, c8, DT);
+            // one 16-byte core-matrix row segment; consecutive lanes walk the 8 rows of a core matrix
+            const int blk = e >> 3, i = 8 * (blk / (DT / 8)) + (e & 7), c8 = 8 * (blk % (DT / 8));
+            const uint32_t off = ctile_off(i, c8, DT);
             float kx[8], qx[8], vx[8], o1[8], o2[8], o3[8], o4[8];
             const __half2 *k2 = reinterpret_cast<const __half2 *>(S.Ks + off);
             const __half2 *q2 = reinterpret_cast<const __half2 *>(S.Qs + off);
@@ -154,8 +185,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_wy_prep(const Params P) {
                 o3[t] = bi * Gi * kx[t];        // beta Gamma K
                 o4[t] = bi * vx[t];             // beta V
             }
-            tc::st_tile8(S.oKt, i, c8, DT, o1);
-            tc::st_tile8(S.oQg, i, c8, DT, o2);
+            *reinterpret_cast<uint4 *>(Ktg + off) = pack8_half(o1);
+            *reinterpret_cast<uint4 *>(Qgg + off) = pack8_half(o2);
             tc::st_tile8(S.Qs, i, c8, DT, o3);
             tc::st_tile8(S.Vs, i, c8, DT, o4);
         }
@@ -202,7 +233,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_wy_prep(const Params P) {
     }
     __syncthreads();
 
-    // ---- W = T (beta Gamma K), U = T (beta V)
+    // ---- W = T (beta Gamma K) into K's tile, then U = T (beta V) into Q's tile
     {
         const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 64;
         float acc[1][8][4];
@@ -210,7 +241,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_wy_prep(const Params P) {
         for (int w = 0; w < 2; ++w) {
             zero_acc(acc);
             warp_mma_ct<1, 8, false, false>(acc, S.oT, CT, w ? S.Vs : S.Qs, DT, m0, n0, CT);
-            unsigned char *dst = w ? S.oU : S.oW;
+            if (w) __syncthreads();  // every warp finished reading beta Gamma K before U overwrites it
+            unsigned char *dst = w ? S.Qs : S.Ks;
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -221,17 +253,14 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_wy_prep(const Params P) {
                 }
         }
     }
-    // ---- bulk stores of every tile
+    // ---- bulk stores of the product tiles
     tc::fence_smem_to_async();
     __syncthreads();
     if (tid == 0) {
         tc::bulk_s2g(P.Tm + u * CT * CT, S.oT, CT * CT * 2);
         tc::bulk_s2g(P.Aqk + u * CT * CT, S.oAqk, CT * CT * 2);
-        tc::bulk_s2g(P.W + u * CT * DT, S.oW, CT * DT * 2);
-        tc::bulk_s2g(P.U + u * CT * DT, S.oU, CT * DT * 2);
-        tc::bulk_s2g(P.Kt + u * CT * DT, S.oKt, CT * DT * 2);
-        tc::bulk_s2g(P.Qg + u * CT * DT, S.oQg, CT * DT * 2);
-        tc::bulk_s2g(P.Dt + u * CT * DT, S.oD, CT * DT * 2);
+        tc::bulk_s2g(P.W + u * CT * DT, S.Ks, CT * DT * 2);
+        tc::bulk_s2g(P.U + u * CT * DT, S.Qs, CT * DT * 2);
         tc::bulk_commit();
         tc::bulk_wait();
     }

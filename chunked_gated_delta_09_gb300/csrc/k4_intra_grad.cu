@@ -37,6 +37,7 @@ struct __align__(1024) K4Smem {
     unsigned char Hs[DT * DT * 2], dHs[DT * DT * 2];    // [v][k]
     unsigned char Ts[CT * CT * 2], Pms[CT * CT * 2];
     float gam[CT];
+    float G[CT], GC[CT];  // exp(gamma), exp(gamma_C - gamma) (scalar gate)
     float beta[CT];
     float dbeta[CT];
     float dgrow[CT];
@@ -44,15 +45,15 @@ struct __align__(1024) K4Smem {
     uint64_t lbar;
 };
 
-// Store 32 accumulator elements (C x K tile of this warp) as an output gradient row block.
+// Store 32 accumulator elements (C x K tile of this warp) as an output gradient row block (column pairs).
 __device__ __forceinline__ void store_ck(const float (&a)[1][8][4], int m0, int n0, int len, int ncols, void *base,
                                          size_t row_stride, int dt) {
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-            if (r < len && c < ncols) store_scalar(base, (size_t)r * row_stride + c, a[0][nt][e], dt);
+        for (int e = 0; e < 4; e += 2) {
+            int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);  // c is even and ncols a multiple of 8
+            if (r < len && c < ncols) store_pair(base, (size_t)r * row_stride + c, a[0][nt][e], a[0][nt][e + 1], dt);
         }
 }
 
@@ -91,10 +92,9 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    stage_ct_pair<Tin, K4_THREADS>(S.Ks, kp, (size_t)P.Hk * P.K, P.K, 1.f, S.Qs, qp, (size_t)P.Hk * P.K, P.K, 1.f, len,
-                                   tid);
-    stage_ct_pair<Tin, K4_THREADS>(S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, len,
-                                   tid);
+    stage_ct_one<Tin, K4_THREADS>(S.Ks, kp, (size_t)P.Hk * P.K, P.K, 1.f, len, tid);
+    stage_ct_one<Tin, K4_THREADS>(S.Qs, qp, (size_t)P.Hk * P.K, P.K, 1.f, len, tid);
+    stage_ct_one<Tin, K4_THREADS>(S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, len, tid);
     if (tid < CT) {
         S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
         S.dbeta[tid] = 0.f;
@@ -105,6 +105,10 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     if (PC)
         for (int e = tid; e < CT * DT; e += K4_THREADS) gamK[e] = P.gam[u * CT * DT + e];
     __syncthreads();  // barrier initialised
+    if (!PC && tid < CT) {
+        S.G[tid] = expf(S.gam[tid]);
+        S.GC[tid] = expf(S.gam[len - 1] - S.gam[tid]);
+    }
     const bool loaded = tc::mbar_wait(&S.lbar, 0, K4_WAIT_LIMIT);
     if (__syncthreads_or(!loaded)) {
         if (tid == 0) flag_status(P.status, ST_TIMEOUT);
@@ -136,9 +140,15 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     }
     __syncthreads();
 
-    float dgam[1][8][4];  // per-element gate-gradient contributions (rows x channels of this warp's tile)
+    // gate-gradient contributions: per element for the per-channel gate, per row for the scalar gate
+    float dgam[1][PC ? 8 : 1][4];
+    float rsg[2] = {0.f, 0.f};
     float dk[1][8][4];
     zero_acc(dgam);
+    auto add_dg = [&](int nt, int e, float x) {
+        if (PC) dgam[0][PC ? nt : 0][e] += x;
+        else rsg[e >> 1] += x;
+    };
     // ---- S2: dq = Gamma (.) (D S_0) + P K   [per-channel: decayed sum per element]
     {
         float dq[1][8][4];
@@ -147,7 +157,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dq[0][nt][e] *= expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e)));
+            for (int e = 0; e < 4; ++e)
+                dq[0][nt][e] *= PC ? expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e))) : S.G[acc_row(m0, 0, e)];
         if (!PC) {
             warp_mma_ct<1, 8, false, false>(dq, S.Pms, CT, S.Ks, DT, m0, n0, CT);
         } else {
@@ -167,7 +178,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                dgam[0][nt][e] += ctile_get(S.Qs, r, c, DT) * dq[0][nt][e];
+                add_dg(nt, e, ctile_get(S.Qs, r, c, DT) * dq[0][nt][e]);
             }
         if (P.G == 1)
             store_ck(dq, m0, n0, len, P.K, reinterpret_cast<char *>(P.dq) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
@@ -197,7 +208,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                dgam[0][nt][e] -= Kv(r, c) * dk[0][nt][e];
+                add_dg(nt, e, -(Kv(r, c) * dk[0][nt][e]));
             }
     }
     __syncthreads();  // Ds, Pms, Qs free
@@ -213,10 +224,10 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                float x = t[0][nt][e] * expf(G_(rl, c) - G_(r, c));
+                float x = t[0][nt][e] * (PC ? expf(G_(rl, c) - G_(r, c)) : S.GC[r]);
                 float kx = Kv(r, c) * x;
                 dk[0][nt][e] += x;
-                dgam[0][nt][e] -= kx;
+                add_dg(nt, e, -(kx));
                 if (PC) atomicAdd(&S.lastrow[c], kx);
                 else part += kx;
             }
@@ -226,13 +237,34 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
             if (lane == 0) atomicAdd(&S.lastrow[0], s);
         }
-        // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate)
-        for (int c = tid; c < DT; c += K4_THREADS) {
-            float s = 0.f;
-            for (int v = 0; v < DT; ++v) s += ctile_get(S.Hs, v, c, DT) * ctile_get(S.dHs, v, c, DT);
-            s *= expf(G_(rl, c));
-            if (PC) atomicAdd(&S.lastrow[c], s);
-            else atomicAdd(&S.lastrow[0], s);
+        // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate): every thread takes
+        // one 8-column chunk of 8 rows (16-byte reads; the same column chunk for all of its rows)
+        {
+            const int c8 = 8 * (tid & 15), v0 = 8 * (tid >> 4);
+            float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int v = v0; v < v0 + 8; ++v) {
+                const uint32_t off = ctile_off(v, c8, DT);
+                const __half2 *a2 = reinterpret_cast<const __half2 *>(S.Hs + off);
+                const __half2 *b2 = reinterpret_cast<const __half2 *>(S.dHs + off);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    float2 a = __half22float2(a2[t]), b = __half22float2(b2[t]);
+                    acc8[2 * t] += a.x * b.x;
+                    acc8[2 * t + 1] += a.y * b.y;
+                }
+            }
+            if (PC) {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) atomicAdd(&S.lastrow[c8 + t], acc8[t] * expf(G_(rl, c8 + t)));
+            } else {
+                float s = 0.f;
+#pragma unroll
+                for (int t = 0; t < 8; ++t) s += acc8[t];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                if (lane == 0) atomicAdd(&S.lastrow[0], s * expf(S.gam[rl]));
+            }
         }
     }
     // ---- S5: dW = -dV_new S_0 (the stored tile is -dV_new^T)  -> dWs;  per-channel: beta Gamma K -> KGb
@@ -268,7 +300,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
-                float x = (PC ? a[0][nt][e] : a[0][nt][e] * S.beta[j] * expf(S.gam[j])) - b[0][nt][e] * S.beta[j];
+                float x = (PC ? a[0][nt][e] : a[0][nt][e] * S.beta[j] * S.G[j]) - b[0][nt][e] * S.beta[j];
                 ctile_set(dTs, r, j, CT, x);
             }
     }
@@ -283,11 +315,11 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                float Gm = expf(G_(r, c));
+                float Gm = PC ? expf(G_(r, c)) : S.G[r];
                 float kv = Kv(r, c);
                 float x = S.beta[r] * Gm * t[0][nt][e];
                 dk[0][nt][e] += x;
-                dgam[0][nt][e] += kv * x;
+                add_dg(nt, e, kv * x);
                 rowb[e >> 1] += t[0][nt][e] * kv * Gm;
             }
     }
@@ -399,7 +431,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                 float kv = Kv(r, c);
                 dk[0][nt][e] += a[0][nt][e] + b[0][nt][e];
-                dgam[0][nt][e] += kv * (a[0][nt][e] - b[0][nt][e]);
+                add_dg(nt, e, kv * (a[0][nt][e] - b[0][nt][e]));
             }
     }
     // ---- dk out
@@ -411,14 +443,9 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 
     // ---- gate gradient of the cumulative gate
     if (!PC) {
-        float rs[2] = {0.f, 0.f};
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) rs[e >> 1] += dgam[0][nt][e];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            float s = rs[h];
+            float s = rsg[h];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
             if ((lane & 3) == 0) atomicAdd(&S.dgrow[m0 + (lane >> 2) + 8 * h], s);
@@ -436,7 +463,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                float x = dgam[0][nt][e] + (r == rl ? S.lastrow[c] : 0.f);
+                float x = dgam[0][PC ? nt : 0][e] + (r == rl ? S.lastrow[c] : 0.f);
                 P.dgam[(u * CT + r) * DT + c] = r < len ? x : 0.f;
             }
         if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = S.dbeta[tid];

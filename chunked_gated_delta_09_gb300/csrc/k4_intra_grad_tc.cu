@@ -100,8 +100,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
     stage_ct_pair<Tin, K4T_THREADS>(S.K, kp, (size_t)P.Hk * P.K, P.K, 1.f, S.Q, qp, (size_t)P.Hk * P.K, P.K, 1.f, len,
                                     tid);
-    stage_ct_pair<Tin, K4T_THREADS>(S.V, vp, (size_t)P.Hv * P.V, P.V, 1.f, S.V, vp, (size_t)P.Hv * P.V, P.V, 1.f, len,
-                                    tid);
+    stage_ct_one<Tin, K4T_THREADS>(S.V, vp, (size_t)P.Hv * P.V, P.V, 1.f, len, tid);
     if (tid < CT) {
         S.G[tid] = expf(S.gam[tid]);
         S.GC[tid] = expf(S.gam[rl] - S.gam[tid]);
