@@ -39,9 +39,11 @@ struct __align__(1024) K4Smem {
     float gam[CT];
     float G[CT], GC[CT];  // exp(gamma), exp(gamma_C - gamma) (scalar gate)
     float beta[CT];
-    float dbeta[CT];
-    float dgrow[CT];
-    float lastrow[DT];
+    // partial sums in fixed slots, added in a fixed order (results do not depend on warp timing)
+    float dbp[4][CT];    // dbeta: [0..1] from dA (by column half), [2..3] from T^T dW / T^T dV_new (by K half)
+    float dgp[2][CT];    // scalar gate: per-row gate-gradient sums by K half
+    float lrs[16];       // scalar gate: last-row terms, [w] from dk_SC and [8 + w] from <S_0, dS_next>
+    float lrp[12][DT];   // per-channel gate: last-row terms, [0..3] from dk_SC (by row block), [4 + w] from S_0
     uint64_t lbar;
 };
 
@@ -97,11 +99,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     stage_ct_one<Tin, K4_THREADS>(S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, len, tid);
     if (tid < CT) {
         S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
-        S.dbeta[tid] = 0.f;
-        S.dgrow[tid] = 0.f;
         if (!PC) S.gam[tid] = P.gam[u * CT + tid];
     }
-    if (tid < DT) S.lastrow[tid] = 0.f;
     if (PC)
         for (int e = tid; e < CT * DT; e += K4_THREADS) gamK[e] = P.gam[u * CT * DT + e];
     __syncthreads();  // barrier initialised
@@ -122,6 +121,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     auto G_ = [&](int r, int c) -> float { return PC ? gamK[r * DT + c] : S.gam[r]; };
     auto Kv = [&](int r, int c) -> float { return ctile_get(S.Ks, r, c, DT); };
     const int rl = len - 1;
+    auto row_dbeta = [&](int r) -> float { return (S.dbp[0][r] + S.dbp[1][r]) + (S.dbp[2][r] + S.dbp[3][r]); };
 
     // ---- S1: P = (D V_new^T) (.) causal mask (.) [scalar: decay]
     {
@@ -218,7 +218,9 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         float t[1][8][4];
         zero_acc(t);
         warp_mma_ct<1, 8, true, false>(t, S.VnT, CT, S.dHs, DT, m0, n0, DT);
-        float part = 0.f;
+        float part = 0.f, colp[PC ? 8 : 1][2];
+#pragma unroll
+        for (int nt = 0; nt < (PC ? 8 : 1); ++nt) colp[nt][0] = colp[nt][1] = 0.f;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -228,14 +230,26 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 float kx = Kv(r, c) * x;
                 dk[0][nt][e] += x;
                 add_dg(nt, e, -(kx));
-                if (PC) atomicAdd(&S.lastrow[c], kx);
+                if (PC) colp[PC ? nt : 0][e & 1] += kx;
                 else part += kx;
             }
         if (!PC) {
             float s = part;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0) atomicAdd(&S.lastrow[0], s);
+            if (lane == 0) S.lrs[wid] = s;
+        } else {
+            // column sums over the warp's 16 rows: lanes that differ in lane / 4 share columns
+#pragma unroll
+            for (int nt = 0; nt < (PC ? 8 : 1); ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float s = colp[nt][h];
+                    s += __shfl_xor_sync(0xffffffffu, s, 4);
+                    s += __shfl_xor_sync(0xffffffffu, s, 8);
+                    s += __shfl_xor_sync(0xffffffffu, s, 16);
+                    if (lane < 4) S.lrp[wid & 3][acc_col(n0, nt, h)] = s;
+                }
         }
         // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate): every thread takes
         // one 8-column chunk of 8 rows (16-byte reads; the same column chunk for all of its rows)
@@ -255,15 +269,19 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 }
             }
             if (PC) {
+                // lanes l and l + 16 hold the same column chunk
 #pragma unroll
-                for (int t = 0; t < 8; ++t) atomicAdd(&S.lastrow[c8 + t], acc8[t] * expf(G_(rl, c8 + t)));
+                for (int t = 0; t < 8; ++t) {
+                    float s = acc8[t] + __shfl_xor_sync(0xffffffffu, acc8[t], 16);
+                    if (lane < 16) S.lrp[4 + wid][c8 + t] = s * expf(G_(rl, c8 + t));
+                }
             } else {
                 float s = 0.f;
 #pragma unroll
                 for (int t = 0; t < 8; ++t) s += acc8[t];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0) atomicAdd(&S.lastrow[0], s * expf(S.gam[rl]));
+                if (lane == 0) S.lrs[8 + wid] = s * expf(S.gam[rl]);
             }
         }
     }
@@ -390,7 +408,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             float s = rb[h];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if ((lane & 3) == 0) atomicAdd(&S.dbeta[cm0 + (lane >> 2) + 8 * h], s);
+            if ((lane & 3) == 0) S.dbp[wid >> 2][cm0 + (lane >> 2) + 8 * h] = s;
         }
     }
 #pragma unroll
@@ -398,7 +416,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         float s = rowb[h];
         s += __shfl_xor_sync(0xffffffffu, s, 1);
         s += __shfl_xor_sync(0xffffffffu, s, 2);
-        if ((lane & 3) == 0) atomicAdd(&S.dbeta[m0 + (lane >> 2) + 8 * h], s);
+        if ((lane & 3) == 0) S.dbp[2 + (wid >> 2)][m0 + (lane >> 2) + 8 * h] = s;
     }
     __syncthreads();
     // ---- S11: dk_Ar = E K (+), dk_Ac = E^T K (-)
@@ -448,13 +466,19 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             float s = rsg[h];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if ((lane & 3) == 0) atomicAdd(&S.dgrow[m0 + (lane >> 2) + 8 * h], s);
+            if ((lane & 3) == 0) S.dgp[wid >> 2][m0 + (lane >> 2) + 8 * h] = s;
         }
         __syncthreads();
         if (tid < CT) {
-            float x = S.dgrow[tid] + (tid == rl ? S.lastrow[0] : 0.f);
+            float x = S.dgp[0][tid] + S.dgp[1][tid];
+            if (tid == rl) {
+                float l = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) l += S.lrs[i];
+                x += l;
+            }
             P.dgam[u * CT + tid] = tid < len ? x : 0.f;
-            if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = S.dbeta[tid];
+            if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = row_dbeta(tid);
         }
     } else {
         __syncthreads();
@@ -463,10 +487,16 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                float x = dgam[0][PC ? nt : 0][e] + (r == rl ? S.lastrow[c] : 0.f);
+                float x = dgam[0][PC ? nt : 0][e];
+                if (r == rl) {
+                    float l = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 12; ++i) l += S.lrp[i][c];
+                    x += l;
+                }
                 P.dgam[(u * CT + r) * DT + c] = r < len ? x : 0.f;
             }
-        if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = S.dbeta[tid];
+        if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = row_dbeta(tid);
     }
 }
 

@@ -332,7 +332,21 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         S.dg_q[q][c0 + lane] = tc::warp_transpose_sum32(dg);
         // last row: Gamma_C <S_0, dS_next> (this warp's half of the v range) + sum_j k_j (.) dk_SC_j
         float hd = 0.f;
-        for (int v = 2 * c0; v < 2 * c0 + 64; ++v) hd += tc::ld_tile(S.H, v, k, DT) * tc::ld_tile(S.dH, v, k, DT);
+        {
+            // <S_0, dS_next> over the whole tile: every thread one 8-column chunk of 8 rows (16-byte reads)
+            const int cc8 = 8 * (tid & 15), v0 = 8 * (tid >> 4);
+#pragma unroll
+            for (int v = v0; v < v0 + 8; ++v) {
+                const uint32_t off = tc::tile_off(v, cc8, DT);
+                const __half2 *a2 = reinterpret_cast<const __half2 *>(S.H + off);
+                const __half2 *b2 = reinterpret_cast<const __half2 *>(S.dH + off);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    float2 a = __half22float2(a2[t]), b = __half22float2(b2[t]);
+                    hd += a.x * b.x + a.y * b.y;
+                }
+            }
+        }
         float tot = lastpart + S.G[rl] * hd;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);

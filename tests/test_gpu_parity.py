@@ -57,6 +57,16 @@ def test_varlen_single_sequence_equals_dense():
         assert (a[key] == b[key]).all(), key
 
 
+@pytest.mark.parametrize("per_channel", [False, True], ids=["scalar", "kda"])
+def test_run_to_run_bit_identical(per_channel):
+    """Every reduction sums in a fixed order: two runs of one problem give the same bits."""
+    prob = make_problem("repeat", Hk=2, Hv=4, K=128, V=128, per_channel=per_channel,
+                        seq_lens=[700, 33, 190], seed=91)
+    a, b = run_gpu(prob), run_gpu(prob)
+    for key in a:
+        assert (a[key] == b[key]).all(), key
+
+
 @pytest.mark.parametrize("name", ["tiny_fp32", "kda_t2k_fp16", "gdn_t8k_bf16"])
 def test_workload_full(name):
     prob = workload(name)
