@@ -28,7 +28,10 @@
 
 namespace gdr {
 
-constexpr int K4_THREADS = 256;
+constexpr int K4_THREADS = 512;
+// warp tiling: 16 warps, four row blocks of 16 rows x four column blocks
+constexpr int NK = 4;  // C x K tiles: 16 x 32 per warp (four n8 tiles)
+constexpr int NC = 2;  // C x C tiles: 16 x 16 per warp (two n8 tiles)
 constexpr uint32_t K4_WAIT_LIMIT = 1u << 24;
 
 struct __align__(1024) K4Smem {
@@ -40,18 +43,19 @@ struct __align__(1024) K4Smem {
     float G[CT], GC[CT];  // exp(gamma), exp(gamma_C - gamma) (scalar gate)
     float beta[CT];
     // partial sums in fixed slots, added in a fixed order (results do not depend on warp timing)
-    float dbp[4][CT];    // dbeta: [0..1] from dA (by column half), [2..3] from T^T dW / T^T dV_new (by K half)
-    float dgp[2][CT];    // scalar gate: per-row gate-gradient sums by K half
-    float lrs[16];       // scalar gate: last-row terms, [w] from dk_SC and [8 + w] from <S_0, dS_next>
+    float dbp[8][CT];    // dbeta: [0..3] from dA (by column block), [4..7] from T^T dW / T^T dV_new (by K block)
+    float dgp[4][CT];    // scalar gate: per-row gate-gradient sums by K block
+    float lrs[24];       // scalar gate: last-row terms, [w] from dk_SC and [16 + w] from <S_0, dS_next>
     float lrp[12][DT];   // per-channel gate: last-row terms, [0..3] from dk_SC (by row block), [4 + w] from S_0
     uint64_t lbar;
 };
 
-// Store 32 accumulator elements (C x K tile of this warp) as an output gradient row block (column pairs).
-__device__ __forceinline__ void store_ck(const float (&a)[1][8][4], int m0, int n0, int len, int ncols, void *base,
+// Store a warp's accumulator tile (16 rows x 8 NT columns of a C x K block) as an output gradient row block (column pairs).
+template <int NT>
+__device__ __forceinline__ void store_ck(const float (&a)[1][NT][4], int m0, int n0, int len, int ncols, void *base,
                                          size_t row_stride, int dt) {
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; e += 2) {
             int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);  // c is even and ncols a multiple of 8
@@ -114,22 +118,27 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         return;
     }
 
-    // C x K tiling: warp w owns rows m0 .. m0+15 and columns n0 .. n0+63
-    const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 64;
-    // C x C tiling: rows cm0 .. cm0+15, columns cn0 .. cn0+31
-    const int cm0 = (wid & 3) * 16, cn0 = (wid >> 2) * 32;
+    // C x K tiling: warp w owns rows m0 .. m0+15 and columns n0 .. n0+31
+    const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * (NK * 8);
+    // C x C tiling: rows cm0 .. cm0+15, columns cn0 .. cn0+15
+    const int cm0 = (wid & 3) * 16, cn0 = (wid >> 2) * (NC * 8);
     auto G_ = [&](int r, int c) -> float { return PC ? gamK[r * DT + c] : S.gam[r]; };
     auto Kv = [&](int r, int c) -> float { return ctile_get(S.Ks, r, c, DT); };
     const int rl = len - 1;
-    auto row_dbeta = [&](int r) -> float { return (S.dbp[0][r] + S.dbp[1][r]) + (S.dbp[2][r] + S.dbp[3][r]); };
+    auto row_dbeta = [&](int r) -> float {
+        float x = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x += S.dbp[i][r];
+        return x;
+    };
 
     // ---- S1: P = (D V_new^T) (.) causal mask (.) [scalar: decay]
     {
-        float g1[1][4][4];
+        float g1[1][NC][4];
         zero_acc(g1);
-        warp_mma_ct<1, 4, false, false>(g1, S.Ds, DT, S.VnT, CT, cm0, cn0, DT);
+        warp_mma_ct<1, NC, false, false>(g1, S.Ds, DT, S.VnT, CT, cm0, cn0, DT);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < NC; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
@@ -141,9 +150,9 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     __syncthreads();
 
     // gate-gradient contributions: per element for the per-channel gate, per row for the scalar gate
-    float dgam[1][PC ? 8 : 1][4];
+    float dgam[1][PC ? NK : 1][4];
     float rsg[2] = {0.f, 0.f};
-    float dk[1][8][4];
+    float dk[1][NK][4];
     zero_acc(dgam);
     auto add_dg = [&](int nt, int e, float x) {
         if (PC) dgam[0][PC ? nt : 0][e] += x;
@@ -151,19 +160,19 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     };
     // ---- S2: dq = Gamma (.) (D S_0) + P K   [per-channel: decayed sum per element]
     {
-        float dq[1][8][4];
+        float dq[1][NK][4];
         zero_acc(dq);
-        warp_mma_ct<1, 8, false, false>(dq, S.Ds, DT, S.Hs, DT, m0, n0, DT);
+        warp_mma_ct<1, NK, false, false>(dq, S.Ds, DT, S.Hs, DT, m0, n0, DT);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 dq[0][nt][e] *= PC ? expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e))) : S.G[acc_row(m0, 0, e)];
         if (!PC) {
-            warp_mma_ct<1, 8, false, false>(dq, S.Pms, CT, S.Ks, DT, m0, n0, CT);
+            warp_mma_ct<1, NK, false, false>(dq, S.Pms, CT, S.Ks, DT, m0, n0, CT);
         } else {
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
@@ -174,7 +183,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 }
         }
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
@@ -190,10 +199,10 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     {
         zero_acc(dk);
         if (!PC) {
-            warp_mma_ct<1, 8, true, false>(dk, S.Pms, CT, S.Qs, DT, m0, n0, CT);
+            warp_mma_ct<1, NK, true, false>(dk, S.Pms, CT, S.Qs, DT, m0, n0, CT);
         } else {
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     int j = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
@@ -204,7 +213,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 }
         }
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
@@ -215,14 +224,14 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 
     // ---- S4: dk_SC = exp(gamma_C - gamma) (.) (V_new dS_next); last-row gate terms
     {
-        float t[1][8][4];
+        float t[1][NK][4];
         zero_acc(t);
-        warp_mma_ct<1, 8, true, false>(t, S.VnT, CT, S.dHs, DT, m0, n0, DT);
-        float part = 0.f, colp[PC ? 8 : 1][2];
+        warp_mma_ct<1, NK, true, false>(t, S.VnT, CT, S.dHs, DT, m0, n0, DT);
+        float part = 0.f, colp[PC ? NK : 1][2];
 #pragma unroll
-        for (int nt = 0; nt < (PC ? 8 : 1); ++nt) colp[nt][0] = colp[nt][1] = 0.f;
+        for (int nt = 0; nt < (PC ? NK : 1); ++nt) colp[nt][0] = colp[nt][1] = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
@@ -241,7 +250,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         } else {
             // column sums over the warp's 16 rows: lanes that differ in lane / 4 share columns
 #pragma unroll
-            for (int nt = 0; nt < (PC ? 8 : 1); ++nt)
+            for (int nt = 0; nt < (PC ? NK : 1); ++nt)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     float s = colp[nt][h];
@@ -251,9 +260,9 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                     if (lane < 4) S.lrp[wid & 3][acc_col(n0, nt, h)] = s;
                 }
         }
-        // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate): every thread takes
-        // one 8-column chunk of 8 rows (16-byte reads; the same column chunk for all of its rows)
-        {
+        // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate): each of the first
+        // eight warps' threads takes one 8-column chunk of 8 rows (16-byte reads; one column chunk per thread)
+        if (wid < 8) {
             const int c8 = 8 * (tid & 15), v0 = 8 * (tid >> 4);
             float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -281,17 +290,17 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 for (int t = 0; t < 8; ++t) s += acc8[t];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0) S.lrs[8 + wid] = s * expf(S.gam[rl]);
+                if (lane == 0) S.lrs[16 + wid] = s * expf(S.gam[rl]);
             }
         }
     }
     // ---- S5: dW = -dV_new S_0 (the stored tile is -dV_new^T)  -> dWs;  per-channel: beta Gamma K -> KGb
     {
-        float t[1][8][4];
+        float t[1][NK][4];
         zero_acc(t);
-        warp_mma_ct<1, 8, true, false>(t, S.NdVT, CT, S.Hs, DT, m0, n0, DT);
+        warp_mma_ct<1, NK, true, false>(t, S.NdVT, CT, S.Hs, DT, m0, n0, DT);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; e += 2) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
@@ -308,13 +317,13 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 
     // ---- S6: dT = dW (beta Gamma K)^T + dV_new (beta V)^T  -> dTs
     {
-        float a[1][4][4], b[1][4][4];
+        float a[1][NC][4], b[1][NC][4];
         zero_acc(a);
         zero_acc(b);
-        warp_mma_ct<1, 4, false, true>(a, dWs, DT, PC ? KGb : S.Ks, DT, cm0, cn0, DT);
-        warp_mma_ct<1, 4, true, true>(b, S.NdVT, CT, S.Vs, DT, cm0, cn0, DT);  // = -(dV_new V^T)
+        warp_mma_ct<1, NC, false, true>(a, dWs, DT, PC ? KGb : S.Ks, DT, cm0, cn0, DT);
+        warp_mma_ct<1, NC, true, true>(b, S.NdVT, CT, S.Vs, DT, cm0, cn0, DT);  // = -(dV_new V^T)
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < NC; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
@@ -325,11 +334,11 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     // ---- S7: T^T dW -> dk_W, dbeta, dgamma
     float rowb[2] = {0.f, 0.f};  // dbeta partials for rows m0 + lane/4 and +8
     {
-        float t[1][8][4];
+        float t[1][NK][4];
         zero_acc(t);
-        warp_mma_ct<1, 8, true, false>(t, S.Ts, CT, dWs, DT, m0, n0, CT);
+        warp_mma_ct<1, NK, true, false>(t, S.Ts, CT, dWs, DT, m0, n0, CT);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
@@ -343,11 +352,11 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     }
     // ---- S8: T^T dV_new -> dv, dbeta  (negated tile: product is -T^T dV_new)
     {
-        float t[1][8][4];
+        float t[1][NK][4];
         zero_acc(t);
-        warp_mma_ct<1, 8, true, true>(t, S.Ts, CT, S.NdVT, CT, m0, n0, CT);
+        warp_mma_ct<1, NK, true, true>(t, S.Ts, CT, S.NdVT, CT, m0, n0, CT);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
@@ -362,11 +371,11 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 
     // ---- S9: X = dT T^T -> Xs
     {
-        float x[1][4][4];
+        float x[1][NC][4];
         zero_acc(x);
-        warp_mma_ct<1, 4, false, true>(x, dTs, CT, S.Ts, CT, cm0, cn0, CT);
+        warp_mma_ct<1, NC, false, true>(x, dTs, CT, S.Ts, CT, cm0, cn0, CT);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < NC; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; e += 2) {
                 int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
@@ -376,16 +385,16 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     __syncthreads();
     // ---- S10: dA = strict_lower(-T^T X); dbeta from A; E = beta (.) L (.) dA -> Es
     {
-        float da[1][4][4], kk[1][4][4];
+        float da[1][NC][4], kk[1][NC][4];
         zero_acc(da);
-        warp_mma_ct<1, 4, true, false>(da, S.Ts, CT, Xs, CT, cm0, cn0, CT);
+        warp_mma_ct<1, NC, true, false>(da, S.Ts, CT, Xs, CT, cm0, cn0, CT);
         if (!PC) {
             zero_acc(kk);
-            warp_mma_ct<1, 4, false, true>(kk, S.Ks, DT, S.Ks, DT, cm0, cn0, DT);
+            warp_mma_ct<1, NC, false, true>(kk, S.Ks, DT, S.Ks, DT, cm0, cn0, DT);
         }
         float rb[2] = {0.f, 0.f};
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < NC; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int i = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
@@ -416,20 +425,20 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         float s = rowb[h];
         s += __shfl_xor_sync(0xffffffffu, s, 1);
         s += __shfl_xor_sync(0xffffffffu, s, 2);
-        if ((lane & 3) == 0) S.dbp[2 + (wid >> 2)][m0 + (lane >> 2) + 8 * h] = s;
+        if ((lane & 3) == 0) S.dbp[4 + (wid >> 2)][m0 + (lane >> 2) + 8 * h] = s;
     }
     __syncthreads();
     // ---- S11: dk_Ar = E K (+), dk_Ac = E^T K (-)
     {
-        float a[1][8][4], b[1][8][4];
+        float a[1][NK][4], b[1][NK][4];
         zero_acc(a);
         zero_acc(b);
         if (!PC) {
-            warp_mma_ct<1, 8, false, false>(a, Es, CT, S.Ks, DT, m0, n0, CT);
-            warp_mma_ct<1, 8, true, false>(b, Es, CT, S.Ks, DT, m0, n0, CT);
+            warp_mma_ct<1, NK, false, false>(a, Es, CT, S.Ks, DT, m0, n0, CT);
+            warp_mma_ct<1, NK, true, false>(b, Es, CT, S.Ks, DT, m0, n0, CT);
         } else {
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
@@ -443,7 +452,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 }
         }
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
@@ -470,11 +479,11 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         }
         __syncthreads();
         if (tid < CT) {
-            float x = S.dgp[0][tid] + S.dgp[1][tid];
+            float x = (S.dgp[0][tid] + S.dgp[1][tid]) + (S.dgp[2][tid] + S.dgp[3][tid]);
             if (tid == rl) {
                 float l = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) l += S.lrs[i];
+                for (int i = 0; i < 24; ++i) l += S.lrs[i];
                 x += l;
             }
             P.dgam[u * CT + tid] = tid < len ? x : 0.f;
@@ -483,7 +492,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     } else {
         __syncthreads();
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
