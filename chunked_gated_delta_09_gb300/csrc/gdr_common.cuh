@@ -334,71 +334,76 @@ __device__ __forceinline__ void warp_mma_ct(float (&acc)[MT][NT][4], const unsig
 // before the first conversion.  Work item `it` of warp w covers rows 8 (it / 4) .. +7 and 16-byte
 // columns 4 (it % 4) .. +3: the 8 lanes of each 16-byte store phase write the 8 rows of one core matrix
 // (distinct banks), and each row reads 64 contiguous bytes from global memory.
-template <typename Tin, int NTHR>
-__device__ __forceinline__ void stage_ct_pair(unsigned char *t0, const Tin *s0, size_t st0, int nc0, float m0,
-                                              unsigned char *t1, const Tin *s1, size_t st1, int nc1, float m1,
-                                              int nrows, int tid) {
-    constexpr int PER = CT * (DT / 8) / NTHR;  // 8-element chunks per thread per tile
+// Eight consecutive input elements as loaded (16 bytes for 16-bit types, 32 for fp32), converted later.
+template <typename Tin> struct Raw8 { uint4 v; };
+template <> struct Raw8<float> { float4 a, b; };
+__device__ __forceinline__ void raw_load(Raw8<float> &x, const float *p) {
+    x.a = *reinterpret_cast<const float4 *>(p);
+    x.b = *reinterpret_cast<const float4 *>(p + 4);
+}
+template <typename Tin> __device__ __forceinline__ void raw_load(Raw8<Tin> &x, const Tin *p) {
+    x.v = *reinterpret_cast<const uint4 *>(p);
+}
+__device__ __forceinline__ void raw_zero(Raw8<float> &x) { x.a = x.b = make_float4(0.f, 0.f, 0.f, 0.f); }
+template <typename Tin> __device__ __forceinline__ void raw_zero(Raw8<Tin> &x) { x.v = make_uint4(0u, 0u, 0u, 0u); }
+__device__ __forceinline__ void raw_get(const Raw8<float> &x, float (&o)[8]) {
+    o[0] = x.a.x; o[1] = x.a.y; o[2] = x.a.z; o[3] = x.a.w;
+    o[4] = x.b.x; o[5] = x.b.y; o[6] = x.b.z; o[7] = x.b.w;
+}
+__device__ __forceinline__ void raw_get(const Raw8<__nv_bfloat16> &x, float (&o)[8]) {
+    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&x.v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __bfloat1622float2(h2[i]);
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void raw_get(const Raw8<__half> &x, float (&o)[8]) {
+    const __half2 *h2 = reinterpret_cast<const __half2 *>(&x.v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __half22float2(h2[i]);
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
+}
+
+// Stage NW row-major [rows x cols] inputs, each times its multiplier, as fp16 core-matrix tiles (CT x DT,
+// zero padded) in shared or global memory.  Every global load of all NW tiles is issued before the first
+// conversion (one memory round trip, not NW).
+template <typename Tin, int NTHR, int NW>
+__device__ __forceinline__ void stage_ct_n(unsigned char *const (&t)[NW], const Tin *const (&src)[NW],
+                                           const size_t (&st)[NW], const int (&nc)[NW], const float (&mul)[NW],
+                                           int nrows, int tid) {
+    constexpr int PER = CT * (DT / 8) / NTHR;
     static_assert(PER * NTHR == CT * (DT / 8), "thread count must divide the tile");
     const int wid = tid >> 5, lane = tid & 31;
-    float x[2][PER][8];
+    Raw8<Tin> x[NW][PER];
 #pragma unroll
-    for (int w = 0; w < 2; ++w) {
-        const Tin *src = w ? s1 : s0;
-        const size_t st = w ? st1 : st0;
-        const int nc = w ? nc1 : nc0;
+    for (int w = 0; w < NW; ++w)
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             int it = wid + (NTHR / 32) * i;
             int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
-            if (r < nrows && c8 + 8 <= nc) {
-                load8(src + (size_t)r * st + c8, x[w][i]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) x[w][i][j] = 0.f;
-            }
+            if (r < nrows && c8 + 8 <= nc[w]) raw_load(x[w][i], src[w] + (size_t)r * st[w] + c8);
+            else raw_zero(x[w][i]);
         }
-    }
 #pragma unroll
-    for (int w = 0; w < 2; ++w)
+    for (int w = 0; w < NW; ++w)
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             int it = wid + (NTHR / 32) * i;
             int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
-            const float m = w ? m1 : m0;
+            float f[8];
+            raw_get(x[w][i], f);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) x[w][i][j] *= m;
-            *reinterpret_cast<uint4 *>((w ? t1 : t0) + ctile_off(r, c8, DT)) = pack8_half(x[w][i]);
+            for (int j = 0; j < 8; ++j) f[j] *= mul[w];
+            *reinterpret_cast<uint4 *>(t[w] + ctile_off(r, c8, DT)) = pack8_half(f);
         }
 }
 
-// Single-block version of stage_ct_pair.
-template <typename Tin, int NTHR>
-__device__ __forceinline__ void stage_ct_one(unsigned char *t0, const Tin *s0, size_t st0, int nc0, float m0, int nrows,
-                                             int tid) {
-    constexpr int PER = CT * (DT / 8) / NTHR;
-    const int wid = tid >> 5, lane = tid & 31;
-    float x[PER][8];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        int it = wid + (NTHR / 32) * i;
-        int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
-        if (r < nrows && c8 + 8 <= nc0) {
-            load8(s0 + (size_t)r * st0 + c8, x[i]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        int it = wid + (NTHR / 32) * i;
-        int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[i][j] *= m0;
-        *reinterpret_cast<uint4 *>(t0 + ctile_off(r, c8, DT)) = pack8_half(x[i]);
-    }
-}
+
 
 // Store two adjacent values (columns c, c+1) of an output row in the output dtype.
 __device__ __forceinline__ void store_pair(void *p, size_t i, float a, float b, int dt) {

@@ -33,34 +33,6 @@ struct __align__(1024) K1Smem {
     float beta[CT];
 };
 
-// Convert a strided [rows][cols] input block to an fp16 [CT][DT] tile written straight to global memory.
-template <typename Tin>
-__device__ __forceinline__ void stage_ct_global(__half *dst, const Tin *src, size_t stride, int ncols, float mul,
-                                                int nrows, int tid) {
-    constexpr int PER = CT * (DT / 8) / K1_THREADS;
-    const int wid = tid >> 5, lane = tid & 31;
-    float x[PER][8];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        int it = wid + (K1_THREADS / 32) * i;
-        int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
-        if (r < nrows && c8 + 8 <= ncols) {
-            load8(src + (size_t)r * stride + c8, x[i]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        int it = wid + (K1_THREADS / 32) * i;
-        int r = 8 * (it >> 2) + (lane & 7), c8 = 8 * (4 * (it & 3) + (lane >> 3));
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[i][j] *= mul;
-        *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(dst) + ctile_off(r, c8, DT)) = pack8_half(x[i]);
-    }
-}
-
 template <typename Tin, bool PC>
 __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Params P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -80,19 +52,28 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
     const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
     const Tin *dop = reinterpret_cast<const Tin *>(P.dO) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    stage_ct_pair<Tin, K1_THREADS>(S.Ks, kp, (size_t)P.Hk * P.K, P.K, 1.f, S.Qs, qp, (size_t)P.Hk * P.K, P.K, 1.f, len,
-                                   tid);
-    stage_ct_one<Tin, K1_THREADS>(S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, len, tid);
-    stage_ct_global(P.Dt + u * CT * DT, dop, (size_t)P.Hv * P.V, P.V, P.scale, len, tid);
+    // the per-token scalars are read first so that their loads overlap the tile loads
+    float beta_r = 0.f, gx0 = 0.f, gx1 = 0.f;
+    if (tid < len) beta_r = load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype);
+    if (!PC && wid == 0) {
+        if (2 * lane < len) gx0 = P.g[(size_t)(ci.tok0 + 2 * lane) * P.Hv + hv];
+        if (2 * lane + 1 < len) gx1 = P.g[(size_t)(ci.tok0 + 2 * lane + 1) * P.Hv + hv];
+    }
+    {
+        unsigned char *const dst[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT)};
+        const Tin *const src[4] = {kp, qp, vp, dop};
+        const size_t st[4] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V, (size_t)P.Hv * P.V};
+        const int nc[4] = {P.K, P.K, P.V, P.V};
+        const float mul[4] = {1.f, 1.f, 1.f, P.scale};
+        stage_ct_n<Tin, K1_THREADS, 4>(dst, src, st, nc, mul, len, tid);
+    }
 
     // ---- beta, gate cumsum
-    if (tid < CT) S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
+    if (tid < CT) S.beta[tid] = beta_r;
     if (!PC) {
         if (wid == 0) {
-            float x0 = 0.f, x1 = 0.f;
-            int r0 = 2 * lane, r1 = 2 * lane + 1;
-            if (r0 < len) x0 = P.g[(size_t)(ci.tok0 + r0) * P.Hv + hv];
-            if (r1 < len) x1 = P.g[(size_t)(ci.tok0 + r1) * P.Hv + hv];
+            const float x0 = gx0, x1 = gx1;
+            const int r0 = 2 * lane, r1 = 2 * lane + 1;
             float s = x0 + x1;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -109,6 +90,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
         if (tid < DT) {
             const int c = tid;
             float run = 0.f;
+#pragma unroll 8
             for (int i = 0; i < CT; ++i) {
                 if (i < len && c < P.K) run += P.g[((size_t)(ci.tok0 + i) * P.Hv + hv) * P.K + c];
                 gamK[i * DT + c] = run;

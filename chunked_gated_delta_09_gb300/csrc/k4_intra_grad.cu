@@ -45,8 +45,9 @@ struct __align__(1024) K4Smem {
     // partial sums in fixed slots, added in a fixed order (results do not depend on warp timing)
     float dbp[8][CT];    // dbeta: [0..3] from dA (by column block), [4..7] from T^T dW / T^T dV_new (by K block)
     float dgp[4][CT];    // scalar gate: per-row gate-gradient sums by K block
-    float lrs[24];       // scalar gate: last-row terms, [w] from dk_SC and [16 + w] from <S_0, dS_next>
-    float lrp[12][DT];   // per-channel gate: last-row terms, [0..3] from dk_SC (by row block), [4 + w] from S_0
+    float lrs[32];       // scalar gate: last-row terms, [w] from dk_SC and [16 + w] from <S_0, dS_next>
+    float lrp[8][DT];    // per-channel gate: last-row terms, [0..3] from dk_SC (by row block), [4..7] from
+                         // <S_0, dS_next> (by row quarter)
     uint64_t lbar;
 };
 
@@ -98,9 +99,14 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    stage_ct_one<Tin, K4_THREADS>(S.Ks, kp, (size_t)P.Hk * P.K, P.K, 1.f, len, tid);
-    stage_ct_one<Tin, K4_THREADS>(S.Qs, qp, (size_t)P.Hk * P.K, P.K, 1.f, len, tid);
-    stage_ct_one<Tin, K4_THREADS>(S.Vs, vp, (size_t)P.Hv * P.V, P.V, 1.f, len, tid);
+    {
+        unsigned char *const dst[3] = {S.Ks, S.Qs, S.Vs};
+        const Tin *const src[3] = {kp, qp, vp};
+        const size_t st[3] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V};
+        const int nc[3] = {P.K, P.K, P.V};
+        const float mul[3] = {1.f, 1.f, 1.f};
+        stage_ct_n<Tin, K4_THREADS, 3>(dst, src, st, nc, mul, len, tid);
+    }
     if (tid < CT) {
         S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
         if (!PC) S.gam[tid] = P.gam[u * CT + tid];
@@ -260,14 +266,15 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                     if (lane < 4) S.lrp[wid & 3][acc_col(n0, nt, h)] = s;
                 }
         }
-        // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate): each of the first
-        // eight warps' threads takes one 8-column chunk of 8 rows (16-byte reads; one column chunk per thread)
-        if (wid < 8) {
-            const int c8 = 8 * (tid & 15), v0 = 8 * (tid >> 4);
+        // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate).  Warp w takes the
+        // 8-column chunk 4 (w % 4) + lane / 8 over rows 32 (w / 4) .. +31; the 8 lanes of a quarter-warp read
+        // the 8 rows of one core matrix (16-byte reads, no bank conflicts)
+        {
+            const int c8 = 8 * (4 * (wid & 3) + (lane >> 3));
             float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int v = v0; v < v0 + 8; ++v) {
-                const uint32_t off = ctile_off(v, c8, DT);
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t off = ctile_off(32 * (wid >> 2) + 8 * j + (lane & 7), c8, DT);
                 const __half2 *a2 = reinterpret_cast<const __half2 *>(S.Hs + off);
                 const __half2 *b2 = reinterpret_cast<const __half2 *>(S.dHs + off);
 #pragma unroll
@@ -278,11 +285,14 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 }
             }
             if (PC) {
-                // lanes l and l + 16 hold the same column chunk
+                // lanes that differ in lane % 8 hold the same column chunk
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
-                    float s = acc8[t] + __shfl_xor_sync(0xffffffffu, acc8[t], 16);
-                    if (lane < 16) S.lrp[4 + wid][c8 + t] = s * expf(G_(rl, c8 + t));
+                    float s = acc8[t];
+                    s += __shfl_xor_sync(0xffffffffu, s, 1);
+                    s += __shfl_xor_sync(0xffffffffu, s, 2);
+                    s += __shfl_xor_sync(0xffffffffu, s, 4);
+                    if ((lane & 7) == 0) S.lrp[4 + (wid >> 2)][c8 + t] = s * expf(G_(rl, c8 + t));
                 }
             } else {
                 float s = 0.f;
@@ -483,7 +493,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             if (tid == rl) {
                 float l = 0.f;
 #pragma unroll
-                for (int i = 0; i < 24; ++i) l += S.lrs[i];
+                for (int i = 0; i < 32; ++i) l += S.lrs[i];
                 x += l;
             }
             P.dgam[u * CT + tid] = tid < len ? x : 0.f;
@@ -500,7 +510,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 if (r == rl) {
                     float l = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 12; ++i) l += S.lrp[i][c];
+                    for (int i = 0; i < 8; ++i) l += S.lrp[i][c];
                     x += l;
                 }
                 P.dgam[(u * CT + r) * DT + c] = r < len ? x : 0.f;

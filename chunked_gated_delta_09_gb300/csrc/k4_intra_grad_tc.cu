@@ -98,9 +98,14 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    stage_ct_pair<Tin, K4T_THREADS>(S.K, kp, (size_t)P.Hk * P.K, P.K, 1.f, S.Q, qp, (size_t)P.Hk * P.K, P.K, 1.f, len,
-                                    tid);
-    stage_ct_one<Tin, K4T_THREADS>(S.V, vp, (size_t)P.Hv * P.V, P.V, 1.f, len, tid);
+    {
+        unsigned char *const dst[3] = {S.K, S.Q, S.V};
+        const Tin *const src[3] = {kp, qp, vp};
+        const size_t st[3] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V};
+        const int nc[3] = {P.K, P.K, P.V};
+        const float mul[3] = {1.f, 1.f, 1.f};
+        stage_ct_n<Tin, K4T_THREADS, 3>(dst, src, st, nc, mul, len, tid);
+    }
     if (tid < CT) {
         S.G[tid] = expf(S.gam[tid]);
         S.GC[tid] = expf(S.gam[rl] - S.gam[tid]);
@@ -333,11 +338,12 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         // last row: Gamma_C <S_0, dS_next> (this warp's half of the v range) + sum_j k_j (.) dk_SC_j
         float hd = 0.f;
         {
-            // <S_0, dS_next> over the whole tile: every thread one 8-column chunk of 8 rows (16-byte reads)
-            const int cc8 = 8 * (tid & 15), v0 = 8 * (tid >> 4);
+            // <S_0, dS_next> over the whole tile: warp w takes the 8-column chunk 4 (w % 4) + lane / 8 over
+            // rows 64 (w / 4) .. +63; a quarter-warp reads the 8 rows of one core matrix (no bank conflicts)
+            const int cc8 = 8 * (4 * (wid & 3) + (lane >> 3));
 #pragma unroll
-            for (int v = v0; v < v0 + 8; ++v) {
-                const uint32_t off = tc::tile_off(v, cc8, DT);
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t off = tc::tile_off(64 * (wid >> 2) + 8 * j + (lane & 7), cc8, DT);
                 const __half2 *a2 = reinterpret_cast<const __half2 *>(S.H + off);
                 const __half2 *b2 = reinterpret_cast<const __half2 *>(S.dH + off);
 #pragma unroll
