@@ -28,10 +28,50 @@ struct __align__(1024) K1Smem {
     unsigned char oT[CT * CT * 2], oAqk[CT * CT * 2];
     float A32[CT][CT + 1];
     float T32[CT][CT + 1];
-    float X32[3][16][17];
+    float X32[32][33];  // scratch of the block products
     float gam[CT];
     float beta[CT];
 };
+
+// One doubling level of the unit-lower-triangular inverse T = (I + A)^-1 held in fp32 shared memory:
+// for every diagonal pair of B x B blocks (lo, hi = lo + B), T[hi][lo] = -T[hi][hi] (A[hi][lo] T[lo][lo]),
+// with the B x B diagonal blocks of T already final.  2 (64 / (2B)) B^2 / 4 two-by-two output blocks.
+template <int B>
+__device__ __forceinline__ void inv_level(const float (&A)[CT][CT + 1], float (&T)[CT][CT + 1], float (&X)[32][33],
+                                          int tid) {
+    constexpr int NP = CT / (2 * B);        // block pairs
+    constexpr int QB = (B / 2) * (B / 2);   // 2 x 2 blocks per pair
+    constexpr int NQ = NP * QB;             // work items (<= K1_THREADS)
+    static_assert(NQ <= K1_THREADS && NP * B <= 32, "one 2 x 2 block per thread");
+    const bool act = tid < NQ;
+    const int p = tid / QB, m = tid % QB;
+    const int rr = 2 * (m / (B / 2)), cc = 2 * (m % (B / 2));
+    const int lo = 2 * B * p, hi = lo + B;
+    if (act) {  // X = A[hi][lo] T[lo][lo]   (stored at X[p B + r][c])
+        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const float a0 = A[hi + rr][lo + k], a1 = A[hi + rr + 1][lo + k];
+            const float t0 = T[lo + k][lo + cc], t1 = T[lo + k][lo + cc + 1];
+            x00 += a0 * t0; x01 += a0 * t1; x10 += a1 * t0; x11 += a1 * t1;
+        }
+        X[p * B + rr][cc] = x00; X[p * B + rr][cc + 1] = x01;
+        X[p * B + rr + 1][cc] = x10; X[p * B + rr + 1][cc + 1] = x11;
+    }
+    __syncthreads();
+    if (act) {  // T[hi][lo] = -T[hi][hi] X
+        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const float a0 = T[hi + rr][hi + k], a1 = T[hi + rr + 1][hi + k];
+            const float x0 = X[p * B + k][cc], x1 = X[p * B + k][cc + 1];
+            y00 += a0 * x0; y01 += a0 * x1; y10 += a1 * x0; y11 += a1 * x1;
+        }
+        T[hi + rr][lo + cc] = -y00; T[hi + rr][lo + cc + 1] = -y01;
+        T[hi + rr + 1][lo + cc] = -y10; T[hi + rr + 1][lo + cc + 1] = -y11;
+    }
+    __syncthreads();
+}
 
 template <typename Tin, bool PC>
 __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Params P) {
@@ -174,7 +214,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
         }
     }
 
-    // ---- T = (I + A_kk)^-1: diagonal 16x16 blocks by per-column forward substitution
+    // ---- T = (I + A_kk)^-1: diagonal 16x16 blocks by per-column forward substitution, then doubling
     if (wid < 4 && lane < 16) {
         const int b0 = wid * 16, m = lane;
         float x[16];
@@ -189,23 +229,11 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
         for (int i = 0; i < 16; ++i) S.T32[b0 + i][b0 + m] = x[i];
     }
     __syncthreads();
-    // off-diagonal blocks, one block row at a time: T_IJ = -T_II * sum_{J<=k<I} A_Ik T_kJ
-    for (int I = 1; I < 4; ++I) {
-        for (int e = tid; e < I * 256; e += K1_THREADS) {
-            int J = e >> 8, a = (e >> 4) & 15, b = e & 15;
-            float acc = 0.f;
-            for (int col = 16 * J; col < 16 * I; ++col) acc += S.A32[16 * I + a][col] * S.T32[col][16 * J + b];
-            S.X32[J][a][b] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < I * 256; e += K1_THREADS) {
-            int J = e >> 8, a = (e >> 4) & 15, b = e & 15;
-            float acc = 0.f;
-            for (int c = 0; c <= a; ++c) acc += S.T32[16 * I + a][16 * I + c] * S.X32[J][c][b];
-            S.T32[16 * I + a][16 * J + b] = -acc;
-        }
-        __syncthreads();
-    }
+    // off-diagonal blocks by recursive doubling: for a lower block split [[T_11, 0], [X, T_22]] of an inverse,
+    // X = -T_22 A_21 T_11.  First the two 32 x 32 diagonal blocks from their 16 x 16 halves, then the whole.
+    // Every thread accumulates a 2 x 2 output block over a fully unrolled inner loop.
+    inv_level<16>(S.A32, S.T32, S.X32, tid);
+    inv_level<32>(S.A32, S.T32, S.X32, tid);
     for (int e = tid; e < CT * CT / 8; e += K1_THREADS) {
         int i = e / (CT / 8), j8 = (e % (CT / 8)) * 8;
         float x[8];
