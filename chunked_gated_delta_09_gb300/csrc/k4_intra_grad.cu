@@ -51,7 +51,8 @@ struct __align__(1024) K4Smem {
     uint64_t lbar;
 };
 
-// Store a warp's accumulator tile (16 rows x 8 NT columns of a C x K block) as an output gradient row block (column pairs).
+// Store a warp's accumulator tile (16 rows x 8 NT columns of a C x K block) as an output gradient row block
+// (column pairs).
 template <int NT>
 __device__ __forceinline__ void store_ck(const float (&a)[1][NT][4], int m0, int n0, int len, int ncols, void *base,
                                          size_t row_stride, int dt) {
@@ -77,445 +78,487 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     unsigned char *Es = S.Pms;     // E                  after X
 
     if (*P.status & ST_BAD_SEQLENS) return;
-    const int n = blockIdx.x, hv = blockIdx.y, hk = hv / P.G;
-    ChunkInfo ci;
-    if (!chunk_info(P, n, ci)) return;
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
-    const size_t u = (size_t)n * P.Hv + hv;
-    const int len = ci.len;
-
-    // ---- stage everything: workspace tiles by bulk copy, inputs converted to fp16 tiles
+    // Persistent CTAs take the items (chunk n, value head hv), item = n Hv + hv, round-robin.  The workspace
+    // tiles of a CTA's next item are bulk-copied into each buffer as soon as the current item is done with
+    // it (three groups, all counted on one barrier phase per item), so their transfer overlaps the compute.
+    const int n_items = P.max_chunks * P.Hv;
+    auto valid_from = [&](int it) -> int {
+        ChunkInfo t;
+        while (it < n_items && !chunk_info(P, it / P.Hv, t)) it += gridDim.x;
+        return it;
+    };
+    constexpr uint32_t kBytesHdH = 2 * DT * DT * 2, kBytesDdV = CT * DT * 2 + DT * CT * 2,
+                       kBytesTVn = CT * CT * 2 + DT * CT * 2;
+    auto issue_HdH = [&](size_t un) {  // expects the whole item's bytes, so it comes first
+        tc::mbar_expect_tx(&S.lbar, kBytesHdH + kBytesDdV + kBytesTVn);
+        tc::bulk_g2s(S.Hs, P.h + un * DT * DT, DT * DT * 2, &S.lbar);
+        tc::bulk_g2s(S.dHs, P.dh + un * DT * DT, DT * DT * 2, &S.lbar);
+    };
+    auto issue_DdV = [&](size_t un) {
+        tc::bulk_g2s(S.Ds, P.Dt + un * CT * DT, CT * DT * 2, &S.lbar);
+        tc::bulk_g2s(S.NdVT, P.dVn + un * DT * CT, DT * CT * 2, &S.lbar);
+    };
+    auto issue_TVn = [&](size_t un) {
+        tc::bulk_g2s(S.Ts, P.Tm + un * CT * CT, CT * CT * 2, &S.lbar);
+        tc::bulk_g2s(S.VnT, P.Vn + un * DT * CT, DT * CT * 2, &S.lbar);
+    };
+    int item = valid_from(blockIdx.x);
+    if (item >= n_items) return;
     if (tid == 0) {
         tc::mbar_init(&S.lbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-        tc::mbar_expect_tx(&S.lbar, 2 * DT * DT * 2 + 2 * DT * CT * 2 + CT * CT * 2 + CT * DT * 2);
-        tc::bulk_g2s(S.Hs, P.h + u * DT * DT, DT * DT * 2, &S.lbar);
-        tc::bulk_g2s(S.dHs, P.dh + u * DT * DT, DT * DT * 2, &S.lbar);
-        tc::bulk_g2s(S.VnT, P.Vn + u * DT * CT, DT * CT * 2, &S.lbar);
-        tc::bulk_g2s(S.NdVT, P.dVn + u * DT * CT, DT * CT * 2, &S.lbar);
-        tc::bulk_g2s(S.Ts, P.Tm + u * CT * CT, CT * CT * 2, &S.lbar);
-        tc::bulk_g2s(S.Ds, P.Dt + u * CT * DT, CT * DT * 2, &S.lbar);
+        issue_HdH(item);
+        issue_DdV(item);
+        issue_TVn(item);
     }
-    const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
-    const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
-    const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    {
-        unsigned char *const dst[3] = {S.Ks, S.Qs, S.Vs};
-        const Tin *const src[3] = {kp, qp, vp};
-        const size_t st[3] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V};
-        const int nc[3] = {P.K, P.K, P.V};
-        const float mul[3] = {1.f, 1.f, 1.f};
-        stage_ct_n<Tin, K4_THREADS, 3>(dst, src, st, nc, mul, len, tid);
-    }
-    if (tid < CT) {
-        S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
-        if (!PC) S.gam[tid] = P.gam[u * CT + tid];
-    }
-    if (PC)
-        for (int e = tid; e < CT * DT; e += K4_THREADS) gamK[e] = P.gam[u * CT * DT + e];
-    __syncthreads();  // barrier initialised
-    if (!PC && tid < CT) {
-        S.G[tid] = expf(S.gam[tid]);
-        S.GC[tid] = expf(S.gam[len - 1] - S.gam[tid]);
-    }
-    const bool loaded = tc::mbar_wait(&S.lbar, 0, K4_WAIT_LIMIT);
-    if (__syncthreads_or(!loaded)) {
-        if (tid == 0) flag_status(P.status, ST_TIMEOUT);
-        return;
-    }
+    uint32_t parity = 0;
+    while (item < n_items) {
+        const int n = item / P.Hv, hv = item % P.Hv, hk = hv / P.G;
+        ChunkInfo ci;
+        chunk_info(P, n, ci);
+        const size_t u = (size_t)item;  // = n Hv + hv
+        const int len = ci.len;
+        const int next = valid_from(item + gridDim.x);
+        const bool has_next = next < n_items;
 
-    // C x K tiling: warp w owns rows m0 .. m0+15 and columns n0 .. n0+31
-    const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * (NK * 8);
-    // C x C tiling: rows cm0 .. cm0+15, columns cn0 .. cn0+15
-    const int cm0 = (wid & 3) * 16, cn0 = (wid >> 2) * (NC * 8);
-    auto G_ = [&](int r, int c) -> float { return PC ? gamK[r * DT + c] : S.gam[r]; };
-    auto Kv = [&](int r, int c) -> float { return ctile_get(S.Ks, r, c, DT); };
-    const int rl = len - 1;
-    auto row_dbeta = [&](int r) -> float {
-        float x = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x += S.dbp[i][r];
-        return x;
-    };
+        // ---- stage the inputs as fp16 tiles (the workspace tiles are already on their way)
+        const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
+        const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
+        const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
+        {
+            unsigned char *const dst[3] = {S.Ks, S.Qs, S.Vs};
+            const Tin *const src[3] = {kp, qp, vp};
+            const size_t st[3] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V};
+            const int nc[3] = {P.K, P.K, P.V};
+            const float mul[3] = {1.f, 1.f, 1.f};
+            stage_ct_n<Tin, K4_THREADS, 3>(dst, src, st, nc, mul, len, tid);
+        }
+        if (tid < CT) {
+            S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
+            if (!PC) S.gam[tid] = P.gam[u * CT + tid];
+        }
+        if (PC)
+            for (int e = tid; e < CT * DT; e += K4_THREADS) gamK[e] = P.gam[u * CT * DT + e];
+        __syncthreads();  // barrier initialised (first item); tiles of the previous item no longer read
+        if (!PC && tid < CT) {
+            S.G[tid] = expf(S.gam[tid]);
+            S.GC[tid] = expf(S.gam[len - 1] - S.gam[tid]);
+        }
+        const bool loaded = tc::mbar_wait(&S.lbar, parity, K4_WAIT_LIMIT);
+        parity ^= 1u;
+        if (__syncthreads_or(!loaded)) {
+            if (tid == 0) flag_status(P.status, ST_TIMEOUT);
+            return;
+        }
 
-    // ---- S1: P = (D V_new^T) (.) causal mask (.) [scalar: decay]
-    {
-        float g1[1][NC][4];
-        zero_acc(g1);
-        warp_mma_ct<1, NC, false, false>(g1, S.Ds, DT, S.VnT, CT, cm0, cn0, DT);
+        // C x K tiling: warp w owns rows m0 .. m0+15 and columns n0 .. n0+31
+        const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * (NK * 8);
+        // C x C tiling: rows cm0 .. cm0+15, columns cn0 .. cn0+15
+        const int cm0 = (wid & 3) * 16, cn0 = (wid >> 2) * (NC * 8);
+        auto G_ = [&](int r, int c) -> float { return PC ? gamK[r * DT + c] : S.gam[r]; };
+        auto Kv = [&](int r, int c) -> float { return ctile_get(S.Ks, r, c, DT); };
+        const int rl = len - 1;
+        auto row_dbeta = [&](int r) -> float {
+            float x = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < NC; ++nt)
+            for (int i = 0; i < 8; ++i) x += S.dbp[i][r];
+            return x;
+        };
+
+        // ---- S1: P = (D V_new^T) (.) causal mask (.) [scalar: decay]
+        {
+            float g1[1][NC][4];
+            zero_acc(g1);
+            warp_mma_ct<1, NC, false, false>(g1, S.Ds, DT, S.VnT, CT, cm0, cn0, DT);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
-                float x = 0.f;
-                if (j <= r) x = PC ? g1[0][nt][e] : g1[0][nt][e] * expf(S.gam[r] - S.gam[j]);
-                ctile_set(S.Pms, r, j, CT, x);
+            for (int nt = 0; nt < NC; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
+                    float x = 0.f;
+                    if (j <= r) x = PC ? g1[0][nt][e] : g1[0][nt][e] * expf(S.gam[r] - S.gam[j]);
+                    ctile_set(S.Pms, r, j, CT, x);
+                }
+        }
+        __syncthreads();
+
+        // gate-gradient contributions: per element for the per-channel gate, per row for the scalar gate
+        float dgam[1][PC ? NK : 1][4];
+        float rsg[2] = {0.f, 0.f};
+        float dk[1][NK][4];
+        zero_acc(dgam);
+        auto add_dg = [&](int nt, int e, float x) {
+            if (PC) dgam[0][PC ? nt : 0][e] += x;
+            else rsg[e >> 1] += x;
+        };
+        // ---- S2: dq = Gamma (.) (D S_0) + P K   [per-channel: decayed sum per element]
+        {
+            float dq[1][NK][4];
+            zero_acc(dq);
+            warp_mma_ct<1, NK, false, false>(dq, S.Ds, DT, S.Hs, DT, m0, n0, DT);
+#pragma unroll
+            for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dq[0][nt][e] *= PC ? expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e))) : S.G[acc_row(m0, 0, e)];
+            if (!PC) {
+                warp_mma_ct<1, NK, false, false>(dq, S.Pms, CT, S.Ks, DT, m0, n0, CT);
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                        float gr = gamK[r * DT + c], s = 0.f;
+                        for (int j = 0; j <= r; ++j)
+                            s += ctile_get(S.Pms, r, j, CT) * Kv(j, c) * expf(gr - gamK[j * DT + c]);
+                        dq[0][nt][e] += s;
+                    }
             }
-    }
-    __syncthreads();
-
-    // gate-gradient contributions: per element for the per-channel gate, per row for the scalar gate
-    float dgam[1][PC ? NK : 1][4];
-    float rsg[2] = {0.f, 0.f};
-    float dk[1][NK][4];
-    zero_acc(dgam);
-    auto add_dg = [&](int nt, int e, float x) {
-        if (PC) dgam[0][PC ? nt : 0][e] += x;
-        else rsg[e >> 1] += x;
-    };
-    // ---- S2: dq = Gamma (.) (D S_0) + P K   [per-channel: decayed sum per element]
-    {
-        float dq[1][NK][4];
-        zero_acc(dq);
-        warp_mma_ct<1, NK, false, false>(dq, S.Ds, DT, S.Hs, DT, m0, n0, DT);
-#pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                dq[0][nt][e] *= PC ? expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e))) : S.G[acc_row(m0, 0, e)];
-        if (!PC) {
-            warp_mma_ct<1, NK, false, false>(dq, S.Pms, CT, S.Ks, DT, m0, n0, CT);
-        } else {
 #pragma unroll
             for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                    float gr = gamK[r * DT + c], s = 0.f;
-                    for (int j = 0; j <= r; ++j)
-                        s += ctile_get(S.Pms, r, j, CT) * Kv(j, c) * expf(gr - gamK[j * DT + c]);
-                    dq[0][nt][e] += s;
+                    add_dg(nt, e, ctile_get(S.Qs, r, c, DT) * dq[0][nt][e]);
                 }
+            if (P.G == 1)
+                store_ck(dq, m0, n0, len, P.K, reinterpret_cast<char *>(P.dq) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
+                         (P.dqdk_dtype == F32 ? 4 : 2), (size_t)P.Hk * P.K, P.dqdk_dtype);
+            else
+                store_ck(dq, m0, n0, len, P.K, P.dq_h + ((size_t)ci.tok0 * P.Hv + hv) * P.K, (size_t)P.Hv * P.K, F32);
         }
+        // ---- S3: dk_O = P^T Q
+        {
+            zero_acc(dk);
+            if (!PC) {
+                warp_mma_ct<1, NK, true, false>(dk, S.Pms, CT, S.Qs, DT, m0, n0, CT);
+            } else {
 #pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
+                for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                add_dg(nt, e, ctile_get(S.Qs, r, c, DT) * dq[0][nt][e]);
+                    for (int e = 0; e < 4; ++e) {
+                        int j = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                        float gj = gamK[j * DT + c], s = 0.f;
+                        for (int r = j; r < CT; ++r)
+                            s += ctile_get(S.Pms, r, j, CT) * ctile_get(S.Qs, r, c, DT) * expf(gamK[r * DT + c] - gj);
+                        dk[0][nt][e] = s;
+                    }
             }
-        if (P.G == 1)
-            store_ck(dq, m0, n0, len, P.K, reinterpret_cast<char *>(P.dq) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
-                     (P.dqdk_dtype == F32 ? 4 : 2), (size_t)P.Hk * P.K, P.dqdk_dtype);
-        else
-            store_ck(dq, m0, n0, len, P.K, P.dq_h + ((size_t)ci.tok0 * P.Hv + hv) * P.K, (size_t)P.Hv * P.K, F32);
-    }
-    // ---- S3: dk_O = P^T Q
-    {
-        zero_acc(dk);
-        if (!PC) {
-            warp_mma_ct<1, NK, true, false>(dk, S.Pms, CT, S.Qs, DT, m0, n0, CT);
-        } else {
 #pragma unroll
             for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    int j = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                    float gj = gamK[j * DT + c], s = 0.f;
-                    for (int r = j; r < CT; ++r)
-                        s += ctile_get(S.Pms, r, j, CT) * ctile_get(S.Qs, r, c, DT) * expf(gamK[r * DT + c] - gj);
-                    dk[0][nt][e] = s;
+                    int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                    add_dg(nt, e, -(Kv(r, c) * dk[0][nt][e]));
                 }
         }
-#pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                add_dg(nt, e, -(Kv(r, c) * dk[0][nt][e]));
-            }
-    }
-    __syncthreads();  // Ds, Pms, Qs free
+        __syncthreads();  // Ds, Pms, Qs free
 
-    // ---- S4: dk_SC = exp(gamma_C - gamma) (.) (V_new dS_next); last-row gate terms
-    {
-        float t[1][NK][4];
-        zero_acc(t);
-        warp_mma_ct<1, NK, true, false>(t, S.VnT, CT, S.dHs, DT, m0, n0, DT);
-        float part = 0.f, colp[PC ? NK : 1][2];
-#pragma unroll
-        for (int nt = 0; nt < (PC ? NK : 1); ++nt) colp[nt][0] = colp[nt][1] = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                float x = t[0][nt][e] * (PC ? expf(G_(rl, c) - G_(r, c)) : S.GC[r]);
-                float kx = Kv(r, c) * x;
-                dk[0][nt][e] += x;
-                add_dg(nt, e, -(kx));
-                if (PC) colp[PC ? nt : 0][e & 1] += kx;
-                else part += kx;
-            }
-        if (!PC) {
-            float s = part;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0) S.lrs[wid] = s;
-        } else {
-            // column sums over the warp's 16 rows: lanes that differ in lane / 4 share columns
-#pragma unroll
-            for (int nt = 0; nt < (PC ? NK : 1); ++nt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float s = colp[nt][h];
-                    s += __shfl_xor_sync(0xffffffffu, s, 4);
-                    s += __shfl_xor_sync(0xffffffffu, s, 8);
-                    s += __shfl_xor_sync(0xffffffffu, s, 16);
-                    if (lane < 4) S.lrp[wid & 3][acc_col(n0, nt, h)] = s;
-                }
-        }
-        // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate).  Warp w takes the
-        // 8-column chunk 4 (w % 4) + lane / 8 over rows 32 (w / 4) .. +31; the 8 lanes of a quarter-warp read
-        // the 8 rows of one core matrix (16-byte reads, no bank conflicts)
+        // ---- S4: dk_SC = exp(gamma_C - gamma) (.) (V_new dS_next); last-row gate terms
         {
-            const int c8 = 8 * (4 * (wid & 3) + (lane >> 3));
-            float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float t[1][NK][4];
+            zero_acc(t);
+            warp_mma_ct<1, NK, true, false>(t, S.VnT, CT, S.dHs, DT, m0, n0, DT);
+            float part = 0.f, colp[PC ? NK : 1][2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t off = ctile_off(32 * (wid >> 2) + 8 * j + (lane & 7), c8, DT);
-                const __half2 *a2 = reinterpret_cast<const __half2 *>(S.Hs + off);
-                const __half2 *b2 = reinterpret_cast<const __half2 *>(S.dHs + off);
+            for (int nt = 0; nt < (PC ? NK : 1); ++nt) colp[nt][0] = colp[nt][1] = 0.f;
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    float2 a = __half22float2(a2[t]), b = __half22float2(b2[t]);
-                    acc8[2 * t] += a.x * b.x;
-                    acc8[2 * t + 1] += a.y * b.y;
+            for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                    float x = t[0][nt][e] * (PC ? expf(G_(rl, c) - G_(r, c)) : S.GC[r]);
+                    float kx = Kv(r, c) * x;
+                    dk[0][nt][e] += x;
+                    add_dg(nt, e, -(kx));
+                    if (PC) colp[PC ? nt : 0][e & 1] += kx;
+                    else part += kx;
                 }
-            }
-            if (PC) {
-                // lanes that differ in lane % 8 hold the same column chunk
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    float s = acc8[t];
-                    s += __shfl_xor_sync(0xffffffffu, s, 1);
-                    s += __shfl_xor_sync(0xffffffffu, s, 2);
-                    s += __shfl_xor_sync(0xffffffffu, s, 4);
-                    if ((lane & 7) == 0) S.lrp[4 + (wid >> 2)][c8 + t] = s * expf(G_(rl, c8 + t));
-                }
-            } else {
-                float s = 0.f;
-#pragma unroll
-                for (int t = 0; t < 8; ++t) s += acc8[t];
+            if (!PC) {
+                float s = part;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0) S.lrs[16 + wid] = s * expf(S.gam[rl]);
+                if (lane == 0) S.lrs[wid] = s;
+            } else {
+                // column sums over the warp's 16 rows: lanes that differ in lane / 4 share columns
+#pragma unroll
+                for (int nt = 0; nt < (PC ? NK : 1); ++nt)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float s = colp[nt][h];
+                        s += __shfl_xor_sync(0xffffffffu, s, 4);
+                        s += __shfl_xor_sync(0xffffffffu, s, 8);
+                        s += __shfl_xor_sync(0xffffffffu, s, 16);
+                        if (lane < 4) S.lrp[wid & 3][acc_col(n0, nt, h)] = s;
+                    }
             }
-        }
-    }
-    // ---- S5: dW = -dV_new S_0 (the stored tile is -dV_new^T)  -> dWs;  per-channel: beta Gamma K -> KGb
-    {
-        float t[1][NK][4];
-        zero_acc(t);
-        warp_mma_ct<1, NK, true, false>(t, S.NdVT, CT, S.Hs, DT, m0, n0, DT);
+            // Gamma_C <S_0, dS_next> per channel (summed over channels for the scalar gate).  Warp w takes the
+            // 8-column chunk 4 (w % 4) + lane / 8 over rows 32 (w / 4) .. +31; the 8 lanes of a quarter-warp read
+            // the 8 rows of one core matrix (16-byte reads, no bank conflicts)
+            {
+                const int c8 = 8 * (4 * (wid & 3) + (lane >> 3));
+                float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t off = ctile_off(32 * (wid >> 2) + 8 * j + (lane & 7), c8, DT);
+                    const __half2 *a2 = reinterpret_cast<const __half2 *>(S.Hs + off);
+                    const __half2 *b2 = reinterpret_cast<const __half2 *>(S.dHs + off);
 #pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                *reinterpret_cast<__half2 *>(dWs + ctile_off(r, c, DT)) = __floats2half2_rn(t[0][nt][e], t[0][nt][e + 1]);
-            }
-        if (PC) {
-            for (int e = tid; e < CT * DT; e += K4_THREADS) {
-                int r = e / DT, c = e % DT;
-                ctile_set(KGb, r, c, DT, S.beta[r] * expf(gamK[e]) * Kv(r, c));
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- S6: dT = dW (beta Gamma K)^T + dV_new (beta V)^T  -> dTs
-    {
-        float a[1][NC][4], b[1][NC][4];
-        zero_acc(a);
-        zero_acc(b);
-        warp_mma_ct<1, NC, false, true>(a, dWs, DT, PC ? KGb : S.Ks, DT, cm0, cn0, DT);
-        warp_mma_ct<1, NC, true, true>(b, S.NdVT, CT, S.Vs, DT, cm0, cn0, DT);  // = -(dV_new V^T)
-#pragma unroll
-        for (int nt = 0; nt < NC; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
-                float x = (PC ? a[0][nt][e] : a[0][nt][e] * S.beta[j] * S.G[j]) - b[0][nt][e] * S.beta[j];
-                ctile_set(dTs, r, j, CT, x);
-            }
-    }
-    // ---- S7: T^T dW -> dk_W, dbeta, dgamma
-    float rowb[2] = {0.f, 0.f};  // dbeta partials for rows m0 + lane/4 and +8
-    {
-        float t[1][NK][4];
-        zero_acc(t);
-        warp_mma_ct<1, NK, true, false>(t, S.Ts, CT, dWs, DT, m0, n0, CT);
-#pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                float Gm = PC ? expf(G_(r, c)) : S.G[r];
-                float kv = Kv(r, c);
-                float x = S.beta[r] * Gm * t[0][nt][e];
-                dk[0][nt][e] += x;
-                add_dg(nt, e, kv * x);
-                rowb[e >> 1] += t[0][nt][e] * kv * Gm;
-            }
-    }
-    // ---- S8: T^T dV_new -> dv, dbeta  (negated tile: product is -T^T dV_new)
-    {
-        float t[1][NK][4];
-        zero_acc(t);
-        warp_mma_ct<1, NK, true, true>(t, S.Ts, CT, S.NdVT, CT, m0, n0, CT);
-#pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                float x = -t[0][nt][e];
-                rowb[e >> 1] += x * ctile_get(S.Vs, r, c, DT);
-                t[0][nt][e] = S.beta[r] * x;
-            }
-        store_ck(t, m0, n0, len, P.V, reinterpret_cast<char *>(P.dv) + ((size_t)ci.tok0 * P.Hv + hv) * P.V *
-                 (P.dv_dtype == F32 ? 4 : 2), (size_t)P.Hv * P.V, P.dv_dtype);
-    }
-    __syncthreads();  // dTs complete; VnT free
-
-    // ---- S9: X = dT T^T -> Xs
-    {
-        float x[1][NC][4];
-        zero_acc(x);
-        warp_mma_ct<1, NC, false, true>(x, dTs, CT, S.Ts, CT, cm0, cn0, CT);
-#pragma unroll
-        for (int nt = 0; nt < NC; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-                int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
-                *reinterpret_cast<__half2 *>(Xs + ctile_off(r, j, CT)) = __floats2half2_rn(x[0][nt][e], x[0][nt][e + 1]);
-            }
-    }
-    __syncthreads();
-    // ---- S10: dA = strict_lower(-T^T X); dbeta from A; E = beta (.) L (.) dA -> Es
-    {
-        float da[1][NC][4], kk[1][NC][4];
-        zero_acc(da);
-        warp_mma_ct<1, NC, true, false>(da, S.Ts, CT, Xs, CT, cm0, cn0, CT);
-        if (!PC) {
-            zero_acc(kk);
-            warp_mma_ct<1, NC, false, true>(kk, S.Ks, DT, S.Ks, DT, cm0, cn0, DT);
-        }
-        float rb[2] = {0.f, 0.f};
-#pragma unroll
-        for (int nt = 0; nt < NC; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int i = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
-                float dA = j < i ? -da[0][nt][e] : 0.f;
-                float L = 1.f, kkd = 0.f;
-                if (j < i) {
-                    if (!PC) {
-                        L = expf(S.gam[i] - S.gam[j]);
-                        kkd = L * kk[0][nt][e];
-                    } else {
-                        for (int c = 0; c < DT; ++c)
-                            kkd += Kv(i, c) * Kv(j, c) * expf(gamK[i * DT + c] - gamK[j * DT + c]);
+                    for (int t = 0; t < 4; ++t) {
+                        float2 a = __half22float2(a2[t]), b = __half22float2(b2[t]);
+                        acc8[2 * t] += a.x * b.x;
+                        acc8[2 * t + 1] += a.y * b.y;
                     }
                 }
-                rb[e >> 1] += dA * kkd;
-                ctile_set(Es, i, j, CT, S.beta[i] * (PC ? 1.f : L) * dA);
+                if (PC) {
+                    // lanes that differ in lane % 8 hold the same column chunk
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        float s = acc8[t];
+                        s += __shfl_xor_sync(0xffffffffu, s, 1);
+                        s += __shfl_xor_sync(0xffffffffu, s, 2);
+                        s += __shfl_xor_sync(0xffffffffu, s, 4);
+                        if ((lane & 7) == 0) S.lrp[4 + (wid >> 2)][c8 + t] = s * expf(G_(rl, c8 + t));
+                    }
+                } else {
+                    float s = 0.f;
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) s += acc8[t];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                    if (lane == 0) S.lrs[16 + wid] = s * expf(S.gam[rl]);
+                }
             }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float s = rb[h];
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if ((lane & 3) == 0) S.dbp[wid >> 2][cm0 + (lane >> 2) + 8 * h] = s;
         }
-    }
+        // ---- S5: dW = -dV_new S_0 (the stored tile is -dV_new^T)  -> dWs;  per-channel: beta Gamma K -> KGb
+        {
+            float t[1][NK][4];
+            zero_acc(t);
+            warp_mma_ct<1, NK, true, false>(t, S.NdVT, CT, S.Hs, DT, m0, n0, DT);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        float s = rowb[h];
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        s += __shfl_xor_sync(0xffffffffu, s, 2);
-        if ((lane & 3) == 0) S.dbp[4 + (wid >> 2)][m0 + (lane >> 2) + 8 * h] = s;
-    }
-    __syncthreads();
-    // ---- S11: dk_Ar = E K (+), dk_Ac = E^T K (-)
-    {
-        float a[1][NK][4], b[1][NK][4];
-        zero_acc(a);
-        zero_acc(b);
-        if (!PC) {
-            warp_mma_ct<1, NK, false, false>(a, Es, CT, S.Ks, DT, m0, n0, CT);
-            warp_mma_ct<1, NK, true, false>(b, Es, CT, S.Ks, DT, m0, n0, CT);
-        } else {
+            for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                    *reinterpret_cast<__half2 *>(dWs + ctile_off(r, c, DT)) = __floats2half2_rn(t[0][nt][e], t[0][nt][e + 1]);
+                }
+            if (PC) {
+                for (int e = tid; e < CT * DT; e += K4_THREADS) {
+                    int r = e / DT, c = e % DT;
+                    ctile_set(KGb, r, c, DT, S.beta[r] * expf(gamK[e]) * Kv(r, c));
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0 && has_next) {  // H and dH are read for the last time in S4 / S5
+            tc::fence_smem_to_async();
+            issue_HdH(next);
+        }
+
+        // ---- S6: dT = dW (beta Gamma K)^T + dV_new (beta V)^T  -> dTs
+        {
+            float a[1][NC][4], b[1][NC][4];
+            zero_acc(a);
+            zero_acc(b);
+            warp_mma_ct<1, NC, false, true>(a, dWs, DT, PC ? KGb : S.Ks, DT, cm0, cn0, DT);
+            warp_mma_ct<1, NC, true, true>(b, S.NdVT, CT, S.Vs, DT, cm0, cn0, DT);  // = -(dV_new V^T)
+#pragma unroll
+            for (int nt = 0; nt < NC; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
+                    float x = (PC ? a[0][nt][e] : a[0][nt][e] * S.beta[j] * S.G[j]) - b[0][nt][e] * S.beta[j];
+                    ctile_set(dTs, r, j, CT, x);
+                }
+        }
+        // ---- S7: T^T dW -> dk_W, dbeta, dgamma
+        float rowb[2] = {0.f, 0.f};  // dbeta partials for rows m0 + lane/4 and +8
+        {
+            float t[1][NK][4];
+            zero_acc(t);
+            warp_mma_ct<1, NK, true, false>(t, S.Ts, CT, dWs, DT, m0, n0, CT);
 #pragma unroll
             for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                    float gr = gamK[r * DT + c], sa = 0.f, sb = 0.f;
-                    for (int j = 0; j < r; ++j)
-                        sa += ctile_get(Es, r, j, CT) * Kv(j, c) * expf(gr - gamK[j * DT + c]);
-                    for (int i = r + 1; i < CT; ++i)
-                        sb += ctile_get(Es, i, r, CT) * Kv(i, c) * expf(gamK[i * DT + c] - gr);
-                    a[0][nt][e] = sa;
-                    b[0][nt][e] = sb;
+                    float Gm = PC ? expf(G_(r, c)) : S.G[r];
+                    float kv = Kv(r, c);
+                    float x = S.beta[r] * Gm * t[0][nt][e];
+                    dk[0][nt][e] += x;
+                    add_dg(nt, e, kv * x);
+                    rowb[e >> 1] += t[0][nt][e] * kv * Gm;
                 }
         }
+        // ---- S8: T^T dV_new -> dv, dbeta  (negated tile: product is -T^T dV_new)
+        {
+            float t[1][NK][4];
+            zero_acc(t);
+            warp_mma_ct<1, NK, true, true>(t, S.Ts, CT, S.NdVT, CT, m0, n0, CT);
 #pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
+            for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                float kv = Kv(r, c);
-                dk[0][nt][e] += a[0][nt][e] + b[0][nt][e];
-                add_dg(nt, e, kv * (a[0][nt][e] - b[0][nt][e]));
-            }
-    }
-    // ---- dk out
-    if (P.G == 1)
-        store_ck(dk, m0, n0, len, P.K, reinterpret_cast<char *>(P.dk) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
-                 (P.dqdk_dtype == F32 ? 4 : 2), (size_t)P.Hk * P.K, P.dqdk_dtype);
-    else
-        store_ck(dk, m0, n0, len, P.K, P.dk_h + ((size_t)ci.tok0 * P.Hv + hv) * P.K, (size_t)P.Hv * P.K, F32);
+                for (int e = 0; e < 4; ++e) {
+                    int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                    float x = -t[0][nt][e];
+                    rowb[e >> 1] += x * ctile_get(S.Vs, r, c, DT);
+                    t[0][nt][e] = S.beta[r] * x;
+                }
+            store_ck(t, m0, n0, len, P.V, reinterpret_cast<char *>(P.dv) + ((size_t)ci.tok0 * P.Hv + hv) * P.V *
+                     (P.dv_dtype == F32 ? 4 : 2), (size_t)P.Hv * P.V, P.dv_dtype);
+        }
+        __syncthreads();  // dTs complete; D (as dW) and -dV_new^T read for the last time
+        if (tid == 0 && has_next) {
+            tc::fence_smem_to_async();
+            issue_DdV(next);
+        }
 
-    // ---- gate gradient of the cumulative gate
-    if (!PC) {
+        // ---- S9: X = dT T^T -> Xs
+        {
+            float x[1][NC][4];
+            zero_acc(x);
+            warp_mma_ct<1, NC, false, true>(x, dTs, CT, S.Ts, CT, cm0, cn0, CT);
+#pragma unroll
+            for (int nt = 0; nt < NC; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
+                    *reinterpret_cast<__half2 *>(Xs + ctile_off(r, j, CT)) = __floats2half2_rn(x[0][nt][e], x[0][nt][e + 1]);
+                }
+        }
+        __syncthreads();
+        // ---- S10: dA = strict_lower(-T^T X); dbeta from A; E = beta (.) L (.) dA -> Es
+        {
+            float da[1][NC][4], kk[1][NC][4];
+            zero_acc(da);
+            warp_mma_ct<1, NC, true, false>(da, S.Ts, CT, Xs, CT, cm0, cn0, CT);
+            if (!PC) {
+                zero_acc(kk);
+                warp_mma_ct<1, NC, false, true>(kk, S.Ks, DT, S.Ks, DT, cm0, cn0, DT);
+            }
+            float rb[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < NC; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int i = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
+                    float dA = j < i ? -da[0][nt][e] : 0.f;
+                    float L = 1.f, kkd = 0.f;
+                    if (j < i) {
+                        if (!PC) {
+                            L = expf(S.gam[i] - S.gam[j]);
+                            kkd = L * kk[0][nt][e];
+                        } else {
+                            for (int c = 0; c < DT; ++c)
+                                kkd += Kv(i, c) * Kv(j, c) * expf(gamK[i * DT + c] - gamK[j * DT + c]);
+                        }
+                    }
+                    rb[e >> 1] += dA * kkd;
+                    ctile_set(Es, i, j, CT, S.beta[i] * (PC ? 1.f : L) * dA);
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float s = rb[h];
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if ((lane & 3) == 0) S.dbp[wid >> 2][cm0 + (lane >> 2) + 8 * h] = s;
+            }
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            float s = rsg[h];
+            float s = rowb[h];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if ((lane & 3) == 0) S.dgp[wid >> 2][m0 + (lane >> 2) + 8 * h] = s;
+            if ((lane & 3) == 0) S.dbp[4 + (wid >> 2)][m0 + (lane >> 2) + 8 * h] = s;
         }
         __syncthreads();
-        if (tid < CT) {
-            float x = (S.dgp[0][tid] + S.dgp[1][tid]) + (S.dgp[2][tid] + S.dgp[3][tid]);
-            if (tid == rl) {
-                float l = 0.f;
+        if (tid == 0 && has_next) {  // T and V_new^T (as X) read for the last time in S10
+            tc::fence_smem_to_async();
+            issue_TVn(next);
+        }
+        // ---- S11: dk_Ar = E K (+), dk_Ac = E^T K (-)
+        {
+            float a[1][NK][4], b[1][NK][4];
+            zero_acc(a);
+            zero_acc(b);
+            if (!PC) {
+                warp_mma_ct<1, NK, false, false>(a, Es, CT, S.Ks, DT, m0, n0, CT);
+                warp_mma_ct<1, NK, true, false>(b, Es, CT, S.Ks, DT, m0, n0, CT);
+            } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) l += S.lrs[i];
-                x += l;
+                for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                        float gr = gamK[r * DT + c], sa = 0.f, sb = 0.f;
+                        for (int j = 0; j < r; ++j)
+                            sa += ctile_get(Es, r, j, CT) * Kv(j, c) * expf(gr - gamK[j * DT + c]);
+                        for (int i = r + 1; i < CT; ++i)
+                            sb += ctile_get(Es, i, r, CT) * Kv(i, c) * expf(gamK[i * DT + c] - gr);
+                        a[0][nt][e] = sa;
+                        b[0][nt][e] = sb;
+                    }
             }
-            P.dgam[u * CT + tid] = tid < len ? x : 0.f;
-            if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = row_dbeta(tid);
+#pragma unroll
+            for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                    float kv = Kv(r, c);
+                    dk[0][nt][e] += a[0][nt][e] + b[0][nt][e];
+                    add_dg(nt, e, kv * (a[0][nt][e] - b[0][nt][e]));
+                }
         }
-    } else {
-        __syncthreads();
+        // ---- dk out
+        if (P.G == 1)
+            store_ck(dk, m0, n0, len, P.K, reinterpret_cast<char *>(P.dk) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
+                     (P.dqdk_dtype == F32 ? 4 : 2), (size_t)P.Hk * P.K, P.dqdk_dtype);
+        else
+            store_ck(dk, m0, n0, len, P.K, P.dk_h + ((size_t)ci.tok0 * P.Hv + hv) * P.K, (size_t)P.Hv * P.K, F32);
+
+        // ---- gate gradient of the cumulative gate
+        if (!PC) {
 #pragma unroll
-        for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                float x = dgam[0][PC ? nt : 0][e];
-                if (r == rl) {
+            for (int h = 0; h < 2; ++h) {
+                float s = rsg[h];
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if ((lane & 3) == 0) S.dgp[wid >> 2][m0 + (lane >> 2) + 8 * h] = s;
+            }
+            __syncthreads();
+            if (tid < CT) {
+                float x = (S.dgp[0][tid] + S.dgp[1][tid]) + (S.dgp[2][tid] + S.dgp[3][tid]);
+                if (tid == rl) {
                     float l = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) l += S.lrp[i][c];
+                    for (int i = 0; i < 32; ++i) l += S.lrs[i];
                     x += l;
                 }
-                P.dgam[(u * CT + r) * DT + c] = r < len ? x : 0.f;
+                P.dgam[u * CT + tid] = tid < len ? x : 0.f;
+                if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = row_dbeta(tid);
             }
-        if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = row_dbeta(tid);
+        } else {
+            __syncthreads();
+#pragma unroll
+            for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                    float x = dgam[0][PC ? nt : 0][e];
+                    if (r == rl) {
+                        float l = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) l += S.lrp[i][c];
+                        x += l;
+                    }
+                    P.dgam[(u * CT + r) * DT + c] = r < len ? x : 0.f;
+                }
+            if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = row_dbeta(tid);
+        }
+        __syncthreads();  // the next item overwrites the staged inputs and the partial-sum slots
+        item = next;
     }
 }
 
@@ -524,7 +567,12 @@ static cudaError_t launch_k4_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(K4Smem) + (PC ? sizeof(float) * CT * DT : 0);
     cudaError_t e = cudaFuncSetAttribute(k4_intra_grad<Tin, PC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(P.max_chunks, P.Hv);
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long items = (long)P.max_chunks * P.Hv;
+    if (items == 0) return cudaSuccess;
+    const int grid = (int)(items < nsm ? items : nsm);  // one persistent CTA per SM
     k4_intra_grad<Tin, PC><<<grid, K4_THREADS, smem, stream>>>(P);
     return cudaGetLastError();
 }
