@@ -131,10 +131,10 @@ gdr_status gdr_bwd_create(const gdr_bwd_desc *desc, gdr_bwd_plan **out) {
         p->NS = (int)ns;
         p->Lseg = maxnc > 0 ? (int)((maxnc + ns - 1) / ns) : 1;
     }
-    // per-chunk gradients: the mma.sync kernel is currently the faster one; GDR_K4_TC=1 selects the
-    // tcgen05 kernel (scalar gate only)
+    // per-chunk gradients: the tcgen05 kernel for the scalar gate, the mma.sync kernel for the per-channel
+    // gate; GDR_K4_TC=0 routes the scalar gate to the mma.sync kernel as well
     const char *k4tc = getenv("GDR_K4_TC");
-    p->k4_tc = !d.gate_per_channel && k4tc && atoi(k4tc) != 0;
+    p->k4_tc = !d.gate_per_channel && !(k4tc && atoi(k4tc) == 0);
     layout(*p);
     *out = p;
     return GDR_OK;

@@ -49,7 +49,7 @@ struct Params {
     float *gam;          // [u][CT] or [u][CT][DT]  chunk-local cumulative gate (fp32)
     __half *Tm;          // tile [r][i]   64 x 64    (I + A_kk)^-1
     __half *Aqk;         // tile [r][j]   64 x 64    M (.) Q K^T (causal, decayed, unscaled)
-    __half *W, *U;       // tile [c][k] / [c][v]     64 x 128
+    __half *W, *U;       // W tile [c][k] 64 x 128; U^T tile [v][c] 128 x 64
     __half *Kt;          // tile [c][k]   64 x 128   K (.) exp(gamma_C - gamma)
     __half *Qg;          // tile [r][k]   64 x 128   Q (.) exp(gamma)
     __half *Dt;          // tile [r][v]   64 x 128   scale * dO

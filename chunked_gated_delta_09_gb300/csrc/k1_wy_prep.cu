@@ -243,22 +243,33 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
     }
     __syncthreads();
 
-    // ---- W = T (beta Gamma K) into K's tile, then U = T (beta V) into Q's tile
+    // ---- W = T (beta Gamma K) into K's tile; U^T = (beta V)^T T^T into Q's tile as a [v][c] tile
     {
-        const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 64;
         float acc[1][8][4];
-#pragma unroll
-        for (int w = 0; w < 2; ++w) {
+        {
+            const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 64;
             zero_acc(acc);
-            warp_mma_ct<1, 8, false, false>(acc, S.oT, CT, w ? S.Vs : S.Qs, DT, m0, n0, CT);
-            if (w) __syncthreads();  // every warp finished reading beta Gamma K before U overwrites it
-            unsigned char *dst = w ? S.Qs : S.Ks;
+            warp_mma_ct<1, 8, false, false>(acc, S.oT, CT, S.Qs, DT, m0, n0, CT);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; e += 2) {
                     int i = acc_row(m0, 0, e), j = acc_col(n0, nt, e);
-                    *reinterpret_cast<__half2 *>(dst + ctile_off(i, j, DT)) =
+                    *reinterpret_cast<__half2 *>(S.Ks + ctile_off(i, j, DT)) =
+                        __floats2half2_rn(acc[0][nt][e], acc[0][nt][e + 1]);
+                }
+        }
+        {
+            const int m0 = wid * 16;  // 8 warps x 16 value rows, all 64 chunk columns
+            zero_acc(acc);
+            warp_mma_ct<1, 8, true, true>(acc, S.Vs, DT, S.oT, CT, m0, 0, CT);
+            __syncthreads();  // every warp finished reading beta Gamma K before U^T overwrites it
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    int v = acc_row(m0, 0, e), c = acc_col(0, nt, e);
+                    *reinterpret_cast<__half2 *>(S.Qs + ctile_off(v, c, CT)) =
                         __floats2half2_rn(acc[0][nt][e], acc[0][nt][e + 1]);
                 }
         }

@@ -26,7 +26,7 @@ constexpr uint32_t SC_WAIT_LIMIT = 1u << 24;
 
 template <bool LOCAL>
 struct __align__(1024) FwdSmem {
-    unsigned char W[2][CT * DT * 2], Kt[2][CT * DT * 2], U[2][CT * DT * 2];
+    unsigned char W[2][CT * DT * 2], Kt[2][CT * DT * 2], U[2][CT * DT * 2];  // U holds U^T tiles [v][c]
     unsigned char Sa[DT * DT * 2];                // state rows as fp16 (A operand; h_n)
     unsigned char Vna[DT * CT * 2];               // V_new^T [v][c] (A operand)
     unsigned char Pa[LOCAL ? DT * DT * 2 : 16];   // transition rows as fp16
@@ -176,7 +176,16 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
             float v[32];
             tc::ld32(tc::taddr(tm, T_VN + c0), v);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = tc::ld_tile(S.U[buf], c0 + t, row, DT) - v[t];
+            for (int j8 = 0; j8 < 32; j8 += 8) {  // U^T row segment: 16-byte reads of the [v][c] tile
+                const __half2 *u2 =
+                    reinterpret_cast<const __half2 *>(S.U[buf] + tc::tile_off(row, c0 + j8, CT));
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float2 f = __half22float2(u2[t]);
+                    v[j8 + 2 * t] = f.x - v[j8 + 2 * t];
+                    v[j8 + 2 * t + 1] = f.y - v[j8 + 2 * t + 1];
+                }
+            }
 #pragma unroll
             for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.Vna, row, c0 + j8, CT, v + j8);
             if (LOCAL) {

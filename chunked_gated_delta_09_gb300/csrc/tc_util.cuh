@@ -141,6 +141,19 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive columns of this warp's 32 lanes -> 16 registers per thread.
+__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 32 registers per thread -> 32 consecutive columns of this warp's 32 lanes.
 __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
     asm volatile(
@@ -178,6 +191,22 @@ __device__ __forceinline__ float warp_transpose_sum32(float (&v)[32]) {
         }
     }
     return v[0];
+}
+
+// Lanes l and l ^ 16 of the warp return the sum over the warp of v[l % 16] (v is consumed).
+__device__ __forceinline__ float warp_transpose_sum16(float (&v)[16]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 8; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            float send = up ? v[i] : v[i + s];
+            float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
 // Write 8 fp32 values as one 16-byte row segment of core matrix (r/8, c0/8) of a tile (c0 % 8 == 0).

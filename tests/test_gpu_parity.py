@@ -90,3 +90,12 @@ def test_segment_parallel_scan_matches_oracle(nseg, per_channel, monkeypatch):
     prob = make_problem(f"nseg{nseg}", B=1, Hk=1, Hv=2, K=64, V=64, per_channel=per_channel,
                         seq_lens=[700, 64, 130, 1], seed=88)
     compare(prob, run_gpu(prob), oracle.problem_backward(prob))
+
+
+@pytest.mark.parametrize("name", ["dense_ragged_bf16", "gqa_varlen_bf16", "fp16_scalar", "fp32_all"])
+def test_scalar_gate_on_mma_sync_kernel(name, monkeypatch):
+    """The scalar gate normally runs on the tcgen05 per-chunk kernel; the warp-MMA kernel (which serves the
+    per-channel gate) computes the same gradients for it when selected."""
+    monkeypatch.setenv("GDR_K4_TC", "0")
+    prob = make_problem(name, seed=zlib.crc32(name.encode()) % 1000, **SMALL[name])
+    compare(prob, run_gpu(prob), oracle.problem_backward(prob))
