@@ -325,13 +325,29 @@ def run_ours(args):
     alg_bytes = counts.algorithmic_bytes(prob)
     t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), alg_bytes / (peaks["hbm_gbs"] * 1e9))
     stage_flops = counts.stage_flops(prob)
+    stage_bytes = counts.stage_bytes(prob)
+    tc_peak, bw_peak = peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9
+
+    def stage_roof(s):
+        """Roofline of one stage: the tensor or HBM bound, whichever is longer for its FLOPs and bytes."""
+        t = stage_ms[s] / 1e3
+        if stage_bytes[s] / bw_peak >= stage_flops[s] / tc_peak:
+            ach = stage_bytes[s] / t / 1e9
+            return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / peaks["hbm_gbs"]}
+        ach = stage_flops[s] / t / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"]}
+
     dom = max(range(nst), key=lambda s: stage_ms[s])
     dom_name = _lib.STAGE_NAMES[dom]
-    achieved = stage_flops[dom] / (stage_ms[dom] / 1e3) / 1e12
-    roof = {"kernel": dom_name, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-            "peak_source": f"{peaks['source']} dense bf16 burst (fp16 operands run at the bf16 rate)",
+    roof = {"kernel": dom_name, **stage_roof(dom),
+            "bytes_per_launch": stage_bytes[dom], "flops_per_launch": stage_flops[dom],
+            "peak_source": f"{peaks['source']} (HBM copy GB/s; dense bf16 burst TFLOP/s, fp16 operands run at "
+                           f"the bf16 rate)",
             "traffic": committed_traffic(dom_name, prob.name)}
+    stage_roofs = {_lib.STAGE_NAMES[s]: {k: v for k, v in stage_roof(s).items() if k in ("bound", "achieved", "frac")}
+                   for s in range(nst) if stage_ms[s] > 0 and (stage_bytes[s] > 0 or stage_flops[s] > 0)}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -343,6 +359,7 @@ def run_ours(args):
                           "tensor_frac": (flops / (ms / 1e3)) / (peaks["bf16_tflops"] * 1e12),
                           "hbm_frac": (alg_bytes / (ms / 1e3)) / (peaks["hbm_gbs"] * 1e9)},
         "stage_ms": {_lib.STAGE_NAMES[s]: stage_ms[s] for s in range(nst)},
+        "stage_roofline": stage_roofs,
         "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": plan.launch_count * args.steps,

@@ -11,6 +11,11 @@ Every started chunk counts as a full one.  Element-wise work (exp, masks, cumsum
 
 Algorithmic bytes are the least any implementation must move: each input read once and each output
 written once (q, k, v, dO, beta, g, h0, dht, cu_seqlens in; dq, dk, dv, dbeta, dg, dh0 out).
+
+Stage bytes (:func:`stage_bytes`) are what each kernel stage of this implementation must read and write
+given the split of the path into stages: its share of the inputs and outputs plus the workspace tiles it
+consumes or produces (fp16 tiles padded to 64 chunk rows and 128 features).  They decide which roofline
+(tensor or HBM) binds each stage.
 """
 from __future__ import annotations
 
@@ -60,3 +65,44 @@ def stage_flops(prob) -> list:
            0.0]
     u = chunk_units(prob)
     return [u * x for x in per]
+
+
+# Segments per sequence of the segment-parallel scans, chosen as the library's plan does: enough
+# sequence x head x segment CTAs to fill the 152 SMs, at least 4 chunks per segment.
+NUM_SMS = 152
+
+
+def scan_segments(prob) -> int:
+    units = prob.N * prob.Hv
+    maxnc = (prob.T + prob.BT - 1) // prob.BT if prob.cu_seqlens is None else \
+        (prob.B * prob.T + prob.BT - 1) // prob.BT
+    ns = NUM_SMS // units if units > 0 else 1
+    ns = min(ns, (maxnc + 3) // 4)
+    return max(ns, 1)
+
+
+def stage_bytes(prob) -> list:
+    """Bytes each of the six stages reads plus writes (see the module docstring), summed over all units."""
+    CT, DT = 64, 128
+    tile_ck, tile_cc, tile_kk = CT * DT * 2, CT * CT * 2, DT * DT * 2  # fp16 workspace tiles
+    u = chunk_units(prob)
+    C, K, V = prob.BT, prob.K, prob.V
+    ib, bb = _nbytes(prob.qkv_dtype), _nbytes(prob.beta_dtype)
+    gk = K if prob.per_channel else 1
+    G = prob.Hv // prob.Hk
+    oq, ov = _nbytes(prob.dqdk_dtype), _nbytes(prob.dv_dtype)
+    state = prob.N * prob.Hv * V * K * 4
+    ns = scan_segments(prob)
+    seg = 6 * prob.N * prob.Hv * ns * DT * DT * 4 if ns > 1 else 0  # segment summaries, all passes
+    k0 = 0 if prob.cu_seqlens is None else 4 * (prob.num_seqs + 1) + 8 * u // prob.Hv + 4 * (prob.num_seqs + 1)
+    k1 = u * (2 * C * K * ib + 2 * C * V * ib + C * bb + C * gk * 4          # q, k, v, dO, beta, g
+              + CT * gk * 4 + 2 * tile_cc + 5 * tile_ck)                      # gamma, T, Aqk, W, U, K~, Q~, D
+    k2 = u * ((3 * tile_ck) * (2 if ns > 1 else 1) + tile_kk + tile_ck) \
+        + (state if prob.h0 is not None else 0) + seg // 2                      # W, U, K~ (+ local pass); h, V_new
+    k3 = u * ((tile_cc + 4 * tile_ck) * (2 if ns > 1 else 1) + tile_kk + tile_ck) \
+        + (state if prob.dht is not None else 0) + state + seg // 2             # Aqk, D, K~, Q~, W; dh, dV_new; dh0
+    dqdk_out = 2 * C * K * (oq if G == 1 else 4)
+    k4 = u * (2 * tile_kk + 3 * tile_ck + tile_cc + 2 * C * K * ib + C * V * ib + C * bb + CT * gk * 4   # reads
+              + dqdk_out + C * V * ov + C * 4 + CT * gk * 4)                                           # writes
+    k5 = u * (CT * gk * 4 + C * gk * 4) + (0 if G == 1 else u * 2 * C * K * 4 + (u // G) * 2 * C * K * oq)
+    return [float(k0), float(k1), float(k2), float(k3), float(k4), float(k5)]
