@@ -38,8 +38,8 @@ constexpr uint32_t K4T_WAIT_LIMIT = 1u << 24;  // mbarrier polls before a wait i
 // tensor-memory column map, 64 columns per region (C_* regions use the M = 64 lane layout)
 constexpr int R_DKSC = 0, R_DWT = 64, R_TDU = 128, R_VT = 192, R_KT = 256, C_G1 = 320, C_DT2 = 384,
               R_DQI = 448;                                                              // phase 1
-constexpr int R_DQA = 0, R_DKO = 64, R_TDW = 128, R_QT = 192, C_KK = 256, C_DT1 = 320;  // phase 2
-constexpr int C_X = 0;                                                                  // phase 3
+constexpr int R_DQA = 0, R_DKO = 64, R_TDW = 128, R_QT = 192, C_DT1 = 320;              // phase 2
+constexpr int C_X = 0, C_KK = 256;                                                      // phase 3
 constexpr int C_DA = 64;                                                                // phase 4
 constexpr int R_DKAR = 128, R_DKAC = 192;                                               // phase 5
 
@@ -57,7 +57,7 @@ struct __align__(1024) K4TSmem {
     // dbeta: 4 lane quarters x (TdU, TdW) + 4 column quarters (A term); dgamma rows: 4 lane quarters;
     // last row: 16 warps
     float db_tdu[4][CT], db_tdw[4][CT], db_a[4][CT], dg_q[4][CT], last_w[16];
-    uint64_t bar, lbar;
+    uint64_t bar, bar2, lbar;  // MMA groups 1 and 2 of a phase; bulk loads
     uint32_t tslot;
 };
 
@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     if (wid == 0) tc::tmem_alloc(&S.tslot, K4T_TMEM_COLS);
     if (tid == 0) {
         tc::mbar_init(&S.bar, 1);
+        tc::mbar_init(&S.bar2, 1);
         tc::mbar_init(&S.lbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -188,20 +189,27 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         fetch_raw(item, 1, S.Q);
         fetch_raw(item, 2, S.V);
     }
-    uint32_t lpar = 0, mpar = 0;
+    uint32_t lpar = 0, mpar = 0, mpar2 = 0;
     bool lost = false;
-    // Each phase: one thread issues, everyone waits (bounded) and agrees on the outcome.
+    // Each phase: one thread issues (group 1, committed to bar, and in phases 1 and 2 a group 2 committed
+    // to bar2 right after it), everyone waits (bounded) for group 1 and agrees on the outcome; the
+    // epilogue starts on group 1's results while group 2 still runs.
     auto finish_phase = [&](bool fail) {
-        if (tid == 0) tc::commit(&S.bar);
         bool ok = tc::mbar_wait(&S.bar, mpar, K4T_WAIT_LIMIT);
         mpar ^= 1u;
         lost = __syncthreads_or(!ok || fail || lost) != 0;
         tc::fence_after();
     };
-    auto publish_tiles = [&]() {  // make epilogue-written tiles visible to the next phase's MMAs
+    auto wait_group2 = [&]() -> bool {  // per thread; the outcome is agreed at the next publish_tiles
+        bool ok = tc::mbar_wait(&S.bar2, mpar2, K4T_WAIT_LIMIT);
+        mpar2 ^= 1u;
+        tc::fence_after();
+        return ok;
+    };
+    auto publish_tiles = [&](bool ok) {  // make epilogue-written tiles visible to the next phase's MMAs
         tc::fence_smem_to_async();
         tc::fence_before();
-        __syncthreads();
+        lost = __syncthreads_or(!ok || lost) != 0;
         tc::fence_after();
     };
 
@@ -254,15 +262,19 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (tid == 0) {
             fail = !tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);
             if (!fail) {
-                tc::gemm(tm + R_DKSC, sdH, DT, true, sVn, CT, true, 128, 64, DT, false);
-                tc::gemm(tm + R_DWT, sH, DT, true, sdVn, CT, true, 128, 64, DT, false);
-                tc::gemm(tm + R_TDU, sdVn, CT, false, sT, CT, true, 128, 64, CT, false);
-                tc::gemm(tm + R_VT, sV, DT, true, sI, CT, false, 128, 64, CT, false);
                 tc::gemm(tm + R_KT, sK, DT, true, sI, CT, false, 128, 64, CT, false);
+                tc::gemm(tm + R_VT, sV, DT, true, sI, CT, false, 128, 64, CT, false);
+                tc::gemm(tm + R_DWT, sH, DT, true, sdVn, CT, true, 128, 64, DT, false);
+                tc::gemm(tm + R_DKSC, sdH, DT, true, sVn, CT, true, 128, 64, DT, false);
+                tc::gemm(tm + R_TDU, sdVn, CT, false, sT, CT, true, 128, 64, CT, false);
+            }
+            tc::commit(&S.bar);
+            if (!fail) {
                 tc::gemm(tm + C_G1, sD, DT, false, sVn, CT, true, 64, 64, DT, false);
                 tc::gemm(tm + C_DT2, sdVn, CT, true, sV, DT, false, 64, 64, DT, false);
                 tc::gemm(tm + R_DQI, sH, DT, true, sD, DT, false, 128, 64, DT, false);
             }
+            tc::commit(&S.bar2);
         }
         lpar ^= 1u;
         finish_phase(fail);
@@ -273,18 +285,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         {
             float g[16], vreg[16];
             tc::ld16(tc::taddr(tm, R_VT + c0), vreg);
-            // P = (D V_new^T) (.) M  -> Pm tile
-            tc::ld16(tc::taddr(tm, C_G1 + c0), g);
-            if (own64) {
-                const float gr = S.gam[r64];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const int j = c0 + t;
-                    g[t] = j <= r64 ? g[t] * __expf(gr - S.gam[j]) : 0.f;
-                }
-                tc::st_tile8(S.Pm, r64, c0, CT, g);
-                tc::st_tile8(S.Pm, r64, c0 + 8, CT, g + 8);
-            }
             // dW^T -> dWT tile (the stored dV tile is negated, so the product already is dW^T)
             tc::ld16(tc::taddr(tm, R_DWT + c0), g);
             tc::st_tile8(S.dWT, k, c0, CT, g);
@@ -337,7 +337,24 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
             if (lane == 0) S.last_w[wid] = tot;
         }
-        publish_tiles();
+        const bool ok1 = wait_group2();
+        {
+            // P = (D V_new^T) (.) M  -> Pm tile
+            float g[16];
+            tc::ld16(tc::taddr(tm, C_G1 + c0), g);
+            if (own64) {
+                const float gr = S.gam[r64];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const int j = c0 + t;
+                    g[t] = j <= r64 ? g[t] * __expf(gr - S.gam[j]) : 0.f;
+                }
+                tc::st_tile8(S.Pm, r64, c0, CT, g);
+                tc::st_tile8(S.Pm, r64, c0 + 8, CT, g + 8);
+            }
+        }
+        publish_tiles(ok1);
+        if (lost) break;
         // S_0, dS_next, D, V_new^T, -dV_new^T and V are not read again in this item
         if (has_next) {
             if (tid == 0) issue_ws1(next);
@@ -346,15 +363,17 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 
         // ---------------- phase 2
         if (tid == 0) {
+            tc::gemm(tm + R_QT, sQ, DT, true, sI, CT, false, 128, 64, CT, false);
             tc::gemm(tm + R_DQA, sK, DT, true, sPm, CT, false, 128, 64, CT, false);
+            tc::commit(&S.bar);
             tc::gemm(tm + R_DKO, sQ, DT, true, sPm, CT, true, 128, 64, CT, false);
             tc::gemm(tm + R_TDW, sdWT, CT, false, sT, CT, true, 128, 64, CT, false);
-            tc::gemm(tm + R_QT, sQ, DT, true, sI, CT, false, 128, 64, CT, false);
-            tc::gemm(tm + C_KK, sK, DT, false, sK, DT, false, 64, 64, DT, false);
             tc::gemm(tm + C_DT1, sdWT, CT, true, sK, DT, false, 64, 64, DT, false);
+            tc::commit(&S.bar2);
         }
         finish_phase(false);
         if (lost) break;
+        bool ok2;
         {
             float a[16], b[16], qreg[16];
             tc::ld16(tc::taddr(tm, R_QT + c0), qreg);
@@ -375,6 +394,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                     store_col16(P.dq_h + ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, F32, (size_t)P.Hv * P.K,
                                 nrow, a);
             }
+            ok2 = wait_group2();
             // dk_O
             tc::ld16(tc::taddr(tm, R_DKO + c0), a);
 #pragma unroll
@@ -407,11 +427,16 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                 tc::st_tile8(S.dT, r64, c0 + 8, CT, a + 8);
             }
         }
-        publish_tiles();
+        publish_tiles(ok2);
+        if (lost) break;
         if (has_next && kRaw) fetch_raw(next, 1, S.Q);  // Q is not read again in this item
 
         // ---------------- phase 3: X = dT T^T
-        if (tid == 0) tc::gemm(tm + C_X, sdT, CT, false, sT, CT, false, 64, 64, CT, false);
+        if (tid == 0) {
+            tc::gemm(tm + C_X, sdT, CT, false, sT, CT, false, 64, 64, CT, false);
+            tc::gemm(tm + C_KK, sK, DT, false, sK, DT, false, 64, 64, DT, false);
+            tc::commit(&S.bar);
+        }
         finish_phase(false);
         if (lost) break;
         {
@@ -422,10 +447,14 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                 tc::st_tile8(Xs, r64, c0 + 8, CT, a + 8);
             }
         }
-        publish_tiles();
+        publish_tiles(true);
+        if (lost) break;
 
         // ---------------- phase 4: dA' = T^T X; dA = strict_lower(-dA'); E = beta L dA
-        if (tid == 0) tc::gemm(tm + C_DA, sT, CT, true, sX, CT, true, 64, 64, CT, false);
+        if (tid == 0) {
+            tc::gemm(tm + C_DA, sT, CT, true, sX, CT, true, 64, 64, CT, false);
+            tc::commit(&S.bar);
+        }
         finish_phase(false);
         if (lost) break;
         if (tid == 0 && has_next) issue_ws2(next);  // T is not read again in this item
@@ -454,12 +483,14 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                 S.db_a[wid >> 2][i] = rb;
             }
         }
-        publish_tiles();
+        publish_tiles(true);
+        if (lost) break;
 
         // ---------------- phase 5: dk_Ar^T = K^T E^T (+), dk_Ac^T = K^T E (-)
         if (tid == 0) {
             tc::gemm(tm + R_DKAR, sK, DT, true, sE, CT, false, 128, 64, CT, false);
             tc::gemm(tm + R_DKAC, sK, DT, true, sE, CT, true, 128, 64, CT, false);
+            tc::commit(&S.bar);
         }
         finish_phase(false);
         if (lost) break;

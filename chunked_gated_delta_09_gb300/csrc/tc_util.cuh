@@ -57,11 +57,15 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uin
 __device__ __forceinline__ void gemm(uint32_t d_tmem, uint32_t a_tile, int a_C, bool a_mn, uint32_t b_tile, int b_C,
                                      bool b_mn, int M, int N, int Kr, bool accumulate) {
     const uint32_t id = idesc_f16(M, N, a_mn, b_mn);
-    for (int kk = 0; kk < Kr / 16; ++kk) {
-        uint64_t a = a_mn ? desc_mn(a_tile, a_C, kk) : desc_k(a_tile, a_C, kk);
-        uint64_t b = b_mn ? desc_mn(b_tile, b_C, kk) : desc_k(b_tile, b_C, kk);
-        mma(d_tmem, a, b, id, (accumulate || kk > 0) ? 1u : 0u);
-    }
+    // only the start-address field changes between reduction steps (shared addresses stay below 2^18,
+    // so adding the 16-byte-unit offset cannot carry out of the 14-bit field)
+    const uint64_t a0 = a_mn ? desc_mn(a_tile, a_C, 0) : desc_k(a_tile, a_C, 0);
+    const uint64_t b0 = b_mn ? desc_mn(b_tile, b_C, 0) : desc_k(b_tile, b_C, 0);
+    const uint32_t a_step = a_mn ? 2 * (a_C >> 3) * 128 / 16 : 256 / 16;
+    const uint32_t b_step = b_mn ? 2 * (b_C >> 3) * 128 / 16 : 256 / 16;
+    for (int kk = 0; kk < Kr / 16; ++kk)
+        mma(d_tmem, a0 + (uint64_t)(kk * a_step), b0 + (uint64_t)(kk * b_step), id,
+            (accumulate || kk > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ void commit(uint64_t *bar) {
