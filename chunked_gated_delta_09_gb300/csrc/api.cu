@@ -144,25 +144,9 @@ size_t gdr_bwd_workspace_bytes(const gdr_bwd_plan *plan) { return plan ? plan->t
 
 void gdr_bwd_destroy(gdr_bwd_plan *plan) { delete plan; }
 
-static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *workspace, size_t ws_bytes, void *stream_,
-                           void *const *events) {
-    if (!plan || !a) return GDR_ERR_INVALID_ARG;
+// Sizes and workspace regions of a plan (inputs and outputs are set by the caller).
+static void fill_common(const gdr_bwd_plan *plan, char *ws, Params &P) {
     const gdr_bwd_desc &d = plan->d;
-    cudaStream_t stream = (cudaStream_t)stream_;
-    if (!a->q || !a->k || !a->v || !a->beta || !a->g || !a->dO) return GDR_ERR_INVALID_ARG;
-    if (!a->dq || !a->dk || !a->dv || !a->dbeta || !a->dg) return GDR_ERR_INVALID_ARG;
-    if ((d.has_h0 && !a->h0) || (d.has_dht && !a->dht)) return GDR_ERR_INVALID_ARG;
-    if (!plan->dense && !a->cu_seqlens) return GDR_ERR_INVALID_ARG;
-    const void *vec[] = {a->q, a->k, a->v, a->dO, a->dq, a->dk, a->dv};
-    for (const void *ptr : vec)
-        if (!aligned(ptr, 16)) return GDR_ERR_INVALID_ARG;
-    const void *nat[] = {a->beta, a->g, a->dbeta, a->dg, a->h0, a->dht, a->dh0, a->cu_seqlens};
-    for (const void *ptr : nat)
-        if (ptr && !aligned(ptr, 4)) return GDR_ERR_INVALID_ARG;
-    if (!workspace || !aligned(workspace, 256) || ws_bytes < plan->total) return GDR_ERR_INVALID_ARG;
-
-    char *ws = reinterpret_cast<char *>(workspace);
-    Params P;
     memset(&P, 0, sizeof(P));
     P.B = d.B;
     P.T = d.T;
@@ -182,21 +166,6 @@ static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *work
     P.beta_dtype = d.beta_dtype;
     P.dqdk_dtype = d.dqdk_dtype;
     P.dv_dtype = d.dv_dtype;
-    P.q = a->q;
-    P.k = a->k;
-    P.v = a->v;
-    P.beta = a->beta;
-    P.dO = a->dO;
-    P.g = reinterpret_cast<const float *>(a->g);
-    P.h0 = d.has_h0 ? reinterpret_cast<const float *>(a->h0) : nullptr;
-    P.dht = d.has_dht ? reinterpret_cast<const float *>(a->dht) : nullptr;
-    P.cu = plan->dense ? nullptr : a->cu_seqlens;
-    P.dq = a->dq;
-    P.dk = a->dk;
-    P.dv = a->dv;
-    P.dbeta = reinterpret_cast<float *>(a->dbeta);
-    P.dg = reinterpret_cast<float *>(a->dg);
-    P.dh0 = reinterpret_cast<float *>(a->dh0);
     P.status = reinterpret_cast<int *>(ws + plan->o_status);
     P.chunk_idx = reinterpret_cast<int32_t *>(ws + plan->o_cidx);
     P.chunk_off = reinterpret_cast<int32_t *>(ws + plan->o_coff);
@@ -227,6 +196,43 @@ static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *work
         P.segSin = seg + 4 * one;
         P.segdS = seg + 5 * one;
     }
+}
+
+static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *workspace, size_t ws_bytes, void *stream_,
+                           void *const *events) {
+    if (!plan || !a) return GDR_ERR_INVALID_ARG;
+    const gdr_bwd_desc &d = plan->d;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (!a->q || !a->k || !a->v || !a->beta || !a->g || !a->dO) return GDR_ERR_INVALID_ARG;
+    if (!a->dq || !a->dk || !a->dv || !a->dbeta || !a->dg) return GDR_ERR_INVALID_ARG;
+    if ((d.has_h0 && !a->h0) || (d.has_dht && !a->dht)) return GDR_ERR_INVALID_ARG;
+    if (!plan->dense && !a->cu_seqlens) return GDR_ERR_INVALID_ARG;
+    const void *vec[] = {a->q, a->k, a->v, a->dO, a->dq, a->dk, a->dv};
+    for (const void *ptr : vec)
+        if (!aligned(ptr, 16)) return GDR_ERR_INVALID_ARG;
+    const void *nat[] = {a->beta, a->g, a->dbeta, a->dg, a->h0, a->dht, a->dh0, a->cu_seqlens};
+    for (const void *ptr : nat)
+        if (ptr && !aligned(ptr, 4)) return GDR_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < plan->total) return GDR_ERR_INVALID_ARG;
+
+    char *ws = reinterpret_cast<char *>(workspace);
+    Params P;
+    fill_common(plan, ws, P);
+    P.q = a->q;
+    P.k = a->k;
+    P.v = a->v;
+    P.beta = a->beta;
+    P.dO = a->dO;
+    P.g = reinterpret_cast<const float *>(a->g);
+    P.h0 = d.has_h0 ? reinterpret_cast<const float *>(a->h0) : nullptr;
+    P.dht = d.has_dht ? reinterpret_cast<const float *>(a->dht) : nullptr;
+    P.cu = plan->dense ? nullptr : a->cu_seqlens;
+    P.dq = a->dq;
+    P.dk = a->dk;
+    P.dv = a->dv;
+    P.dbeta = reinterpret_cast<float *>(a->dbeta);
+    P.dg = reinterpret_cast<float *>(a->dg);
+    P.dh0 = reinterpret_cast<float *>(a->dh0);
 
     auto mark = [&](int i) -> bool {
         return !events || cudaEventRecord((cudaEvent_t)events[i], stream) == cudaSuccess;
@@ -280,6 +286,59 @@ int gdr_bwd_launch_count(const gdr_bwd_plan *plan) {
     n += 1;                       // the final state-gradient scan always runs (it also writes dh0)
     if (plan->max_chunks > 0) n += 4;  // K1, forward scan, K4, K5
     if (plan->max_chunks > 0 && plan->NS > 1) n += 4;  // local scans and combines
+    return n;
+}
+
+gdr_status gdr_fwd_run(gdr_bwd_plan *plan, const gdr_fwd_args *a, void *workspace, size_t ws_bytes, void *stream_) {
+    if (!plan || !a) return GDR_ERR_INVALID_ARG;
+    const gdr_bwd_desc &d = plan->d;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (!a->q || !a->k || !a->v || !a->beta || !a->g || !a->o) return GDR_ERR_INVALID_ARG;
+    if (d.has_h0 && !a->h0) return GDR_ERR_INVALID_ARG;
+    if (!plan->dense && !a->cu_seqlens) return GDR_ERR_INVALID_ARG;
+    const void *vec[] = {a->q, a->k, a->v, a->o};
+    for (const void *ptr : vec)
+        if (!aligned(ptr, 16)) return GDR_ERR_INVALID_ARG;
+    const void *nat[] = {a->beta, a->g, a->h0, a->ht, a->cu_seqlens};
+    for (const void *ptr : nat)
+        if (ptr && !aligned(ptr, 4)) return GDR_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < plan->total) return GDR_ERR_INVALID_ARG;
+
+    Params P;
+    fill_common(plan, reinterpret_cast<char *>(workspace), P);
+    P.q = a->q;
+    P.k = a->k;
+    P.v = a->v;
+    P.beta = a->beta;
+    P.g = reinterpret_cast<const float *>(a->g);
+    P.h0 = d.has_h0 ? reinterpret_cast<const float *>(a->h0) : nullptr;
+    P.cu = plan->dense ? nullptr : a->cu_seqlens;
+    P.o = a->o;
+    P.ht = a->ht;
+    // the forward: chunk bookkeeping, WY preparation without dO, the state recompute (which also writes
+    // the final state), then the per-chunk output
+    if (cudaMemsetAsync(P.status, 0, sizeof(int), stream) != cudaSuccess) return GDR_ERR_CUDA;
+    if (!plan->dense &&
+        launch_k0(a->cu_seqlens, plan->N, d.BT, plan->max_chunks, d.T, P.chunk_idx, P.chunk_off, P.status, stream) !=
+            cudaSuccess)
+        return GDR_ERR_CUDA;
+    const bool any_chunks = plan->max_chunks > 0;
+    if (any_chunks && launch_k1(P, stream) != cudaSuccess) return GDR_ERR_CUDA;
+    if (any_chunks && plan->NS > 1) {
+        if (launch_k2_scan(P, true, stream) != cudaSuccess) return GDR_ERR_CUDA;
+        if (launch_k23_combine(P, true, stream) != cudaSuccess) return GDR_ERR_CUDA;
+    }
+    if ((any_chunks || P.ht) && launch_k2_scan(P, false, stream) != cudaSuccess) return GDR_ERR_CUDA;
+    if (any_chunks && launch_k6_fwd_output(P, stream) != cudaSuccess) return GDR_ERR_CUDA;
+    return GDR_OK;
+}
+
+int gdr_fwd_launch_count(const gdr_bwd_plan *plan) {
+    if (!plan) return 0;
+    int n = plan->dense ? 0 : 1;                             // K0
+    n += 1;                                                  // the final state scan (final state)
+    if (plan->max_chunks > 0) n += 2;                        // K1, output
+    if (plan->max_chunks > 0 && plan->NS > 1) n += 2;        // local scan and combine
     return n;
 }
 

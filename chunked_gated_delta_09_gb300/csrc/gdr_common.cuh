@@ -37,9 +37,12 @@ struct Params {
     const void *q, *k, *v, *beta, *dO;
     const float *g, *h0, *dht;
     const int32_t *cu;
-    // outputs
+    // outputs (backward)
     void *dq, *dk, *dv;
     float *dbeta, *dg, *dh0;
+    // outputs (forward): o [T][Hv][V] in qkv dtype, final state ht [N][Hv][V][K] fp32 (may be null)
+    void *o;
+    float *ht;
     // workspace
     int *status;
     int32_t *chunk_idx;  // [max_chunks][2]
@@ -147,6 +150,11 @@ __device__ __forceinline__ uint4 pack8_half(const float (&x)[8]) {
     for (int i = 0; i < 4; ++i) h2[i] = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
     return r;
 }
+
+template <typename To> __device__ __forceinline__ To to_out_t(float x);
+template <> __device__ __forceinline__ float to_out_t<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 to_out_t<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <> __device__ __forceinline__ __half to_out_t<__half>(float x) { return __float2half_rn(x); }
 
 __device__ __forceinline__ float load_scalar(const void *p, size_t i, int dt) {
     if (dt == F32) return reinterpret_cast<const float *>(p)[i];

@@ -25,5 +25,7 @@ cudaError_t launch_k4(const Params &P, cudaStream_t stream);
 cudaError_t launch_k4_tc(const Params &P, cudaStream_t stream);
 // K5: reverse cumsum of the gate gradient and GQA reduction of dq / dk.
 cudaError_t launch_k5(const Params &P, cudaStream_t stream);
+// forward output o = scale (diag(Gamma) Q S_0^T + (M (.) Q K^T) V_new) per chunk
+cudaError_t launch_k6_fwd_output(const Params &P, cudaStream_t stream);
 
 }  // namespace gdr

@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
     const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
     const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
-    const Tin *dop = reinterpret_cast<const Tin *>(P.dO) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
+    const Tin *dop = P.dO ? reinterpret_cast<const Tin *>(P.dO) + ((size_t)ci.tok0 * P.Hv + hv) * P.V : nullptr;
     // the per-token scalars are read first so that their loads overlap the tile loads
     float beta_r = 0.f, gx0 = 0.f, gx1 = 0.f;
     if (tid < len) beta_r = load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype);
@@ -99,13 +99,20 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
         if (2 * lane < len) gx0 = P.g[(size_t)(ci.tok0 + 2 * lane) * P.Hv + hv];
         if (2 * lane + 1 < len) gx1 = P.g[(size_t)(ci.tok0 + 2 * lane + 1) * P.Hv + hv];
     }
-    {
+    if (P.dO) {  // backward: also D = scale dO, written straight to its workspace tile
         unsigned char *const dst[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT)};
         const Tin *const src[4] = {kp, qp, vp, dop};
         const size_t st[4] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V, (size_t)P.Hv * P.V};
         const int nc[4] = {P.K, P.K, P.V, P.V};
         const float mul[4] = {1.f, 1.f, 1.f, P.scale};
         stage_ct_n<Tin, K1_THREADS, 4>(dst, src, st, nc, mul, len, tid);
+    } else {     // forward: no output gradient
+        unsigned char *const dst[3] = {S.Ks, S.Qs, S.Vs};
+        const Tin *const src[3] = {kp, qp, vp};
+        const size_t st[3] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V};
+        const int nc[3] = {P.K, P.K, P.V};
+        const float mul[3] = {1.f, 1.f, 1.f};
+        stage_ct_n<Tin, K1_THREADS, 3>(dst, src, st, nc, mul, len, tid);
     }
 
     // ---- beta, gate cumsum

@@ -47,7 +47,15 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
     seq_range(P, s, bos, eos);
     const int nc = (eos - bos + P.BT - 1) / P.BT;
     const int c_lo = seg * P.Lseg, c_hi = min(nc, c_lo + P.Lseg);
-    if (c_lo >= c_hi) return;  // segment without chunks
+    if (c_lo >= c_hi) {  // segment without chunks; the forward's final state of an empty sequence is h0
+        if (!LOCAL && P.ht && nc == 0 && seg == 0) {
+            const int hv0 = (blockIdx.x / NS) % P.Hv;
+            float *dst = P.ht + ((size_t)s * P.Hv + hv0) * P.V * P.K;
+            const float *src = P.h0 ? P.h0 + ((size_t)s * P.Hv + hv0) * P.V * P.K : nullptr;
+            for (int e = threadIdx.x; e < P.V * P.K; e += SC_THREADS) dst[e] = src ? src[e] : 0.f;
+        }
+        return;
+    }
     const int base = seq_chunk_base(P, s);
     const size_t su = ((size_t)s * P.Hv + hv) * NS + seg;
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
@@ -229,6 +237,20 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
 #pragma unroll
                     for (int t = 0; t < 32; ++t) dT[(size_t)(c0 + t) * DT] = v[t];
                 }
+            }
+        }
+    }
+    if (!LOCAL && !lost && P.ht && c_hi == nc) {  // forward: the final state of the sequence
+        float *dst = P.ht + ((size_t)s * P.Hv + hv) * P.V * P.K + (size_t)row * P.K;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c0 = 64 * half + 32 * h;
+            float v[32];
+            tc::ld32(tc::taddr(tm, T_S + c0), v);
+            if (row < P.V) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    if (c0 + t < P.K) dst[c0 + t] = v[t];
             }
         }
     }

@@ -61,16 +61,11 @@ struct __align__(1024) K4TSmem {
     uint32_t tslot;
 };
 
-template <typename To> __device__ __forceinline__ To to_out(float x);
-template <> __device__ __forceinline__ float to_out<float>(float x) { return x; }
-template <> __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
-template <> __device__ __forceinline__ __half to_out<__half>(float x) { return __float2half_rn(x); }
-
 template <typename To>
 __device__ __forceinline__ void col16_t(To *p, size_t rs, int n, const float (&x)[16]) {
 #pragma unroll
     for (int t = 0; t < 16; ++t)
-        if (t < n) p[(size_t)t * rs] = to_out<To>(x[t]);
+        if (t < n) p[(size_t)t * rs] = to_out_t<To>(x[t]);
 }
 // x[t] -> element (t, 0) of a row-major output with row stride rs (elements), for the first n rows.
 __device__ __forceinline__ void store_col16(void *p, int dt, size_t rs, int n, const float (&x)[16]) {

@@ -1,7 +1,8 @@
 """Torch-facing wrapper of the C ABI: the same calls, with torch tensors for device memory and streams.
 
-Every step of the backward runs in libgdrbwd.so's kernels; this module only checks tensor placement,
-allocates outputs and workspace with torch, and passes raw pointers.  A missing library raises.
+Every step of the forward and the backward runs in libgdrbwd.so's kernels; this module only checks
+tensor placement, allocates outputs and workspace with torch, and passes raw pointers.  A missing
+library raises.  :class:`ChunkGatedDeltaRule` joins the two as a torch.autograd.Function.
 """
 from __future__ import annotations
 
@@ -12,7 +13,7 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import GdrBwdArgs, GdrBwdDesc, GdrError
+from ._lib import GdrBwdArgs, GdrBwdDesc, GdrError, GdrFwdArgs
 
 _DT = {torch.float32: _lib.GDR_F32, torch.bfloat16: _lib.GDR_BF16, torch.float16: _lib.GDR_F16}
 
@@ -104,6 +105,26 @@ class GdrBwdPlan:
         if st != _lib.GDR_OK:
             raise GdrError(st, "gdr_bwd_run_noalloc")
 
+    def alloc_forward_outputs(self, device="cuda", qkv_dtype=None) -> dict:
+        s = self.shape
+        N = s["B"] if s["num_seqs"] == 0 else s["num_seqs"]
+        dt = qkv_dtype or {v: k for k, v in _DT.items()}[self.desc.qkv_dtype]
+        return dict(o=torch.empty(s["B"], s["T"], s["Hv"], s["V"], dtype=dt, device=device),
+                    ht=torch.empty(N, s["Hv"], s["V"], s["K"], dtype=torch.float32, device=device))
+
+    def run_forward(self, *, q, k, v, beta, g, h0=None, cu_seqlens=None, out: dict, workspace, stream=None):
+        """Queue gdr_fwd_run (o and, if ``out`` has it, the final state ht) on `stream`.  Asynchronous."""
+        args = GdrFwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), beta=_ptr(beta), g=_ptr(g), h0=_ptr(h0),
+                          cu_seqlens=_ptr(cu_seqlens), o=_ptr(out["o"]), ht=_ptr(out.get("ht")))
+        st = self.lib.gdr_fwd_run(self.handle, ctypes.byref(args), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+        if st != _lib.GDR_OK:
+            raise GdrError(st, "gdr_fwd_run")
+
+    @property
+    def forward_launch_count(self) -> int:
+        return int(self.lib.gdr_fwd_launch_count(self.handle))
+
     @property
     def launch_count(self) -> int:
         return int(self.lib.gdr_bwd_launch_count(self.handle))
@@ -153,6 +174,76 @@ def gdr_bwd(q, k, v, beta, g, dO, h0=None, dht=None, cu_seqlens=None, *, scale=N
         if st != _lib.GDR_OK:
             raise GdrError(st, "gdr_bwd_get_status")
     return out
+
+
+def gdr_fwd(q, k, v, beta, g, h0=None, cu_seqlens=None, *, scale=None, BT=64, stream=None,
+            check_status=False):
+    """Forward of the chunked gated delta rule on CUDA tensors (shapes as :func:`gdr_bwd`).
+
+    Returns (o [B, T, Hv, V] in q's dtype, ht fp32 [N, Hv, V, K], the final state per sequence).
+    """
+    _check_cuda(q=q, k=k, v=v, beta=beta, g=g, h0=h0, cu_seqlens=cu_seqlens)
+    B, T, Hk, K = q.shape
+    Hv, V = v.shape[2], v.shape[3]
+    num_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    plan = GdrBwdPlan(B=B, T=T, Hk=Hk, Hv=Hv, K=K, V=V, BT=BT, num_seqs=num_seqs, per_channel=g.dim() == 4,
+                      scale=scale, qkv_dtype=q.dtype, beta_dtype=beta.dtype, has_h0=h0 is not None)
+    out = plan.alloc_forward_outputs(q.device)
+    ws = plan.alloc_workspace(q.device)
+    plan.run_forward(q=q, k=k, v=v, beta=beta, g=g, h0=h0, cu_seqlens=cu_seqlens, out=out, workspace=ws,
+                     stream=stream)
+    if check_status:
+        st = plan.get_status(ws, stream)
+        if st != _lib.GDR_OK:
+            raise GdrError(st, "gdr_bwd_get_status")
+    return out["o"], out["ht"]
+
+
+class ChunkGatedDeltaRule(torch.autograd.Function):
+    """o, ht = forward(q, k, v, beta, g, h0, cu_seqlens, scale, BT): the chunked gated delta rule with its
+    exact backward, both on the GPU kernels.  Gradients flow to q, k, v, beta, g (raw log-gate) and h0;
+    the backward recomputes the chunk states from the inputs (nothing but the inputs is saved)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, beta, g, h0=None, cu_seqlens=None, scale=None, BT=64):
+        for t in (q, k, v, beta, g, h0):
+            if t is not None and not t.is_contiguous():
+                raise ValueError("inputs must be contiguous")
+        B, T, Hk, K = q.shape
+        Hv, V = v.shape[2], v.shape[3]
+        num_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+        plan = GdrBwdPlan(B=B, T=T, Hk=Hk, Hv=Hv, K=K, V=V, BT=BT, num_seqs=num_seqs, per_channel=g.dim() == 4,
+                          scale=scale, qkv_dtype=q.dtype, beta_dtype=beta.dtype, has_h0=h0 is not None,
+                          has_dht=True)
+        out = plan.alloc_forward_outputs(q.device)
+        ws = plan.alloc_workspace(q.device)
+        plan.run_forward(q=q, k=k, v=v, beta=beta, g=g, h0=h0, cu_seqlens=cu_seqlens, out=out, workspace=ws)
+        ctx.plan = plan  # the workspace is released here; the backward takes a fresh one
+        ctx.save_for_backward(q, k, v, beta, g, h0, cu_seqlens)
+        return out["o"], out["ht"]
+
+    @staticmethod
+    def backward(ctx, do, dht):
+        q, k, v, beta, g, h0, cu_seqlens = ctx.saved_tensors
+        plan = ctx.plan
+        if do is None:
+            do = torch.zeros(*q.shape[:2], v.shape[2], v.shape[3], dtype=q.dtype, device=q.device)
+        if dht is None:
+            N = q.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
+            dht = torch.zeros(N, v.shape[2], v.shape[3], q.shape[3], dtype=torch.float32, device=q.device)
+        do, dht = do.contiguous(), dht.contiguous().float()
+        ws = plan.alloc_workspace(q.device)
+        out = plan.alloc_outputs(q.device)
+        plan.run(q=q, k=k, v=v, beta=beta, g=g, dO=do.to(q.dtype), h0=h0, dht=dht, cu_seqlens=cu_seqlens,
+                 out=out, workspace=ws)
+        return (out["dq"], out["dk"], out["dv"], out["dbeta"].to(beta.dtype), out["dg"],
+                out["dh0"] if h0 is not None else None, None, None, None)
+
+
+def chunk_gated_delta_rule(q, k, v, beta, g, h0=None, cu_seqlens=None, *, scale=None, BT=64):
+    """Differentiable chunked gated delta rule: returns (o, ht); see :class:`ChunkGatedDeltaRule`."""
+    _check_cuda(q=q, k=k, v=v, beta=beta, g=g, h0=h0, cu_seqlens=cu_seqlens)
+    return ChunkGatedDeltaRule.apply(q, k, v, beta, g, h0, cu_seqlens, scale, BT)
 
 
 def chunk_indices(cu_seqlens: torch.Tensor, BT: int, max_chunks: Optional[int] = None, stream=None):

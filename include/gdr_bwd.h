@@ -136,6 +136,33 @@ gdr_status gdr_bwd_get_status(gdr_bwd_plan *plan, void *workspace, void *stream)
 #define GDR_BWD_NOALLOC_MAX_WORKSPACE (64u << 20)
 gdr_status gdr_bwd_run_noalloc(gdr_bwd_plan *plan, const gdr_bwd_args *args, void *stream);
 
+/* ---- Forward pass (the output and final state that the backward above differentiates).
+ * Per sequence and value head, S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T and
+ * o_t = scale S_t q_t, computed chunkwise: the WY preparation and the state recompute of the backward,
+ * then per chunk o = scale (diag(Gamma) Q S_0^T + (M (.) Q K^T) V_new) ("FlashQLA backward explained",
+ * section 1: the forward whose saved state the backward recomputes; MindSpeed-Ops chunk_kda_bwd.md, input
+ * table: the chunk states h and v_new).  The per-channel gate acts on the K index as in the backward.
+ * Uses the backward's plan and workspace (gdr_bwd_workspace_bytes); dO, dht and the gradient fields of
+ * the descriptor are ignored.
+ *   q, k      [B, T, Hk, K]  qkv_dtype       v [B, T, Hv, V] qkv_dtype     beta [B, T, Hv] beta_dtype
+ *   g         fp32 [B, T, Hv] or [B, T, Hv, K] (raw log-gate)                h0 fp32 [N, Hv, V, K] or NULL
+ *   o         [B, T, Hv, V] in qkv_dtype, fully overwritten
+ *   ht        fp32 [N, Hv, V, K] final state per sequence and value head, or NULL (not returned)
+ * All device pointers are caller-owned; q, k, v and o 16-byte aligned, the others 4-byte aligned.
+ * Asynchronous on `stream`; GDR_ERR_INVALID_ARG for null required pointers, misalignment or a small
+ * workspace; device-side problems are read with gdr_bwd_get_status as for the backward. */
+typedef struct {
+    const void *q, *k, *v, *beta, *g, *h0;
+    const int32_t *cu_seqlens;
+    void *o;
+    float *ht;
+} gdr_fwd_args;
+gdr_status gdr_fwd_run(gdr_bwd_plan *plan, const gdr_fwd_args *args, void *workspace, size_t ws_bytes,
+                       void *stream);
+
+/* Number of kernel launches one gdr_fwd_run of this plan queues (0 for a NULL plan). */
+int gdr_fwd_launch_count(const gdr_bwd_plan *plan);
+
 /* Free the plan (NULL is accepted). */
 void gdr_bwd_destroy(gdr_bwd_plan *plan);
 
