@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="gdn_t32k_bf16")
     ap.add_argument("--cpu-sample-tokens", type=int, default=32768)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="which", choices=("bwd", "fwd"), default="bwd",
+                    help="bwd: the backward (the headline); fwd: the forward pass (o and the final state)")
     return ap.parse_args(argv)
 
 
@@ -247,6 +249,8 @@ def run_ours(args):
     build()
 
     prob = workload(args.workload)
+    if args.which == "fwd":
+        return run_forward_bench(args, prob, world, rank, local)
     plan = ops.plan_for(prob)
     dev = ops.problem_to_device(prob, "cuda")
     out = plan.alloc_outputs("cuda")
@@ -368,6 +372,54 @@ def run_ours(args):
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
+    print(json.dumps(line), flush=True)
+
+
+def run_forward_bench(args, prob, world, rank, local):
+    """The forward pass (gdr_fwd_run) on the same workload: device time with CUDA events, whole-path
+    roofline by the forward FLOP / byte conventions of counts.py."""
+    import torch
+    from chunked_gated_delta_09_gb300 import counts, ops
+
+    plan = ops.plan_for(prob)
+    dev = ops.problem_to_device(prob, "cuda")
+    fin = {k: dev[k] for k in ("q", "k", "v", "beta", "g", "h0", "cu_seqlens")}
+    out = plan.alloc_forward_outputs("cuda")
+    ws = plan.alloc_workspace("cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        plan.run_forward(out=out, workspace=ws, **fin)
+    torch.cuda.synchronize()
+    if plan.get_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    t0.record(stream)
+    for _ in range(args.steps):
+        plan.run_forward(out=out, workspace=ws, **fin)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world)
+    if plan.get_status(ws) != 0:
+        raise RuntimeError("device status after timing")
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    flops = counts.forward_total_flops(prob)
+    alg = counts.forward_algorithmic_bytes(prob)
+    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), alg / (peaks["hbm_gbs"] * 1e9))
+    line = {"metric": "GDN chunked fwd ms & TFLOP/s (o and final state), % of roofline",
+            "value": world * flops / (ms / 1e3) / 1e12, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "data": "synthetic", "pass": "fwd",
+            "config": workload_config(prob, world),
+            "path_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms / 1e3), "flops": flops,
+                              "algorithmic_bytes": alg},
+            "gpu_launches": plan.forward_launch_count * args.steps, "clocks": clk}
     print(json.dumps(line), flush=True)
 
 

@@ -106,3 +106,24 @@ def stage_bytes(prob) -> list:
               + dqdk_out + C * V * ov + C * 4 + CT * gk * 4)                                           # writes
     k5 = u * (CT * gk * 4 + C * gk * 4) + (0 if G == 1 else u * 2 * C * K * 4 + (u // G) * 2 * C * K * oq)
     return [float(k0), float(k1), float(k2), float(k3), float(k4), float(k5)]
+
+
+def forward_flops_per_chunk(C: int, K: int, V: int) -> float:
+    """The forward by the same convention: WY preparation (K K^T, Q K^T, W 2 C^2 K each; U 2 C^2 V; the
+    inverse 2/3 C^3), state recompute 4 C K V, output (Q~ S_0^T 2 C K V, Aqk V_new 2 C^2 V)."""
+    return 6.0 * C * K * V + 6.0 * C * C * K + 4.0 * C * C * V + (2.0 / 3.0) * C ** 3
+
+
+def forward_total_flops(prob) -> float:
+    return chunk_units(prob) * forward_flops_per_chunk(prob.BT, prob.K, prob.V)
+
+
+def forward_algorithmic_bytes(prob) -> int:
+    """Inputs q, k, v, beta, g, h0 read once; outputs o and the final state written once."""
+    T = prob.B * prob.T
+    gk = prob.K if prob.per_channel else 1
+    ib = _nbytes(prob.qkv_dtype)
+    state = prob.N * prob.Hv * prob.V * prob.K * 4
+    return int(2 * T * prob.Hk * prob.K * ib + T * prob.Hv * prob.V * ib + T * prob.Hv * _nbytes(prob.beta_dtype)
+               + T * prob.Hv * gk * 4 + (state if prob.h0 is not None else 0)
+               + T * prob.Hv * prob.V * ib + state)
