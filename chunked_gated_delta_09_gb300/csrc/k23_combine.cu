@@ -6,22 +6,23 @@
 // transitions (k2_scan_tc.cu writes Phi_s and Phi_s^T, k3_scan_tc.cu writes F_s).  Rows of the state are
 // independent, so a CTA owns CB_ROWS rows of one sequence x head (one wave of CTAs for the usual head
 // counts) and walks the segments serially, prefetching the next segment's transition and summary rows
-// with cp.async while it multiplies by the current ones.
+// with cp.async while it multiplies by the current ones.  Each thread accumulates four columns of all
+// the CTA's rows over one warp's slice of the reduction, so every transition element read from shared
+// memory serves 16 rows; the slices are summed in a fixed order.
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
 
 namespace gdr {
 
-constexpr int CB_THREADS = 1024;  // 16 rows x 32 column quads x 2 slices of the reduction
-constexpr int CB_ROWS = 16;
-constexpr int CB_LD = DT + 4;  // fp32 pitch of a transition tile (16-byte aligned rows)
+constexpr int CB_THREADS = 256;  // 8 warps = 8 slices of 16 reduction indices; lane = 4 output columns
+constexpr int CB_ROWS = 16;      // rows of the state per CTA (all of them in every thread)
+constexpr int CB_PP = DT + 4;    // fp32 pitch of a partial-sum row (16-byte reads without bank conflicts)
 
 template <bool FWD>
 __global__ void __launch_bounds__(CB_THREADS) k23_combine(const Params P) {
-    __shared__ __align__(16) float X[CB_ROWS][DT];
-    __shared__ __align__(16) float part[CB_ROWS][DT];  // partial sums of reduction slice 1
-    extern __shared__ __align__(16) float dyn[];         // Ph [2][DT][CB_LD], Ad [2][CB_ROWS][DT]
-    float *Ph = dyn, *Ad = dyn + 2 * DT * CB_LD;
+    __shared__ __align__(16) float XT[DT][CB_ROWS];  // the current rows, transposed: XT[j][r]
+    extern __shared__ __align__(16) float dyn[];     // Ph [2][DT][DT], Ad [2][CB_ROWS][DT], part [8][CB_ROWS][CB_PP]
+    float *Ph = dyn, *Ad = dyn + 2 * DT * DT, *part = Ad + 2 * CB_ROWS * DT;
     if (*P.status & ST_BAD_SEQLENS) return;
     const int s = blockIdx.x / P.Hv, hv = blockIdx.x % P.Hv, r0 = blockIdx.y * CB_ROWS;
     int bos, eos;
@@ -29,9 +30,7 @@ __global__ void __launch_bounds__(CB_THREADS) k23_combine(const Params P) {
     const int nc = (eos - bos + P.BT - 1) / P.BT;
     const int nss = (nc + P.Lseg - 1) / P.Lseg;  // segments holding chunks
     if (nss == 0) return;
-    const int tid = threadIdx.x;
-    const int js = tid >> 9;                                         // reduction slice: j in [64 js, 64 js + 64)
-    const int r = (tid >> 5) & (CB_ROWS - 1), k0 = (tid & 31) * 4;  // 4 outputs per thread
+    const int tid = threadIdx.x, w = tid >> 5, k0 = (tid & 31) * 4;
     const size_t su0 = ((size_t)s * P.Hv + hv) * P.NS;
     float *out = FWD ? P.segSin : P.segdS;
     const float *init = FWD ? P.h0 : P.dht;
@@ -42,11 +41,8 @@ __global__ void __launch_bounds__(CB_THREADS) k23_combine(const Params P) {
     auto prefetch = [&](int step, int buf) {
         const int sg = FWD ? step : nss - 1 - step;
         const float *src = trans + (su0 + sg) * DT * DT;
-        float *dst = Ph + buf * DT * CB_LD;
-        for (int e = tid; e < DT * DT / 4; e += CB_THREADS) {
-            int j = e / (DT / 4), k4 = (e % (DT / 4)) * 4;
-            cp_async16(dst + j * CB_LD + k4, src + (size_t)j * DT + k4);
-        }
+        float *dst = Ph + buf * DT * DT;
+        for (int e = tid; e < DT * DT / 4; e += CB_THREADS) cp_async16(dst + 4 * e, src + 4 * e);
         const float *asrc = adds + (su0 + sg) * DT * DT + (size_t)r0 * DT;
         float *adst = Ad + buf * CB_ROWS * DT;
         for (int e = tid; e < CB_ROWS * DT / 4; e += CB_THREADS) cp_async16(adst + 4 * e, asrc + 4 * e);
@@ -58,7 +54,7 @@ __global__ void __launch_bounds__(CB_THREADS) k23_combine(const Params P) {
         int rr = e / DT, k = e % DT, v = r0 + rr;
         float x = 0.f;
         if (init && v < P.V && k < P.K) x = init[(((size_t)s * P.Hv + hv) * P.V + v) * P.K + k];
-        X[rr][k] = x;
+        XT[k][rr] = x;
         out[(su0 + (FWD ? 0 : nss - 1)) * DT * DT + (size_t)v * DT + k] = x;
     }
     for (int step = 0; step < nss - 1; ++step) {
@@ -66,36 +62,59 @@ __global__ void __launch_bounds__(CB_THREADS) k23_combine(const Params P) {
         const int sg = FWD ? step : nss - 1 - step;  // segment whose summary is applied
         const int dst = FWD ? sg + 1 : sg - 1;
         cp_async_wait<0>();
-        __syncthreads();  // transition and summary of this step and X visible; previous step's readers done
+        __syncthreads();  // this step's transition and summary, and XT, visible; last step's readers done
         if (step + 1 < nss - 1) prefetch(step + 1, buf ^ 1);
-        const float *ph = Ph + buf * DT * CB_LD;
-        float4 y = js == 0 ? *reinterpret_cast<const float4 *>(Ad + buf * CB_ROWS * DT + r * DT + k0)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int j = 64 * js; j < 64 * js + 64; ++j) {
-            const float x = X[r][j];
-            const float4 a = *reinterpret_cast<const float4 *>(&ph[j * CB_LD + k0]);
-            y.x += x * a.x;
-            y.y += x * a.y;
-            y.z += x * a.z;
-            y.w += x * a.w;
+        // partial products of this warp's 16 reduction indices: all 16 rows x columns k0 .. k0+3
+        const float *ph = Ph + buf * DT * DT;
+        float acc[CB_ROWS][4];
+#pragma unroll
+        for (int r = 0; r < CB_ROWS; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+#pragma unroll 4
+        for (int j = 16 * w; j < 16 * w + 16; ++j) {
+            const float4 a = *reinterpret_cast<const float4 *>(ph + j * DT + k0);
+#pragma unroll
+            for (int r4 = 0; r4 < CB_ROWS; r4 += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(&XT[j][r4]);
+                const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[r4 + i][0] += xs[i] * a.x;
+                    acc[r4 + i][1] += xs[i] * a.y;
+                    acc[r4 + i][2] += xs[i] * a.z;
+                    acc[r4 + i][3] += xs[i] * a.w;
+                }
+            }
         }
-        if (js > 0) *reinterpret_cast<float4 *>(&part[r][k0]) = y;
-        __syncthreads();  // partials written; everyone done reading X
-        if (js == 0) {
-            const float4 z = *reinterpret_cast<const float4 *>(&part[r][k0]);
-            y.x += z.x;
-            y.y += z.y;
-            y.z += z.z;
-            y.w += z.w;
-            *reinterpret_cast<float4 *>(&X[r][k0]) = y;
-            *reinterpret_cast<float4 *>(out + (su0 + dst) * DT * DT + (size_t)(r0 + r) * DT + k0) = y;
+#pragma unroll
+        for (int r = 0; r < CB_ROWS; ++r)
+            *reinterpret_cast<float4 *>(part + (w * CB_ROWS + r) * CB_PP + k0) =
+                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+        __syncthreads();  // partials written; everyone done reading XT
+        // sum the 8 slices in a fixed order, add the summary rows; lanes walk rows so that the transposed
+        // writes hit distinct banks
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int r = tid & 15, kq = 4 * ((tid >> 4) + 16 * p);
+            float4 y = *reinterpret_cast<const float4 *>(Ad + buf * CB_ROWS * DT + r * DT + kq);
+#pragma unroll
+            for (int ww = 0; ww < 8; ++ww) {
+                const float4 z = *reinterpret_cast<const float4 *>(part + (ww * CB_ROWS + r) * CB_PP + kq);
+                y.x += z.x;
+                y.y += z.y;
+                y.z += z.z;
+                y.w += z.w;
+            }
+            XT[kq][r] = y.x;
+            XT[kq + 1][r] = y.y;
+            XT[kq + 2][r] = y.z;
+            XT[kq + 3][r] = y.w;
+            *reinterpret_cast<float4 *>(out + (su0 + dst) * DT * DT + (size_t)(r0 + r) * DT + kq) = y;
         }
     }
 }
 
 cudaError_t launch_k23_combine(const Params &P, bool fwd, cudaStream_t stream) {
-    size_t smem = sizeof(float) * (2 * DT * CB_LD + 2 * CB_ROWS * DT);
+    size_t smem = sizeof(float) * (2 * DT * DT + 2 * CB_ROWS * DT + 8 * CB_ROWS * CB_PP);
     cudaError_t e;
     dim3 grid(P.N * P.Hv, DT / CB_ROWS);
     if (fwd) {
