@@ -11,9 +11,10 @@
 // K~ = K (.) exp(gamma_C - gamma) and Q~ = Q (.) exp(gamma) that the two scans use, and D = scale dO.
 // Per-channel gate: each exp(gamma_a - gamma_b) is taken per key channel inside the K contraction.
 //
-// Every matrix output is written in the core-matrix tile layout that the tensor-core kernels read:
-// element-wise outputs straight from registers (8 lanes write one contiguous 128-byte core matrix),
-// matrix products through shared memory and one bulk copy per tile.
+// Every matrix output is written in the core-matrix tile layout that the tensor-core kernels read,
+// straight from registers: 8 lanes of an element-wise pass write one contiguous 128-byte core matrix, and
+// a warp's pair stores of an MMA accumulator cover whole core matrices (no store waits at the end of a
+// CTA, so the next CTA on the SM starts at once).  The forward pass runs the same kernel without dO.
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
 #include "tc_util.cuh"
@@ -23,9 +24,9 @@ namespace gdr {
 constexpr int K1_THREADS = 256;
 
 struct __align__(1024) K1Smem {
-    // Ks later holds W, Qs holds beta Gamma K then U, Vs holds beta V
+    // Qs later holds beta Gamma K, Vs beta V
     unsigned char Ks[CT * DT * 2], Qs[CT * DT * 2], Vs[CT * DT * 2];
-    unsigned char oT[CT * CT * 2], oAqk[CT * CT * 2];
+    unsigned char oT[CT * CT * 2];  // T as the fp16 operand of the W and U products
     float A32[CT][CT + 1];
     float T32[CT][CT + 1];
     float X32[32][33];  // scratch of the block products
@@ -156,14 +157,20 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
         zero_acc(qk);
         warp_mma_ct<1, 4, false, true>(kk, S.Ks, DT, S.Ks, DT, m0, n0, DT);
         warp_mma_ct<1, 4, false, true>(qk, S.Qs, DT, S.Ks, DT, m0, n0, DT);
+        unsigned char *aqk_g = reinterpret_cast<unsigned char *>(P.Aqk + u * CT * CT);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int i = acc_row(m0, 0, e), j = acc_col(n0, nt, e);
-                float d = expf(S.gam[i] - S.gam[j]);
-                S.A32[i][j] = j < i ? S.beta[i] * d * kk[0][nt][e] : 0.f;
-                ctile_set(S.oAqk, i, j, CT, j <= i ? d * qk[0][nt][e] : 0.f);
+            for (int e = 0; e < 4; e += 2) {
+                const int i = acc_row(m0, 0, e), j = acc_col(n0, nt, e);
+                float aq[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float d = expf(S.gam[i] - S.gam[j + h]);
+                    S.A32[i][j + h] = j + h < i ? S.beta[i] * d * kk[0][nt][e + h] : 0.f;
+                    aq[h] = j + h <= i ? d * qk[0][nt][e + h] : 0.f;
+                }
+                *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j, CT)) = __floats2half2_rn(aq[0], aq[1]);
             }
     } else {
         for (int e = tid; e < CT * CT; e += K1_THREADS) {
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
                 }
             }
             S.A32[i][j] = j < i ? S.beta[i] * akk : 0.f;
-            ctile_set(S.oAqk, i, j, CT, j <= i ? aqk : 0.f);
+            ctile_set(reinterpret_cast<unsigned char *>(P.Aqk + u * CT * CT), i, j, CT, j <= i ? aqk : 0.f);
         }
     }
     __syncthreads();
@@ -247,10 +254,11 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
 #pragma unroll
         for (int t = 0; t < 8; ++t) x[t] = S.T32[i][j8 + t];
         tc::st_tile8(S.oT, i, j8, CT, x);
+        tc::st_tile8(reinterpret_cast<unsigned char *>(P.Tm + u * CT * CT), i, j8, CT, x);
     }
     __syncthreads();
 
-    // ---- W = T (beta Gamma K) into K's tile; U^T = (beta V)^T T^T into Q's tile as a [v][c] tile
+    // ---- W = T (beta Gamma K) and U^T = (beta V)^T T^T (a [v][c] tile), stored from the accumulators
     {
         float acc[1][8][4];
         {
@@ -262,35 +270,23 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
 #pragma unroll
                 for (int e = 0; e < 4; e += 2) {
                     int i = acc_row(m0, 0, e), j = acc_col(n0, nt, e);
-                    *reinterpret_cast<__half2 *>(S.Ks + ctile_off(i, j, DT)) =
-                        __floats2half2_rn(acc[0][nt][e], acc[0][nt][e + 1]);
+                    *reinterpret_cast<__half2 *>(reinterpret_cast<unsigned char *>(P.W + u * CT * DT) +
+                                                 ctile_off(i, j, DT)) = __floats2half2_rn(acc[0][nt][e], acc[0][nt][e + 1]);
                 }
         }
         {
             const int m0 = wid * 16;  // 8 warps x 16 value rows, all 64 chunk columns
             zero_acc(acc);
             warp_mma_ct<1, 8, true, true>(acc, S.Vs, DT, S.oT, CT, m0, 0, CT);
-            __syncthreads();  // every warp finished reading beta Gamma K before U^T overwrites it
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; e += 2) {
                     int v = acc_row(m0, 0, e), c = acc_col(0, nt, e);
-                    *reinterpret_cast<__half2 *>(S.Qs + ctile_off(v, c, CT)) =
-                        __floats2half2_rn(acc[0][nt][e], acc[0][nt][e + 1]);
+                    *reinterpret_cast<__half2 *>(reinterpret_cast<unsigned char *>(P.U + u * CT * DT) +
+                                                 ctile_off(v, c, CT)) = __floats2half2_rn(acc[0][nt][e], acc[0][nt][e + 1]);
                 }
         }
-    }
-    // ---- bulk stores of the product tiles
-    tc::fence_smem_to_async();
-    __syncthreads();
-    if (tid == 0) {
-        tc::bulk_s2g(P.Tm + u * CT * CT, S.oT, CT * CT * 2);
-        tc::bulk_s2g(P.Aqk + u * CT * CT, S.oAqk, CT * CT * 2);
-        tc::bulk_s2g(P.W + u * CT * DT, S.Ks, CT * DT * 2);
-        tc::bulk_s2g(P.U + u * CT * DT, S.Qs, CT * DT * 2);
-        tc::bulk_commit();
-        tc::bulk_wait();
     }
 }
 
