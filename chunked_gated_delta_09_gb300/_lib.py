@@ -14,7 +14,7 @@ GDR_F32, GDR_BF16, GDR_F16 = 0, 1, 2
 # every function the header declares
 EXPORTS = ("gdr_bwd_create", "gdr_bwd_workspace_bytes", "gdr_bwd_run", "gdr_bwd_run_profiled",
            "gdr_bwd_launch_count", "gdr_bwd_get_status", "gdr_bwd_run_noalloc", "gdr_bwd_destroy",
-           "gdr_chunk_indices", "gdr_status_string", "gdr_fwd_run", "gdr_fwd_launch_count")
+           "gdr_chunk_indices", "gdr_status_string", "gdr_fwd_run", "gdr_fwd_launch_count", "gdr_wy_bwd_run")
 NOALLOC_MAX_WORKSPACE = 64 << 20
 NUM_STAGES = 6
 STAGE_NAMES = ("k0_chunk_indices", "k1_wy_prep", "k2_fused_gdr_h", "k3_dh_scan", "k4_intra_grad", "k5_dg_reduce")
@@ -35,6 +35,11 @@ class GdrBwdArgs(ctypes.Structure):
 
 class GdrFwdArgs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "beta", "g", "h0", "cu_seqlens", "o", "ht")]
+
+
+class GdrWyArgs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "v_new", "beta", "A", "dO", "dv", "g", "h", "dh",
+                                                "cu_seqlens", "dq", "dk", "dv_out", "db", "dg", "dA")]
 
 
 class GdrError(RuntimeError):
@@ -80,6 +85,8 @@ def load(path: str | None = None):
         lib.gdr_fwd_run.restype = ci
         lib.gdr_fwd_launch_count.argtypes = [vp]
         lib.gdr_fwd_launch_count.restype = ci
+        lib.gdr_wy_bwd_run.argtypes = [vp, ctypes.POINTER(GdrWyArgs), vp, sz, vp]
+        lib.gdr_wy_bwd_run.restype = ci
         lib.gdr_status_string.argtypes = [ci]
         lib.gdr_status_string.restype = ctypes.c_char_p
         _lib = lib

@@ -333,6 +333,53 @@ gdr_status gdr_fwd_run(gdr_bwd_plan *plan, const gdr_fwd_args *a, void *workspac
     return GDR_OK;
 }
 
+gdr_status gdr_wy_bwd_run(gdr_bwd_plan *plan, const gdr_wy_args *a, void *workspace, size_t ws_bytes,
+                          void *stream_) {
+    if (!plan || !a) return GDR_ERR_INVALID_ARG;
+    const gdr_bwd_desc &d = plan->d;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (!d.gate_per_channel || d.Hk != d.Hv || d.dqdk_dtype != GDR_F32 || d.beta_dtype != d.qkv_dtype ||
+        d.dv_dtype != d.qkv_dtype)
+        return GDR_ERR_UNSUPPORTED;
+    const void *req[] = {a->q, a->k, a->v, a->v_new, a->beta, a->A, a->dO, a->dv, a->g, a->h, a->dh,
+                         a->dq, a->dk, a->dv_out, a->db, a->dg, a->dA};
+    for (const void *ptr : req)
+        if (!ptr) return GDR_ERR_INVALID_ARG;
+    if (!plan->dense && !a->cu_seqlens) return GDR_ERR_INVALID_ARG;
+    const void *vec[] = {a->q, a->k, a->v, a->v_new, a->dO, a->dv, a->A, a->dq, a->dk, a->dv_out, a->dA};
+    for (const void *ptr : vec)
+        if (!aligned(ptr, 16)) return GDR_ERR_INVALID_ARG;
+    const void *nat[] = {a->beta, a->g, a->h, a->dh, a->db, a->dg, a->cu_seqlens};
+    for (const void *ptr : nat)
+        if (ptr && !aligned(ptr, 4)) return GDR_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < plan->total) return GDR_ERR_INVALID_ARG;
+
+    Params P;
+    fill_common(plan, reinterpret_cast<char *>(workspace), P);
+    P.q = a->q;
+    P.k = a->k;
+    P.v = a->v;
+    P.beta = a->beta;
+    P.dO = a->dO;
+    P.g = a->g;
+    P.cu = plan->dense ? nullptr : a->cu_seqlens;
+    P.dq = a->dq;
+    P.dk = a->dk;
+    P.dv = a->dv_out;
+    P.dbeta = a->db;
+    P.dg = a->dg;
+    P.dA_out = a->dA;
+    if (cudaMemsetAsync(P.status, 0, sizeof(int), stream) != cudaSuccess) return GDR_ERR_CUDA;
+    if (!plan->dense &&
+        launch_k0(a->cu_seqlens, plan->N, d.BT, plan->max_chunks, d.T, P.chunk_idx, P.chunk_off, P.status, stream) !=
+            cudaSuccess)
+        return GDR_ERR_CUDA;
+    if (plan->max_chunks == 0) return GDR_OK;
+    if (launch_k7_wy_inputs(P, a->A, a->v_new, a->dv, a->h, a->dh, stream) != cudaSuccess) return GDR_ERR_CUDA;
+    if (launch_k4_wy(P, stream) != cudaSuccess) return GDR_ERR_CUDA;
+    return GDR_OK;
+}
+
 int gdr_fwd_launch_count(const gdr_bwd_plan *plan) {
     if (!plan) return 0;
     int n = plan->dense ? 0 : 1;                             // K0

@@ -43,6 +43,8 @@ struct Params {
     // outputs (forward): o [T][Hv][V] in qkv dtype, final state ht [N][Hv][V][K] fp32 (may be null)
     void *o;
     float *ht;
+    // output of the WY-gradient stage taken alone: dA [T][Hv][BT] fp32 (gradient with respect to A_kk)
+    float *dA_out;
     // workspace
     int *status;
     int32_t *chunk_idx;  // [max_chunks][2]

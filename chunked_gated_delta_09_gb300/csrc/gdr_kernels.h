@@ -27,5 +27,9 @@ cudaError_t launch_k4_tc(const Params &P, cudaStream_t stream);
 cudaError_t launch_k5(const Params &P, cudaStream_t stream);
 // forward output o = scale (diag(Gamma) Q S_0^T + (M (.) Q K^T) V_new) per chunk
 cudaError_t launch_k6_fwd_output(const Params &P, cudaStream_t stream);
+// the WY-gradient stage taken alone: its inputs as workspace tiles, then the per-chunk kernel in that mode
+cudaError_t launch_k7_wy_inputs(const Params &P, const void *A, const void *v_new, const void *dv_in, const float *h,
+                                const float *dh, cudaStream_t stream);
+cudaError_t launch_k4_wy(const Params &P, cudaStream_t stream);
 
 }  // namespace gdr

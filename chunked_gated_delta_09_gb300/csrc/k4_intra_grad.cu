@@ -65,7 +65,11 @@ __device__ __forceinline__ void store_ck(const float (&a)[1][NT][4], int m0, int
         }
 }
 
-template <typename Tin, bool PC>
+// WY = true: the WY-gradient stage taken alone (MindSpeed-Ops chunk_kda_bwd.md,
+// chunk_kda_bwd_wy_dqkg_fused): no intra-chunk attention terms (P, dq_intra, dk_O) and no terms through A_kk
+// (E, dk_Ar, dk_Ac, the A part of dbeta); instead dA = strict_lower(-T^T dT T^T) is written out, and the
+// gradient of the cumulative gate goes straight to dg (no reverse cumsum follows).
+template <typename Tin, bool PC, bool WY>
 __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     K4Smem &S = *reinterpret_cast<K4Smem *>(smem_raw);
@@ -162,12 +166,12 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         auto row_dbeta = [&](int r) -> float {
             float x = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x += S.dbp[i][r];
+            for (int i = WY ? 4 : 0; i < 8; ++i) x += S.dbp[i][r];
             return x;
         };
 
         // ---- S1: P = (D V_new^T) (.) causal mask (.) [scalar: decay]
-        {
+        if (!WY) {
             float g1[1][NC][4];
             zero_acc(g1);
             warp_mma_ct<1, NC, false, false>(g1, S.Ds, DT, S.VnT, CT, cm0, cn0, DT);
@@ -202,7 +206,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     dq[0][nt][e] *= PC ? expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e))) : S.G[acc_row(m0, 0, e)];
-            if (!PC) {
+            if (WY) {
+            } else if (!PC) {
                 warp_mma_ct<1, NK, false, false>(dq, S.Pms, CT, S.Ks, DT, m0, n0, CT);
             } else {
 #pragma unroll
@@ -232,7 +237,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         // ---- S3: dk_O = P^T Q
         {
             zero_acc(dk);
-            if (!PC) {
+            if (WY) {
+            } else if (!PC) {
                 warp_mma_ct<1, NK, true, false>(dk, S.Pms, CT, S.Qs, DT, m0, n0, CT);
             } else {
 #pragma unroll
@@ -434,7 +440,19 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             float da[1][NC][4], kk[1][NC][4];
             zero_acc(da);
             warp_mma_ct<1, NC, true, false>(da, S.Ts, CT, Xs, CT, cm0, cn0, CT);
-            if (!PC) {
+            if (WY) {  // the stage's output: dA [token][chunk position], strictly lower, fp32
+#pragma unroll
+                for (int nt = 0; nt < NC; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; e += 2) {
+                        const int i = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);  // j even
+                        if (i < len && j < P.BT) {
+                            float2 x = make_float2(j < i ? -da[0][nt][e] : 0.f, j + 1 < i ? -da[0][nt][e + 1] : 0.f);
+                            *reinterpret_cast<float2 *>(P.dA_out + ((size_t)(ci.tok0 + i) * P.Hv + hv) * P.BT + j) = x;
+                        }
+                    }
+            }
+            if (!PC && !WY) {
                 zero_acc(kk);
                 warp_mma_ct<1, NC, false, true>(kk, S.Ks, DT, S.Ks, DT, cm0, cn0, DT);
             }
@@ -446,7 +464,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                     int i = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
                     float dA = j < i ? -da[0][nt][e] : 0.f;
                     float L = 1.f, kkd = 0.f;
-                    if (j < i) {
+                    if (!WY && j < i) {
                         if (!PC) {
                             L = expf(S.gam[i] - S.gam[j]);
                             kkd = L * kk[0][nt][e];
@@ -456,7 +474,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                         }
                     }
                     rb[e >> 1] += dA * kkd;
-                    ctile_set(Es, i, j, CT, S.beta[i] * (PC ? 1.f : L) * dA);
+                    if (!WY) ctile_set(Es, i, j, CT, S.beta[i] * (PC ? 1.f : L) * dA);
                 }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -479,7 +497,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             issue_TVn(next);
         }
         // ---- S11: dk_Ar = E K (+), dk_Ac = E^T K (-)
-        {
+        if (!WY) {
             float a[1][NK][4], b[1][NK][4];
             zero_acc(a);
             zero_acc(b);
@@ -553,7 +571,11 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                         for (int i = 0; i < 8; ++i) l += S.lrp[i][c];
                         x += l;
                     }
-                    P.dgam[(u * CT + r) * DT + c] = r < len ? x : 0.f;
+                    if (WY) {  // gradient of the cumulative gate, straight to the output
+                        if (r < len && c < P.K) P.dg[((size_t)(ci.tok0 + r) * P.Hv + hv) * P.K + c] = x;
+                    } else {
+                        P.dgam[(u * CT + r) * DT + c] = r < len ? x : 0.f;
+                    }
                 }
             if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = row_dbeta(tid);
         }
@@ -562,10 +584,10 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     }
 }
 
-template <typename Tin, bool PC>
+template <typename Tin, bool PC, bool WY = false>
 static cudaError_t launch_k4_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(K4Smem) + (PC ? sizeof(float) * CT * DT : 0);
-    cudaError_t e = cudaFuncSetAttribute(k4_intra_grad<Tin, PC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k4_intra_grad<Tin, PC, WY>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, nsm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -573,7 +595,7 @@ static cudaError_t launch_k4_t(const Params &P, cudaStream_t stream) {
     const long items = (long)P.max_chunks * P.Hv;
     if (items == 0) return cudaSuccess;
     const int grid = (int)(items < nsm ? items : nsm);  // one persistent CTA per SM
-    k4_intra_grad<Tin, PC><<<grid, K4_THREADS, smem, stream>>>(P);
+    k4_intra_grad<Tin, PC, WY><<<grid, K4_THREADS, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
@@ -582,6 +604,13 @@ cudaError_t launch_k4(const Params &P, cudaStream_t stream) {
     if (P.qkv_dtype == BF16)
         return P.per_channel ? launch_k4_t<__nv_bfloat16, true>(P, stream) : launch_k4_t<__nv_bfloat16, false>(P, stream);
     return P.per_channel ? launch_k4_t<__half, true>(P, stream) : launch_k4_t<__half, false>(P, stream);
+}
+
+// The WY-gradient stage alone (per-channel gate, dq / dk in fp32).
+cudaError_t launch_k4_wy(const Params &P, cudaStream_t stream) {
+    if (P.qkv_dtype == F32) return launch_k4_t<float, true, true>(P, stream);
+    if (P.qkv_dtype == BF16) return launch_k4_t<__nv_bfloat16, true, true>(P, stream);
+    return launch_k4_t<__half, true, true>(P, stream);
 }
 
 }  // namespace gdr

@@ -13,7 +13,7 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import GdrBwdArgs, GdrBwdDesc, GdrError, GdrFwdArgs
+from ._lib import GdrBwdArgs, GdrBwdDesc, GdrError, GdrFwdArgs, GdrWyArgs
 
 _DT = {torch.float32: _lib.GDR_F32, torch.bfloat16: _lib.GDR_BF16, torch.float16: _lib.GDR_F16}
 
@@ -244,6 +244,43 @@ def chunk_gated_delta_rule(q, k, v, beta, g, h0=None, cu_seqlens=None, *, scale=
     """Differentiable chunked gated delta rule: returns (o, ht); see :class:`ChunkGatedDeltaRule`."""
     _check_cuda(q=q, k=k, v=v, beta=beta, g=g, h0=h0, cu_seqlens=cu_seqlens)
     return ChunkGatedDeltaRule.apply(q, k, v, beta, g, h0, cu_seqlens, scale, BT)
+
+
+def gdr_wy_bwd(q, k, v, v_new, g, beta, A, h, do, dh, dv, scale=None, cu_seqlens=None, chunk_size=64,
+               stream=None, check_status=False):
+    """The WY-gradient stage taken alone (gdr_wy_bwd_run; per-channel gate), with the argument order and
+    return order (dq, dk, dv, db, dg, dA) of the operation it follows.  q, k [B, T, H, K]; v, v_new, do, dv
+    [B, T, H, V]; beta [B, T, H]; A [B, T, H, BT] (one dtype: fp16, bf16 or fp32); g fp32 [B, T, H, K]
+    (chunk-local cumulative gate); h, dh fp32 [B, NT, H, K, V]; cu_seqlens int32 [N+1] (B == 1) or None."""
+    _check_cuda(q=q, k=k, v=v, v_new=v_new, g=g, beta=beta, A=A, h=h, do=do, dh=dh, dv=dv, cu_seqlens=cu_seqlens)
+    B, T, H, K = q.shape
+    V = v.shape[3]
+    if A.shape[-1] != chunk_size:
+        raise ValueError("chunk_size must equal A.shape[-1]")
+    num_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    plan = GdrBwdPlan(B=B, T=T, Hk=H, Hv=H, K=K, V=V, BT=chunk_size, num_seqs=num_seqs, per_channel=True,
+                      scale=scale, qkv_dtype=q.dtype, beta_dtype=q.dtype, dqdk_dtype=torch.float32,
+                      dv_dtype=q.dtype)
+    dev = q.device
+    out = dict(dq=torch.empty(B, T, H, K, dtype=torch.float32, device=dev),
+               dk=torch.empty(B, T, H, K, dtype=torch.float32, device=dev),
+               dv=torch.empty(B, T, H, V, dtype=q.dtype, device=dev),
+               db=torch.empty(B, T, H, dtype=torch.float32, device=dev),
+               dg=torch.empty(B, T, H, K, dtype=torch.float32, device=dev),
+               dA=torch.empty(B, T, H, chunk_size, dtype=torch.float32, device=dev))
+    ws = plan.alloc_workspace(dev)
+    args = GdrWyArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), v_new=_ptr(v_new), beta=_ptr(beta), A=_ptr(A), dO=_ptr(do),
+                     dv=_ptr(dv), g=_ptr(g), h=_ptr(h), dh=_ptr(dh), cu_seqlens=_ptr(cu_seqlens),
+                     dq=_ptr(out["dq"]), dk=_ptr(out["dk"]), dv_out=_ptr(out["dv"]), db=_ptr(out["db"]),
+                     dg=_ptr(out["dg"]), dA=_ptr(out["dA"]))
+    st = plan.lib.gdr_wy_bwd_run(plan.handle, ctypes.byref(args), _ptr(ws), ws.numel(), _stream_ptr(stream))
+    if st != _lib.GDR_OK:
+        raise GdrError(st, "gdr_wy_bwd_run")
+    if check_status:
+        st = plan.get_status(ws, stream)
+        if st != _lib.GDR_OK:
+            raise GdrError(st, "gdr_bwd_get_status")
+    return out["dq"], out["dk"], out["dv"], out["db"], out["dg"], out["dA"]
 
 
 def chunk_indices(cu_seqlens: torch.Tensor, BT: int, max_chunks: Optional[int] = None, stream=None):

@@ -163,6 +163,33 @@ gdr_status gdr_fwd_run(gdr_bwd_plan *plan, const gdr_fwd_args *args, void *works
 /* Number of kernel launches one gdr_fwd_run of this plan queues (0 for a NULL plan). */
 int gdr_fwd_launch_count(const gdr_bwd_plan *plan);
 
+/* ---- The WY-gradient stage taken alone (MindSpeed-Ops chunk_kda_bwd.md: chunk_kda_bwd_wy_dqkg_fused;
+ * signature, input / output tables and "implementation principle").  For the per-channel (KDA) gate
+ * only: the plan must have gate_per_channel = 1, Hk == Hv (= H), dqdk_dtype GDR_F32, beta_dtype and
+ * dv_dtype equal to qkv_dtype; otherwise GDR_ERR_UNSUPPORTED.  Per chunk and head it returns the gradients
+ * that flow through the chunk's state terms and its WY factors W = A diag(beta) (K (.) exp(g)),
+ * U = A diag(beta) V, with h, dh, v_new, dv and do held fixed (the intra-chunk Q K^T terms and the terms
+ * through A_kk are left to later stages, which receive dA):
+ *   inputs  q, k [B, T, H, K]; v, v_new, do, dv [B, T, H, V]; beta [B, T, H]; A [B, T, H, BT]  (qkv_dtype)
+ *           g  fp32 [B, T, H, K]   chunk-local cumulative log gate
+ *           h, dh fp32 [B, NT, H, K, V]   state entering each chunk / gradient of the state leaving it
+ *           (varlen: B = 1 and NT = total chunks, numbered sequence-major)
+ *   outputs dq, dk fp32 [B, T, H, K]; dv_out [B, T, H, V] (qkv_dtype); db fp32 [B, T, H];
+ *           dg fp32 [B, T, H, K] (with respect to the cumulative gate); dA fp32 [B, T, H, BT], the gradient
+ *           with respect to A_kk where A = (I + A_kk)^-1 (strictly lower; other entries are zero).
+ * scale multiplies dq; all pointers are device, caller-owned; q, k, v, v_new, do, dv, A, dq, dk, dv_out and
+ * dA 16-byte aligned, the others 4-byte aligned.  Uses the plan's workspace; asynchronous on `stream`. */
+typedef struct {
+    const void *q, *k, *v, *v_new, *beta, *A, *dO, *dv;
+    const float *g, *h, *dh;
+    const int32_t *cu_seqlens;
+    float *dq, *dk;
+    void *dv_out;
+    float *db, *dg, *dA;
+} gdr_wy_args;
+gdr_status gdr_wy_bwd_run(gdr_bwd_plan *plan, const gdr_wy_args *args, void *workspace, size_t ws_bytes,
+                          void *stream);
+
 /* Free the plan (NULL is accepted). */
 void gdr_bwd_destroy(gdr_bwd_plan *plan);
 

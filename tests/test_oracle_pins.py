@@ -297,3 +297,78 @@ def test_chunk_index_enumeration_matches_golden():
         idx, off = enumerate_chunks(c["cu_seqlens"], c["BT"])
         assert [list(x) for x in idx] == c["chunk_indices"]
         assert off == c["chunk_offsets"]
+
+
+# ---------------------------------------------------------------- the WY-gradient stage taken alone (row f4)
+def _wy_inputs(seed, C, K, V):
+    rng = np.random.default_rng(seed)
+    q, k = rng.standard_normal((C, K)), rng.standard_normal((C, K))
+    v, v_new, do, dv = (rng.standard_normal((C, V)) for _ in range(4))
+    g = np.cumsum(-np.log1p(np.exp(-rng.standard_normal((C, K)))), axis=0)  # cumulative logsigmoid
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal(C)))
+    A_kk = np.tril(0.3 * rng.standard_normal((C, C)), -1)
+    h, dh = rng.standard_normal((K, V)), rng.standard_normal((K, V))
+    return dict(q=q, k=k, v=v, v_new=v_new, g=g, beta=beta, A_kk=A_kk, h=h, do=do, dh=dh, dv=dv)
+
+
+@pytest.mark.parametrize("C,K,V", [(5, 3, 4), (1, 2, 2), (4, 4, 3)])
+def test_wy_stage_gradients_match_finite_differences(C, K, V):
+    """Every output of the WY-stage oracle (dq, dk, dv, db, dg, and dA through A = (I + A_kk)^-1) is the
+    central finite difference of its defining scalar, element by element."""
+    from oracle import wy_stage
+    x = _wy_inputs(11 + C, C, K, V)
+    scale = 0.7
+
+    def loss(d):
+        A = np.linalg.inv(np.eye(C) + d["A_kk"])
+        return wy_stage.chunk_loss(d["q"], d["k"], d["v"], d["v_new"], d["g"], d["beta"], A, d["h"], d["do"],
+                                   d["dh"], d["dv"], scale)
+
+    A = np.linalg.inv(np.eye(C) + x["A_kk"])
+    got = wy_stage.chunk_grads(x["q"], x["k"], x["v"], x["v_new"], x["g"], x["beta"], A, x["h"], x["do"],
+                               x["dh"], x["dv"], scale)
+    eps = 1e-6
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("beta", "db"), ("g", "dg"), ("A_kk", "dA")):
+        fd = np.zeros_like(x[name])
+        for idx in np.ndindex(*x[name].shape):
+            if name == "A_kk" and idx[1] >= idx[0]:
+                continue  # A_kk is strictly lower
+            xp = {kk: vv.copy() for kk, vv in x.items()}
+            xm = {kk: vv.copy() for kk, vv in x.items()}
+            xp[name][idx] += eps
+            xm[name][idx] -= eps
+            fd[idx] = (loss(xp) - loss(xm)) / (2 * eps)
+        err = np.abs(got[key] - fd).max() / max(1.0, np.abs(fd).max())
+        assert err < 1e-6, (key, err)
+
+
+def test_wy_stage_pieces_against_the_full_gradient_terms():
+    """Cross-check with the full oracle's chunk algebra: when h, dh, v_new and dv are the true chunk
+    quantities of a one-chunk problem whose state starts at h, the stage's dv equals beta A^T dV_new, and the
+    stage's dq plus the intra-chunk term P K (P = (D V_new^T) (.) M) equals the token-recurrence oracle's dq."""
+    import oracle
+    from oracle import wy_forward, wy_stage
+    rng = np.random.default_rng(5)
+    C, K, V, scale = 6, 3, 3, 0.5
+    q = rng.standard_normal((C, K)); k = rng.standard_normal((C, K)); v = rng.standard_normal((C, V))
+    gr = -np.log1p(np.exp(-rng.standard_normal((C, K))))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal(C)))
+    S0 = 0.3 * rng.standard_normal((V, K)); dO = rng.standard_normal((C, V)); dht = rng.standard_normal((V, K))
+    cu = np.array([0, C])
+    f = lambda a: a[:, None, :]
+    full = oracle.backward(cu, 1, 1, K, V, True, scale, f(q), f(k), f(v), beta[:, None], f(gr), S0[None, None],
+                           f(dO), dht[None, None])
+    _, _, parts = wy_forward.chunk_forward(S0, q, k, v, beta, gr, scale, True)
+    g = parts["gamma"]
+    A = parts["T"]
+    v_new = parts["V_new"]
+    # dV_new and the state gradient of the one-chunk problem: dS_next = dht, dV_new = P^T-side terms
+    Mq = np.einsum("ic,jc,ijc->ij", q, k, np.exp(g[:, None, :] - g[None, :, :])) * np.tril(np.ones((C, C)))
+    D = scale * dO
+    dv_new = Mq.T @ D + (k * np.exp(g[-1][None, :] - g)) @ dht.T
+    st = wy_stage.chunk_grads(q, k, v, v_new, g, beta, A, S0.T, dO, dht.T, dv_new, scale)
+    # dq of the full problem = stage's inter-chunk dq + intra-chunk (P K with per-channel decay)
+    P = (D @ v_new.T) * np.tril(np.ones((C, C)))
+    dq_intra = np.einsum("ij,jc,ijc->ic", P, k, np.exp(g[:, None, :] - g[None, :, :]))
+    np.testing.assert_allclose(st["dq"] + dq_intra, full["dq"][:, 0], rtol=1e-9, atol=1e-10)
+    np.testing.assert_allclose(st["dv"], beta[:, None] * (A.T @ dv_new), rtol=1e-12, atol=1e-12)
