@@ -46,8 +46,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="gdn_t32k_bf16")
     ap.add_argument("--cpu-sample-tokens", type=int, default=32768)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pass", dest="which", choices=("bwd", "fwd"), default="bwd",
-                    help="bwd: the backward (the headline); fwd: the forward pass (o and the final state)")
+    ap.add_argument("--pass", dest="which", choices=("bwd", "fwd", "wy"), default="bwd",
+                    help="bwd: the backward (the headline); fwd: the forward pass (o and the final state); "
+                         "wy: the WY-gradient stage taken alone at its own model shape (T=2048, H=32, fp16)")
     return ap.parse_args(argv)
 
 
@@ -248,6 +249,8 @@ def run_ours(args):
     barrier(world)
     build()
 
+    if args.which == "wy":
+        return run_wy_bench(args, world, rank, local)
     prob = workload(args.workload)
     if args.which == "fwd":
         return run_forward_bench(args, prob, world, rank, local)
@@ -420,6 +423,57 @@ def run_forward_bench(args, prob, world, rank, local):
             "path_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms / 1e3), "flops": flops,
                               "algorithmic_bytes": alg},
             "gpu_launches": plan.forward_launch_count * args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
+def run_wy_bench(args, world, rank, local):
+    """The WY-gradient stage taken alone (gdr_wy_bwd_run) on the shape its page names: B=1, T=2048, H=32,
+    K=V=128, BT=64, fp16, inputs drawn like its usage example (cumulative gate, A a true inverse)."""
+    import torch
+    from chunked_gated_delta_09_gb300 import counts, ops
+
+    B, T, H, K, V, BT = 1, 2048, 32, 128, 128, 64
+    gen = torch.Generator().manual_seed(2024)
+    rn = lambda *s_: torch.randn(*s_, generator=gen)
+    dt = torch.float16
+    q, k, v, v_new, do, dv = (rn(B, T, H, s_).to(dt).cuda() for s_ in (K, K, V, V, V, V))
+    beta = torch.sigmoid(rn(B, T, H)).to(dt).cuda()
+    g = torch.nn.functional.logsigmoid(rn(B, T // BT, BT, H, K)).cumsum(2).reshape(B, T, H, K).cuda()
+    Akk = torch.tril(0.2 * rn(B * T // BT, H, BT, BT), -1)
+    A = torch.linalg.inv(torch.eye(BT) + Akk).permute(0, 2, 1, 3).reshape(B, T, H, BT).to(dt).cuda()
+    h, dh = rn(B, T // BT, H, K, V).cuda(), rn(B, T // BT, H, K, V).cuda()
+    call = lambda: ops.gdr_wy_bwd(q, k, v, v_new, g, beta, A, h, do, dh, dv, scale=K ** -0.5, chunk_size=BT)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    t0.record(stream)
+    for _ in range(args.steps):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world)
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    flops = B * (T // BT) * H * counts.wy_stage_flops_per_chunk(BT, K, V)
+    alg = counts.wy_stage_bytes(B, T, H, K, V, BT, 2)
+    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), alg / (peaks["hbm_gbs"] * 1e9))
+    line = {"metric": "KDA WY-gradient stage alone (chunk_kda_bwd_wy_dqkg_fused) ms, % of roofline",
+            "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "accumulate": "f32", "data": "synthetic", "pass": "wy",
+            "config": {"workload": "kda_wy_t2k_h32_fp16", "B": B, "T": T, "H": H, "K": K, "V": V, "BT": BT,
+                       "timing": "includes the host-side plan creation and output allocation of each call"},
+            "path_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms / 1e3), "flops": flops,
+                              "algorithmic_bytes": alg, "achieved_gbs": alg / (ms / 1e3) / 1e9},
+            "clocks": clk}
     print(json.dumps(line), flush=True)
 
 

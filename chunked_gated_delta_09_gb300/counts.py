@@ -127,3 +127,18 @@ def forward_algorithmic_bytes(prob) -> int:
     return int(2 * T * prob.Hk * prob.K * ib + T * prob.Hv * prob.V * ib + T * prob.Hv * _nbytes(prob.beta_dtype)
                + T * prob.Hv * gk * 4 + (state if prob.h0 is not None else 0)
                + T * prob.Hv * prob.V * ib + state)
+
+
+def wy_stage_flops_per_chunk(C: int, K: int, V: int) -> float:
+    """The WY-gradient stage taken alone: D S_0, V_new dS, dV S_0 (2 C K V each); dT from dW and dV
+    (2 C^2 K + 2 C^2 V); T^T dW (2 C^2 K), T^T dV (2 C^2 V); dT T^T and T^T X (2 C^3 each)."""
+    return 6.0 * C * K * V + 4.0 * C * C * K + 4.0 * C * C * V + 4.0 * C ** 3
+
+
+def wy_stage_bytes(B, T, H, K, V, BT, ib) -> int:
+    """Its inputs read once and outputs written once: q, k, v, v_new, do, dv, beta, A (ib bytes each), g and
+    the fp32 states h, dh; dq, dk, db, dg, dA (fp32) and dv (ib)."""
+    NT = B * ((T + BT - 1) // BT)
+    tok = B * T * H
+    return int(tok * (2 * K + 4 * V + 1 + BT) * ib + tok * K * 4 + 2 * NT * H * K * V * 4
+               + tok * (2 * K + 1 + K + BT) * 4 + tok * V * ib)
