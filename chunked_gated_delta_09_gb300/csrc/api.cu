@@ -20,6 +20,7 @@ struct gdr_bwd_plan {
     gdr_bwd_desc d;
     int G, N, dense, nts, max_chunks;
     int k4_tc;  // per-chunk gradients on tcgen05 (scalar gate); the per-channel gate uses the mma.sync kernel
+    int dh_factored;  // factored local pass of the state-gradient scan (QR = Q~ - Aqk W), GDR_DH_FACTORED=1
     int NS, Lseg;  // segment-parallel scans: segments per sequence and chunks per segment
     long long tokens;  // B * T
     // workspace byte offsets
@@ -135,6 +136,8 @@ gdr_status gdr_bwd_create(const gdr_bwd_desc *desc, gdr_bwd_plan **out) {
     // gate; GDR_K4_TC=0 routes the scalar gate to the mma.sync kernel as well
     const char *k4tc = getenv("GDR_K4_TC");
     p->k4_tc = !d.gate_per_channel && !(k4tc && atoi(k4tc) == 0);
+    const char *fact = getenv("GDR_DH_FACTORED");
+    p->dh_factored = fact && atoi(fact) != 0;
     layout(*p);
     *out = p;
     return GDR_OK;
@@ -255,7 +258,12 @@ static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *work
     if (any_chunks && (e = launch_k2_scan(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     if (!mark(3)) return GDR_ERR_CUDA;
     if (any_chunks && plan->NS > 1) {
+        if (plan->dh_factored) {  // QR into the U^T region, which the forward scan no longer needs
+            P.QR = P.U;
+            if ((e = launch_k8_qr(P, P.QR, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+        }
         if ((e = launch_k3_scan(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+        P.QR = nullptr;
         if ((e = launch_k23_combine(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     }
     if ((e = launch_k3_scan(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
@@ -285,7 +293,7 @@ int gdr_bwd_launch_count(const gdr_bwd_plan *plan) {
     int n = plan->dense ? 0 : 1;  // K0
     n += 1;                       // the final state-gradient scan always runs (it also writes dh0)
     if (plan->max_chunks > 0) n += 4;  // K1, forward scan, K4, K5
-    if (plan->max_chunks > 0 && plan->NS > 1) n += 4;  // local scans and combines
+    if (plan->max_chunks > 0 && plan->NS > 1) n += 4 + (plan->dh_factored ? 1 : 0);  // local scans, combines (QR)
     return n;
 }
 

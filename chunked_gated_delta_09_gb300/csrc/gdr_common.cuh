@@ -69,6 +69,9 @@ struct Params {
     // exact entry state Sin and exact exit gradient dS
     int NS, Lseg;
     float *segE, *segPhi, *segPhiT, *segF, *segSin, *segdS;
+    // factored state-gradient local pass (null: unfactored): QR = Q~ - Aqk W per unit, tile [r][k], in the
+    // U^T region (dead once the forward scan has run)
+    __half *QR;
 };
 
 // ---------------------------------------------------------------- sequence / chunk bookkeeping

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace gdr {
@@ -31,5 +32,7 @@ cudaError_t launch_k6_fwd_output(const Params &P, cudaStream_t stream);
 cudaError_t launch_k7_wy_inputs(const Params &P, const void *A, const void *v_new, const void *dv_in, const float *h,
                                 const float *dh, cudaStream_t stream);
 cudaError_t launch_k4_wy(const Params &P, cudaStream_t stream);
+// QR = Q~ - Aqk W per chunk for the factored local pass of the state-gradient scan
+cudaError_t launch_k8_qr(const Params &P, __half *QR, cudaStream_t stream);
 
 }  // namespace gdr

@@ -12,6 +12,9 @@
 //     -dV_new^T; segment 0 also writes dh0.
 // One CTA holds the 128 x 128 fp32 dS in tensor memory; each step issues two MMA groups.  Operand tiles
 // arrive by bulk copy one chunk ahead; dh_n and -dV_new^T leave by bulk copy from the operand tiles.
+// FACT (local pass only): the factored step of the dh-gradient kernel of section 3 of the same page,
+// dS <- Gamma_C dS + D^T QR - (dS K~^T) W with QR = Q~ - Aqk W formed per chunk by k8_qr.cu, which needs
+// neither Aqk nor dV_new inside the step (selected with GDR_DH_FACTORED=1).
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
 #include "tc_util.cuh"
@@ -30,7 +33,7 @@ struct __align__(1024) BwdSmem {
     uint32_t tslot;
 };
 
-template <bool PC, bool LOCAL>
+template <bool PC, bool LOCAL, bool FACT = false>
 __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     BwdSmem &S = *reinterpret_cast<BwdSmem *>(smem_raw);
@@ -72,11 +75,11 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
         const size_t u = (size_t)(base + c) * P.Hv + hv;
         const uint32_t gbytes = PC ? DT * 4 : CT * 4;
         const float *gsrc = PC ? P.gam + (u * CT + chunk_len(c) - 1) * DT : P.gam + u * CT;
-        tc::mbar_expect_tx(&S.lbar[buf], CT * CT * 2 + 4 * CT * DT * 2 + gbytes);
-        tc::bulk_g2s(S.Aq[buf], P.Aqk + u * CT * CT, CT * CT * 2, &S.lbar[buf]);
+        tc::mbar_expect_tx(&S.lbar[buf], (FACT ? 0 : CT * CT * 2) + 4 * CT * DT * 2 + gbytes);
+        if (!FACT) tc::bulk_g2s(S.Aq[buf], P.Aqk + u * CT * CT, CT * CT * 2, &S.lbar[buf]);
         tc::bulk_g2s(S.D[buf], P.Dt + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
         tc::bulk_g2s(S.Kt[buf], P.Kt + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
-        tc::bulk_g2s(S.Qg[buf], P.Qg + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
+        tc::bulk_g2s(S.Qg[buf], (FACT ? P.QR : P.Qg) + u * CT * DT, CT * DT * 2, &S.lbar[buf]);  // QR if FACT
         tc::bulk_g2s(S.W[buf], P.W + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
         tc::bulk_g2s(S.gam[buf], gsrc, gbytes, &S.lbar[buf]);
     };
@@ -154,9 +157,10 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
         __syncthreads();
         tc::fence_after();
         // MMA 1: dV_new^T = D^T Aqk + dS K~^T;  dh_n leaves by bulk copy
-        if (tid == 0) {
-            tc::gemm(tm + T_DV, smem_u32(S.D[buf]), DT, true, smem_u32(S.Aq[buf]), CT, true, 128, 64, CT, false);
-            tc::gemm(tm + T_DV, sdSa, DT, false, smem_u32(S.Kt[buf]), DT, false, 128, 64, DT, true);
+        if (tid == 0) {  // (FACT: only Y = dS K~^T)
+            if (!FACT)
+                tc::gemm(tm + T_DV, smem_u32(S.D[buf]), DT, true, smem_u32(S.Aq[buf]), CT, true, 128, 64, CT, false);
+            tc::gemm(tm + T_DV, sdSa, DT, false, smem_u32(S.Kt[buf]), DT, false, 128, 64, DT, !FACT);
             if (!LOCAL) tc::bulk_s2g(P.dh + u * DT * DT, S.dSa, DT * DT * 2);
         }
         mma_done();
@@ -216,16 +220,19 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
     }
 }
 
-template <bool PC, bool LOCAL>
+template <bool PC, bool LOCAL, bool FACT = false>
 static cudaError_t launch_bwd_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(BwdSmem);
-    cudaError_t e = cudaFuncSetAttribute(k3_scan_tc<PC, LOCAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(k3_scan_tc<PC, LOCAL, FACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k3_scan_tc<PC, LOCAL><<<P.N * P.Hv * P.NS, SB_THREADS, smem, stream>>>(P);
+    k3_scan_tc<PC, LOCAL, FACT><<<P.N * P.Hv * P.NS, SB_THREADS, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
 cudaError_t launch_k3_scan(const Params &P, bool local, cudaStream_t stream) {
+    if (local && P.QR)
+        return P.per_channel ? launch_bwd_t<true, true, true>(P, stream) : launch_bwd_t<false, true, true>(P, stream);
     if (local) return P.per_channel ? launch_bwd_t<true, true>(P, stream) : launch_bwd_t<false, true>(P, stream);
     return P.per_channel ? launch_bwd_t<true, false>(P, stream) : launch_bwd_t<false, false>(P, stream);
 }

@@ -99,3 +99,21 @@ def test_scalar_gate_on_mma_sync_kernel(name, monkeypatch):
     monkeypatch.setenv("GDR_K4_TC", "0")
     prob = make_problem(name, seed=zlib.crc32(name.encode()) % 1000, **SMALL[name])
     compare(prob, run_gpu(prob), oracle.problem_backward(prob))
+
+
+@pytest.mark.parametrize("nseg", [2, 3, 7])
+@pytest.mark.parametrize("per_channel", [False, True], ids=["scalar", "kda"])
+def test_factored_state_gradient_local_pass(nseg, per_channel, monkeypatch):
+    """The factored local pass of the state-gradient scan (QR = Q~ - Aqk W; dS <- Gamma_C dS + D^T QR -
+    (dS K~^T) W) gives the oracle's gradients like the unfactored one."""
+    monkeypatch.setenv("GDR_NSEG", str(nseg))
+    monkeypatch.setenv("GDR_DH_FACTORED", "1")
+    prob = make_problem(f"fact_nseg{nseg}", B=1, Hk=1, Hv=2, K=64, V=64, per_channel=per_channel,
+                        seq_lens=[700, 64, 130, 1], seed=90)
+    compare(prob, run_gpu(prob), oracle.problem_backward(prob))
+
+
+def test_factored_state_gradient_on_the_t8k_workload(monkeypatch):
+    monkeypatch.setenv("GDR_DH_FACTORED", "1")
+    prob = workload("gdn_t8k_bf16")
+    compare(prob, run_gpu(prob), oracle.problem_backward(prob))

@@ -76,3 +76,12 @@ def test_stage_bytes_of_the_per_chunk_gradient_stage():
     assert all(b > 0 for b in sb[1:])
     # the gradient stage sits below the ridge: HBM-bound at any peaks with ratio above 80 FLOP per byte
     assert counts.stage_flops(p)[4] / sb[4] < 80
+
+
+def test_factored_scan_adds_one_launch(monkeypatch):
+    """GDR_DH_FACTORED=1 adds the per-chunk QR kernel to a segmented plan (host-only plan creation)."""
+    from chunked_gated_delta_09_gb300 import ops
+    kw = dict(B=1, T=32768, Hk=16, Hv=16, K=128, V=128)
+    base = ops.GdrBwdPlan(**kw).launch_count
+    monkeypatch.setenv("GDR_DH_FACTORED", "1")
+    assert ops.GdrBwdPlan(**kw).launch_count == base + 1
