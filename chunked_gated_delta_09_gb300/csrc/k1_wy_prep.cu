@@ -24,12 +24,11 @@ namespace gdr {
 constexpr int K1_THREADS = 256;
 
 struct __align__(1024) K1Smem {
-    // Qs later holds beta Gamma K, Vs beta V
+    // Ks holds K, then (once the decayed copies are written) T as the fp16 operand of the W and U products
+    // and the scratch of the inverse's block products; Qs later holds beta Gamma K, Vs beta V.  AT holds the
+    // raw dO rows on their way to the D tile, then A_kk, then in place its inverse T (fp32).
     unsigned char Ks[CT * DT * 2], Qs[CT * DT * 2], Vs[CT * DT * 2];
-    unsigned char oT[CT * CT * 2];  // T as the fp16 operand of the W and U products
-    float A32[CT][CT + 1];
-    float T32[CT][CT + 1];
-    float X32[32][33];  // scratch of the block products
+    float AT[CT][CT + 1];
     float gam[CT];
     float beta[CT];
 };
@@ -37,6 +36,7 @@ struct __align__(1024) K1Smem {
 // One doubling level of the unit-lower-triangular inverse T = (I + A)^-1 held in fp32 shared memory:
 // for every diagonal pair of B x B blocks (lo, hi = lo + B), T[hi][lo] = -T[hi][hi] (A[hi][lo] T[lo][lo]),
 // with the B x B diagonal blocks of T already final.  2 (64 / (2B)) B^2 / 4 two-by-two output blocks.
+// A and T may be one array (T built in place over A): a level reads A only in the blocks it then overwrites.
 template <int B>
 __device__ __forceinline__ void inv_level(const float (&A)[CT][CT + 1], float (&T)[CT][CT + 1], float (&X)[32][33],
                                           int tid) {
@@ -75,7 +75,7 @@ __device__ __forceinline__ void inv_level(const float (&A)[CT][CT + 1], float (&
 }
 
 template <typename Tin, bool PC>
-__global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Params P) {
+__global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Params P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     K1Smem &S = *reinterpret_cast<K1Smem *>(smem_raw);
     float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K1Smem));  // [CT][DT], per-channel only
@@ -100,7 +100,45 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
         if (2 * lane < len) gx0 = P.g[(size_t)(ci.tok0 + 2 * lane) * P.Hv + hv];
         if (2 * lane + 1 < len) gx1 = P.g[(size_t)(ci.tok0 + 2 * lane + 1) * P.Hv + hv];
     }
-    if (P.dO) {  // backward: also D = scale dO, written straight to its workspace tile
+    if constexpr (sizeof(Tin) == 2) {
+        // raw rows into their tile slots (dO into the A / T buffer, not yet in use), one round trip for all
+        constexpr int PER = CT * (DT / 8) / K1_THREADS;
+        const int nin = P.dO ? 4 : 3;
+        unsigned char *const slot[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(&S.AT[0][0])};
+        const Tin *const src[4] = {kp, qp, vp, dop};
+        const size_t st[4] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V, (size_t)P.Hv * P.V};
+        const int nc[4] = {P.K, P.K, P.V, P.V};
+        for (int w = 0; w < nin; ++w)
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int c = wid + (K1_THREADS / 32) * i;
+                const int r = 8 * (c >> 2) + (lane & 7), c8 = 8 * (4 * (c & 3) + (lane >> 3));
+                const bool ok = r < len && c8 + 8 <= nc[w];
+                cp_async16_zfill(slot[w] + ctile_off(r, c8, DT), ok ? src[w] + (size_t)r * st[w] + c8 : src[w],
+                                 ok ? 16 : 0);
+            }
+        cp_async_commit();
+        cp_async_wait<0>();
+        for (int w = 0; w < nin; ++w)
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {  // each thread converts the chunks it fetched
+                const int c = wid + (K1_THREADS / 32) * i;
+                const int r = 8 * (c >> 2) + (lane & 7), c8 = 8 * (4 * (c & 3) + (lane >> 3));
+                const uint32_t off = ctile_off(r, c8, DT);
+                Raw8<Tin> x;
+                x.v = *reinterpret_cast<const uint4 *>(slot[w] + off);
+                float f[8];
+                raw_get(x, f);
+                if (w == 3) {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) f[t] *= P.scale;
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT) + off) =
+                        pack8_half(f);
+                } else {
+                    *reinterpret_cast<uint4 *>(slot[w] + off) = pack8_half(f);
+                }
+            }
+    } else if (P.dO) {  // backward: also D = scale dO, written straight to its workspace tile
         unsigned char *const dst[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT)};
         const Tin *const src[4] = {kp, qp, vp, dop};
         const size_t st[4] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V, (size_t)P.Hv * P.V};
@@ -146,7 +184,6 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
             }
         }
     }
-    for (int e = tid; e < CT * (CT + 1); e += K1_THREADS) (&S.T32[0][0])[e] = 0.f;
     __syncthreads();
 
     // ---- A_kk (fp32, shared) and Aqk (fp16 tile)
@@ -167,7 +204,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const float d = expf(S.gam[i] - S.gam[j + h]);
-                    S.A32[i][j + h] = j + h < i ? S.beta[i] * d * kk[0][nt][e + h] : 0.f;
+                    S.AT[i][j + h] = j + h < i ? S.beta[i] * d * kk[0][nt][e + h] : 0.f;
                     aq[h] = j + h <= i ? d * qk[0][nt][e + h] : 0.f;
                 }
                 *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j, CT)) = __floats2half2_rn(aq[0], aq[1]);
@@ -184,7 +221,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
                     aqk += ctile_get(S.Qs, i, c, DT) * kj * d;
                 }
             }
-            S.A32[i][j] = j < i ? S.beta[i] * akk : 0.f;
+            S.AT[i][j] = j < i ? S.beta[i] * akk : 0.f;
             ctile_set(reinterpret_cast<unsigned char *>(P.Aqk + u * CT * CT), i, j, CT, j <= i ? aqk : 0.f);
         }
     }
@@ -229,31 +266,40 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
     }
 
     // ---- T = (I + A_kk)^-1: diagonal 16x16 blocks by per-column forward substitution, then doubling
-    if (wid < 4 && lane < 16) {
+    // (in place: every thread has read its diagonal block of A before any T column is written)
+    {
+        const bool dact = wid < 4 && lane < 16;
         const int b0 = wid * 16, m = lane;
         float x[16];
+        if (dact) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float acc = (i == m) ? 1.f : 0.f;
+            for (int i = 0; i < 16; ++i) {
+                float acc = (i == m) ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < i; ++j) acc -= S.A32[b0 + i][b0 + j] * x[j];
-            x[i] = acc;
+                for (int j = 0; j < i; ++j) acc -= S.AT[b0 + i][b0 + j] * x[j];
+                x[i] = acc;
+            }
         }
+        __syncthreads();
+        if (dact) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) S.T32[b0 + i][b0 + m] = x[i];
+            for (int i = 0; i < 16; ++i) S.AT[b0 + i][b0 + m] = x[i];
+        }
     }
     __syncthreads();
+    unsigned char *const oT = S.Ks;  // K is no longer needed
+    float (&X32)[32][33] = *reinterpret_cast<float (*)[32][33]>(S.Ks + CT * CT * 2);
     // off-diagonal blocks by recursive doubling: for a lower block split [[T_11, 0], [X, T_22]] of an inverse,
     // X = -T_22 A_21 T_11.  First the two 32 x 32 diagonal blocks from their 16 x 16 halves, then the whole.
     // Every thread accumulates a 2 x 2 output block over a fully unrolled inner loop.
-    inv_level<16>(S.A32, S.T32, S.X32, tid);
-    inv_level<32>(S.A32, S.T32, S.X32, tid);
+    inv_level<16>(S.AT, S.AT, X32, tid);
+    inv_level<32>(S.AT, S.AT, X32, tid);
     for (int e = tid; e < CT * CT / 8; e += K1_THREADS) {
         int i = e / (CT / 8), j8 = (e % (CT / 8)) * 8;
         float x[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = S.T32[i][j8 + t];
-        tc::st_tile8(S.oT, i, j8, CT, x);
+        for (int t = 0; t < 8; ++t) x[t] = S.AT[i][j8 + t];
+        tc::st_tile8(oT, i, j8, CT, x);
         tc::st_tile8(reinterpret_cast<unsigned char *>(P.Tm + u * CT * CT), i, j8, CT, x);
     }
     __syncthreads();
@@ -264,7 +310,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
         {
             const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 64;
             zero_acc(acc);
-            warp_mma_ct<1, 8, false, false>(acc, S.oT, CT, S.Qs, DT, m0, n0, CT);
+            warp_mma_ct<1, 8, false, false>(acc, oT, CT, S.Qs, DT, m0, n0, CT);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -277,7 +323,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 1 : 2) k1_wy_prep(const Param
         {
             const int m0 = wid * 16;  // 8 warps x 16 value rows, all 64 chunk columns
             zero_acc(acc);
-            warp_mma_ct<1, 8, true, true>(acc, S.Vs, DT, S.oT, CT, m0, 0, CT);
+            warp_mma_ct<1, 8, true, true>(acc, S.Vs, DT, oT, CT, m0, 0, CT);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
