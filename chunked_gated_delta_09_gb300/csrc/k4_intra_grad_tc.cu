@@ -19,10 +19,13 @@
 //    their tile slots, converted to fp16 in place when the item starts).
 //
 // Five MMA phases, each followed by an epilogue that produces the next phase's operands:
-//   1: dk_SC^T = dS^T V_new^T, dW^T = -S0^T dV^T, TdU^T = dV^T T, V^T, K^T, P0 = D V_new^T, dT2 = dV V^T,
+//   1: dk_SC^T = dS^T V_new^T, dW^T = -S0^T dV^T, TdU^T = dV^T T, K^T, P0 = D V_new^T, dT2 = dV V^T,
 //      dq_inter^T = S0^T D^T
 //   2: dq_intra^T = K^T P^T, dk_O^T = Q^T P, TdW^T = dW^T T, Q^T, KK = K K^T, dT1 = dW K^T
 //   3: X = dT T^T        4: dA' = T^T X        5: dk_Ar^T = K^T E^T, dk_Ac^T = K^T E
+// The WY part of dbeta, sum_k (T^T dW)_jk Gamma_j k_jk + sum_v (T^T dU)_jv v_jv, equals the column sum
+// sum_i T_ij (Gamma_j dT1_ij + dT2_ij) of two chunk x chunk products, so it is taken there.  The epilogues of
+// M = 64 products spread each row's 16 columns over both half-warps.
 #include <type_traits>
 
 #include "gdr_common.cuh"
@@ -36,7 +39,7 @@ constexpr uint32_t K4T_TMEM_COLS = 512;
 constexpr uint32_t K4T_WAIT_LIMIT = 1u << 24;  // mbarrier polls before a wait is declared lost
 
 // tensor-memory column map, 64 columns per region (C_* regions use the M = 64 lane layout)
-constexpr int R_DKSC = 0, R_DWT = 64, R_TDU = 128, R_VT = 192, R_KT = 256, C_G1 = 320, C_DT2 = 384,
+constexpr int R_DKSC = 0, R_DWT = 64, R_TDU = 128, R_KT = 256, C_G1 = 320, C_DT2 = 384,
               R_DQI = 448;                                                              // phase 1
 constexpr int R_DQA = 0, R_DKO = 64, R_TDW = 128, R_QT = 192, C_DT1 = 320;              // phase 2
 constexpr int C_X = 0, C_KK = 256;                                                      // phase 3
@@ -54,9 +57,9 @@ struct __align__(1024) K4TSmem {
     unsigned char I[CT * CT * 2];    // identity
     float gam[CT], G[CT], GC[CT], beta[CT];
     // partial sums in fixed slots, added in a fixed order at the end (run-to-run reproducible):
-    // dbeta: 4 lane quarters x (TdU, TdW) + 4 column quarters (A term); dgamma rows: 4 lane quarters;
-    // last row: 16 warps
-    float db_tdu[4][CT], db_tdw[4][CT], db_a[4][CT], dg_q[4][CT], last_w[16];
+    // dbeta: 4 row quarters (WY term), 4 column quarters (A term); dgamma rows: 4 lane quarters; last row:
+    // 16 warps
+    float db_wy[4][CT], db_a[4][CT], dg_q[4][CT], last_w[16];
     uint64_t bar, bar2, lbar;  // MMA groups 1 and 2 of a phase; bulk loads
     uint32_t tslot;
 };
@@ -213,6 +216,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     const int k = 32 * q + lane;    // feature row in M = 128 regions
     const int r64 = 16 * q + lane;  // chunk row in M = 64 regions (lanes 0..15)
     const bool own64 = lane < 16;
+    // M = 64 epilogues after split_rows16: row i64, columns jh .. jh + 7
+    const int i64 = 16 * q + (lane & 15), jh = c0 + 8 * (lane >> 4);
 
     while (item < n_items && !lost) {
         const int n = item / P.Hv, hv = item % P.Hv, hk = hv / P.G;
@@ -258,7 +263,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             fail = !tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);
             if (!fail) {
                 tc::gemm(tm + R_KT, sK, DT, true, sI, CT, false, 128, 64, CT, false);
-                tc::gemm(tm + R_VT, sV, DT, true, sI, CT, false, 128, 64, CT, false);
                 tc::gemm(tm + R_DWT, sH, DT, true, sdVn, CT, true, 128, 64, DT, false);
                 tc::gemm(tm + R_DKSC, sdH, DT, true, sVn, CT, true, 128, 64, DT, false);
                 tc::gemm(tm + R_TDU, sdVn, CT, false, sT, CT, true, 128, 64, CT, false);
@@ -278,8 +282,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         float lastpart = 0.f;
         tc::ld16(tc::taddr(tm, R_KT + c0), kreg);
         {
-            float g[16], vreg[16];
-            tc::ld16(tc::taddr(tm, R_VT + c0), vreg);
+            float g[16];
             // dW^T -> dWT tile (the stored dV tile is negated, so the product already is dW^T)
             tc::ld16(tc::taddr(tm, R_DWT + c0), g);
             tc::st_tile8(S.dWT, k, c0, CT, g);
@@ -294,21 +297,14 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                 dg[t] = -kx;
                 lastpart += kx;
             }
-            // TdU^T -> dv (rows c0.., column k), dbeta += rowsum(TdU (.) V)   (negated dV tile)
+            // TdU^T -> dv (rows c0.., column k)   (negated dV tile)
             tc::ld16(tc::taddr(tm, R_TDU + c0), g);
-            float o[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                g[t] = -g[t];
-                o[t] = S.beta[c0 + t] * g[t];
-                g[t] *= vreg[t];
-            }
+            for (int t = 0; t < 16; ++t) g[t] = -S.beta[c0 + t] * g[t];
             if (k < P.V)
                 store_col16(reinterpret_cast<char *>(P.dv) +
                                 (((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.V + k) * esize(P.dv_dtype),
-                            P.dv_dtype, (size_t)P.Hv * P.V, nrow, o);
-            const float s = tc::warp_transpose_sum16(g);
-            if (lane < 16) S.db_tdu[q][c0 + lane] = s;
+                            P.dv_dtype, (size_t)P.Hv * P.V, nrow, g);
         }
         {
             // last row: Gamma_C <S_0, dS_next> + sum_j k_j (.) dk_SC_j.  Warp w takes the 8-column chunk
@@ -334,19 +330,17 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         }
         const bool ok1 = wait_group2();
         {
-            // P = (D V_new^T) (.) M  -> Pm tile
-            float g[16];
+            // P = (D V_new^T) (.) M  -> Pm tile (row i, columns jh .. jh + 7)
+            float g[16], x[8];
             tc::ld16(tc::taddr(tm, C_G1 + c0), g);
-            if (own64) {
-                const float gr = S.gam[r64];
+            tc::split_rows16(g, x);
+            const float gr = S.gam[i64];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const int j = c0 + t;
-                    g[t] = j <= r64 ? g[t] * __expf(gr - S.gam[j]) : 0.f;
-                }
-                tc::st_tile8(S.Pm, r64, c0, CT, g);
-                tc::st_tile8(S.Pm, r64, c0 + 8, CT, g + 8);
+            for (int t = 0; t < 8; ++t) {
+                const int j = jh + t;
+                x[t] = j <= i64 ? x[t] * __expf(gr - S.gam[j]) : 0.f;
             }
+            tc::st_tile8(S.Pm, i64, jh, CT, x);
         }
         publish_tiles(ok1);
         if (lost) break;
@@ -397,7 +391,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                 dk[t] += a[t];
                 dg[t] -= kreg[t] * a[t];
             }
-            // TdW^T -> dk_W, dbeta
+            // TdW^T -> dk_W
             tc::ld16(tc::taddr(tm, R_TDW + c0), a);
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
@@ -405,22 +399,34 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                 const float x = S.beta[j] * S.G[j] * a[t];
                 dk[t] += x;
                 dg[t] += kreg[t] * x;
-                b[t] = S.G[j] * kreg[t] * a[t];
             }
-            const float s = tc::warp_transpose_sum16(b);
-            if (lane < 16) S.db_tdw[q][c0 + lane] = s;
-            // dT = dT1 (.) beta Gamma + dT2 (.) beta   -> dT tile (dT2 came negated)
+            // s = Gamma_j dT1 + dT2 (dT2 came negated); dT = beta_j s -> dT tile; dbeta_j (WY part) =
+            // sum_i T_ij s_ij over this warp's 16 rows
             tc::ld16(tc::taddr(tm, C_DT1 + c0), a);
             tc::ld16(tc::taddr(tm, C_DT2 + c0), b);
-            if (own64) {
+            float x[8], y[8], tr[8];
+            tc::split_rows16(a, x);
+            tc::split_rows16(b, y);
+            {
+                const uint4 tv = *reinterpret_cast<const uint4 *>(S.T + tc::tile_off(i64, jh, CT));
+                const __half2 *t2 = reinterpret_cast<const __half2 *>(&tv);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const int j = c0 + t;
-                    a[t] = S.beta[j] * (S.G[j] * a[t] - b[t]);
+                for (int t = 0; t < 4; ++t) {
+                    const float2 f = __half22float2(t2[t]);
+                    tr[2 * t] = f.x;
+                    tr[2 * t + 1] = f.y;
                 }
-                tc::st_tile8(S.dT, r64, c0, CT, a);
-                tc::st_tile8(S.dT, r64, c0 + 8, CT, a + 8);
             }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int j = jh + t;
+                const float sv = S.G[j] * x[t] - y[t];
+                x[t] = S.beta[j] * sv;
+                tr[t] *= sv;
+            }
+            tc::st_tile8(S.dT, i64, jh, CT, x);
+            const float s = tc::half_transpose_sum8(tr);
+            if ((lane & 8) == 0) S.db_wy[q][jh + (lane & 7)] = s;
         }
         publish_tiles(ok2);
         if (lost) break;
@@ -454,29 +460,29 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (lost) break;
         if (tid == 0 && has_next) issue_ws2(next);  // T is not read again in this item
         {
-            float a[16], kk[16];
+            float a[16], kk[16], x[8], y[8];
             tc::ld16(tc::taddr(tm, C_DA + c0), a);
             tc::ld16(tc::taddr(tm, C_KK + c0), kk);
-            if (own64) {
-                const int i = r64;
-                const float gi = S.gam[i], bi = S.beta[i];
-                float rb = 0.f;
+            tc::split_rows16(a, x);
+            tc::split_rows16(kk, y);
+            const int i = i64;
+            const float gi = S.gam[i], bi = S.beta[i];
+            float rb = 0.f;
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const int j = c0 + t;
-                    float e = 0.f;
-                    if (j < i) {
-                        const float L = __expf(gi - S.gam[j]);
-                        const float dA = -a[t];
-                        rb += dA * L * kk[t];
-                        e = bi * L * dA;
-                    }
-                    a[t] = e;
+            for (int t = 0; t < 8; ++t) {
+                const int j = jh + t;
+                float e = 0.f;
+                if (j < i) {
+                    const float L = __expf(gi - S.gam[j]);
+                    const float dA = -x[t];
+                    rb += dA * L * y[t];
+                    e = bi * L * dA;
                 }
-                tc::st_tile8(Es, i, c0, CT, a);
-                tc::st_tile8(Es, i, c0 + 8, CT, a + 8);
-                S.db_a[wid >> 2][i] = rb;
+                x[t] = e;
             }
+            tc::st_tile8(Es, i, jh, CT, x);
+            rb += __shfl_xor_sync(0xffffffffu, rb, 16);
+            if (lane < 16) S.db_a[wid >> 2][i] = rb;
         }
         publish_tiles(true);
         if (lost) break;
@@ -523,8 +529,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                 x += l;
             }
             P.dgam[u * CT + tid] = tid < len ? x : 0.f;
-            float b = (S.db_tdu[0][tid] + S.db_tdu[1][tid]) + (S.db_tdu[2][tid] + S.db_tdu[3][tid]);
-            b += (S.db_tdw[0][tid] + S.db_tdw[1][tid]) + (S.db_tdw[2][tid] + S.db_tdw[3][tid]);
+            float b = (S.db_wy[0][tid] + S.db_wy[1][tid]) + (S.db_wy[2][tid] + S.db_wy[3][tid]);
             b += (S.db_a[0][tid] + S.db_a[1][tid]) + (S.db_a[2][tid] + S.db_a[3][tid]);
             if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = b;
         }

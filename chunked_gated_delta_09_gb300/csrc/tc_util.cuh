@@ -213,6 +213,34 @@ __device__ __forceinline__ float warp_transpose_sum16(float (&v)[16]) {
     return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
+// Lanes l and l ^ 8 return the sum over the 16 lanes of their half-warp of v[l % 8] (v is consumed).
+__device__ __forceinline__ float half_transpose_sum8(float (&v)[8]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 4; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            float send = up ? v[i] : v[i + s];
+            float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 8);
+}
+
+// The rows of an M = 64 accumulator sit in lanes 0..15 of a lane quarter.  After a 16-column load, lane l
+// gets in x the columns 8 (l / 16) .. +7 of row l % 16 (lanes 16..31 take the upper half from lane l - 16),
+// so that all 32 lanes share the element-wise work.
+__device__ __forceinline__ void split_rows16(const float (&v)[16], float (&x)[8]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const float hi = __shfl_sync(0xffffffffu, v[8 + t], lane & 15);
+        x[t] = lane < 16 ? v[t] : hi;
+    }
+}
+
 // Write 8 fp32 values as one 16-byte row segment of core matrix (r/8, c0/8) of a tile (c0 % 8 == 0).
 __device__ __forceinline__ void st_tile8(unsigned char *tile, int r, int c0, int C, const float *x) {
     uint4 p;
