@@ -77,6 +77,11 @@ __device__ __forceinline__ void store_col16(void *p, int dt, size_t rs, int n, c
     else col16_t(reinterpret_cast<float *>(p), rs, n, x);
 }
 __device__ __forceinline__ size_t esize(int dt) { return dt == F32 ? 4 : 2; }
+// 8 consecutive floats of a 16-byte aligned shared array as two vector loads
+__device__ __forceinline__ void lds8(const float *p, float (&v)[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+}
 
 template <typename Tin>
 __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params P) {
@@ -290,17 +295,28 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             // dk_SC = exp(gamma_C - gamma_j) (V_new dS)_j
             tc::ld16(tc::taddr(tm, R_DKSC + c0), g);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const float x = g[t] * S.GC[c0 + t];
-                const float kx = kreg[t] * x;
-                dk[t] = x;
-                dg[t] = -kx;
-                lastpart += kx;
+            for (int h = 0; h < 2; ++h) {
+                float gc[8];
+                lds8(S.GC + c0 + 8 * h, gc);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = 8 * h + u;
+                    const float x = g[t] * gc[u];
+                    const float kx = kreg[t] * x;
+                    dk[t] = x;
+                    dg[t] = -kx;
+                    lastpart += kx;
+                }
             }
             // TdU^T -> dv (rows c0.., column k)   (negated dV tile)
             tc::ld16(tc::taddr(tm, R_TDU + c0), g);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) g[t] = -S.beta[c0 + t] * g[t];
+            for (int h = 0; h < 2; ++h) {
+                float bv[8];
+                lds8(S.beta + c0 + 8 * h, bv);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) g[8 * h + u] *= -bv[u];
+            }
             if (k < P.V)
                 store_col16(reinterpret_cast<char *>(P.dv) +
                                 (((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.V + k) * esize(P.dv_dtype),
@@ -315,8 +331,10 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t off = tc::tile_off(32 * (wid >> 2) + 8 * j + (lane & 7), cc8, DT);
-                const __half2 *a2 = reinterpret_cast<const __half2 *>(S.H + off);
-                const __half2 *b2 = reinterpret_cast<const __half2 *>(S.dH + off);
+                const uint4 av = *reinterpret_cast<const uint4 *>(S.H + off);
+                const uint4 bv = *reinterpret_cast<const uint4 *>(S.dH + off);
+                const __half2 *a2 = reinterpret_cast<const __half2 *>(&av);
+                const __half2 *b2 = reinterpret_cast<const __half2 *>(&bv);
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const float2 a = __half22float2(a2[t]), b = __half22float2(b2[t]);
@@ -335,10 +353,12 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::ld16(tc::taddr(tm, C_G1 + c0), g);
             tc::split_rows16(g, x);
             const float gr = S.gam[i64];
+            float gj[8];
+            lds8(S.gam + jh, gj);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 const int j = jh + t;
-                x[t] = j <= i64 ? x[t] * __expf(gr - S.gam[j]) : 0.f;
+                x[t] = j <= i64 ? x[t] * __expf(gr - gj[t]) : 0.f;
             }
             tc::st_tile8(S.Pm, i64, jh, CT, x);
         }
@@ -370,9 +390,15 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::ld16(tc::taddr(tm, R_DQI + c0), a);
             tc::ld16(tc::taddr(tm, R_DQA + c0), b);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                a[t] = S.G[c0 + t] * a[t] + b[t];
-                dg[t] += qreg[t] * a[t];
+            for (int h = 0; h < 2; ++h) {
+                float gv[8];
+                lds8(S.G + c0 + 8 * h, gv);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = 8 * h + u;
+                    a[t] = gv[u] * a[t] + b[t];
+                    dg[t] += qreg[t] * a[t];
+                }
             }
             if (k < P.K) {
                 if (P.G == 1)
@@ -394,11 +420,17 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             // TdW^T -> dk_W
             tc::ld16(tc::taddr(tm, R_TDW + c0), a);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const int j = c0 + t;
-                const float x = S.beta[j] * S.G[j] * a[t];
-                dk[t] += x;
-                dg[t] += kreg[t] * x;
+            for (int h = 0; h < 2; ++h) {
+                float gv[8], bv[8];
+                lds8(S.G + c0 + 8 * h, gv);
+                lds8(S.beta + c0 + 8 * h, bv);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = 8 * h + u;
+                    const float x = bv[u] * gv[u] * a[t];
+                    dk[t] += x;
+                    dg[t] += kreg[t] * x;
+                }
             }
             // s = Gamma_j dT1 + dT2 (dT2 came negated); dT = beta_j s -> dT tile; dbeta_j (WY part) =
             // sum_i T_ij s_ij over this warp's 16 rows
@@ -417,12 +449,16 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                     tr[2 * t + 1] = f.y;
                 }
             }
+            {
+                float gv[8], bv[8];
+                lds8(S.G + jh, gv);
+                lds8(S.beta + jh, bv);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int j = jh + t;
-                const float sv = S.G[j] * x[t] - y[t];
-                x[t] = S.beta[j] * sv;
-                tr[t] *= sv;
+                for (int t = 0; t < 8; ++t) {
+                    const float sv = gv[t] * x[t] - y[t];
+                    x[t] = bv[t] * sv;
+                    tr[t] *= sv;
+                }
             }
             tc::st_tile8(S.dT, i64, jh, CT, x);
             const float s = tc::half_transpose_sum8(tr);
@@ -467,13 +503,14 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::split_rows16(kk, y);
             const int i = i64;
             const float gi = S.gam[i], bi = S.beta[i];
-            float rb = 0.f;
+            float rb = 0.f, gj[8];
+            lds8(S.gam + jh, gj);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 const int j = jh + t;
                 float e = 0.f;
                 if (j < i) {
-                    const float L = __expf(gi - S.gam[j]);
+                    const float L = __expf(gi - gj[t]);
                     const float dA = -x[t];
                     rb += dA * L * y[t];
                     e = bi * L * dA;
