@@ -64,17 +64,31 @@ struct __align__(1024) K4TSmem {
     uint32_t tslot;
 };
 
-template <typename To>
-__device__ __forceinline__ void col16_t(To *p, size_t rs, int n, const float (&x)[16]) {
-#pragma unroll
-    for (int t = 0; t < 16; ++t)
-        if (t < n) p[(size_t)t * rs] = to_out_t<To>(x[t]);
+__device__ __forceinline__ void st2(__nv_bfloat16 *p, float lo, float hi) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(lo, hi);
 }
-// x[t] -> element (t, 0) of a row-major output with row stride rs (elements), for the first n rows.
-__device__ __forceinline__ void store_col16(void *p, int dt, size_t rs, int n, const float (&x)[16]) {
-    if (dt == BF16) col16_t(reinterpret_cast<__nv_bfloat16 *>(p), rs, n, x);
-    else if (dt == F16) col16_t(reinterpret_cast<__half *>(p), rs, n, x);
-    else col16_t(reinterpret_cast<float *>(p), rs, n, x);
+__device__ __forceinline__ void st2(__half *p, float lo, float hi) {
+    *reinterpret_cast<__half2 *>(p) = __floats2half2_rn(lo, hi);
+}
+__device__ __forceinline__ void st2(float *p, float lo, float hi) { *reinterpret_cast<float2 *>(p) = make_float2(lo, hi); }
+template <typename To>
+__device__ __forceinline__ void pairs16_t(To *p, size_t rs, int n, bool act, const float (&x)[16]) {
+    const bool odd = (threadIdx.x & 1) != 0;
+    To *q = odd ? p - 1 + rs : p;  // the pair's even column, on the first row this lane writes
+#pragma unroll
+    for (int t = 0; t < 16; t += 2) {
+        const float recv = __shfl_xor_sync(0xffffffffu, odd ? x[t] : x[t + 1], 1);
+        if (act && t + (odd ? 1 : 0) < n) st2(q + (size_t)t * rs, odd ? recv : x[t], odd ? x[t + 1] : recv);
+    }
+}
+// x[t] -> element (t, 0) of a row-major output with row stride rs (elements), for the first n rows.  Lanes
+// 2m and 2m + 1 hold adjacent columns; the even lane writes rows 0, 2, .. and the odd lane rows 1, 3, .. of
+// both columns with one 2-element store each.  Every lane of the warp calls it (shuffles); act says whether
+// this lane's column exists (the same for both lanes of a pair: the feature sizes are even).
+__device__ __forceinline__ void store_pairs16(void *p, int dt, size_t rs, int n, bool act, const float (&x)[16]) {
+    if (dt == BF16) pairs16_t(reinterpret_cast<__nv_bfloat16 *>(p), rs, n, act, x);
+    else if (dt == F16) pairs16_t(reinterpret_cast<__half *>(p), rs, n, act, x);
+    else pairs16_t(reinterpret_cast<float *>(p), rs, n, act, x);
 }
 __device__ __forceinline__ size_t esize(int dt) { return dt == F32 ? 4 : 2; }
 // 8 consecutive floats of a 16-byte aligned shared array as two vector loads
@@ -285,15 +299,14 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (lost) break;
         float dk[16], dg[16], kreg[16];
         float lastpart = 0.f;
-        tc::ld16(tc::taddr(tm, R_KT + c0), kreg);
         {
-            float g[16];
+            float g[16], g2[16];
             // dW^T -> dWT tile (the stored dV tile is negated, so the product already is dW^T)
-            tc::ld16(tc::taddr(tm, R_DWT + c0), g);
+            tc::ld16x2(tc::taddr(tm, R_KT + c0), kreg, tc::taddr(tm, R_DWT + c0), g);
             tc::st_tile8(S.dWT, k, c0, CT, g);
             tc::st_tile8(S.dWT, k, c0 + 8, CT, g + 8);
             // dk_SC = exp(gamma_C - gamma_j) (V_new dS)_j
-            tc::ld16(tc::taddr(tm, R_DKSC + c0), g);
+            tc::ld16x2(tc::taddr(tm, R_DKSC + c0), g, tc::taddr(tm, R_TDU + c0), g2);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float gc[8];
@@ -309,18 +322,16 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                 }
             }
             // TdU^T -> dv (rows c0.., column k)   (negated dV tile)
-            tc::ld16(tc::taddr(tm, R_TDU + c0), g);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float bv[8];
                 lds8(S.beta + c0 + 8 * h, bv);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) g[8 * h + u] *= -bv[u];
+                for (int u = 0; u < 8; ++u) g2[8 * h + u] *= -bv[u];
             }
-            if (k < P.V)
-                store_col16(reinterpret_cast<char *>(P.dv) +
-                                (((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.V + k) * esize(P.dv_dtype),
-                            P.dv_dtype, (size_t)P.Hv * P.V, nrow, g);
+            store_pairs16(reinterpret_cast<char *>(P.dv) +
+                              (((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.V + k) * esize(P.dv_dtype),
+                          P.dv_dtype, (size_t)P.Hv * P.V, nrow, k < P.V, g2);
         }
         {
             // last row: Gamma_C <S_0, dS_next> + sum_j k_j (.) dk_SC_j.  Warp w takes the 8-column chunk
@@ -387,8 +398,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             float a[16], b[16], qreg[16];
             tc::ld16(tc::taddr(tm, R_QT + c0), qreg);
             // dq = Gamma (.) dq_inter + dq_intra
-            tc::ld16(tc::taddr(tm, R_DQI + c0), a);
-            tc::ld16(tc::taddr(tm, R_DQA + c0), b);
+            tc::ld16x2(tc::taddr(tm, R_DQI + c0), a, tc::taddr(tm, R_DQA + c0), b);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float gv[8];
@@ -400,25 +410,22 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                     dg[t] += qreg[t] * a[t];
                 }
             }
-            if (k < P.K) {
-                if (P.G == 1)
-                    store_col16(reinterpret_cast<char *>(P.dq) +
-                                    (((size_t)(ci.tok0 + c0) * P.Hk + hk) * P.K + k) * esize(P.dqdk_dtype),
-                                P.dqdk_dtype, (size_t)P.Hk * P.K, nrow, a);
-                else
-                    store_col16(P.dq_h + ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, F32, (size_t)P.Hv * P.K,
-                                nrow, a);
-            }
+            if (P.G == 1)
+                store_pairs16(reinterpret_cast<char *>(P.dq) +
+                                  (((size_t)(ci.tok0 + c0) * P.Hk + hk) * P.K + k) * esize(P.dqdk_dtype),
+                              P.dqdk_dtype, (size_t)P.Hk * P.K, nrow, k < P.K, a);
+            else
+                store_pairs16(P.dq_h + ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, F32, (size_t)P.Hv * P.K,
+                              nrow, k < P.K, a);
             ok2 = wait_group2();
             // dk_O
-            tc::ld16(tc::taddr(tm, R_DKO + c0), a);
+            tc::ld16x2(tc::taddr(tm, R_DKO + c0), b, tc::taddr(tm, R_TDW + c0), a);
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
-                dk[t] += a[t];
-                dg[t] -= kreg[t] * a[t];
+                dk[t] += b[t];
+                dg[t] -= kreg[t] * b[t];
             }
             // TdW^T -> dk_W
-            tc::ld16(tc::taddr(tm, R_TDW + c0), a);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float gv[8], bv[8];
@@ -434,8 +441,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             }
             // s = Gamma_j dT1 + dT2 (dT2 came negated); dT = beta_j s -> dT tile; dbeta_j (WY part) =
             // sum_i T_ij s_ij over this warp's 16 rows
-            tc::ld16(tc::taddr(tm, C_DT1 + c0), a);
-            tc::ld16(tc::taddr(tm, C_DT2 + c0), b);
+            tc::ld16x2(tc::taddr(tm, C_DT1 + c0), a, tc::taddr(tm, C_DT2 + c0), b);
             float x[8], y[8], tr[8];
             tc::split_rows16(a, x);
             tc::split_rows16(b, y);
@@ -497,8 +503,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (tid == 0 && has_next) issue_ws2(next);  // T is not read again in this item
         {
             float a[16], kk[16], x[8], y[8];
-            tc::ld16(tc::taddr(tm, C_DA + c0), a);
-            tc::ld16(tc::taddr(tm, C_KK + c0), kk);
+            tc::ld16x2(tc::taddr(tm, C_DA + c0), a, tc::taddr(tm, C_KK + c0), kk);
             tc::split_rows16(a, x);
             tc::split_rows16(kk, y);
             const int i = i64;
@@ -535,22 +540,19 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (has_next && kRaw) fetch_raw(next, 0, S.K);  // K is not read again in this item
         {
             float a[16], b[16];
-            tc::ld16(tc::taddr(tm, R_DKAR + c0), a);
-            tc::ld16(tc::taddr(tm, R_DKAC + c0), b);
+            tc::ld16x2(tc::taddr(tm, R_DKAR + c0), a, tc::taddr(tm, R_DKAC + c0), b);
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
                 dk[t] += a[t] + b[t];
                 dg[t] += kreg[t] * (a[t] - b[t]);
             }
-            if (k < P.K) {
-                if (P.G == 1)
-                    store_col16(reinterpret_cast<char *>(P.dk) +
-                                    (((size_t)(ci.tok0 + c0) * P.Hk + hk) * P.K + k) * esize(P.dqdk_dtype),
-                                P.dqdk_dtype, (size_t)P.Hk * P.K, nrow, dk);
-                else
-                    store_col16(P.dk_h + ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, F32, (size_t)P.Hv * P.K,
-                                nrow, dk);
-            }
+            if (P.G == 1)
+                store_pairs16(reinterpret_cast<char *>(P.dk) +
+                                  (((size_t)(ci.tok0 + c0) * P.Hk + hk) * P.K + k) * esize(P.dqdk_dtype),
+                              P.dqdk_dtype, (size_t)P.Hk * P.K, nrow, k < P.K, dk);
+            else
+                store_pairs16(P.dk_h + ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, F32, (size_t)P.Hv * P.K,
+                              nrow, k < P.K, dk);
             // gate gradient: column sums over the feature rows
             const float s = tc::warp_transpose_sum16(dg);
             if (lane < 16) S.dg_q[q][c0 + lane] = s;
