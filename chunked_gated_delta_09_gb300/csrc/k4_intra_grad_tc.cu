@@ -35,6 +35,10 @@
 namespace gdr {
 
 constexpr int K4T_THREADS = 512;
+// MMA issue: lane 0 of warps 0..3 issues the products of a phase's group 1 (one product each, committed to
+// its mbarrier), lane 0 of warps 4..7 those of group 2; an issuer without a product commits empty.  No warp
+// is held up by more than one product's issue before its own epilogue work.
+constexpr int K4T_ISSUERS = 4;
 constexpr uint32_t K4T_TMEM_COLS = 512;
 constexpr uint32_t K4T_WAIT_LIMIT = 1u << 24;  // mbarrier polls before a wait is declared lost
 
@@ -117,8 +121,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 
     if (wid == 0) tc::tmem_alloc(&S.tslot, K4T_TMEM_COLS);
     if (tid == 0) {
-        tc::mbar_init(&S.bar, 1);
-        tc::mbar_init(&S.bar2, 1);
+        tc::mbar_init(&S.bar, K4T_ISSUERS);
+        tc::mbar_init(&S.bar2, K4T_ISSUERS);
         tc::mbar_init(&S.lbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -208,9 +212,9 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     }
     uint32_t lpar = 0, mpar = 0, mpar2 = 0;
     bool lost = false;
-    // Each phase: one thread issues (group 1, committed to bar, and in phases 1 and 2 a group 2 committed
-    // to bar2 right after it), everyone waits (bounded) for group 1 and agrees on the outcome; the
-    // epilogue starts on group 1's results while group 2 still runs.
+    // Each phase: the issuers issue group 1 (committed to bar) and, in phases 1 and 2, group 2 (committed to
+    // bar2); everyone waits (bounded) for group 1 and agrees on the outcome; the epilogue starts on group
+    // 1's results while group 2 still runs.
     auto finish_phase = [&](bool fail) {
         bool ok = tc::mbar_wait(&S.bar, mpar, K4T_WAIT_LIMIT);
         mpar ^= 1u;
@@ -235,6 +239,9 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     const int k = 32 * q + lane;    // feature row in M = 128 regions
     const int r64 = 16 * q + lane;  // chunk row in M = 64 regions (lanes 0..15)
     const bool own64 = lane < 16;
+    const bool iss1 = lane == 0 && wid < K4T_ISSUERS;                            // group-1 issuer
+    const bool iss2 = lane == 0 && wid >= K4T_ISSUERS && wid < 2 * K4T_ISSUERS;  // group-2 issuer
+    const int slot = wid & (K4T_ISSUERS - 1);
     // M = 64 epilogues after split_rows16: row i64, columns jh .. jh + 7
     const int i64 = 16 * q + (lane & 15), jh = c0 + 8 * (lane >> 4);
 
@@ -278,21 +285,21 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 
         // ---------------- phase 1
         bool fail = false;
-        if (tid == 0) {
+        if (iss1 || iss2) {  // every issuer waits for the workspace tiles itself
             fail = !tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);
             if (!fail) {
-                tc::gemm(tm + R_KT, sK, DT, true, sI, CT, false, 128, 64, CT, false);
-                tc::gemm(tm + R_DWT, sH, DT, true, sdVn, CT, true, 128, 64, DT, false);
-                tc::gemm(tm + R_DKSC, sdH, DT, true, sVn, CT, true, 128, 64, DT, false);
-                tc::gemm(tm + R_TDU, sdVn, CT, false, sT, CT, true, 128, 64, CT, false);
+                if (iss1) {
+                    if (slot == 0) tc::gemm(tm + R_KT, sK, DT, true, sI, CT, false, 128, 64, CT, false);
+                    else if (slot == 1) tc::gemm(tm + R_DWT, sH, DT, true, sdVn, CT, true, 128, 64, DT, false);
+                    else if (slot == 2) tc::gemm(tm + R_DKSC, sdH, DT, true, sVn, CT, true, 128, 64, DT, false);
+                    else tc::gemm(tm + R_TDU, sdVn, CT, false, sT, CT, true, 128, 64, CT, false);
+                } else {
+                    if (slot == 0) tc::gemm(tm + C_G1, sD, DT, false, sVn, CT, true, 64, 64, DT, false);
+                    else if (slot == 1) tc::gemm(tm + C_DT2, sdVn, CT, true, sV, DT, false, 64, 64, DT, false);
+                    else if (slot == 2) tc::gemm(tm + R_DQI, sH, DT, true, sD, DT, false, 128, 64, DT, false);
+                }
             }
-            tc::commit(&S.bar);
-            if (!fail) {
-                tc::gemm(tm + C_G1, sD, DT, false, sVn, CT, true, 64, 64, DT, false);
-                tc::gemm(tm + C_DT2, sdVn, CT, true, sV, DT, false, 64, 64, DT, false);
-                tc::gemm(tm + R_DQI, sH, DT, true, sD, DT, false, 128, 64, DT, false);
-            }
-            tc::commit(&S.bar2);
+            tc::commit(iss1 ? &S.bar : &S.bar2);
         }
         lpar ^= 1u;
         finish_phase(fail);
@@ -382,13 +389,14 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         }
 
         // ---------------- phase 2
-        if (tid == 0) {
-            tc::gemm(tm + R_QT, sQ, DT, true, sI, CT, false, 128, 64, CT, false);
-            tc::gemm(tm + R_DQA, sK, DT, true, sPm, CT, false, 128, 64, CT, false);
+        if (iss1) {
+            if (slot == 0) tc::gemm(tm + R_QT, sQ, DT, true, sI, CT, false, 128, 64, CT, false);
+            else if (slot == 1) tc::gemm(tm + R_DQA, sK, DT, true, sPm, CT, false, 128, 64, CT, false);
             tc::commit(&S.bar);
-            tc::gemm(tm + R_DKO, sQ, DT, true, sPm, CT, true, 128, 64, CT, false);
-            tc::gemm(tm + R_TDW, sdWT, CT, false, sT, CT, true, 128, 64, CT, false);
-            tc::gemm(tm + C_DT1, sdWT, CT, true, sK, DT, false, 64, 64, DT, false);
+        } else if (iss2) {
+            if (slot == 0) tc::gemm(tm + R_DKO, sQ, DT, true, sPm, CT, true, 128, 64, CT, false);
+            else if (slot == 1) tc::gemm(tm + R_TDW, sdWT, CT, false, sT, CT, true, 128, 64, CT, false);
+            else if (slot == 2) tc::gemm(tm + C_DT1, sdWT, CT, true, sK, DT, false, 64, 64, DT, false);
             tc::commit(&S.bar2);
         }
         finish_phase(false);
@@ -475,9 +483,9 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (has_next && kRaw) fetch_raw(next, 1, S.Q);  // Q is not read again in this item
 
         // ---------------- phase 3: X = dT T^T
-        if (tid == 0) {
-            tc::gemm(tm + C_X, sdT, CT, false, sT, CT, false, 64, 64, CT, false);
-            tc::gemm(tm + C_KK, sK, DT, false, sK, DT, false, 64, 64, DT, false);
+        if (iss1) {
+            if (slot == 0) tc::gemm(tm + C_X, sdT, CT, false, sT, CT, false, 64, 64, CT, false);
+            else if (slot == 1) tc::gemm(tm + C_KK, sK, DT, false, sK, DT, false, 64, 64, DT, false);
             tc::commit(&S.bar);
         }
         finish_phase(false);
@@ -494,8 +502,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (lost) break;
 
         // ---------------- phase 4: dA' = T^T X; dA = strict_lower(-dA'); E = beta L dA
-        if (tid == 0) {
-            tc::gemm(tm + C_DA, sT, CT, true, sX, CT, true, 64, 64, CT, false);
+        if (iss1) {
+            if (slot == 0) tc::gemm(tm + C_DA, sT, CT, true, sX, CT, true, 64, 64, CT, false);
             tc::commit(&S.bar);
         }
         finish_phase(false);
@@ -530,9 +538,9 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (lost) break;
 
         // ---------------- phase 5: dk_Ar^T = K^T E^T (+), dk_Ac^T = K^T E (-)
-        if (tid == 0) {
-            tc::gemm(tm + R_DKAR, sK, DT, true, sE, CT, false, 128, 64, CT, false);
-            tc::gemm(tm + R_DKAC, sK, DT, true, sE, CT, true, 128, 64, CT, false);
+        if (iss1) {
+            if (slot == 0) tc::gemm(tm + R_DKAR, sK, DT, true, sE, CT, false, 128, 64, CT, false);
+            else if (slot == 1) tc::gemm(tm + R_DKAC, sK, DT, true, sE, CT, true, 128, 64, CT, false);
             tc::commit(&S.bar);
         }
         finish_phase(false);
