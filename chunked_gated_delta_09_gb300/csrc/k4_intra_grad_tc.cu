@@ -285,25 +285,28 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 
         // ---------------- phase 1
         bool fail = false;
-        if (iss1 || iss2) {  // every issuer waits for the workspace tiles itself
+        if (iss1) {  // every issuer waits for the workspace tiles itself
             fail = !tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);
             if (!fail) {
-                if (iss1) {
-                    if (slot == 0) tc::gemm(tm + R_KT, sK, DT, true, sI, CT, false, 128, 64, CT, false);
-                    else if (slot == 1) tc::gemm(tm + R_DWT, sH, DT, true, sdVn, CT, true, 128, 64, DT, false);
-                    else if (slot == 2) tc::gemm(tm + R_DKSC, sdH, DT, true, sVn, CT, true, 128, 64, DT, false);
-                    else tc::gemm(tm + R_TDU, sdVn, CT, false, sT, CT, true, 128, 64, CT, false);
-                } else {
-                    if (slot == 0) tc::gemm(tm + C_G1, sD, DT, false, sVn, CT, true, 64, 64, DT, false);
-                    else if (slot == 1) tc::gemm(tm + C_DT2, sdVn, CT, true, sV, DT, false, 64, 64, DT, false);
-                    else if (slot == 2) tc::gemm(tm + R_DQI, sH, DT, true, sD, DT, false, 128, 64, DT, false);
-                }
+                if (slot == 0) tc::gemm(tm + R_KT, sK, DT, true, sI, CT, false, 128, 64, CT, false);
+                else if (slot == 1) tc::gemm(tm + R_DWT, sH, DT, true, sdVn, CT, true, 128, 64, DT, false);
+                else if (slot == 2) tc::gemm(tm + R_DKSC, sdH, DT, true, sVn, CT, true, 128, 64, DT, false);
+                else tc::gemm(tm + R_TDU, sdVn, CT, false, sT, CT, true, 128, 64, CT, false);
             }
-            tc::commit(iss1 ? &S.bar : &S.bar2);
+            tc::commit(&S.bar);
         }
-        lpar ^= 1u;
         finish_phase(fail);
         if (lost) break;
+        if (iss2) {  // group 2 once group 1 is done: it runs during group 1's epilogue
+            const bool ok = tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);  // (complete: returns at once)
+            if (ok) {
+                if (slot == 0) tc::gemm(tm + C_G1, sD, DT, false, sVn, CT, true, 64, 64, DT, false);
+                else if (slot == 1) tc::gemm(tm + C_DT2, sdVn, CT, true, sV, DT, false, 64, 64, DT, false);
+                else if (slot == 2) tc::gemm(tm + R_DQI, sH, DT, true, sD, DT, false, 128, 64, DT, false);
+            }
+            tc::commit(&S.bar2);
+        }
+        lpar ^= 1u;
         float dk[16], dg[16], kreg[16];
         float lastpart = 0.f;
         {
@@ -393,14 +396,15 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             if (slot == 0) tc::gemm(tm + R_QT, sQ, DT, true, sI, CT, false, 128, 64, CT, false);
             else if (slot == 1) tc::gemm(tm + R_DQA, sK, DT, true, sPm, CT, false, 128, 64, CT, false);
             tc::commit(&S.bar);
-        } else if (iss2) {
+        }
+        finish_phase(false);
+        if (lost) break;
+        if (iss2) {
             if (slot == 0) tc::gemm(tm + R_DKO, sQ, DT, true, sPm, CT, true, 128, 64, CT, false);
             else if (slot == 1) tc::gemm(tm + R_TDW, sdWT, CT, false, sT, CT, true, 128, 64, CT, false);
             else if (slot == 2) tc::gemm(tm + C_DT1, sdWT, CT, true, sK, DT, false, 64, 64, DT, false);
             tc::commit(&S.bar2);
         }
-        finish_phase(false);
-        if (lost) break;
         bool ok2;
         {
             float a[16], b[16], qreg[16];
