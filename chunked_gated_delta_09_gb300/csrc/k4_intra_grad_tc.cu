@@ -211,14 +211,14 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         fetch_raw(item, 2, S.V);
     }
     uint32_t lpar = 0, mpar = 0, mpar2 = 0;
-    bool lost = false;
+    bool lost = false, okq = true;
     // Each phase: the issuers issue group 1 (committed to bar) and, in phases 1 and 2, group 2 (committed to
-    // bar2); everyone waits (bounded) for group 1 and agrees on the outcome; the epilogue starts on group
-    // 1's results while group 2 still runs.
+    // bar2); every thread waits (bounded) for group 1 itself, and the outcomes of all waits since the last
+    // agreement are agreed at the next block-wide barrier (publish_tiles or the end of the item); the
+    // epilogue starts on group 1's results while group 2 still runs.
     auto finish_phase = [&](bool fail) {
-        bool ok = tc::mbar_wait(&S.bar, mpar, K4T_WAIT_LIMIT);
+        okq &= tc::mbar_wait(&S.bar, mpar, K4T_WAIT_LIMIT) && !fail;
         mpar ^= 1u;
-        lost = __syncthreads_or(!ok || fail || lost) != 0;
         tc::fence_after();
     };
     auto wait_group2 = [&]() -> bool {  // per thread; the outcome is agreed at the next publish_tiles
@@ -230,7 +230,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     auto publish_tiles = [&](bool ok) {  // make epilogue-written tiles visible to the next phase's MMAs
         tc::fence_smem_to_async();
         tc::fence_before();
-        lost = __syncthreads_or(!ok || lost) != 0;
+        lost = __syncthreads_or(!ok || !okq || lost) != 0;
+        okq = true;
         tc::fence_after();
     };
 
@@ -284,9 +285,9 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         tc::fence_after();
 
         // ---------------- phase 1
-        bool fail = false;
-        if (iss1) {  // every issuer waits for the workspace tiles itself
-            fail = !tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);
+        // every thread waits for the workspace tiles itself (the epilogues read some of them directly)
+        bool fail = !tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);
+        if (iss1) {
             if (!fail) {
                 if (slot == 0) tc::gemm(tm + R_KT, sK, DT, true, sI, CT, false, 128, 64, CT, false);
                 else if (slot == 1) tc::gemm(tm + R_DWT, sH, DT, true, sdVn, CT, true, 128, 64, DT, false);
@@ -296,10 +297,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::commit(&S.bar);
         }
         finish_phase(fail);
-        if (lost) break;
         if (iss2) {  // group 2 once group 1 is done: it runs during group 1's epilogue
-            const bool ok = tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);  // (complete: returns at once)
-            if (ok) {
+            if (!fail) {
                 if (slot == 0) tc::gemm(tm + C_G1, sD, DT, false, sVn, CT, true, 64, 64, DT, false);
                 else if (slot == 1) tc::gemm(tm + C_DT2, sdVn, CT, true, sV, DT, false, 64, 64, DT, false);
                 else if (slot == 2) tc::gemm(tm + R_DQI, sH, DT, true, sD, DT, false, 128, 64, DT, false);
@@ -398,7 +397,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::commit(&S.bar);
         }
         finish_phase(false);
-        if (lost) break;
         if (iss2) {
             if (slot == 0) tc::gemm(tm + R_DKO, sQ, DT, true, sPm, CT, true, 128, 64, CT, false);
             else if (slot == 1) tc::gemm(tm + R_TDW, sdWT, CT, false, sT, CT, true, 128, 64, CT, false);
@@ -493,7 +491,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::commit(&S.bar);
         }
         finish_phase(false);
-        if (lost) break;
         {
             float a[16];
             tc::ld16(tc::taddr(tm, C_X + c0), a);
@@ -511,7 +508,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::commit(&S.bar);
         }
         finish_phase(false);
-        if (lost) break;
         if (tid == 0 && has_next) issue_ws2(next);  // T is not read again in this item
         {
             float a[16], kk[16], x[8], y[8];
@@ -548,7 +544,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::commit(&S.bar);
         }
         finish_phase(false);
-        if (lost) break;
         if (has_next && kRaw) fetch_raw(next, 0, S.K);  // K is not read again in this item
         {
             float a[16], b[16];
@@ -570,7 +565,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             if (lane < 16) S.dg_q[q][c0 + lane] = s;
         }
         tc::fence_before();
-        __syncthreads();
+        lost = __syncthreads_or(!okq || lost) != 0;
+        okq = true;
         if (tid < CT) {
             float x = (S.dg_q[0][tid] + S.dg_q[1][tid]) + (S.dg_q[2][tid] + S.dg_q[3][tid]);
             if (tid == rl) {
