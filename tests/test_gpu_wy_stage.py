@@ -52,7 +52,9 @@ def make_wy_inputs(B, T, H, K, V, BT, dtype, seq_lens=None, seed=0):
     dict(B=1, T=0, H=2, K=64, V=32, BT=16, dtype=torch.float16, seq_lens=[70, 5, 130]),
     dict(B=1, T=300, H=1, K=32, V=64, BT=16, dtype=torch.bfloat16),
     dict(B=1, T=2048, H=32, K=128, V=128, BT=64, dtype=torch.float16),  # the operation's model shape
-], ids=["dense_fp16", "fp32", "varlen_bt16_fp16", "bt16_bf16", "model_shape_fp16"])
+    # feature sizes that leave lanes of a warp without a column, ragged chunks of 1 and 33 tokens
+    dict(B=1, T=0, H=3, K=40, V=24, BT=32, dtype=torch.bfloat16, seq_lens=[33, 64, 1, 95]),
+], ids=["dense_fp16", "fp32", "varlen_bt16_fp16", "bt16_bf16", "model_shape_fp16", "varlen_bt32_k40_v24_bf16"])
 def test_wy_stage_matches_oracle(case):
     case = dict(case)
     dtype, seq_lens = case.pop("dtype"), case.pop("seq_lens", None)
