@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                 float aq[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const float d = expf(S.gam[i] - S.gam[j + h]);
+                    const float d = __expf(S.gam[i] - S.gam[j + h]);  // selected only where the argument is <= 0
                     S.AT[i][j + h] = j + h < i ? S.beta[i] * d * kk[0][nt][e + h] : 0.f;
                     aq[h] = j + h <= i ? d * qk[0][nt][e + h] : 0.f;
                 }
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
             float akk = 0.f, aqk = 0.f;
             if (j <= i && i < len) {
                 for (int c = 0; c < DT; ++c) {
-                    float d = expf(gamK[i * DT + c] - gamK[j * DT + c]);
+                    float d = __expf(gamK[i * DT + c] - gamK[j * DT + c]);
                     float kj = ctile_get(S.Ks, j, c, DT);
                     akk += ctile_get(S.Ks, i, c, DT) * kj * d;
                     aqk += ctile_get(S.Qs, i, c, DT) * kj * d;
@@ -252,8 +252,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
             for (int t = 0; t < 8; ++t) {
                 float gi = PC ? gamK[i * DT + c8 + t] : S.gam[i];
                 float gc = PC ? gamK[(len - 1) * DT + c8 + t] : gC;
-                float Gi = expf(gi);
-                o1[t] = kx[t] * expf(gc - gi);  // K~
+                float Gi = __expf(gi);
+                o1[t] = kx[t] * __expf(gc - gi);  // K~
                 o2[t] = qx[t] * Gi;             // Q~
                 o3[t] = bi * Gi * kx[t];        // beta Gamma K
                 o4[t] = bi * vx[t];             // beta V

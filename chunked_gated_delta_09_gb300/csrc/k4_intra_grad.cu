@@ -18,7 +18,10 @@
 //            Gamma_C <S_0, dS_next> + sum_j k_j (.) (K~ term)_j
 // (for the scalar gate the dgamma row is summed over channels).  The per-channel (KDA) gate turns each
 // decayed C x C product into a per-channel sum that the owner of each output element evaluates directly;
-// this kernel serves that gate (the scalar gate runs on k4_intra_grad_tc.cu).
+// this kernel serves that gate (the scalar gate runs on k4_intra_grad_tc.cu).  Every decay factor is
+// exp of a non-positive argument (a later minus an earlier cumulative log-decay, or a cumulative log-decay
+// itself) and is taken with the fast hardware exponential (relative error about 1e-6, below the fp16
+// rounding of the operand tiles).
 //
 // All operands live in shared memory as core-matrix tiles (ctile_off); the workspace tiles arrive by
 // bulk copy.  The workspace holds V_new^T and -dV_new^T (tiles [v][c]).
@@ -146,8 +149,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             for (int e = tid; e < CT * DT; e += K4_THREADS) gamK[e] = P.gam[u * CT * DT + e];
         __syncthreads();  // barrier initialised (first item); tiles of the previous item no longer read
         if (!PC && tid < CT) {
-            S.G[tid] = expf(S.gam[tid]);
-            S.GC[tid] = expf(S.gam[len - 1] - S.gam[tid]);
+            S.G[tid] = __expf(S.gam[tid]);
+            S.GC[tid] = __expf(S.gam[len - 1] - S.gam[tid]);
         }
         const bool loaded = tc::mbar_wait(&S.lbar, parity, K4_WAIT_LIMIT);
         parity ^= 1u;
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 for (int e = 0; e < 4; ++e) {
                     int r = acc_row(cm0, 0, e), j = acc_col(cn0, nt, e);
                     float x = 0.f;
-                    if (j <= r) x = PC ? g1[0][nt][e] : g1[0][nt][e] * expf(S.gam[r] - S.gam[j]);
+                    if (j <= r) x = PC ? g1[0][nt][e] : g1[0][nt][e] * __expf(S.gam[r] - S.gam[j]);
                     ctile_set(S.Pms, r, j, CT, x);
                 }
         }
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    dq[0][nt][e] *= PC ? expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e))) : S.G[acc_row(m0, 0, e)];
+                    dq[0][nt][e] *= PC ? __expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e))) : S.G[acc_row(m0, 0, e)];
             if (WY) {
             } else if (!PC) {
                 warp_mma_ct<1, NK, false, false>(dq, S.Pms, CT, S.Ks, DT, m0, n0, CT);
@@ -217,7 +220,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                         int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                         float gr = gamK[r * DT + c], s = 0.f;
                         for (int j = 0; j <= r; ++j)
-                            s += ctile_get(S.Pms, r, j, CT) * Kv(j, c) * expf(gr - gamK[j * DT + c]);
+                            s += ctile_get(S.Pms, r, j, CT) * Kv(j, c) * __expf(gr - gamK[j * DT + c]);
                         dq[0][nt][e] += s;
                     }
             }
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                         int j = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                         float gj = gamK[j * DT + c], s = 0.f;
                         for (int r = j; r < CT; ++r)
-                            s += ctile_get(S.Pms, r, j, CT) * ctile_get(S.Qs, r, c, DT) * expf(gamK[r * DT + c] - gj);
+                            s += ctile_get(S.Pms, r, j, CT) * ctile_get(S.Qs, r, c, DT) * __expf(gamK[r * DT + c] - gj);
                         dk[0][nt][e] = s;
                     }
             }
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                    float x = t[0][nt][e] * (PC ? expf(G_(rl, c) - G_(r, c)) : S.GC[r]);
+                    float x = t[0][nt][e] * (PC ? __expf(G_(rl, c) - G_(r, c)) : S.GC[r]);
                     float kx = Kv(r, c) * x;
                     dk[0][nt][e] += x;
                     add_dg(nt, e, -(kx));
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                         s += __shfl_xor_sync(0xffffffffu, s, 1);
                         s += __shfl_xor_sync(0xffffffffu, s, 2);
                         s += __shfl_xor_sync(0xffffffffu, s, 4);
-                        if ((lane & 7) == 0) S.lrp[4 + (wid >> 2)][c8 + t] = s * expf(G_(rl, c8 + t));
+                        if ((lane & 7) == 0) S.lrp[4 + (wid >> 2)][c8 + t] = s * __expf(G_(rl, c8 + t));
                     }
                 } else {
                     float s = 0.f;
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                     for (int t = 0; t < 8; ++t) s += acc8[t];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                    if (lane == 0) S.lrs[16 + wid] = s * expf(S.gam[rl]);
+                    if (lane == 0) S.lrs[16 + wid] = s * __expf(S.gam[rl]);
                 }
             }
         }
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             if (PC) {
                 for (int e = tid; e < CT * DT; e += K4_THREADS) {
                     int r = e / DT, c = e % DT;
-                    ctile_set(KGb, r, c, DT, S.beta[r] * expf(gamK[e]) * Kv(r, c));
+                    ctile_set(KGb, r, c, DT, S.beta[r] * __expf(gamK[e]) * Kv(r, c));
                 }
             }
         }
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                    float Gm = PC ? expf(G_(r, c)) : S.G[r];
+                    float Gm = PC ? __expf(G_(r, c)) : S.G[r];
                     float kv = Kv(r, c);
                     float x = S.beta[r] * Gm * t[0][nt][e];
                     dk[0][nt][e] += x;
@@ -466,11 +469,11 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                     float L = 1.f, kkd = 0.f;
                     if (!WY && j < i) {
                         if (!PC) {
-                            L = expf(S.gam[i] - S.gam[j]);
+                            L = __expf(S.gam[i] - S.gam[j]);
                             kkd = L * kk[0][nt][e];
                         } else {
                             for (int c = 0; c < DT; ++c)
-                                kkd += Kv(i, c) * Kv(j, c) * expf(gamK[i * DT + c] - gamK[j * DT + c]);
+                                kkd += Kv(i, c) * Kv(j, c) * __expf(gamK[i * DT + c] - gamK[j * DT + c]);
                         }
                     }
                     rb[e >> 1] += dA * kkd;
@@ -512,9 +515,9 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                         int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                         float gr = gamK[r * DT + c], sa = 0.f, sb = 0.f;
                         for (int j = 0; j < r; ++j)
-                            sa += ctile_get(Es, r, j, CT) * Kv(j, c) * expf(gr - gamK[j * DT + c]);
+                            sa += ctile_get(Es, r, j, CT) * Kv(j, c) * __expf(gr - gamK[j * DT + c]);
                         for (int i = r + 1; i < CT; ++i)
-                            sb += ctile_get(Es, i, r, CT) * Kv(i, c) * expf(gamK[i * DT + c] - gr);
+                            sb += ctile_get(Es, i, r, CT) * Kv(i, c) * __expf(gamK[i * DT + c] - gr);
                         a[0][nt][e] = sa;
                         b[0][nt][e] = sb;
                     }

@@ -13,6 +13,19 @@ namespace gdr {
 
 constexpr int K5_THREADS = 128;
 
+// four consecutive outputs (index i a multiple of 4 in a 16-byte aligned array): one 8- or 16-byte store
+__device__ __forceinline__ void store4(void *p, size_t i, float4 x, int dt) {
+    if (dt == F32) {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p) + i) = x;
+    } else if (dt == BF16) {
+        __nv_bfloat162 v[2] = {__floats2bfloat162_rn(x.x, x.y), __floats2bfloat162_rn(x.z, x.w)};
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p) + i) = *reinterpret_cast<uint2 *>(v);
+    } else {
+        __half2 v[2] = {__floats2half2_rn(x.x, x.y), __floats2half2_rn(x.z, x.w)};
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(p) + i) = *reinterpret_cast<uint2 *>(v);
+    }
+}
+
 template <bool PC>
 __global__ void __launch_bounds__(K5_THREADS) k5_dg_reduce(const Params P) {
     if (*P.status & ST_BAD_SEQLENS) return;
@@ -51,18 +64,22 @@ __global__ void __launch_bounds__(K5_THREADS) k5_dg_reduce(const Params P) {
             }
         }
     }
-    // GQA: dq[t, hk] = sum over the group's value heads (only when Hv > Hk)
+    // GQA: dq[t, hk] = sum over the group's value heads (only when Hv > Hk), four channels per thread: the
+    // per-head rows are 16-byte aligned workspace rows (K a multiple of 8), summed in head order
     if (P.G > 1) {
-        for (int e = tid; e < len * P.K; e += K5_THREADS) {
-            int r = e / P.K, c = e % P.K;
-            size_t t = (size_t)ci.tok0 + r;
-            float sq = 0.f, sk = 0.f;
+        const int k4n = P.K / 4;
+        for (int e = tid; e < len * k4n; e += K5_THREADS) {
+            const int r = e / k4n, c = 4 * (e % k4n);
+            const size_t t = (size_t)ci.tok0 + r;
+            float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
             for (int hv = hk * P.G; hv < (hk + 1) * P.G; ++hv) {
-                sq += P.dq_h[(t * P.Hv + hv) * P.K + c];
-                sk += P.dk_h[(t * P.Hv + hv) * P.K + c];
+                const float4 a = *reinterpret_cast<const float4 *>(P.dq_h + (t * P.Hv + hv) * P.K + c);
+                const float4 b = *reinterpret_cast<const float4 *>(P.dk_h + (t * P.Hv + hv) * P.K + c);
+                sq.x += a.x, sq.y += a.y, sq.z += a.z, sq.w += a.w;
+                sk.x += b.x, sk.y += b.y, sk.z += b.z, sk.w += b.w;
             }
-            store_scalar(P.dq, (t * P.Hk + hk) * P.K + c, sq, P.dqdk_dtype);
-            store_scalar(P.dk, (t * P.Hk + hk) * P.K + c, sk, P.dqdk_dtype);
+            store4(P.dq, (t * P.Hk + hk) * P.K + c, sq, P.dqdk_dtype);
+            store4(P.dk, (t * P.Hk + hk) * P.K + c, sk, P.dqdk_dtype);
         }
     }
 }
