@@ -22,6 +22,19 @@
 namespace gdr {
 
 constexpr int K1_THREADS = 256;
+constexpr int GKLD = DT + 4;  // row stride of the per-channel cumulative gate in shared memory (rows 16 bytes
+                              // apart in bank terms, so a quarter-warp's 16-byte row reads do not collide)
+
+// 8 consecutive fp16 values of a core-matrix tile row segment / 8 fp32 values (16-byte aligned) as floats
+__device__ __forceinline__ void ld8h(const unsigned char *p, float (&x)[8]) {
+    Raw8<__half> r;
+    r.v = *reinterpret_cast<const uint4 *>(p);
+    raw_get(r, x);
+}
+__device__ __forceinline__ void ld8f(const float *p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
 
 struct __align__(1024) K1Smem {
     // Ks holds K, then (once the decayed copies are written) T as the fp16 operand of the W and U products
@@ -78,7 +91,7 @@ template <typename Tin, bool PC>
 __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Params P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     K1Smem &S = *reinterpret_cast<K1Smem *>(smem_raw);
-    float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K1Smem));  // [CT][DT], per-channel only
+    float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K1Smem));  // [CT][GKLD], per-channel only
 
     if (*P.status & ST_BAD_SEQLENS) return;
     const int n = blockIdx.x, hv = blockIdx.y, hk = hv / P.G;
@@ -179,7 +192,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
 #pragma unroll 8
             for (int i = 0; i < CT; ++i) {
                 if (i < len && c < P.K) run += P.g[((size_t)(ci.tok0 + i) * P.Hv + hv) * P.K + c];
-                gamK[i * DT + c] = run;
+                gamK[i * GKLD + c] = run;
                 P.gam[(u * CT + i) * DT + c] = run;
             }
         }
@@ -210,19 +223,61 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                 *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j, CT)) = __floats2half2_rn(aq[0], aq[1]);
             }
     } else {
-        for (int e = tid; e < CT * CT; e += K1_THREADS) {
-            int i = e / CT, j = e % CT;
-            float akk = 0.f, aqk = 0.f;
-            if (j <= i && i < len) {
-                for (int c = 0; c < DT; ++c) {
-                    float d = __expf(gamK[i * DT + c] - gamK[j * DT + c]);
-                    float kj = ctile_get(S.Ks, j, c, DT);
-                    akk += ctile_get(S.Ks, i, c, DT) * kj * d;
-                    aqk += ctile_get(S.Qs, i, c, DT) * kj * d;
+        // per-channel sums sum_c x_ic k_jc exp(gamma_i[c] - gamma_j[c]) over the causal 2 x 2 blocks (bi >= bj)
+        // of the chunk, spread evenly over the threads, 8 channels per step; the blocks above the diagonal
+        // are zero
+        constexpr int NB = CT / 2, NLOW = NB * (NB + 1) / 2;
+        unsigned char *aqk_g = reinterpret_cast<unsigned char *>(P.Aqk + u * CT * CT);
+        for (int b = tid; b < NLOW; b += K1_THREADS) {
+            int bi = (int)((sqrtf(8.f * (float)b + 1.f) - 1.f) * 0.5f);  // row of b in the lower triangle
+            while ((bi + 1) * (bi + 2) / 2 <= b) ++bi;
+            while (bi * (bi + 1) / 2 > b) --bi;
+            const int i0 = 2 * bi, j0 = 2 * (b - bi * (bi + 1) / 2);
+            float akk[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, aqk[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            if (i0 < len) {
+                for (int c8 = 0; c8 < DT; c8 += 8) {
+                    float ki[2][8], qi[2][8], kj[2][8], gi[2][8], gj[2][8];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        ld8h(S.Ks + ctile_off(i0 + r, c8, DT), ki[r]);
+                        ld8h(S.Qs + ctile_off(i0 + r, c8, DT), qi[r]);
+                        ld8h(S.Ks + ctile_off(j0 + r, c8, DT), kj[r]);
+                        ld8f(gamK + (i0 + r) * GKLD + c8, gi[r]);
+                        ld8f(gamK + (j0 + r) * GKLD + c8, gj[r]);
+                    }
+#pragma unroll
+                    for (int a = 0; a < 2; ++a)
+#pragma unroll
+                        for (int bb = 0; bb < 2; ++bb)
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) {
+                                // (exponent <= 0 on every element that is kept below)
+                                const float kd = kj[bb][t] * __expf(gi[a][t] - gj[bb][t]);
+                                akk[a][bb] += ki[a][t] * kd;
+                                aqk[a][bb] += qi[a][t] * kd;
+                            }
                 }
             }
-            S.AT[i][j] = j < i ? S.beta[i] * akk : 0.f;
-            ctile_set(reinterpret_cast<unsigned char *>(P.Aqk + u * CT * CT), i, j, CT, j <= i ? aqk : 0.f);
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+                const int i = i0 + a;
+                float aq[2];
+#pragma unroll
+                for (int bb = 0; bb < 2; ++bb) {
+                    const int j = j0 + bb;
+                    S.AT[i][j] = (j < i && i < len) ? S.beta[i] * akk[a][bb] : 0.f;
+                    aq[bb] = (j <= i && i < len) ? aqk[a][bb] : 0.f;
+                }
+                *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j0, CT)) = __floats2half2_rn(aq[0], aq[1]);
+            }
+        }
+        for (int e = tid; e < CT * CT / 2; e += K1_THREADS) {  // pairs (i, j0 .. j0 + 1) above the diagonal blocks
+            const int i = e / (CT / 2), j0 = 2 * (e % (CT / 2));
+            if (j0 / 2 > i / 2) {
+                S.AT[i][j0] = 0.f;
+                S.AT[i][j0 + 1] = 0.f;
+                *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j0, CT)) = __floats2half2_rn(0.f, 0.f);
+            }
         }
     }
     __syncthreads();
@@ -250,8 +305,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
             const float bi = S.beta[i];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                float gi = PC ? gamK[i * DT + c8 + t] : S.gam[i];
-                float gc = PC ? gamK[(len - 1) * DT + c8 + t] : gC;
+                float gi = PC ? gamK[i * GKLD + c8 + t] : S.gam[i];
+                float gc = PC ? gamK[(len - 1) * GKLD + c8 + t] : gC;
                 float Gi = __expf(gi);
                 o1[t] = kx[t] * __expf(gc - gi);  // K~
                 o2[t] = qx[t] * Gi;             // Q~
@@ -338,7 +393,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
 
 template <typename Tin, bool PC>
 static cudaError_t launch_k1_t(const Params &P, cudaStream_t stream) {
-    size_t smem = sizeof(K1Smem) + (PC ? sizeof(float) * CT * DT : 0);
+    size_t smem = sizeof(K1Smem) + (PC ? sizeof(float) * CT * GKLD : 0);
     cudaError_t e = cudaFuncSetAttribute(k1_wy_prep<Tin, PC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(P.max_chunks, P.Hv);
