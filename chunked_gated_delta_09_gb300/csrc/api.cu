@@ -25,7 +25,7 @@ struct gdr_bwd_plan {
     long long tokens;  // B * T
     // workspace byte offsets
     size_t o_status, o_cidx, o_coff, o_gam, o_T, o_Aqk, o_W, o_U, o_Kt, o_Qg, o_Dt, o_h, o_dh, o_Vn, o_dVn, o_dgam, o_dqh,
-        o_dkh, o_seg, total;
+        o_dkh, o_seg, o_sc, total;
 };
 
 namespace {
@@ -67,6 +67,7 @@ void layout(gdr_bwd_plan &p) {
     p.o_dkh = take(per_head);
     size_t seg_units = p.NS > 1 ? (size_t)p.N * d.Hv * p.NS : 0;
     p.o_seg = take(6 * sizeof(float) * seg_units * DT * DT);
+    p.o_sc = take(d.gate_per_channel ? 0 : sizeof(float) * units * 4 * CT);
     p.total = off;
 }
 
@@ -173,6 +174,7 @@ static void fill_common(const gdr_bwd_plan *plan, char *ws, Params &P) {
     P.chunk_idx = reinterpret_cast<int32_t *>(ws + plan->o_cidx);
     P.chunk_off = reinterpret_cast<int32_t *>(ws + plan->o_coff);
     P.gam = reinterpret_cast<float *>(ws + plan->o_gam);
+    P.sc = plan->d.gate_per_channel ? nullptr : reinterpret_cast<float *>(ws + plan->o_sc);
     P.Tm = reinterpret_cast<__half *>(ws + plan->o_T);
     P.Aqk = reinterpret_cast<__half *>(ws + plan->o_Aqk);
     P.W = reinterpret_cast<__half *>(ws + plan->o_W);

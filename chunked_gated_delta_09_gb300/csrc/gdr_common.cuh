@@ -52,6 +52,7 @@ struct Params {
     // Per chunk x value head unit u = n Hv + hv.  fp16 matrices are stored as core-matrix tiles
     // ("tile [R][C]": see ctile_off), each moved whole by bulk copies.
     float *gam;          // [u][CT] or [u][CT][DT]  chunk-local cumulative gate (fp32)
+    float *sc;           // [u][4][CT] scalar gate, backward: beta, exp(gamma), exp(gamma_C - gamma), gamma
     __half *Tm;          // tile [r][i]   64 x 64    (I + A_kk)^-1
     __half *Aqk;         // tile [r][j]   64 x 64    M (.) Q K^T (causal, decayed, unscaled)
     __half *W, *U;       // W tile [c][k] 64 x 128; U^T tile [v][c] 128 x 64

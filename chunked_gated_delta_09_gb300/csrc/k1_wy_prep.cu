@@ -198,6 +198,14 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
         }
     }
     __syncthreads();
+    if (!PC && P.sc && P.dO && tid < CT) {  // backward: the per-token record the gradient kernel fetches whole
+        float *rec = P.sc + u * 4 * CT;
+        const float gt = S.gam[tid], gl = S.gam[len - 1];
+        rec[tid] = S.beta[tid];
+        rec[CT + tid] = expf(gt);
+        rec[2 * CT + tid] = expf(gl - gt);
+        rec[3 * CT + tid] = gt;
+    }
 
     // ---- A_kk (fp32, shared) and Aqk (fp16 tile)
     if (!PC) {

@@ -60,6 +60,7 @@ struct __align__(1024) K4TSmem {
     unsigned char dT[CT * CT * 2];   // dT, later E
     unsigned char I[CT * CT * 2];    // identity
     float gam[CT], G[CT], GC[CT], beta[CT];
+    float scal[4][CT];  // the next item's per-token record (beta, exp(gamma), exp(gamma_C - gamma), gamma)
     // partial sums in fixed slots, added in a fixed order at the end (run-to-run reproducible):
     // dbeta: 4 row quarters (WY term), 4 column quarters (A term); dgamma rows: 4 lane quarters; last row:
     // 16 warps
@@ -147,7 +148,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 
     // workspace tiles of an item: everything the first phase reads, then T (read until phase 4)
     auto issue_ws1 = [&](size_t un) {
-        tc::mbar_expect_tx(&S.lbar, 2 * DT * DT * 2 + CT * DT * 2 + 2 * DT * CT * 2 + CT * CT * 2);
+        tc::mbar_expect_tx(&S.lbar, 2 * DT * DT * 2 + CT * DT * 2 + 2 * DT * CT * 2 + CT * CT * 2 + 4 * CT * 4);
+        tc::bulk_g2s(&S.scal[0][0], P.sc + un * 4 * CT, 4 * CT * 4, &S.lbar);
         tc::bulk_g2s(S.H, P.h + un * DT * DT, DT * DT * 2, &S.lbar);
         tc::bulk_g2s(S.dH, P.dh + un * DT * DT, DT * DT * 2, &S.lbar);
         tc::bulk_g2s(S.D, P.Dt + un * CT * DT, CT * DT * 2, &S.lbar);
@@ -272,12 +274,14 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             const float mul[3] = {1.f, 1.f, 1.f};
             stage_ct_n<Tin, K4T_THREADS, 3>(dst, srcc, st, nc, mul, len, tid);
         }
+        // every thread waits for the workspace tiles itself (the epilogues read some of them directly); the
+        // per-token record came with them
+        bool fail = !tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);
         if (tid < CT) {
-            const float gt = P.gam[u * CT + tid], gl = P.gam[u * CT + rl];
-            S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
-            S.gam[tid] = gt;
-            S.G[tid] = expf(gt);
-            S.GC[tid] = expf(gl - gt);
+            S.beta[tid] = S.scal[0][tid];
+            S.G[tid] = S.scal[1][tid];
+            S.GC[tid] = S.scal[2][tid];
+            S.gam[tid] = S.scal[3][tid];
         }
         tc::fence_smem_to_async();
         tc::fence_before();
@@ -285,8 +289,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         tc::fence_after();
 
         // ---------------- phase 1
-        // every thread waits for the workspace tiles itself (the epilogues read some of them directly)
-        bool fail = !tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);
         if (iss1) {
             if (!fail) {
                 if (slot == 0) tc::gemm(tm + R_KT, sK, DT, true, sI, CT, false, 128, 64, CT, false);

@@ -64,12 +64,13 @@ def test_stage_flops_sum_to_the_total():
 
 def test_stage_bytes_of_the_per_chunk_gradient_stage():
     """Per chunk x head unit at the T=32768 bf16 shape the gradient stage reads S_0, dS_next (2 x 32 KB),
-    V_new^T, -dV_new^T, D (3 x 16 KB), T (8 KB), q, k, v (3 x 16 KB), beta and gamma (256 B each) and
-    writes dq, dk, dv (3 x 16 KB), dbeta and d(gamma) (256 B each)."""
+    V_new^T, -dV_new^T, D (3 x 16 KB), T (8 KB), q, k, v (3 x 16 KB) and the per-token record of the scalar
+    gate (beta, exp(gamma), exp(gamma_C - gamma), gamma: 1 KB) and writes dq, dk, dv (3 x 16 KB), dbeta and
+    d(gamma) (256 B each)."""
     from chunked_gated_delta_09_gb300 import counts
     from chunked_gated_delta_09_gb300.inputs import workload
     p = workload("gdn_t32k_bf16")
-    per_unit = 2 * 32768 + 3 * 16384 + 8192 + 3 * 16384 + 2 * 256 + 3 * 16384 + 2 * 256
+    per_unit = 2 * 32768 + 3 * 16384 + 8192 + 3 * 16384 + 1024 + 3 * 16384 + 2 * 256
     sb = counts.stage_bytes(p)
     assert sb[4] == 8192 * per_unit
     assert counts.scan_segments(p) == 9
