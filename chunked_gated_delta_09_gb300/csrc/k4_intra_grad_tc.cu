@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     const bool iss1 = lane == 0 && wid < K4T_ISSUERS;                            // group-1 issuer
     const bool iss2 = lane == 0 && wid >= K4T_ISSUERS && wid < 2 * K4T_ISSUERS;  // group-2 issuer
     const int slot = wid & (K4T_ISSUERS - 1);
+    const bool loader = tid == 32 * 2 * K4T_ISSUERS;  // issues the bulk copies (lane 0 of the first non-issuing warp)
     // M = 64 epilogues after split_rows16: row i64, columns jh .. jh + 7
     const int i64 = 16 * q + (lane & 15), jh = c0 + 8 * (lane >> 4);
 
@@ -386,17 +387,18 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         }
         publish_tiles(ok1);
         if (lost) break;
-        // S_0, dS_next, D, V_new^T, -dV_new^T and V are not read again in this item
-        if (has_next) {
-            if (tid == 0) issue_ws1(next);
-            if (kRaw) fetch_raw(next, 2, S.V);
-        }
 
         // ---------------- phase 2
         if (iss1) {
             if (slot == 0) tc::gemm(tm + R_QT, sQ, DT, true, sI, CT, false, 128, 64, CT, false);
             else if (slot == 1) tc::gemm(tm + R_DQA, sK, DT, true, sPm, CT, false, 128, 64, CT, false);
             tc::commit(&S.bar);
+        }
+        // S_0, dS_next, D, V_new^T, -dV_new^T and V are not read again in this item (after the MMA issue, so
+        // that no issuer waits behind the copies)
+        if (has_next) {
+            if (loader) issue_ws1(next);
+            if (kRaw) fetch_raw(next, 2, S.V);
         }
         finish_phase(false);
         if (iss2) {
@@ -484,7 +486,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         }
         publish_tiles(ok2);
         if (lost) break;
-        if (has_next && kRaw) fetch_raw(next, 1, S.Q);  // Q is not read again in this item
 
         // ---------------- phase 3: X = dT T^T
         if (iss1) {
@@ -492,6 +493,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             else if (slot == 1) tc::gemm(tm + C_KK, sK, DT, false, sK, DT, false, 64, 64, DT, false);
             tc::commit(&S.bar);
         }
+        if (has_next && kRaw) fetch_raw(next, 1, S.Q);  // Q is not read again in this item
         finish_phase(false);
         {
             float a[16];
@@ -510,7 +512,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::commit(&S.bar);
         }
         finish_phase(false);
-        if (tid == 0 && has_next) issue_ws2(next);  // T is not read again in this item
+        if (loader && has_next) issue_ws2(next);  // T is not read again in this item
         {
             float a[16], kk[16], x[8], y[8];
             tc::ld16x2(tc::taddr(tm, C_DA + c0), a, tc::taddr(tm, C_KK + c0), kk);
