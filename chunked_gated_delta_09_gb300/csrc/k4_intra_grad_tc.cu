@@ -263,8 +263,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if constexpr (kRaw) {
             cp_async_wait<0>();
             convert_raw(S.K);
-            convert_raw(S.Q);
-            convert_raw(S.V);
+            convert_raw(S.V);  // (Q, first read in phase 2, is converted while phase 1 runs)
         } else {
             unsigned char *const dst[3] = {S.K, S.Q, S.V};
             const Tin *src[3];
@@ -299,6 +298,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             }
             tc::commit(&S.bar);
         }
+        convert_raw(S.Q);  // published to phase 2 by the tile barrier after the first epilogue
         finish_phase(fail);
         if (iss2) {  // group 2 once group 1 is done: it runs during group 1's epilogue
             if (!fail) {
