@@ -64,7 +64,9 @@ struct __align__(1024) K4TSmem {
     // partial sums in fixed slots, added in a fixed order at the end (run-to-run reproducible):
     // dbeta: 4 row quarters (WY term), 4 column quarters (A term); dgamma rows: 4 lane quarters; last row:
     // 16 warps
-    float db_wy[4][CT], db_a[4][CT], dg_q[4][CT], last_w[16];
+    // (two sets, by item parity: an item's sums are added during the next item's first MMA phase)
+    float db_wy[2][4][CT], db_a[2][4][CT], dg_q[2][4][CT], last_w[2][16];
+    int red_u, red_len, red_tok0, red_hv, red_b;  // the item whose sums are pending (red_u < 0: none), its set
     uint64_t bar, bar2, lbar;  // MMA groups 1 and 2 of a phase; bulk loads
     uint32_t tslot;
 };
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         tc::mbar_init(&S.bar, K4T_ISSUERS);
         tc::mbar_init(&S.bar2, K4T_ISSUERS);
         tc::mbar_init(&S.lbar, 1);
+        S.red_u = -1;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     for (int e = tid; e < CT * CT / 8; e += K4T_THREADS) {
@@ -229,6 +232,22 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         tc::fence_after();
         return ok;
     };
+    // threads < CT: dbeta and d(gamma) of the pending item from its partial set, added in a fixed order
+    auto reduce_pending = [&]() {
+        const int ru = S.red_u, rlen = S.red_len, b = S.red_b;
+        if (ru < 0) return;
+        float x = (S.dg_q[b][0][tid] + S.dg_q[b][1][tid]) + (S.dg_q[b][2][tid] + S.dg_q[b][3][tid]);
+        if (tid == rlen - 1) {
+            float l = 0.f;
+#pragma unroll
+            for (int w = 0; w < 16; ++w) l += S.last_w[b][w];
+            x += l;
+        }
+        P.dgam[(size_t)ru * CT + tid] = tid < rlen ? x : 0.f;
+        float bb = (S.db_wy[b][0][tid] + S.db_wy[b][1][tid]) + (S.db_wy[b][2][tid] + S.db_wy[b][3][tid]);
+        bb += (S.db_a[b][0][tid] + S.db_a[b][1][tid]) + (S.db_a[b][2][tid] + S.db_a[b][3][tid]);
+        if (tid < rlen) P.dbeta[(size_t)(S.red_tok0 + tid) * P.Hv + S.red_hv] = bb;
+    };
     auto publish_tiles = [&](bool ok) {  // make epilogue-written tiles visible to the next phase's MMAs
         tc::fence_smem_to_async();
         tc::fence_before();
@@ -258,6 +277,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         const int next = valid_from(item + gridDim.x);
         const bool has_next = next < n_items;
         const int nrow = len - c0 < 0 ? 0 : (len - c0 > 16 ? 16 : len - c0);  // valid rows among c0 .. c0+15
+        // partial-sum set of this item: its position in the CTA's sequence (invalid items only trail the list)
+        const int pb = ((item - (int)blockIdx.x) / (int)gridDim.x) & 1;
 
         // ---- inputs as fp16 tiles (the workspace tiles are on their way by bulk copy)
         if constexpr (kRaw) {
@@ -285,7 +306,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         }
         tc::fence_smem_to_async();
         tc::fence_before();
-        __syncthreads();
+        lost = __syncthreads_or(!okq || lost) != 0;  // (also orders the previous item's partial sums)
+        okq = true;
         tc::fence_after();
 
         // ---------------- phase 1
@@ -299,6 +321,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::commit(&S.bar);
         }
         convert_raw(S.Q);  // published to phase 2 by the tile barrier after the first epilogue
+        if (tid < CT) reduce_pending();  // the previous item's sums, while phase 1 runs
         finish_phase(fail);
         if (iss2) {  // group 2 once group 1 is done: it runs during group 1's epilogue
             if (!fail) {
@@ -367,7 +390,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             float tot = lastpart + S.G[rl] * hd;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-            if (lane == 0) S.last_w[wid] = tot;
+            if (lane == 0) S.last_w[pb][wid] = tot;
         }
         const bool ok1 = wait_group2();
         {
@@ -482,7 +505,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             }
             tc::st_tile8(S.dT, i64, jh, CT, x);
             const float s = tc::half_transpose_sum8(tr);
-            if ((lane & 8) == 0) S.db_wy[q][jh + (lane & 7)] = s;
+            if ((lane & 8) == 0) S.db_wy[pb][q][jh + (lane & 7)] = s;
         }
         publish_tiles(ok2);
         if (lost) break;
@@ -536,7 +559,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             }
             tc::st_tile8(Es, i, jh, CT, x);
             rb += __shfl_xor_sync(0xffffffffu, rb, 16);
-            if (lane < 16) S.db_a[wid >> 2][i] = rb;
+            if (lane < 16) S.db_a[pb][wid >> 2][i] = rb;
         }
         publish_tiles(true);
         if (lost) break;
@@ -566,26 +589,20 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                               nrow, k < P.K, dk);
             // gate gradient: column sums over the feature rows
             const float s = tc::warp_transpose_sum16(dg);
-            if (lane < 16) S.dg_q[q][c0 + lane] = s;
+            if (lane < 16) S.dg_q[pb][q][c0 + lane] = s;
+        }
+        if (tid == 0) {  // its sums are added during the next item's first phase (or after the loop)
+            S.red_u = (int)u;
+            S.red_len = len;
+            S.red_tok0 = ci.tok0;
+            S.red_hv = hv;
+            S.red_b = pb;
         }
         tc::fence_before();
-        lost = __syncthreads_or(!okq || lost) != 0;
-        okq = true;
-        if (tid < CT) {
-            float x = (S.dg_q[0][tid] + S.dg_q[1][tid]) + (S.dg_q[2][tid] + S.dg_q[3][tid]);
-            if (tid == rl) {
-                float l = 0.f;
-#pragma unroll
-                for (int w = 0; w < 16; ++w) l += S.last_w[w];
-                x += l;
-            }
-            P.dgam[u * CT + tid] = tid < len ? x : 0.f;
-            float b = (S.db_wy[0][tid] + S.db_wy[1][tid]) + (S.db_wy[2][tid] + S.db_wy[3][tid]);
-            b += (S.db_a[0][tid] + S.db_a[1][tid]) + (S.db_a[2][tid] + S.db_a[3][tid]);
-            if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = b;
-        }
         item = next;
     }
+    lost = __syncthreads_or(!okq || lost) != 0;
+    if (!lost && tid < CT) reduce_pending();  // the last item's sums
     if (lost && tid == 0) flag_status(P.status, ST_TIMEOUT);
     cp_async_wait<0>();  // no copy of this thread may still be landing when the CTA exits
     tc::fence_before();
