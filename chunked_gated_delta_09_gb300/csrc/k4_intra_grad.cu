@@ -35,6 +35,50 @@ constexpr int K4_THREADS = 512;
 // warp tiling: 16 warps, four row blocks of 16 rows x four column blocks
 constexpr int NK = 4;  // C x K tiles: 16 x 32 per warp (four n8 tiles)
 constexpr int NC = 2;  // C x C tiles: 16 x 16 per warp (two n8 tiles)
+
+// Per-channel decayed products on the accumulator layout of a 16 x (8 NK) warp tile (rows r0 = m0 + lane / 4
+// and r0 + 8, column pairs c = n0 + 8 nt + 2 (lane % 4) + {0, 1}), A a C x C and X a C x DT fp16 tile, g the
+// per-channel cumulative gate [CT][DT]:
+//   LOWER:  acc[r][c] += sum_{j <= r (INCL) or j < r} A[r][j] X[j][c] exp(g[r][c] - g[j][c])
+//   else:   acc[r][c] += sum_{i >= r (INCL) or i > r} A[i][r] X[i][c] exp(g[i][c] - g[r][c])
+// One pass over the inner index serves all 16 elements of a thread (two A loads, a column pair of X and of g
+// per n-tile); terms outside a row's range are dropped by selection, never by a zero factor.
+template <bool LOWER, bool INCL>
+__device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsigned char *A, const unsigned char *X,
+                                            const float *g, int m0, int n0, int lane) {
+    const int r0 = m0 + (lane >> 2), cq = n0 + 2 * (lane & 3);
+    float gr[2][NK][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int nt = 0; nt < NK; ++nt) {
+            const float2 v = *reinterpret_cast<const float2 *>(g + (r0 + 8 * h) * DT + cq + 8 * nt);
+            gr[h][nt][0] = v.x;
+            gr[h][nt][1] = v.y;
+        }
+    const int lo = LOWER ? 0 : (INCL ? r0 : r0 + 1), hi = LOWER ? (INCL ? r0 + 8 : r0 + 7) : CT - 1;
+    for (int j = lo; j <= hi; ++j) {
+        // LOWER: row r0 uses j only up to r0 (every j of the loop serves row r0 + 8); else row r0 + 8 uses
+        // i only from r0 + 8 on (every i of the loop serves row r0)
+        const bool v0 = LOWER ? (INCL ? j <= r0 : j < r0) : true;
+        const bool v1 = LOWER ? true : (INCL ? j >= r0 + 8 : j > r0 + 8);
+        const float a0 = LOWER ? ctile_get(A, r0, j, CT) : ctile_get(A, j, r0, CT);
+        const float a1 = LOWER ? ctile_get(A, r0 + 8, j, CT) : ctile_get(A, j, r0 + 8, CT);
+#pragma unroll
+        for (int nt = 0; nt < NK; ++nt) {
+            const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(X + ctile_off(j, cq + 8 * nt, DT)));
+            const float2 gj = *reinterpret_cast<const float2 *>(g + j * DT + cq + 8 * nt);
+            const float e00 = __expf(LOWER ? gr[0][nt][0] - gj.x : gj.x - gr[0][nt][0]);
+            const float e01 = __expf(LOWER ? gr[0][nt][1] - gj.y : gj.y - gr[0][nt][1]);
+            const float e10 = __expf(LOWER ? gr[1][nt][0] - gj.x : gj.x - gr[1][nt][0]);
+            const float e11 = __expf(LOWER ? gr[1][nt][1] - gj.y : gj.y - gr[1][nt][1]);
+            acc[0][nt][0] += v0 ? a0 * x.x * e00 : 0.f;
+            acc[0][nt][1] += v0 ? a0 * x.y * e01 : 0.f;
+            acc[0][nt][2] += v1 ? a1 * x.x * e10 : 0.f;
+            acc[0][nt][3] += v1 ? a1 * x.y * e11 : 0.f;
+        }
+    }
+}
 constexpr uint32_t K4_WAIT_LIMIT = 1u << 24;
 
 struct __align__(1024) K4Smem {
@@ -213,16 +257,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             } else if (!PC) {
                 warp_mma_ct<1, NK, false, false>(dq, S.Pms, CT, S.Ks, DT, m0, n0, CT);
             } else {
-#pragma unroll
-                for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                        float gr = gamK[r * DT + c], s = 0.f;
-                        for (int j = 0; j <= r; ++j)
-                            s += ctile_get(S.Pms, r, j, CT) * Kv(j, c) * __expf(gr - gamK[j * DT + c]);
-                        dq[0][nt][e] += s;
-                    }
+                decayed_acc<true, true>(dq, S.Pms, S.Ks, gamK, m0, n0, lane);
             }
 #pragma unroll
             for (int nt = 0; nt < NK; ++nt)
@@ -244,16 +279,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             } else if (!PC) {
                 warp_mma_ct<1, NK, true, false>(dk, S.Pms, CT, S.Qs, DT, m0, n0, CT);
             } else {
-#pragma unroll
-                for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        int j = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                        float gj = gamK[j * DT + c], s = 0.f;
-                        for (int r = j; r < CT; ++r)
-                            s += ctile_get(S.Pms, r, j, CT) * ctile_get(S.Qs, r, c, DT) * __expf(gamK[r * DT + c] - gj);
-                        dk[0][nt][e] = s;
-                    }
+                decayed_acc<false, true>(dk, S.Pms, S.Qs, gamK, m0, n0, lane);
             }
 #pragma unroll
             for (int nt = 0; nt < NK; ++nt)
@@ -508,19 +534,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 warp_mma_ct<1, NK, false, false>(a, Es, CT, S.Ks, DT, m0, n0, CT);
                 warp_mma_ct<1, NK, true, false>(b, Es, CT, S.Ks, DT, m0, n0, CT);
             } else {
-#pragma unroll
-                for (int nt = 0; nt < NK; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                        float gr = gamK[r * DT + c], sa = 0.f, sb = 0.f;
-                        for (int j = 0; j < r; ++j)
-                            sa += ctile_get(Es, r, j, CT) * Kv(j, c) * __expf(gr - gamK[j * DT + c]);
-                        for (int i = r + 1; i < CT; ++i)
-                            sb += ctile_get(Es, i, r, CT) * Kv(i, c) * __expf(gamK[i * DT + c] - gr);
-                        a[0][nt][e] = sa;
-                        b[0][nt][e] = sb;
-                    }
+                decayed_acc<true, false>(a, Es, S.Ks, gamK, m0, n0, lane);
+                decayed_acc<false, false>(b, Es, S.Ks, gamK, m0, n0, lane);
             }
 #pragma unroll
             for (int nt = 0; nt < NK; ++nt)
