@@ -298,12 +298,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         // every thread waits for the workspace tiles itself (the epilogues read some of them directly); the
         // per-token record came with them
         bool fail = !tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);
-        if (tid < CT) {
-            S.beta[tid] = S.scal[0][tid];
-            S.G[tid] = S.scal[1][tid];
-            S.GC[tid] = S.scal[2][tid];
-            S.gam[tid] = S.scal[3][tid];
-        }
         tc::fence_smem_to_async();
         tc::fence_before();
         lost = __syncthreads_or(!okq || lost) != 0;  // (also orders the previous item's partial sums)
@@ -321,7 +315,15 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::commit(&S.bar);
         }
         convert_raw(S.Q);  // published to phase 2 by the tile barrier after the first epilogue
-        if (tid < CT) reduce_pending();  // the previous item's sums, while phase 1 runs
+        if (tid < CT) {
+            reduce_pending();  // the previous item's sums, while phase 1 runs
+            // the record into the arrays the later epilogues read (the first reads it in place; the next
+            // item's record lands over it after the first tile barrier)
+            S.beta[tid] = S.scal[0][tid];
+            S.G[tid] = S.scal[1][tid];
+            S.GC[tid] = S.scal[2][tid];
+            S.gam[tid] = S.scal[3][tid];
+        }
         finish_phase(fail);
         if (iss2) {  // group 2 once group 1 is done: it runs during group 1's epilogue
             if (!fail) {
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float gc[8];
-                lds8(S.GC + c0 + 8 * h, gc);
+                lds8(S.scal[2] + c0 + 8 * h, gc);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int t = 8 * h + u;
@@ -360,7 +362,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float bv[8];
-                lds8(S.beta + c0 + 8 * h, bv);
+                lds8(S.scal[0] + c0 + 8 * h, bv);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) g2[8 * h + u] *= -bv[u];
             }
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
                     hd += a.x * b.x + a.y * b.y;
                 }
             }
-            float tot = lastpart + S.G[rl] * hd;
+            float tot = lastpart + S.scal[1][rl] * hd;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
             if (lane == 0) S.last_w[pb][wid] = tot;
@@ -398,9 +400,9 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             float g[16], x[8];
             tc::ld16(tc::taddr(tm, C_G1 + c0), g);
             tc::split_rows16(g, x);
-            const float gr = S.gam[i64];
+            const float gr = S.scal[3][i64];
             float gj[8];
-            lds8(S.gam + jh, gj);
+            lds8(S.scal[3] + jh, gj);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 const int j = jh + t;
