@@ -44,6 +44,7 @@ struct __align__(1024) K1Smem {
     float AT[CT][CT + 1];
     float gam[CT];
     float beta[CT];
+    uint64_t rbar;  // 16-bit inputs: the raw rows' bulk copies
 };
 
 // One doubling level of the unit-lower-triangular inverse T = (I + A)^-1 held in fp32 shared memory:
@@ -114,34 +115,57 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
         if (2 * lane + 1 < len) gx1 = P.g[(size_t)(ci.tok0 + 2 * lane + 1) * P.Hv + hv];
     }
     if constexpr (sizeof(Tin) == 2) {
-        // raw rows into their tile slots (dO into the A / T buffer, not yet in use), one round trip for all
-        constexpr int PER = CT * (DT / 8) / K1_THREADS;
+        // The chunk's raw rows, row-major at a 256-byte pitch, by bulk copy into the tile slots (dO into the
+        // A / T buffer, not yet in use): thread t copies row t % 64 of input t / 64, all on one mbarrier that
+        // thread 0 arms with the total before anyone issues.  Each tile is then read row-major and, after a
+        // barrier, written back in place as the fp16 core-matrix tile (dO, scaled, to its workspace tile).
         const int nin = P.dO ? 4 : 3;
         unsigned char *const slot[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(&S.AT[0][0])};
         const Tin *const src[4] = {kp, qp, vp, dop};
         const size_t st[4] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V, (size_t)P.Hv * P.V};
         const int nc[4] = {P.K, P.K, P.V, P.V};
-        for (int w = 0; w < nin; ++w)
+        if (tid == 0) {
+            tc::mbar_init(&S.rbar, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+            tc::mbar_expect_tx(&S.rbar, (uint32_t)(len * (2 * P.K + (nin - 2) * P.V) * 2));
+        }
+        __syncthreads();
+        {
+            const int w = tid / CT, r = tid % CT;
+            if (w < nin && r < len)
+                tc::bulk_g2s(slot[w] + r * DT * 2, src[w] + (size_t)r * st[w], (uint32_t)(nc[w] * 2), &S.rbar);
+        }
+        const bool landed = tc::mbar_wait(&S.rbar, 0, 1u << 24);
+        if (__syncthreads_or(!landed)) {
+            if (tid == 0) flag_status(P.status, ST_TIMEOUT);
+            return;
+        }
+        constexpr int PER = CT * (DT / 8) / K1_THREADS;  // 16-byte chunks per thread and tile
+        for (int w = 0; w < nin; ++w) {
+            // chunk g -> row r, column c8: a quarter-warp takes the 8 rows of one 8-row block at 8 different
+            // column chunks (conflict-free row-major reads and core-matrix writes)
+            uint4 raw[PER];
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
-                const int c = wid + (K1_THREADS / 32) * i;
-                const int r = 8 * (c >> 2) + (lane & 7), c8 = 8 * (4 * (c & 3) + (lane >> 3));
-                const bool ok = r < len && c8 + 8 <= nc[w];
-                cp_async16_zfill(slot[w] + ctile_off(r, c8, DT), ok ? src[w] + (size_t)r * st[w] + c8 : src[w],
-                                 ok ? 16 : 0);
+                const int g = tid + K1_THREADS * i, l8 = g & 7;
+                const int r = 8 * (g >> 7) + l8, c8 = 8 * ((((g & 127) >> 3) + l8) & 15);
+                raw[i] = *reinterpret_cast<const uint4 *>(slot[w] + r * DT * 2 + c8 * 2);
             }
-        cp_async_commit();
-        cp_async_wait<0>();
-        for (int w = 0; w < nin; ++w)
+            if (w < 3) __syncthreads();  // every chunk of this tile read before the in-place writes
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {  // each thread converts the chunks it fetched
-                const int c = wid + (K1_THREADS / 32) * i;
-                const int r = 8 * (c >> 2) + (lane & 7), c8 = 8 * (4 * (c & 3) + (lane >> 3));
+            for (int i = 0; i < PER; ++i) {
+                const int g = tid + K1_THREADS * i, l8 = g & 7;
+                const int r = 8 * (g >> 7) + l8, c8 = 8 * ((((g & 127) >> 3) + l8) & 15);
                 const uint32_t off = ctile_off(r, c8, DT);
-                Raw8<Tin> x;
-                x.v = *reinterpret_cast<const uint4 *>(slot[w] + off);
                 float f[8];
-                raw_get(x, f);
+                if (r < len && c8 < nc[w]) {
+                    Raw8<Tin> x;
+                    x.v = raw[i];
+                    raw_get(x, f);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) f[t] = 0.f;
+                }
                 if (w == 3) {
 #pragma unroll
                     for (int t = 0; t < 8; ++t) f[t] *= P.scale;
@@ -151,6 +175,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                     *reinterpret_cast<uint4 *>(slot[w] + off) = pack8_half(f);
                 }
             }
+        }
     } else if (P.dO) {  // backward: also D = scale dO, written straight to its workspace tile
         unsigned char *const dst[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT)};
         const Tin *const src[4] = {kp, qp, vp, dop};
