@@ -132,8 +132,11 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
         __syncthreads();
         {
             const int w = tid / CT, r = tid % CT;
-            if (w < nin && r < len)
-                tc::bulk_g2s(slot[w] + r * DT * 2, src[w] + (size_t)r * st[w], (uint32_t)(nc[w] * 2), &S.rbar);
+            unsigned char *const dst = w == 0 ? S.Ks : w == 1 ? S.Qs : w == 2 ? S.Vs : slot[3];
+            const Tin *const sp = w == 0 ? kp : w == 1 ? qp : w == 2 ? vp : dop;
+            const size_t sst = w < 2 ? (size_t)P.Hk * P.K : (size_t)P.Hv * P.V;
+            const int snc = w < 2 ? P.K : P.V;
+            if (w < nin && r < len) tc::bulk_g2s(dst + r * DT * 2, sp + (size_t)r * sst, (uint32_t)(snc * 2), &S.rbar);
         }
         const bool landed = tc::mbar_wait(&S.rbar, 0, 1u << 24);
         if (__syncthreads_or(!landed)) {
@@ -141,7 +144,9 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
             return;
         }
         constexpr int PER = CT * (DT / 8) / K1_THREADS;  // 16-byte chunks per thread and tile
-        for (int w = 0; w < nin; ++w) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            if (w >= nin) break;
             // chunk g -> row r, column c8: a quarter-warp takes the 8 rows of one 8-row block at 8 different
             // column chunks (conflict-free row-major reads and core-matrix writes)
             uint4 raw[PER];
