@@ -9,7 +9,10 @@
 // then writes the WY factors W = T diag(beta Gamma) K and U = T diag(beta) V, the decayed attention
 // matrix Aqk = M (.) Q K^T (M[i, j] = exp(gamma_i - gamma_j), j <= i), the decayed copies
 // K~ = K (.) exp(gamma_C - gamma) and Q~ = Q (.) exp(gamma) that the two scans use, and D = scale dO.
-// Per-channel gate: each exp(gamma_a - gamma_b) is taken per key channel inside the K contraction.
+// Per-channel gate: each exp(gamma_a - gamma_b) is taken per key channel inside the K contraction.  For the
+// scalar gate's backward it also writes each unit's per-token record (beta, exp(gamma), exp(gamma_C - gamma),
+// gamma) that the per-chunk gradient kernel fetches whole.  16-bit input rows arrive by bulk copy (one row
+// per thread) and are rearranged in place into the core-matrix tiles.
 //
 // Every matrix output is written in the core-matrix tile layout that the tensor-core kernels read,
 // straight from registers: 8 lanes of an element-wise pass write one contiguous 128-byte core matrix, and
