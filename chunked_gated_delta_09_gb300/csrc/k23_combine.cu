@@ -8,9 +8,12 @@
 // counts) and walks the segments serially, prefetching the next segment's transition and summary rows
 // with cp.async while it multiplies by the current ones.  Each thread accumulates four columns of all
 // the CTA's rows over one warp's slice of the reduction, so every transition element read from shared
-// memory serves 16 rows; the slices are summed in a fixed order.
+// memory serves 16 rows; the slices are summed in a fixed order.  The prefetch is two bulk copies (the
+// transition, 64 KB, and the CTA's summary rows, 8 KB, both contiguous) by one thread on the buffer's
+// mbarrier.
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
+#include "tc_util.cuh"
 
 namespace gdr {
 
@@ -21,6 +24,7 @@ constexpr int CB_PP = DT + 4;    // fp32 pitch of a partial-sum row (16-byte rea
 template <bool FWD>
 __global__ void __launch_bounds__(CB_THREADS) k23_combine(const Params P) {
     __shared__ __align__(16) float XT[DT][CB_ROWS];  // the current rows, transposed: XT[j][r]
+    __shared__ uint64_t pbar[2];                     // the two prefetch buffers' bulk copies
     extern __shared__ __align__(16) float dyn[];     // Ph [2][DT][DT], Ad [2][CB_ROWS][DT], part [8][CB_ROWS][CB_PP]
     float *Ph = dyn, *Ad = dyn + 2 * DT * DT, *part = Ad + 2 * CB_ROWS * DT;
     if (*P.status & ST_BAD_SEQLENS) return;
@@ -37,18 +41,21 @@ __global__ void __launch_bounds__(CB_THREADS) k23_combine(const Params P) {
     const float *trans = FWD ? P.segPhi : P.segPhiT;  // row j of the matrix applied on the right
     const float *adds = FWD ? P.segE : P.segF;
 
-    // the next step's transition and summary rows, in flight while the current step multiplies
+    // the next step's transition and summary rows, in flight while the current step multiplies (thread 0)
     auto prefetch = [&](int step, int buf) {
         const int sg = FWD ? step : nss - 1 - step;
-        const float *src = trans + (su0 + sg) * DT * DT;
-        float *dst = Ph + buf * DT * DT;
-        for (int e = tid; e < DT * DT / 4; e += CB_THREADS) cp_async16(dst + 4 * e, src + 4 * e);
-        const float *asrc = adds + (su0 + sg) * DT * DT + (size_t)r0 * DT;
-        float *adst = Ad + buf * CB_ROWS * DT;
-        for (int e = tid; e < CB_ROWS * DT / 4; e += CB_THREADS) cp_async16(adst + 4 * e, asrc + 4 * e);
-        cp_async_commit();
+        tc::mbar_expect_tx(&pbar[buf], (DT * DT + CB_ROWS * DT) * 4);
+        tc::bulk_g2s(Ph + buf * DT * DT, trans + (su0 + sg) * DT * DT, DT * DT * 4, &pbar[buf]);
+        tc::bulk_g2s(Ad + buf * CB_ROWS * DT, adds + (su0 + sg) * DT * DT + (size_t)r0 * DT, CB_ROWS * DT * 4,
+                     &pbar[buf]);
     };
-    if (nss > 1) prefetch(0, 0);
+    if (tid == 0) {
+        tc::mbar_init(&pbar[0], 1);
+        tc::mbar_init(&pbar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+    if (nss > 1 && tid == 0) prefetch(0, 0);
     // starting rows: h0 / dht (absent = 0)
     for (int e = tid; e < CB_ROWS * DT; e += CB_THREADS) {
         int rr = e / DT, k = e % DT, v = r0 + rr;
@@ -61,9 +68,12 @@ __global__ void __launch_bounds__(CB_THREADS) k23_combine(const Params P) {
         const int buf = step & 1;
         const int sg = FWD ? step : nss - 1 - step;  // segment whose summary is applied
         const int dst = FWD ? sg + 1 : sg - 1;
-        cp_async_wait<0>();
-        __syncthreads();  // this step's transition and summary, and XT, visible; last step's readers done
-        if (step + 1 < nss - 1) prefetch(step + 1, buf ^ 1);
+        const bool landed = tc::mbar_wait(&pbar[buf], (uint32_t)(step >> 1) & 1u, 1u << 24);
+        if (__syncthreads_or(!landed)) {  // (this step's rows, and XT, visible; last step's readers done)
+            if (tid == 0) flag_status(P.status, ST_TIMEOUT);
+            return;
+        }
+        if (step + 1 < nss - 1 && tid == 0) prefetch(step + 1, buf ^ 1);
         // partial products of this warp's 16 reduction indices: all 16 rows x columns k0 .. k0+3
         const float *ph = Ph + buf * DT * DT;
         float acc[CB_ROWS][4];
