@@ -40,11 +40,13 @@ L2_BYTES = 129 * 2 ** 20
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="gdn_t32k_bf16")
     ap.add_argument("--cpu-sample-tokens", type=int, default=32768)
+    ap.add_argument("--flush-steps", type=int, default=20,
+                    help="calls timed one by one with a 512 MB write between them (L2 flushed)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pass", dest="which", choices=("bwd", "fwd", "wy"), default="bwd",
                     help="bwd: the backward (the headline); fwd: the forward pass (o and the final state); "
@@ -162,7 +164,8 @@ def workload_config(prob, world):
             "inputs": f"{str(prob.qkv_dtype).split('.')[-1]} q/k/v/dO, {str(prob.beta_dtype).split('.')[-1]} beta, "
                       f"fp32 g, fp32 h0/dht" + ("" if prob.h0 is not None else " (h0 absent)"),
             "problems_per_rank": 1, "global_batch": world, "parallelism": f"replicas x{world} (no collective)",
-            "l2": "inputs + workspace larger than L2 (129 MB); no flush between steps"}
+            "l2": "inputs + workspace larger than L2 (129 MB); value: no flush between steps; l2_flushed: a "
+                  "512 MB write between calls"}
 
 
 # ---------------------------------------------------------------- oracle timing (CPU baseline / reference arm)
@@ -289,6 +292,20 @@ def run_ours(args):
     wall = time.perf_counter() - wall0
     ms_local = t0.elapsed_time(t1) / args.steps
     stage_ms = [statistics.mean(evs[i][s].elapsed_time(evs[i][s + 1]) for i in range(args.steps)) for s in range(nst)]
+    step_ms = [evs[i][0].elapsed_time(evs[i][nst]) for i in range(args.steps)]
+
+    # ---- the same call timed one at a time with L2 flushed before each (a 512 MB write on the stream)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    fl_ms = []
+    for _ in range(max(args.flush_steps, 1)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        plan.run(out=out, workspace=ws, **dev)
+        b.record(stream)
+        b.synchronize()
+        fl_ms.append(a.elapsed_time(b))
+    del flush
 
     # ---- end to end through the C ABI with host buffers (pinned).  Every step copies its inputs in and its
     # results out inside the timed region; the copies run on their own streams so that step i+1's inputs and
@@ -354,6 +371,8 @@ def run_ours(args):
     stage_flops = counts.stage_flops(prob)
     stage_bytes = counts.stage_bytes(prob)
     tc_peak, bw_peak = peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9
+    step_med = statistics.median(step_ms)
+    flushed_med = statistics.median(fl_ms)
 
     def stage_roof(s):
         """Roofline of one stage: the tensor or HBM bound, whichever is longer for its FLOPs and bytes."""
@@ -368,11 +387,26 @@ def run_ours(args):
 
     dom = max(range(nst), key=lambda s: stage_ms[s])
     dom_name = _lib.STAGE_NAMES[dom]
-    roof = {"kernel": dom_name, **stage_roof(dom),
-            "bytes_per_launch": stage_bytes[dom], "flops_per_launch": stage_flops[dom],
+    # the dominant kernel against the least it must move (its algorithmic bytes) or compute, whichever
+    # bound is longer; the design's own stage bytes and the ncu-measured DRAM bytes stand beside it
+    t_dom = stage_ms[dom] / 1e3
+    dom_alg = counts.gradient_stage_algorithmic_bytes(prob) if dom_name == "k4_intra_grad" else stage_bytes[dom]
+    if dom_alg / bw_peak >= stage_flops[dom] / tc_peak:
+        dom_roof = {"bound": "hbm", "achieved": dom_alg / t_dom / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": dom_alg / t_dom / bw_peak}
+    else:
+        dom_roof = {"bound": "tensor", "achieved": stage_flops[dom] / t_dom / 1e12, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": stage_flops[dom] / t_dom / tc_peak}
+    traffic = committed_traffic(dom_name, prob.name)
+    roof = {"kernel": dom_name, **dom_roof,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": dom_alg, "stage_bytes_per_launch": stage_bytes[dom],
+            "flops_per_launch": stage_flops[dom],
+            "tensor_frac": stage_flops[dom] / t_dom / tc_peak,
+            "wasted_traffic_ratio": (traffic / dom_alg) if traffic else None,
+            "ms_per_launch": stage_ms[dom],
             "peak_source": f"{peaks['source']} (HBM copy GB/s; dense bf16 burst TFLOP/s, fp16 operands run at "
-                           f"the bf16 rate)",
-            "traffic": committed_traffic(dom_name, prob.name)}
+                           f"the bf16 rate)"}
     stage_roofs = {_lib.STAGE_NAMES[s]: {k: v for k, v in stage_roof(s).items() if k in ("bound", "achieved", "frac")}
                    for s in range(nst) if stage_ms[s] > 0 and (stage_bytes[s] > 0 or stage_flops[s] > 0)}
     line = {
@@ -380,6 +414,10 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "data": "synthetic",
         "config": workload_config(prob, world),
+        "backward_roofline_frac": t_roof / (ms / 1e3),
+        "median_ms_per_step": step_med,
+        "l2_flushed": {"median_ms": flushed_med, "calls": len(fl_ms), "flush_bytes": 512 * 2 ** 20,
+                       "backward_roofline_frac": t_roof / (flushed_med / 1e3)},
         "roofline": roof,
         "path_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms / 1e3), "flops": flops,
                           "algorithmic_bytes": alg_bytes,

@@ -13,7 +13,8 @@ GDR_F32, GDR_BF16, GDR_F16 = 0, 1, 2
 
 # every function the header declares
 EXPORTS = ("gdr_bwd_create", "gdr_bwd_workspace_bytes", "gdr_bwd_run", "gdr_bwd_run_profiled",
-           "gdr_bwd_launch_count", "gdr_bwd_get_status", "gdr_bwd_run_noalloc", "gdr_bwd_destroy",
+           "gdr_bwd_launch_count", "gdr_bwd_get_status", "gdr_bwd_run_noalloc", "gdr_bwd_get_status_noalloc",
+           "gdr_bwd_destroy",
            "gdr_chunk_indices", "gdr_status_string", "gdr_fwd_run", "gdr_fwd_launch_count", "gdr_wy_bwd_run")
 NOALLOC_MAX_WORKSPACE = 64 << 20
 NUM_STAGES = 6
@@ -77,6 +78,8 @@ def load(path: str | None = None):
         lib.gdr_bwd_run_noalloc.restype = ci
         lib.gdr_bwd_get_status.argtypes = [vp, vp, vp]
         lib.gdr_bwd_get_status.restype = ci
+        lib.gdr_bwd_get_status_noalloc.argtypes = [vp, vp]
+        lib.gdr_bwd_get_status_noalloc.restype = ci
         lib.gdr_bwd_destroy.argtypes = [vp]
         lib.gdr_bwd_destroy.restype = None
         lib.gdr_chunk_indices.argtypes = [vp, ci, ci, ci, vp, vp, vp]

@@ -52,6 +52,19 @@ def algorithmic_bytes(prob) -> int:
     return int(inputs + outputs)
 
 
+def gradient_stage_algorithmic_bytes(prob) -> int:
+    """The least the per-chunk gradient stage must move, whatever the split of the path: the inputs it
+    differentiates read once (q, k, v, dO, beta, g) and its outputs written once (dq, dk, dv, dbeta).  The
+    dominant kernel's roofline is taken against these bytes, not against the workspace tiles this design
+    passes between its stages."""
+    T = prob.B * prob.T
+    ib = _nbytes(prob.qkv_dtype)
+    gk = prob.K if prob.per_channel else 1
+    return int(2 * T * prob.Hk * prob.K * ib + 2 * T * prob.Hv * prob.V * ib + T * prob.Hv * _nbytes(prob.beta_dtype)
+               + T * prob.Hv * gk * 4 + 2 * T * prob.Hk * prob.K * _nbytes(prob.dqdk_dtype)
+               + T * prob.Hv * prob.V * _nbytes(prob.dv_dtype) + T * prob.Hv * 4)
+
+
 def stage_flops(prob) -> list:
     """The FLOP convention split over the six kernel stages (chunk bookkeeping, WY preparation, state
     recompute, state-gradient scan, per-chunk gradients, gate cumsum / GQA reduction); sums to

@@ -8,7 +8,10 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+#include <mutex>
 #include <new>
+#include <unordered_map>
 
 #include "../../include/gdr_bwd.h"
 #include "gdr_common.cuh"
@@ -22,15 +25,69 @@ struct gdr_bwd_plan {
     int k4_tc;  // per-chunk gradients on tcgen05 (scalar gate); the per-channel gate uses the mma.sync kernel
     int dh_factored;  // factored local pass of the state-gradient scan (QR = Q~ - Aqk W), GDR_DH_FACTORED=1
     int NS, Lseg;  // segment-parallel scans: segments per sequence and chunks per segment
+    uint32_t spin;  // polls of a bounded device wait (GDR_SPIN_LIMIT, a test knob; default 2^24)
     long long tokens;  // B * T
     // workspace byte offsets
     size_t o_status, o_cidx, o_coff, o_gam, o_T, o_Aqk, o_W, o_U, o_Kt, o_Qg, o_Dt, o_h, o_dh, o_Vn, o_dVn, o_dgam, o_dqh,
         o_dkh, o_seg, o_sc, total;
 };
 
+namespace gdr {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::mutex g_attr_mu;
+std::unordered_map<const void *, uint64_t> g_attr_set;  // kernel -> bit mask of devices already opted in
+}  // namespace
+
+cudaError_t device_sm_count(int *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    *out = n;
+    return cudaSuccess;
+}
+
+cudaError_t smem_opt_in(const void *kernel, size_t bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < kMaxDevices ? (1ull << dev) : 0;
+    {
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        auto it = g_attr_set.find(kernel);
+        if (bit && it != g_attr_set.end() && (it->second & bit)) return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    if (bit) {
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        g_attr_set[kernel] |= bit;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace gdr
+
 namespace {
 
-constexpr int kNumSMs = 152;
+// SM count that sizes the segment-parallel scans: the current device's, or GB300's 152 when no device
+// can be queried (a plan built on a host without a GPU).
+int plan_sm_count() {
+    int n = 0;
+    if (gdr::device_sm_count(&n) != cudaSuccess || n <= 0) {
+        cudaGetLastError();  // clear the query's error
+        return 152;
+    }
+    return n;
+}
 
 bool valid_dtype(int d) { return d == GDR_F32 || d == GDR_BF16 || d == GDR_F16; }
 
@@ -125,7 +182,7 @@ gdr_status gdr_bwd_create(const gdr_bwd_desc *desc, gdr_bwd_plan **out) {
         // segments: enough (sequence x head x segment) CTAs to give every SM one, at least 4 chunks each
         long long units = (long long)p->N * d.Hv;
         long long maxnc = p->dense ? p->nts : ((long long)d.T + d.BT - 1) / d.BT;
-        long long ns = units > 0 ? kNumSMs / units : 1;
+        long long ns = units > 0 ? plan_sm_count() / units : 1;
         ns = ns < (maxnc + 3) / 4 ? ns : (maxnc + 3) / 4;
         const char *env = getenv("GDR_NSEG");
         if (env && atoi(env) > 0) ns = atoi(env);
@@ -139,6 +196,9 @@ gdr_status gdr_bwd_create(const gdr_bwd_desc *desc, gdr_bwd_plan **out) {
     p->k4_tc = !d.gate_per_channel && !(k4tc && atoi(k4tc) == 0);
     const char *fact = getenv("GDR_DH_FACTORED");
     p->dh_factored = fact && atoi(fact) != 0;
+    // bounded device waits give up after this many polls; tests lower it to make a real wait run out
+    const char *spin = getenv("GDR_SPIN_LIMIT");
+    p->spin = (spin && atol(spin) > 0) ? (uint32_t)atol(spin) : WAIT_LIMIT_DEFAULT;
     layout(*p);
     *out = p;
     return GDR_OK;
@@ -170,6 +230,7 @@ static void fill_common(const gdr_bwd_plan *plan, char *ws, Params &P) {
     P.beta_dtype = d.beta_dtype;
     P.dqdk_dtype = d.dqdk_dtype;
     P.dv_dtype = d.dv_dtype;
+    P.spin = plan->spin;
     P.status = reinterpret_cast<int *>(ws + plan->o_status);
     P.chunk_idx = reinterpret_cast<int32_t *>(ws + plan->o_cidx);
     P.chunk_off = reinterpret_cast<int32_t *>(ws + plan->o_coff);
@@ -408,7 +469,7 @@ gdr_status gdr_bwd_get_status(gdr_bwd_plan *plan, void *workspace, void *stream_
     if (cudaMemcpy(&word, dev, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GDR_ERR_CUDA;
     if (cudaMemset(dev, 0, sizeof(int)) != cudaSuccess) return GDR_ERR_CUDA;
     if (word & ST_TIMEOUT) return GDR_ERR_TIMEOUT;
-    if (word & ST_BAD_SEQLENS) return GDR_ERR_DEVICE;
+    if (word & (ST_BAD_SEQLENS | ST_RANGE)) return GDR_ERR_DEVICE;
     return GDR_OK;
 }
 

@@ -24,6 +24,15 @@ constexpr int LDC = CT + PADH;  // pitch (halves) of a [*][CT] shared tile
 // Device status bits (OR-ed into the workspace status word).
 constexpr int ST_BAD_SEQLENS = 1;
 constexpr int ST_TIMEOUT = 2;
+constexpr int ST_RANGE = 4;  // an input value does not fit the fp16 tensor-core operands (|x| > 65504, inf, nan)
+
+// Bounded waits.  A wait that gives up after its plan's poll limit (Params::spin) flags ST_TIMEOUT; before
+// the CTA moves on it waits once more, up to DRAIN_LIMIT polls, for every copy or tensor-core operation that
+// is still tracked by an armed barrier phase, so that nothing lands in shared or tensor memory after the
+// CTA has released it.
+constexpr uint32_t WAIT_LIMIT_DEFAULT = 1u << 24;
+constexpr uint32_t DRAIN_LIMIT = 1u << 24;
+constexpr float F16_MAX = 65504.f;
 
 enum DType { F32 = 0, BF16 = 1, F16 = 2 };
 
@@ -33,6 +42,7 @@ struct Params {
     int B, T, Hk, Hv, K, V, BT, G, N, per_channel, dense, max_chunks, nts;  // nts: chunks per dense seq
     float scale;
     int qkv_dtype, beta_dtype, dqdk_dtype, dv_dtype;
+    uint32_t spin;  // polls of a bounded mbarrier wait before it is declared lost
     // inputs
     const void *q, *k, *v, *beta, *dO;
     const float *g, *h0, *dht;
@@ -155,6 +165,14 @@ __device__ __forceinline__ uint4 pack8_half(const float (&x)[8]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) h2[i] = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
     return r;
+}
+
+// Whether any of the 8 values cannot be an fp16 operand (|x| > 65504, inf or nan).
+__device__ __forceinline__ bool out_of_f16(const float (&x)[8]) {
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bad |= !(fabsf(x[i]) <= F16_MAX);
+    return bad;
 }
 
 template <typename To> __device__ __forceinline__ To to_out_t(float x);
@@ -386,14 +404,16 @@ __device__ __forceinline__ void raw_get(const Raw8<__half> &x, float (&o)[8]) {
 // Stage NW row-major [rows x cols] inputs, each times its multiplier, as fp16 core-matrix tiles (CT x DT,
 // zero padded) in shared or global memory.  Every global load of all NW tiles is issued before the first
 // conversion (one memory round trip, not NW).
+// A non-null range_status gets ST_RANGE when a converted value does not fit fp16.
 template <typename Tin, int NTHR, int NW>
 __device__ __forceinline__ void stage_ct_n(unsigned char *const (&t)[NW], const Tin *const (&src)[NW],
                                            const size_t (&st)[NW], const int (&nc)[NW], const float (&mul)[NW],
-                                           int nrows, int tid) {
+                                           int nrows, int tid, int *range_status = nullptr) {
     constexpr int PER = CT * (DT / 8) / NTHR;
     static_assert(PER * NTHR == CT * (DT / 8), "thread count must divide the tile");
     const int wid = tid >> 5, lane = tid & 31;
     Raw8<Tin> x[NW][PER];
+    bool bad = false;
 #pragma unroll
     for (int w = 0; w < NW; ++w)
 #pragma unroll
@@ -413,8 +433,10 @@ __device__ __forceinline__ void stage_ct_n(unsigned char *const (&t)[NW], const 
             raw_get(x[w][i], f);
 #pragma unroll
             for (int j = 0; j < 8; ++j) f[j] *= mul[w];
+            bad |= out_of_f16(f);
             *reinterpret_cast<uint4 *>(t[w] + ctile_off(r, c8, DT)) = pack8_half(f);
         }
+    if (bad && range_status) atomicOr(range_status, ST_RANGE);
 }
 
 

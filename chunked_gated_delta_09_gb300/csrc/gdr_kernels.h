@@ -9,6 +9,11 @@ namespace gdr {
 
 struct Params;
 
+// Opt a kernel in to `bytes` of dynamic shared memory, once per (kernel, device); later calls return at once.
+cudaError_t smem_opt_in(const void *kernel, size_t bytes);
+// Streaming-multiprocessor count of the current device (queried once per device).
+cudaError_t device_sm_count(int *out);
+
 // K0: varlen chunk bookkeeping (one block).  expect_total_tokens < 0 skips the cu[N] == T check.
 cudaError_t launch_k0(const int32_t *cu, int N, int BT, int max_chunks, int expect_total_tokens, int32_t *chunk_idx,
                       int32_t *chunk_off, int *status, cudaStream_t stream);

@@ -141,12 +141,16 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
             const int snc = w < 2 ? P.K : P.V;
             if (w < nin && r < len) tc::bulk_g2s(dst + r * DT * 2, sp + (size_t)r * sst, (uint32_t)(snc * 2), &S.rbar);
         }
-        const bool landed = tc::mbar_wait(&S.rbar, 0, 1u << 24);
+        const bool landed = tc::mbar_wait(&S.rbar, 0, P.spin);
         if (__syncthreads_or(!landed)) {
-            if (tid == 0) flag_status(P.status, ST_TIMEOUT);
+            if (tid == 0) {
+                flag_status(P.status, ST_TIMEOUT);
+                tc::mbar_wait(&S.rbar, 0, DRAIN_LIMIT);  // the rows still in flight land before the CTA exits
+            }
             return;
         }
         constexpr int PER = CT * (DT / 8) / K1_THREADS;  // 16-byte chunks per thread and tile
+        bool bad = false;  // an input value that fp16 operands cannot hold
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             if (w >= nin) break;
@@ -182,22 +186,24 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                 } else {
                     *reinterpret_cast<uint4 *>(slot[w] + off) = pack8_half(f);
                 }
+                bad |= out_of_f16(f);
             }
         }
+        if (bad) flag_status(P.status, ST_RANGE);
     } else if (P.dO) {  // backward: also D = scale dO, written straight to its workspace tile
         unsigned char *const dst[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT)};
         const Tin *const src[4] = {kp, qp, vp, dop};
         const size_t st[4] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V, (size_t)P.Hv * P.V};
         const int nc[4] = {P.K, P.K, P.V, P.V};
         const float mul[4] = {1.f, 1.f, 1.f, P.scale};
-        stage_ct_n<Tin, K1_THREADS, 4>(dst, src, st, nc, mul, len, tid);
+        stage_ct_n<Tin, K1_THREADS, 4>(dst, src, st, nc, mul, len, tid, P.status);
     } else {     // forward: no output gradient
         unsigned char *const dst[3] = {S.Ks, S.Qs, S.Vs};
         const Tin *const src[3] = {kp, qp, vp};
         const size_t st[3] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V};
         const int nc[3] = {P.K, P.K, P.V};
         const float mul[3] = {1.f, 1.f, 1.f};
-        stage_ct_n<Tin, K1_THREADS, 3>(dst, src, st, nc, mul, len, tid);
+        stage_ct_n<Tin, K1_THREADS, 3>(dst, src, st, nc, mul, len, tid, P.status);
     }
 
     // ---- beta, gate cumsum
@@ -435,7 +441,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
 template <typename Tin, bool PC>
 static cudaError_t launch_k1_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(K1Smem) + (PC ? sizeof(float) * CT * GKLD : 0);
-    cudaError_t e = cudaFuncSetAttribute(k1_wy_prep<Tin, PC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_opt_in((const void *)k1_wy_prep<Tin, PC>, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(P.max_chunks, P.Hv);
     k1_wy_prep<Tin, PC><<<grid, K1_THREADS, smem, stream>>>(P);

@@ -68,9 +68,13 @@ __global__ void __launch_bounds__(CB_THREADS) k23_combine(const Params P) {
         const int buf = step & 1;
         const int sg = FWD ? step : nss - 1 - step;  // segment whose summary is applied
         const int dst = FWD ? sg + 1 : sg - 1;
-        const bool landed = tc::mbar_wait(&pbar[buf], (uint32_t)(step >> 1) & 1u, 1u << 24);
+        const bool landed = tc::mbar_wait(&pbar[buf], (uint32_t)(step >> 1) & 1u, P.spin);
         if (__syncthreads_or(!landed)) {  // (this step's rows, and XT, visible; last step's readers done)
-            if (tid == 0) flag_status(P.status, ST_TIMEOUT);
+            if (tid == 0) {  // the status is flagged whether or not the copies then land in time
+                flag_status(P.status, ST_TIMEOUT);
+                // this step's two copies are the only ones in flight: they land before the CTA exits
+                tc::mbar_wait(&pbar[buf], (uint32_t)(step >> 1) & 1u, DRAIN_LIMIT);
+            }
             return;
         }
         if (step + 1 < nss - 1 && tid == 0) prefetch(step + 1, buf ^ 1);
@@ -128,11 +132,11 @@ cudaError_t launch_k23_combine(const Params &P, bool fwd, cudaStream_t stream) {
     cudaError_t e;
     dim3 grid(P.N * P.Hv, DT / CB_ROWS);
     if (fwd) {
-        e = cudaFuncSetAttribute(k23_combine<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = smem_opt_in((const void *)k23_combine<true>, smem);
         if (e != cudaSuccess) return e;
         k23_combine<true><<<grid, CB_THREADS, smem, stream>>>(P);
     } else {
-        e = cudaFuncSetAttribute(k23_combine<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = smem_opt_in((const void *)k23_combine<false>, smem);
         if (e != cudaSuccess) return e;
         k23_combine<false><<<grid, CB_THREADS, smem, stream>>>(P);
     }

@@ -22,7 +22,6 @@
 namespace gdr {
 
 constexpr int SC_THREADS = 256;
-constexpr uint32_t SC_WAIT_LIMIT = 1u << 24;
 
 template <bool LOCAL>
 struct __align__(1024) FwdSmem {
@@ -32,7 +31,7 @@ struct __align__(1024) FwdSmem {
     unsigned char Pa[LOCAL ? DT * DT * 2 : 16];   // transition rows as fp16
     unsigned char Vpa[LOCAL ? DT * CT * 2 : 16];  // -(Phi W^T)
     float gam[2][DT];                             // gate row block of the chunk (scalar: first CT used)
-    uint64_t bar, lbar[2];
+    uint64_t bar, lbar[2];  // MMA completion, the two tile buffers' loads
     uint32_t tslot;
 };
 
@@ -87,6 +86,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    // armed0 / armed1: a buffer's loads are in flight and not yet waited for (tracked by every thread alike)
+    bool armed0 = true, armed1 = false;
     if (tid == 0) issue(c_lo, 0);
     const uint32_t tm = S.tslot;
     constexpr int T_S = 0, T_P = 128, T_VN = LOCAL ? 256 : 128, T_VP = 320;
@@ -120,11 +121,12 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
     const uint32_t sSa = smem_u32(S.Sa), sVna = smem_u32(S.Vna), sPa = smem_u32(S.Pa), sVpa = smem_u32(S.Vpa);
     uint32_t parity = 0, lpar0 = 0, lpar1 = 0;
     bool lost = false;
+    bool mma_ok = true;  // false: the last MMA commit's phase is still pending (the exit drains it)
     auto mma_done = [&]() {
         if (tid == 0) tc::commit(&S.bar);
-        bool ok = tc::mbar_wait(&S.bar, parity, SC_WAIT_LIMIT);
-        parity ^= 1u;
-        lost = __syncthreads_or(!ok) != 0;
+        mma_ok = tc::mbar_wait(&S.bar, parity, P.spin);
+        if (mma_ok) parity ^= 1u;
+        lost = __syncthreads_or(!mma_ok) != 0;
         tc::fence_after();
     };
 
@@ -132,15 +134,21 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
         const int buf = (c - c_lo) & 1;
         const size_t u = (size_t)(base + c) * P.Hv + hv;
         // chunk c's tiles landed; the previous step's bulk stores no longer read Sa / Vna
-        bool ok = tc::mbar_wait(&S.lbar[buf], buf ? lpar1 : lpar0, SC_WAIT_LIMIT);
-        if (buf) lpar1 ^= 1u;
-        else lpar0 ^= 1u;
+        bool ok = tc::mbar_wait(&S.lbar[buf], buf ? lpar1 : lpar0, P.spin);
+        if (ok) {  // (a failed wait leaves the phase armed: the exit drains it)
+            if (buf) lpar1 ^= 1u, armed1 = false;
+            else lpar0 ^= 1u, armed0 = false;
+        }
         if (!LOCAL && tid == 0) tc::bulk_wait_read();
         tc::fence_before();
         lost = __syncthreads_or(!ok) != 0;
         tc::fence_after();
         if (lost) break;
-        if (c + 1 < c_hi && tid == 0) issue(c + 1, buf ^ 1);
+        if (c + 1 < c_hi) {
+            if (tid == 0) issue(c + 1, buf ^ 1);
+            if (buf) armed0 = true;
+            else armed1 = true;
+        }
         const float gl = PC ? 0.f : S.gam[buf][chunk_len(c) - 1];
         // epilogue 0: state rows -> fp16 operand (= h_n), then scale by Gamma_C in place
 #pragma unroll
@@ -254,7 +262,14 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
             }
         }
     }
-    if (lost && tid == 0) flag_status(P.status, ST_TIMEOUT);
+    if (lost && tid == 0) {
+        flag_status(P.status, ST_TIMEOUT);
+        // drain: the MMAs of a commit whose wait gave up, and the tile loads still armed, complete before
+        // the exit (every MMA is followed by its commit and wait, so nothing else can be in flight)
+        if (!mma_ok) tc::mbar_wait(&S.bar, parity, DRAIN_LIMIT);
+        if (armed0) tc::mbar_wait(&S.lbar[0], lpar0, DRAIN_LIMIT);
+        if (armed1) tc::mbar_wait(&S.lbar[1], lpar1, DRAIN_LIMIT);
+    }
     if (tid == 0) tc::bulk_wait();
     tc::fence_before();
     __syncthreads();
@@ -267,7 +282,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
 template <bool PC, bool LOCAL>
 static cudaError_t launch_fwd_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(FwdSmem<LOCAL>);
-    cudaError_t e = cudaFuncSetAttribute(k2_scan_tc<PC, LOCAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_opt_in((const void *)k2_scan_tc<PC, LOCAL>, smem);
     if (e != cudaSuccess) return e;
     k2_scan_tc<PC, LOCAL><<<P.N * P.Hv * P.NS, SC_THREADS, smem, stream>>>(P);
     return cudaGetLastError();

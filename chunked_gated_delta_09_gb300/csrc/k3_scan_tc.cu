@@ -22,14 +22,13 @@
 namespace gdr {
 
 constexpr int SB_THREADS = 256;
-constexpr uint32_t SB_WAIT_LIMIT = 1u << 24;
 
 struct __align__(1024) BwdSmem {
     unsigned char Aq[2][CT * CT * 2], D[2][CT * DT * 2], Kt[2][CT * DT * 2], Qg[2][CT * DT * 2], W[2][CT * DT * 2];
     unsigned char dSa[DT * DT * 2];  // dS rows as fp16 (A operand; dh_n)
     unsigned char dVa[DT * CT * 2];  // -dV_new^T [v][c] (A operand)
     float gam[2][DT];
-    uint64_t bar, lbar[2];
+    uint64_t bar, lbar[2];  // MMA completion, the two tile buffers' loads
     uint32_t tslot;
 };
 
@@ -86,6 +85,8 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    // armed0 / armed1: a buffer's loads are in flight and not yet waited for (tracked by every thread alike)
+    bool armed0 = ((c_hi - 1 - c_lo) & 1) == 0, armed1 = !armed0;
     if (tid == 0) issue(c_hi - 1, (c_hi - 1 - c_lo) & 1);
     const uint32_t tm = S.tslot;
     constexpr int T_S = 0, T_DV = 128;
@@ -112,26 +113,33 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
     const uint32_t sdSa = smem_u32(S.dSa), sdVa = smem_u32(S.dVa);
     uint32_t parity = 0, lpar0 = 0, lpar1 = 0;
     bool lost = false;
+    bool mma_ok = true;  // false: the last MMA commit's phase is still pending (the exit drains it)
     auto mma_done = [&]() {
         if (tid == 0) tc::commit(&S.bar);
-        bool ok = tc::mbar_wait(&S.bar, parity, SB_WAIT_LIMIT);
-        parity ^= 1u;
-        lost = __syncthreads_or(!ok) != 0;
+        mma_ok = tc::mbar_wait(&S.bar, parity, P.spin);
+        if (mma_ok) parity ^= 1u;
+        lost = __syncthreads_or(!mma_ok) != 0;
         tc::fence_after();
     };
 
     for (int c = c_hi - 1; c >= c_lo && !lost; --c) {
         const int buf = (c - c_lo) & 1;
         const size_t u = (size_t)(base + c) * P.Hv + hv;
-        bool ok = tc::mbar_wait(&S.lbar[buf], buf ? lpar1 : lpar0, SB_WAIT_LIMIT);
-        if (buf) lpar1 ^= 1u;
-        else lpar0 ^= 1u;
+        bool ok = tc::mbar_wait(&S.lbar[buf], buf ? lpar1 : lpar0, P.spin);
+        if (ok) {  // (a failed wait leaves the phase armed: the exit drains it)
+            if (buf) lpar1 ^= 1u, armed1 = false;
+            else lpar0 ^= 1u, armed0 = false;
+        }
         if (!LOCAL && tid == 0) tc::bulk_wait_read();
         tc::fence_before();
         lost = __syncthreads_or(!ok) != 0;
         tc::fence_after();
         if (lost) break;
-        if (c > c_lo && tid == 0) issue(c - 1, buf ^ 1);
+        if (c > c_lo) {
+            if (tid == 0) issue(c - 1, buf ^ 1);
+            if (buf) armed0 = true;
+            else armed1 = true;
+        }
         const float gl = PC ? 0.f : S.gam[buf][chunk_len(c) - 1];
         // epilogue 0: dS rows -> fp16 operand (= dh_n), then scale by Gamma_C in place
 #pragma unroll
@@ -210,7 +218,14 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
             }
         }
     }
-    if (lost && tid == 0) flag_status(P.status, ST_TIMEOUT);
+    if (lost && tid == 0) {
+        flag_status(P.status, ST_TIMEOUT);
+        // drain: the MMAs of a commit whose wait gave up, and the tile loads still armed, complete before
+        // the exit (every MMA is followed by its commit and wait, so nothing else can be in flight)
+        if (!mma_ok) tc::mbar_wait(&S.bar, parity, DRAIN_LIMIT);
+        if (armed0) tc::mbar_wait(&S.lbar[0], lpar0, DRAIN_LIMIT);
+        if (armed1) tc::mbar_wait(&S.lbar[1], lpar1, DRAIN_LIMIT);
+    }
     if (tid == 0) tc::bulk_wait();
     tc::fence_before();
     __syncthreads();
@@ -224,7 +239,7 @@ template <bool PC, bool LOCAL, bool FACT = false>
 static cudaError_t launch_bwd_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(BwdSmem);
     cudaError_t e =
-        cudaFuncSetAttribute(k3_scan_tc<PC, LOCAL, FACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        smem_opt_in((const void *)k3_scan_tc<PC, LOCAL, FACT>, smem);
     if (e != cudaSuccess) return e;
     k3_scan_tc<PC, LOCAL, FACT><<<P.N * P.Hv * P.NS, SB_THREADS, smem, stream>>>(P);
     return cudaGetLastError();

@@ -79,7 +79,6 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
         }
     }
 }
-constexpr uint32_t K4_WAIT_LIMIT = 1u << 24;
 
 struct __align__(1024) K4Smem {
     unsigned char Qs[CT * DT * 2], Ks[CT * DT * 2], Vs[CT * DT * 2], Ds[CT * DT * 2];
@@ -196,12 +195,15 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             S.G[tid] = __expf(S.gam[tid]);
             S.GC[tid] = __expf(S.gam[len - 1] - S.gam[tid]);
         }
-        const bool loaded = tc::mbar_wait(&S.lbar, parity, K4_WAIT_LIMIT);
-        parity ^= 1u;
+        const bool loaded = tc::mbar_wait(&S.lbar, parity, P.spin);
         if (__syncthreads_or(!loaded)) {
-            if (tid == 0) flag_status(P.status, ST_TIMEOUT);
+            if (tid == 0) {
+                flag_status(P.status, ST_TIMEOUT);
+                tc::mbar_wait(&S.lbar, parity, DRAIN_LIMIT);  // this item's tiles land before the CTA exits
+            }
             return;
         }
+        parity ^= 1u;
 
         // C x K tiling: warp w owns rows m0 .. m0+15 and columns n0 .. n0+31
         const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * (NK * 8);
@@ -605,11 +607,10 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 template <typename Tin, bool PC, bool WY = false>
 static cudaError_t launch_k4_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(K4Smem) + (PC ? sizeof(float) * CT * DT : 0);
-    cudaError_t e = cudaFuncSetAttribute(k4_intra_grad<Tin, PC, WY>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_opt_in((const void *)k4_intra_grad<Tin, PC, WY>, smem);
     if (e != cudaSuccess) return e;
-    int dev = 0, nsm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int nsm = 0;
+    if ((e = device_sm_count(&nsm)) != cudaSuccess) return e;
     const long items = (long)P.max_chunks * P.Hv;
     if (items == 0) return cudaSuccess;
     const int grid = (int)(items < nsm ? items : nsm);  // one persistent CTA per SM

@@ -14,7 +14,8 @@
 //  * the feature-major copies K^T, V^T, Q^T that those epilogues need come from products with a 64 x 64
 //    identity tile: one tensor-memory load replaces 16 scattered 2-byte shared-memory reads;
 //  * each buffer is refilled for the CTA's next item as soon as its last reader is done: S_0, dS_next, D,
-//    V_new^T, -dV_new^T after phase 1 and T after phase 4 (bulk copies on one barrier phase per item);
+//    V_new^T, -dV_new^T after phase 1 and T after phase 4 (bulk copies: one barrier phase per item for the
+//    first group, one on a second barrier for T);
 //    for 16-bit inputs V after phase 1, Q after phase 2 and K after phase 5 (cp.async of the raw rows into
 //    their tile slots, converted to fp16 in place when the item starts).
 //
@@ -40,7 +41,6 @@ constexpr int K4T_THREADS = 512;
 // is held up by more than one product's issue before its own epilogue work.
 constexpr int K4T_ISSUERS = 4;
 constexpr uint32_t K4T_TMEM_COLS = 512;
-constexpr uint32_t K4T_WAIT_LIMIT = 1u << 24;  // mbarrier polls before a wait is declared lost
 
 // tensor-memory column map, 64 columns per region (C_* regions use the M = 64 lane layout)
 constexpr int R_DKSC = 0, R_DWT = 64, R_TDU = 128, R_KT = 256, C_G1 = 320, C_DT2 = 384,
@@ -67,7 +67,7 @@ struct __align__(1024) K4TSmem {
     // (two sets, by item parity: an item's sums are added during the next item's first MMA phase)
     float db_wy[2][4][CT], db_a[2][4][CT], dg_q[2][4][CT], last_w[2][16];
     int red_u, red_len, red_tok0, red_hv, red_b;  // the item whose sums are pending (red_u < 0: none), its set
-    uint64_t bar, bar2, lbar;  // MMA groups 1 and 2 of a phase; bulk loads
+    uint64_t bar, bar2, lbar, tbar;  // MMA groups 1 and 2 of a phase; bulk loads (T on its own barrier)
     uint32_t tslot;
 };
 
@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         tc::mbar_init(&S.bar, K4T_ISSUERS);
         tc::mbar_init(&S.bar2, K4T_ISSUERS);
         tc::mbar_init(&S.lbar, 1);
+        tc::mbar_init(&S.tbar, 1);
         S.red_u = -1;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 
     // workspace tiles of an item: everything the first phase reads, then T (read until phase 4)
     auto issue_ws1 = [&](size_t un) {
-        tc::mbar_expect_tx(&S.lbar, 2 * DT * DT * 2 + CT * DT * 2 + 2 * DT * CT * 2 + CT * CT * 2 + 4 * CT * 4);
+        tc::mbar_expect_tx(&S.lbar, 2 * DT * DT * 2 + CT * DT * 2 + 2 * DT * CT * 2 + 4 * CT * 4);
         tc::bulk_g2s(&S.scal[0][0], P.sc + un * 4 * CT, 4 * CT * 4, &S.lbar);
         tc::bulk_g2s(S.H, P.h + un * DT * DT, DT * DT * 2, &S.lbar);
         tc::bulk_g2s(S.dH, P.dh + un * DT * DT, DT * DT * 2, &S.lbar);
@@ -159,7 +160,10 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         tc::bulk_g2s(S.Vn, P.Vn + un * DT * CT, DT * CT * 2, &S.lbar);
         tc::bulk_g2s(S.dVn, P.dVn + un * DT * CT, DT * CT * 2, &S.lbar);
     };
-    auto issue_ws2 = [&](size_t un) { tc::bulk_g2s(S.T, P.Tm + un * CT * CT, CT * CT * 2, &S.lbar); };
+    auto issue_ws2 = [&](size_t un) {
+        tc::mbar_expect_tx(&S.tbar, CT * CT * 2);
+        tc::bulk_g2s(S.T, P.Tm + un * CT * CT, CT * CT * 2, &S.tbar);
+    };
     // input rows of an item (key head for q / k, value head for v); which: 0 = k, 1 = q, 2 = v
     auto input_src = [&](int it, int which, const Tin *&src, size_t &st, int &nc, int &len_) {
         ChunkInfo c2;
@@ -215,20 +219,27 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         fetch_raw(item, 1, S.Q);
         fetch_raw(item, 2, S.V);
     }
-    uint32_t lpar = 0, mpar = 0, mpar2 = 0;
+    uint32_t lpar = 0, tpar = 0, mpar = 0, mpar2 = 0;
     bool lost = false, okq = true;
+    // Barrier phases this thread has not yet seen complete: loads armed and not waited for (the same for every
+    // thread: the arming points are passed by all), and MMA commits whose wait gave up.  A wait that gives up
+    // leaves its parity unflipped; the exit drains every pending phase before the CTA releases its memory.
+    bool l_pend = true, t_pend = true, m_pend = false, m2_pend = false;
     // Each phase: the issuers issue group 1 (committed to bar) and, in phases 1 and 2, group 2 (committed to
     // bar2); every thread waits (bounded) for group 1 itself, and the outcomes of all waits since the last
     // agreement are agreed at the next block-wide barrier (publish_tiles or the end of the item); the
     // epilogue starts on group 1's results while group 2 still runs.
     auto finish_phase = [&](bool fail) {
-        okq &= tc::mbar_wait(&S.bar, mpar, K4T_WAIT_LIMIT) && !fail;
-        mpar ^= 1u;
+        const bool ok = tc::mbar_wait(&S.bar, mpar, P.spin);
+        if (ok) mpar ^= 1u;
+        m_pend = !ok;
+        okq &= ok && !fail;
         tc::fence_after();
     };
     auto wait_group2 = [&]() -> bool {  // per thread; the outcome is agreed at the next publish_tiles
-        bool ok = tc::mbar_wait(&S.bar2, mpar2, K4T_WAIT_LIMIT);
-        mpar2 ^= 1u;
+        const bool ok = tc::mbar_wait(&S.bar2, mpar2, P.spin);
+        if (ok) mpar2 ^= 1u;
+        m2_pend = !ok;
         tc::fence_after();
         return ok;
     };
@@ -297,7 +308,11 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         }
         // every thread waits for the workspace tiles itself (the epilogues read some of them directly); the
         // per-token record came with them
-        bool fail = !tc::mbar_wait(&S.lbar, lpar, K4T_WAIT_LIMIT);
+        bool fail = false;
+        if (tc::mbar_wait(&S.lbar, lpar, P.spin)) lpar ^= 1u, l_pend = false;
+        else fail = true;
+        if (tc::mbar_wait(&S.tbar, tpar, P.spin)) tpar ^= 1u, t_pend = false;
+        else fail = true;
         tc::fence_smem_to_async();
         tc::fence_before();
         lost = __syncthreads_or(!okq || lost) != 0;  // (also orders the previous item's partial sums)
@@ -333,7 +348,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             }
             tc::commit(&S.bar2);
         }
-        lpar ^= 1u;
         float dk[16], dg[16], kreg[16];
         float lastpart = 0.f;
         {
@@ -423,6 +437,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         // that no issuer waits behind the copies)
         if (has_next) {
             if (loader) issue_ws1(next);
+            l_pend = true;
             if (kRaw) fetch_raw(next, 2, S.V);
         }
         finish_phase(false);
@@ -537,7 +552,10 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             tc::commit(&S.bar);
         }
         finish_phase(false);
-        if (loader && has_next) issue_ws2(next);  // T is not read again in this item
+        if (has_next) {  // T is not read again in this item
+            if (loader) issue_ws2(next);
+            t_pend = true;
+        }
         {
             float a[16], kk[16], x[8], y[8];
             tc::ld16x2(tc::taddr(tm, C_DA + c0), a, tc::taddr(tm, C_KK + c0), kk);
@@ -605,7 +623,15 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
     }
     lost = __syncthreads_or(!okq || lost) != 0;
     if (!lost && tid < CT) reduce_pending();  // the last item's sums
-    if (lost && tid == 0) flag_status(P.status, ST_TIMEOUT);
+    if (lost) {
+        if (tid == 0) flag_status(P.status, ST_TIMEOUT);
+        // every barrier phase this thread saw pending completes before the CTA releases its shared and
+        // tensor memory: the MMAs of a commit whose wait gave up, the loads armed and not waited for
+        if (m_pend) tc::mbar_wait(&S.bar, mpar, DRAIN_LIMIT);
+        if (m2_pend) tc::mbar_wait(&S.bar2, mpar2, DRAIN_LIMIT);
+        if (l_pend) tc::mbar_wait(&S.lbar, lpar, DRAIN_LIMIT);
+        if (t_pend) tc::mbar_wait(&S.tbar, tpar, DRAIN_LIMIT);
+    }
     cp_async_wait<0>();  // no copy of this thread may still be landing when the CTA exits
     tc::fence_before();
     __syncthreads();
@@ -618,11 +644,10 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 template <typename Tin>
 static cudaError_t launch_k4_tc_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(K4TSmem);
-    cudaError_t e = cudaFuncSetAttribute(k4_intra_grad_tc<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_opt_in((const void *)k4_intra_grad_tc<Tin>, smem);
     if (e != cudaSuccess) return e;
-    int dev = 0, nsm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int nsm = 0;
+    if ((e = device_sm_count(&nsm)) != cudaSuccess) return e;
     const long items = (long)P.max_chunks * P.Hv;
     if (items == 0) return cudaSuccess;
     const int grid = (int)(items < nsm ? items : nsm);  // one persistent CTA per SM

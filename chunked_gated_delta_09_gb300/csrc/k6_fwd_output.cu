@@ -15,7 +15,6 @@
 namespace gdr {
 
 constexpr int K6_THREADS = 128;
-constexpr uint32_t K6_WAIT_LIMIT = 1u << 24;
 
 struct __align__(1024) K6Smem {
     unsigned char Qg[CT * DT * 2];   // Q~ [r][k]
@@ -52,16 +51,17 @@ __global__ void __launch_bounds__(K6_THREADS) k6_fwd_output(const Params P) {
     __syncthreads();  // barriers initialised, tensor-memory address visible
     tc::fence_after();
     const uint32_t tm = S.tslot;
-    bool ok = true;
+    bool ok = true, loads_ok = true;
     if (tid == 0) {
-        ok = tc::mbar_wait(&S.lbar, 0, K6_WAIT_LIMIT);
+        loads_ok = ok = tc::mbar_wait(&S.lbar, 0, P.spin);
         if (ok) {
             tc::gemm(tm, smem_u32(S.H), DT, false, smem_u32(S.Qg), DT, false, 128, 64, DT, false);
             tc::gemm(tm, smem_u32(S.Vn), CT, false, smem_u32(S.Aqk), CT, false, 128, 64, CT, true);
         }
         tc::commit(&S.bar);
     }
-    ok = tc::mbar_wait(&S.bar, 0, K6_WAIT_LIMIT) && ok;
+    const bool mma_ok = tc::mbar_wait(&S.bar, 0, P.spin);
+    ok = mma_ok && ok;
     const bool lost = __syncthreads_or(!ok) != 0;
     tc::fence_after();
     if (!lost) {
@@ -82,6 +82,9 @@ __global__ void __launch_bounds__(K6_THREADS) k6_fwd_output(const Params P) {
         }
     } else if (tid == 0) {
         flag_status(P.status, ST_TIMEOUT);
+        // the loads and MMAs still tracked by a barrier that gave up complete before the CTA exits
+        if (!loads_ok) tc::mbar_wait(&S.lbar, 0, DRAIN_LIMIT);
+        if (!mma_ok) tc::mbar_wait(&S.bar, 0, DRAIN_LIMIT);
     }
     tc::fence_before();
     __syncthreads();
@@ -94,7 +97,7 @@ __global__ void __launch_bounds__(K6_THREADS) k6_fwd_output(const Params P) {
 template <typename To>
 static cudaError_t launch_k6_t(const Params &P, cudaStream_t stream) {
     const size_t smem = sizeof(K6Smem);
-    cudaError_t e = cudaFuncSetAttribute(k6_fwd_output<To>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_opt_in((const void *)k6_fwd_output<To>, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(P.max_chunks, P.Hv);
     k6_fwd_output<To><<<grid, K6_THREADS, smem, stream>>>(P);

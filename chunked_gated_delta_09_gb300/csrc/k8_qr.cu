@@ -13,7 +13,6 @@
 namespace gdr {
 
 constexpr int K8_THREADS = 256;
-constexpr uint32_t K8_WAIT_LIMIT = 1u << 24;
 
 struct __align__(1024) K8Smem {
     unsigned char Aq[CT * CT * 2], W[CT * DT * 2], Qg[CT * DT * 2];
@@ -38,9 +37,12 @@ __global__ void __launch_bounds__(K8_THREADS) k8_qr(const Params P, __half *QR) 
         tc::bulk_g2s(S.Qg, P.Qg + u * CT * DT, CT * DT * 2, &S.lbar);
     }
     __syncthreads();  // barrier initialised
-    const bool ok = tc::mbar_wait(&S.lbar, 0, K8_WAIT_LIMIT);
+    const bool ok = tc::mbar_wait(&S.lbar, 0, P.spin);
     if (__syncthreads_or(!ok)) {
-        if (tid == 0) flag_status(P.status, ST_TIMEOUT);
+        if (tid == 0) {
+            flag_status(P.status, ST_TIMEOUT);
+            tc::mbar_wait(&S.lbar, 0, DRAIN_LIMIT);  // the tiles land before the CTA exits
+        }
         return;
     }
     // QR [r][k] = Q~ - Aqk W: warp w owns rows 16 (w % 4) .. +15 and columns 64 (w / 4) .. +63
@@ -62,7 +64,7 @@ __global__ void __launch_bounds__(K8_THREADS) k8_qr(const Params P, __half *QR) 
 
 cudaError_t launch_k8_qr(const Params &P, __half *QR, cudaStream_t stream) {
     const size_t smem = sizeof(K8Smem);
-    cudaError_t e = cudaFuncSetAttribute(k8_qr, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = smem_opt_in((const void *)k8_qr, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(P.max_chunks, P.Hv);
     k8_qr<<<grid, K8_THREADS, smem, stream>>>(P, QR);

@@ -46,6 +46,17 @@ gdr_status scratch_address(void **out) {
 
 }  // namespace
 
+// The status word of the last run_noalloc on the current device lives in the shared array, where
+// gdr_bwd_get_status finds it given the array's address as the workspace.
+extern "C" gdr_status gdr_bwd_get_status_noalloc(gdr_bwd_plan *plan, void *stream) {
+    if (!plan) return GDR_ERR_INVALID_ARG;
+    if (gdr_bwd_workspace_bytes(plan) > kScratchBytes) return GDR_ERR_UNSUPPORTED;
+    void *ws = nullptr;
+    gdr_status st = scratch_address(&ws);
+    if (st != GDR_OK) return st;
+    return gdr_bwd_get_status(plan, ws, stream);
+}
+
 extern "C" gdr_status gdr_bwd_run_noalloc(gdr_bwd_plan *plan, const gdr_bwd_args *args, void *stream) {
     if (!plan || !args) return GDR_ERR_INVALID_ARG;
     if (gdr_bwd_workspace_bytes(plan) > kScratchBytes) return GDR_ERR_UNSUPPORTED;

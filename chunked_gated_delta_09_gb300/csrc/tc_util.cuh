@@ -78,8 +78,22 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, int count) {
 }
 
 // Wait for the mbarrier phase with the given parity; gives up after `limit` polls and returns false.
+// A poll is a try_wait, which the hardware may suspend for a while before it reports an incomplete phase.
+// Limits below 2^16 (set only to make waits run out in tests) poll with the non-blocking test_wait
+// instead, so that a short limit really is short.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
     uint32_t done = 0;
+    if (limit < (1u << 16)) {
+        for (uint32_t it = 0; it < limit; ++it) {
+            asm volatile(
+                "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                : "=r"(done)
+                : "r"(smem_u32(bar)), "r"(parity)
+                : "memory");
+            if (done) return true;
+        }
+        return false;
+    }
     for (uint32_t it = 0; it < limit; ++it) {
         asm volatile(
             "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"

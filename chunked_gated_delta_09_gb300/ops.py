@@ -132,6 +132,10 @@ class GdrBwdPlan:
     def get_status(self, workspace, stream=None) -> int:
         return int(self.lib.gdr_bwd_get_status(self.handle, _ptr(workspace), _stream_ptr(stream)))
 
+    def get_status_noalloc(self, stream=None) -> int:
+        """Status word of the last :meth:`run_noalloc` on the current device (gdr_bwd_get_status_noalloc)."""
+        return int(self.lib.gdr_bwd_get_status_noalloc(self.handle, _stream_ptr(stream)))
+
     def __del__(self):
         h = getattr(self, "handle", None)
         if h is not None and h.value:

@@ -62,7 +62,9 @@ typedef enum {
     GDR_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
     GDR_ERR_OOM = 4,         /* host allocation of the plan failed */
     GDR_ERR_TIMEOUT = 5,     /* a device-side bounded wait expired (read by gdr_bwd_get_status) */
-    GDR_ERR_DEVICE = 6       /* a kernel flagged malformed device input, e.g. cu_seqlens */
+    GDR_ERR_DEVICE = 6       /* a kernel flagged malformed device input: cu_seqlens that are not
+                                non-decreasing from 0 to T, or an input value that the fp16
+                                tensor-core operands cannot hold (|x| > 65504, inf, nan) */
 } gdr_status;
 
 typedef enum { GDR_F32 = 0, GDR_BF16 = 1, GDR_F16 = 2 } gdr_dtype;
@@ -91,7 +93,11 @@ typedef struct {
 
 typedef struct gdr_bwd_plan gdr_bwd_plan;
 
-/* Validate a descriptor and build a plan (host only; no device memory, no CUDA call).
+/* Validate a descriptor and build a plan (host only; no device memory).  The plan sizes its
+ * segment-parallel scans for the current device's SM count (queried once per device; 152, GB300's
+ * count, when no device can be queried), so build it with the device current that will run it.
+ * The environment variable GDR_SPIN_LIMIT (a positive integer, read here) lowers the number of polls
+ * after which a device-side wait gives up; it exists so that tests can make a real wait run out.
  * Returns GDR_ERR_INVALID_ARG for bad sizes, GDR_ERR_OOM if the host allocation fails. */
 gdr_status gdr_bwd_create(const gdr_bwd_desc *desc, gdr_bwd_plan **out);
 
@@ -120,7 +126,10 @@ gdr_status gdr_bwd_run_profiled(gdr_bwd_plan *plan, const gdr_bwd_args *args, vo
 int gdr_bwd_launch_count(const gdr_bwd_plan *plan);
 
 /* Synchronise `stream` and read the device status word that the last run on this workspace left:
- * GDR_OK, GDR_ERR_TIMEOUT or GDR_ERR_DEVICE.  Also clears the word. */
+ * GDR_OK, GDR_ERR_TIMEOUT (a bounded wait gave up; that CTA released its memory only after every copy
+ * and tensor-core operation it had started completed) or GDR_ERR_DEVICE (malformed cu_seqlens, or an
+ * input value outside fp16 range).  Also clears the word.  After either error the outputs are not
+ * valid. */
 gdr_status gdr_bwd_get_status(gdr_bwd_plan *plan, void *workspace, void *stream);
 
 /* No counterpart on the pages.  The whole backward without a caller-provided workspace, for callers
@@ -131,10 +140,16 @@ gdr_status gdr_bwd_get_status(gdr_bwd_plan *plan, void *workspace, void *stream)
  * allocating routine.  Plans whose gdr_bwd_workspace_bytes() exceeds the maximum are rejected with
  * GDR_ERR_UNSUPPORTED before anything is launched.  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current; make that first call before any
- * stream capture starts.  All calls share the array: calls that overlap on the GPU race, and the
- * device status word of these calls cannot be read with gdr_bwd_get_status. */
+ * stream capture starts.  All calls share the array: calls that overlap on the GPU race.  Their device
+ * status word is read with gdr_bwd_get_status_noalloc. */
 #define GDR_BWD_NOALLOC_MAX_WORKSPACE (64u << 20)
 gdr_status gdr_bwd_run_noalloc(gdr_bwd_plan *plan, const gdr_bwd_args *args, void *stream);
+
+/* No counterpart on the pages.  The device status word of the last gdr_bwd_run_noalloc on the current
+ * device (it lives in the shared array, so gdr_bwd_get_status cannot reach it): synchronises `stream`,
+ * returns GDR_OK, GDR_ERR_TIMEOUT or GDR_ERR_DEVICE as gdr_bwd_get_status does, and clears the word.
+ * GDR_ERR_UNSUPPORTED for a plan beyond the array's size; allocates nothing. */
+gdr_status gdr_bwd_get_status_noalloc(gdr_bwd_plan *plan, void *stream);
 
 /* ---- Forward pass (the output and final state that the backward above differentiates).
  * Per sequence and value head, S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T and

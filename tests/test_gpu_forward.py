@@ -15,7 +15,7 @@ import torch
 import oracle
 from chunked_gated_delta_09_gb300 import ops
 from chunked_gated_delta_09_gb300.inputs import make_problem, workload
-from parity_util import TOL, compare, rel_l2
+from parity_util import TOL, compare, parity_error
 from test_gpu_parity import SMALL
 
 pytestmark = pytest.mark.gpu
@@ -47,7 +47,7 @@ def check_forward(prob, got, ref):
         g, r = got[key], ref[key]
         assert g.shape == r.shape, (key, g.shape, r.shape)
         assert np.all(np.isfinite(g)), f"{key} has non-finite values"
-        res[key] = (rel_l2(g, r), bar)
+        res[key] = parity_error(g, r, bar, prob)
     log = os.environ.get("GDR_PARITY_LOG")
     if log:
         with open(log, "a") as f:

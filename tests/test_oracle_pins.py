@@ -372,3 +372,37 @@ def test_wy_stage_pieces_against_the_full_gradient_terms():
     dq_intra = np.einsum("ij,jc,ijc->ic", P, k, np.exp(g[:, None, :] - g[None, :, :]))
     np.testing.assert_allclose(st["dq"] + dq_intra, full["dq"][:, 0], rtol=1e-9, atol=1e-10)
     np.testing.assert_allclose(st["dv"], beta[:, None] * (A.T @ dv_new), rtol=1e-12, atol=1e-12)
+
+
+def test_wy_stage_packed_driver_assembles_the_chunks():
+    """The packed, varlen driver of the WY stage (wy_stage.wy_stage) equals per-chunk calls of chunk_grads
+    placed by hand: two sequences of 23 and 37 tokens with BT = 16 give the chunks [0, 16), [16, 23) of the
+    first and [23, 39), [39, 55), [55, 60) of the second, numbered 0..4 for h and dh; the rows of dA beyond a
+    chunk's length stay zero."""
+    from oracle import wy_stage
+    rng = np.random.default_rng(31)
+    H, K, V, BT, scale = 2, 4, 3, 16, 0.6
+    Tt = 60
+    cu = np.array([0, 23, 60])
+    q, k = rng.standard_normal((Tt, H, K)), rng.standard_normal((Tt, H, K))
+    v, v_new, do, dv = (rng.standard_normal((Tt, H, V)) for _ in range(4))
+    g = -np.abs(rng.standard_normal((Tt, H, K)))
+    beta = rng.random((Tt, H))
+    A = rng.standard_normal((Tt, H, BT))
+    h, dh = rng.standard_normal((5, H, K, V)), rng.standard_normal((5, H, K, V))
+    got = wy_stage.wy_stage(cu, H, K, V, BT, scale, q, k, v, v_new, g, beta, A, h, do, dh, dv)
+    chunks = [(0, 16, 0), (16, 23, 1), (23, 39, 2), (39, 55, 3), (55, 60, 4)]
+    want = {key: np.zeros_like(val) for key, val in got.items()}
+    for c0, c1, n in chunks:
+        C = c1 - c0
+        for hh in range(H):
+            r = wy_stage.chunk_grads(q[c0:c1, hh], k[c0:c1, hh], v[c0:c1, hh], v_new[c0:c1, hh], g[c0:c1, hh],
+                                     beta[c0:c1, hh], A[c0:c1, hh, :C], h[n, hh], do[c0:c1, hh], dh[n, hh],
+                                     dv[c0:c1, hh], scale)
+            for key in ("dq", "dk", "dv", "db", "dg"):
+                want[key][c0:c1, hh] = r[key]
+            want["dA"][c0:c1, hh, :C] = r["dA"]
+    for key in want:
+        np.testing.assert_array_equal(got[key], want[key], err_msg=key)
+    # a chunk's dA columns beyond its length are zero (the 7-token and 5-token chunks)
+    assert not got["dA"][16:23, :, 7:].any() and not got["dA"][55:60, :, 5:].any()
