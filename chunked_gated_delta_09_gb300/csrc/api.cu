@@ -29,7 +29,7 @@ struct gdr_bwd_plan {
     long long tokens;  // B * T
     // workspace byte offsets
     size_t o_status, o_cidx, o_coff, o_gam, o_T, o_Aqk, o_W, o_U, o_Kt, o_Qg, o_Dt, o_h, o_dh, o_Vn, o_dVn, o_dgam, o_dqh,
-        o_dkh, o_seg, o_sc, total;
+        o_dkh, o_seg, o_sc, o_kd, total;
 };
 
 namespace gdr {
@@ -125,6 +125,7 @@ void layout(gdr_bwd_plan &p) {
     size_t seg_units = p.NS > 1 ? (size_t)p.N * d.Hv * p.NS : 0;
     p.o_seg = take(6 * sizeof(float) * seg_units * DT * DT);
     p.o_sc = take(d.gate_per_channel ? 0 : sizeof(float) * units * 4 * CT);
+    p.o_kd = take(d.gate_per_channel ? sizeof(__half) * units * CT * CT : 0);
     p.total = off;
 }
 
@@ -236,6 +237,7 @@ static void fill_common(const gdr_bwd_plan *plan, char *ws, Params &P) {
     P.chunk_off = reinterpret_cast<int32_t *>(ws + plan->o_coff);
     P.gam = reinterpret_cast<float *>(ws + plan->o_gam);
     P.sc = plan->d.gate_per_channel ? nullptr : reinterpret_cast<float *>(ws + plan->o_sc);
+    P.Kd = plan->d.gate_per_channel ? reinterpret_cast<__half *>(ws + plan->o_kd) : nullptr;
     P.Tm = reinterpret_cast<__half *>(ws + plan->o_T);
     P.Aqk = reinterpret_cast<__half *>(ws + plan->o_Aqk);
     P.W = reinterpret_cast<__half *>(ws + plan->o_W);
@@ -386,6 +388,7 @@ gdr_status gdr_fwd_run(gdr_bwd_plan *plan, const gdr_fwd_args *a, void *workspac
     P.cu = plan->dense ? nullptr : a->cu_seqlens;
     P.o = a->o;
     P.ht = a->ht;
+    P.Kd = nullptr;  // the decayed key Gram serves only the backward's dbeta
     // the forward: chunk bookkeeping, WY preparation without dO, the state recompute (which also writes
     // the final state), then the per-chunk output
     if (cudaMemsetAsync(P.status, 0, sizeof(int), stream) != cudaSuccess) return GDR_ERR_CUDA;

@@ -65,6 +65,7 @@ struct Params {
     float *sc;           // [u][4][CT] scalar gate, backward: beta, exp(gamma), exp(gamma_C - gamma), gamma
     __half *Tm;          // tile [r][i]   64 x 64    (I + A_kk)^-1
     __half *Aqk;         // tile [r][j]   64 x 64    M (.) Q K^T (causal, decayed, unscaled)
+    __half *Kd;          // tile [i][j]   64 x 64    per-channel gate: sum_k k_i k_j exp(gamma_i - gamma_j), j < i
     __half *W, *U;       // W tile [c][k] 64 x 128; U^T tile [v][c] 128 x 64
     __half *Kt;          // tile [c][k]   64 x 128   K (.) exp(gamma_C - gamma)
     __half *Qg;          // tile [r][k]   64 x 128   Q (.) exp(gamma)

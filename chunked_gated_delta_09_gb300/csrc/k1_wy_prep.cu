@@ -275,6 +275,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
         // are zero
         constexpr int NB = CT / 2, NLOW = NB * (NB + 1) / 2;
         unsigned char *aqk_g = reinterpret_cast<unsigned char *>(P.Aqk + u * CT * CT);
+        // the decayed key Gram itself (before beta) for the gradient kernel's dbeta, when it is wanted
+        unsigned char *kd_g = P.Kd ? reinterpret_cast<unsigned char *>(P.Kd + u * CT * CT) : nullptr;
         for (int b = tid; b < NLOW; b += K1_THREADS) {
             int bi = (int)((sqrtf(8.f * (float)b + 1.f) - 1.f) * 0.5f);  // row of b in the lower triangle
             while ((bi + 1) * (bi + 2) / 2 <= b) ++bi;
@@ -308,14 +310,16 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
 #pragma unroll
             for (int a = 0; a < 2; ++a) {
                 const int i = i0 + a;
-                float aq[2];
+                float aq[2], kd[2];
 #pragma unroll
                 for (int bb = 0; bb < 2; ++bb) {
                     const int j = j0 + bb;
-                    S.AT[i][j] = (j < i && i < len) ? S.beta[i] * akk[a][bb] : 0.f;
+                    kd[bb] = (j < i && i < len) ? akk[a][bb] : 0.f;
+                    S.AT[i][j] = S.beta[i] * kd[bb];
                     aq[bb] = (j <= i && i < len) ? aqk[a][bb] : 0.f;
                 }
                 *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j0, CT)) = __floats2half2_rn(aq[0], aq[1]);
+                if (kd_g) *reinterpret_cast<__half2 *>(kd_g + ctile_off(i, j0, CT)) = __floats2half2_rn(kd[0], kd[1]);
             }
         }
         for (int e = tid; e < CT * CT / 2; e += K1_THREADS) {  // pairs (i, j0 .. j0 + 1) above the diagonal blocks
@@ -324,6 +328,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                 S.AT[i][j0] = 0.f;
                 S.AT[i][j0 + 1] = 0.f;
                 *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j0, CT)) = __floats2half2_rn(0.f, 0.f);
+                if (kd_g) *reinterpret_cast<__half2 *>(kd_g + ctile_off(i, j0, CT)) = __floats2half2_rn(0.f, 0.f);
             }
         }
     }

@@ -41,12 +41,65 @@ constexpr int NC = 2;  // C x C tiles: 16 x 16 per warp (two n8 tiles)
 // per-channel cumulative gate [CT][DT]:
 //   LOWER:  acc[r][c] += sum_{j <= r (INCL) or j < r} A[r][j] X[j][c] exp(g[r][c] - g[j][c])
 //   else:   acc[r][c] += sum_{i >= r (INCL) or i > r} A[i][r] X[i][c] exp(g[i][c] - g[r][c])
-// One pass over the inner index serves all 16 elements of a thread (two A loads, a column pair of X and of g
-// per n-tile); terms outside a row's range are dropped by selection, never by a zero factor.
+// Sub-chunk factorisation: the warp's rows form one 16-row block of the chunk.  The terms from the other
+// blocks (j below the block for LOWER, i above it otherwise) share a reference row ref on the block boundary
+// between them (ref = m0, resp. m0 + 16), and exp(g[r] - g[j]) = exp(g[r] - g[ref]) exp(g[ref] - g[j]) with both
+// factors at most 1 (g is non-increasing along the chunk): those terms are one warp MMA over the rescaled
+// X~[j][c] = X[j][c] exp(g[ref][c] - g[j][c]) (built straight into the B fragments), times exp(g[r][c] -
+// g[ref][c]) per output element.  Only the 16 x 16 diagonal block is evaluated term by term; there one pass over
+// the inner index serves all 16 elements of a thread, and terms outside a row's range are dropped by selection,
+// never by a zero factor.
 template <bool LOWER, bool INCL>
 __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsigned char *A, const unsigned char *X,
                                             const float *g, int m0, int n0, int lane) {
     const int r0 = m0 + (lane >> 2), cq = n0 + 2 * (lane & 3);
+    // ---- off-diagonal blocks on the tensor cores
+    const int ks_lo = LOWER ? 0 : m0 / 16 + 1, ks_hi = LOWER ? m0 / 16 : CT / 16;  // 16-row k-steps [lo, hi)
+    if (ks_lo < ks_hi) {
+        const int ref = LOWER ? m0 : m0 + 16;
+        float off[1][NK][4];
+        zero_acc(off);
+        const int bn = lane >> 2;                 // B fragment: column n = n0 + 8 nt + lane / 4
+        const int bk = 2 * (lane & 3);            // B fragment: k rows bk, bk + 1 and bk + 8, bk + 9
+        float gref_b[NK];
+#pragma unroll
+        for (int nt = 0; nt < NK; ++nt) gref_b[nt] = g[ref * DT + n0 + 8 * nt + bn];
+        const int r8 = lane & 7, mat = lane >> 3;
+        for (int ks = ks_lo; ks < ks_hi; ++ks) {
+            const int k0 = 16 * ks;
+            uint32_t a[4];
+            if (LOWER) ldsm_x4(a, A + ctile_off(m0 + (lane & 15), k0 + (lane >> 4) * 8, CT));
+            else ldsm_x4_t(a, A + ctile_off(k0 + r8 + (mat >> 1) * 8, m0 + (mat & 1) * 8, CT));
+#pragma unroll
+            for (int nt = 0; nt < NK; ++nt) {
+                const int c = n0 + 8 * nt + bn;
+                float v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = k0 + bk + (q & 1) + 8 * (q >> 1);
+                    const float x = ctile_get(X, j, c, DT);
+                    // exponent <= 0 on both sides of the reference row
+                    v[q] = x * __expf(LOWER ? gref_b[nt] - g[j * DT + c] : g[j * DT + c] - gref_b[nt]);
+                }
+                const __half2 b0 = __floats2half2_rn(v[0], v[1]), b1 = __floats2half2_rn(v[2], v[3]);
+                mma16816(off[0][nt], a, *reinterpret_cast<const uint32_t *>(&b0), *reinterpret_cast<const uint32_t *>(&b1));
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = cq + 8 * nt + h;
+                const float gr = g[ref * DT + c];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int r = r0 + 8 * rr;
+                    const float gx = g[r * DT + c];
+                    acc[0][nt][2 * rr + h] += off[0][nt][2 * rr + h] * __expf(LOWER ? gx - gr : gr - gx);
+                }
+            }
+    }
+    // ---- the diagonal block, term by term
     float gr[2][NK][2];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -56,7 +109,7 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
             gr[h][nt][0] = v.x;
             gr[h][nt][1] = v.y;
         }
-    const int lo = LOWER ? 0 : (INCL ? r0 : r0 + 1), hi = LOWER ? (INCL ? r0 + 8 : r0 + 7) : CT - 1;
+    const int lo = LOWER ? m0 : (INCL ? r0 : r0 + 1), hi = LOWER ? (INCL ? r0 + 8 : r0 + 7) : m0 + 15;
     for (int j = lo; j <= hi; ++j) {
         // LOWER: row r0 uses j only up to r0 (every j of the loop serves row r0 + 8); else row r0 + 8 uses
         // i only from r0 + 8 on (every i of the loop serves row r0)
@@ -499,9 +552,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                         if (!PC) {
                             L = __expf(S.gam[i] - S.gam[j]);
                             kkd = L * kk[0][nt][e];
-                        } else {
-                            for (int c = 0; c < DT; ++c)
-                                kkd += Kv(i, c) * Kv(j, c) * __expf(gamK[i * DT + c] - gamK[j * DT + c]);
+                        } else {  // the decayed key Gram, formed by the WY preparation
+                            kkd = ctile_get(reinterpret_cast<const unsigned char *>(P.Kd + u * CT * CT), i, j, CT);
                         }
                     }
                     rb[e >> 1] += dA * kkd;
