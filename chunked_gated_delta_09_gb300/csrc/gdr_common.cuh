@@ -250,6 +250,19 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// m16n8k8: c (16 x 8, fp32) += A (16 x 8, fp16: a0 rows lane/4, a1 rows lane/4 + 8) B (8 x 8, fp16).
+__device__ __forceinline__ void mma1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 // One warp accumulates a (16*MT) x (8*NT) tile: acc += A[m0.., 0:kdim] * B[0:kdim, n0..].
 //   AT = false: A(m, k) = A[m * lda + k]  (row-major M x K)
 //   AT = true : A(m, k) = A[k * lda + m]  (stored transposed, K x M)

@@ -270,21 +270,41 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                 *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j, CT)) = __floats2half2_rn(aq[0], aq[1]);
             }
     } else {
-        // per-channel sums sum_c x_ic k_jc exp(gamma_i[c] - gamma_j[c]) over the causal 2 x 2 blocks (bi >= bj)
-        // of the chunk, spread evenly over the threads, 8 channels per step; the blocks above the diagonal
-        // are zero
-        constexpr int NB = CT / 2, NLOW = NB * (NB + 1) / 2;
+        // per-channel sums sum_c x_ic k_jc exp(gamma_i[c] - gamma_j[c]) (x = k: the decayed key Gram, x = q: Aqk)
+        // over the causal part of the chunk, by 16-row blocks I >= J:
+        //  * I > J: sub-chunk factorisation around the first row ref = 16 I of block I, exp(gamma_i - gamma_j) =
+        //    exp(gamma_i - gamma_ref) exp(gamma_ref - gamma_j), both factors at most 1: one warp per block pair
+        //    runs two MMAs over the rescaled rows (built straight into the fragments), K = 128 channels;
+        //  * I = J: the block splits at its middle row mid = 16 I + 8: the cross 8 x 8 quarter (upper rows, lower
+        //    columns) by the same factorisation around mid (warps 0 and 1, two blocks each), the two 8 x 8
+        //    triangles term by term over their 2 x 2 blocks, the 128 channels split between the two lanes of a pair
+        //    (their halves added by one shuffle).
+        // The blocks above the diagonal are zero.
         unsigned char *aqk_g = reinterpret_cast<unsigned char *>(P.Aqk + u * CT * CT);
         // the decayed key Gram itself (before beta) for the gradient kernel's dbeta, when it is wanted
         unsigned char *kd_g = P.Kd ? reinterpret_cast<unsigned char *>(P.Kd + u * CT * CT) : nullptr;
-        for (int b = tid; b < NLOW; b += K1_THREADS) {
-            int bi = (int)((sqrtf(8.f * (float)b + 1.f) - 1.f) * 0.5f);  // row of b in the lower triangle
-            while ((bi + 1) * (bi + 2) / 2 <= b) ++bi;
-            while (bi * (bi + 1) / 2 > b) --bi;
-            const int i0 = 2 * bi, j0 = 2 * (b - bi * (bi + 1) / 2);
+        auto put2 = [&](int i, int j0, const float (&akk)[2], const float (&aqk)[2]) {  // row i, columns j0, j0 + 1
+            float aq[2], kd[2];
+#pragma unroll
+            for (int bb = 0; bb < 2; ++bb) {
+                const int j = j0 + bb;
+                kd[bb] = (j < i && i < len) ? akk[bb] : 0.f;
+                S.AT[i][j] = S.beta[i] * kd[bb];
+                aq[bb] = (j <= i && i < len) ? aqk[bb] : 0.f;
+            }
+            *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j0, CT)) = __floats2half2_rn(aq[0], aq[1]);
+            if (kd_g) *reinterpret_cast<__half2 *>(kd_g + ctile_off(i, j0, CT)) = __floats2half2_rn(kd[0], kd[1]);
+        };
+        // ---- diagonal triangles: 4 blocks x 2 halves x 10 lower 2 x 2 blocks x 2 channel halves (warps 0..4)
+        constexpr int NDIAG = 4 * 2 * 10 * 2;
+        for (int t = tid; t < NDIAG; t += K1_THREADS) {
+            const int half = t & 1, b2 = t >> 1, blk = b2 / 20, sh = (b2 % 20) / 10, l = b2 % 10;
+            const int li = l < 1 ? 0 : (l < 3 ? 1 : (l < 6 ? 2 : 3));  // row of l in a 4 x 4 lower triangle
+            const int lj = l - li * (li + 1) / 2;
+            const int i0 = 16 * blk + 8 * sh + 2 * li, j0 = 16 * blk + 8 * sh + 2 * lj;
             float akk[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, aqk[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
             if (i0 < len) {
-                for (int c8 = 0; c8 < DT; c8 += 8) {
+                for (int c8 = 64 * half; c8 < 64 * half + 64; c8 += 8) {
                     float ki[2][8], qi[2][8], kj[2][8], gi[2][8], gj[2][8];
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
@@ -299,28 +319,112 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
 #pragma unroll
                         for (int bb = 0; bb < 2; ++bb)
 #pragma unroll
-                            for (int t = 0; t < 8; ++t) {
+                            for (int t8 = 0; t8 < 8; ++t8) {
                                 // (exponent <= 0 on every element that is kept below)
-                                const float kd = kj[bb][t] * __expf(gi[a][t] - gj[bb][t]);
-                                akk[a][bb] += ki[a][t] * kd;
-                                aqk[a][bb] += qi[a][t] * kd;
+                                const float kd = kj[bb][t8] * __expf(gi[a][t8] - gj[bb][t8]);
+                                akk[a][bb] += ki[a][t8] * kd;
+                                aqk[a][bb] += qi[a][t8] * kd;
                             }
                 }
             }
+            // the other channel half is in the partner lane (tasks 2m, 2m + 1 sit in lanes 2m', 2m' + 1)
 #pragma unroll
-            for (int a = 0; a < 2; ++a) {
-                const int i = i0 + a;
-                float aq[2], kd[2];
+            for (int a = 0; a < 2; ++a)
 #pragma unroll
                 for (int bb = 0; bb < 2; ++bb) {
-                    const int j = j0 + bb;
-                    kd[bb] = (j < i && i < len) ? akk[a][bb] : 0.f;
-                    S.AT[i][j] = S.beta[i] * kd[bb];
-                    aq[bb] = (j <= i && i < len) ? aqk[a][bb] : 0.f;
+                    akk[a][bb] += __shfl_xor_sync(0xffffffffu, akk[a][bb], 1);
+                    aqk[a][bb] += __shfl_xor_sync(0xffffffffu, aqk[a][bb], 1);
                 }
-                *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j0, CT)) = __floats2half2_rn(aq[0], aq[1]);
-                if (kd_g) *reinterpret_cast<__half2 *>(kd_g + ctile_off(i, j0, CT)) = __floats2half2_rn(kd[0], kd[1]);
+            if (!half) {
+                put2(i0, j0, akk[0], aqk[0]);
+                put2(i0 + 1, j0, akk[1], aqk[1]);
             }
+        }
+        // ---- cross quarters of the diagonal blocks: warp 0 blocks 0 and 1, warp 1 blocks 2 and 3; the upper 8
+        // rows sit in the fragments' rows 8..15, rows 0..7 stay zero
+        if (wid < 2) {
+            const int g4 = lane >> 2, kq = 2 * (lane & 3);
+            for (int bi = 0; bi < 2; ++bi) {
+                const int blk = 2 * wid + bi, mid = 16 * blk + 8;
+                float kk[4] = {}, qk[4] = {};
+                for (int k0 = 0; k0 < DT; k0 += 16) {
+                    uint32_t ak[4] = {0u, 0u, 0u, 0u}, aq[4] = {0u, 0u, 0u, 0u}, bk[2];
+#pragma unroll
+                    for (int q = 1; q < 4; q += 2) {  // a[1], a[3]: row mid + g4, channels k0 + kq (+8)
+                        const int row = mid + g4, c = k0 + kq + 8 * (q >> 1);
+                        const float2 gr = *reinterpret_cast<const float2 *>(gamK + mid * GKLD + c);
+                        const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
+                        const float e0 = __expf(gx.x - gr.x), e1 = __expf(gx.y - gr.y);
+                        const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(S.Ks + ctile_off(row, c, DT)));
+                        const float2 qv = __half22float2(*reinterpret_cast<const __half2 *>(S.Qs + ctile_off(row, c, DT)));
+                        ak[q] = pack_half2(kv.x * e0, kv.y * e1);
+                        aq[q] = pack_half2(qv.x * e0, qv.y * e1);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {  // key rows 16 blk + g4 (the lower half)
+                        const int row = 16 * blk + g4, c = k0 + kq + 8 * q;
+                        const float2 gr = *reinterpret_cast<const float2 *>(gamK + mid * GKLD + c);
+                        const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
+                        const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(S.Ks + ctile_off(row, c, DT)));
+                        bk[q] = pack_half2(kv.x * __expf(gr.x - gx.x), kv.y * __expf(gr.y - gx.y));
+                    }
+                    mma16816(kk, ak, bk[0], bk[1]);
+                    mma16816(qk, aq, bk[0], bk[1]);
+                }
+                const float a2[2] = {kk[2], kk[3]}, q2[2] = {qk[2], qk[3]};
+                put2(mid + g4, 16 * blk + kq, a2, q2);
+            }
+        }
+        // ---- blocks below the diagonal: warp 2 + p takes the pair p: (I, J) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+        // (warp 0 summed a second round of diagonal tasks above)
+        if (wid >= 2) {
+            const int p = wid - 2;
+            const int I = p < 1 ? 1 : (p < 3 ? 2 : 3), J = p < 1 ? 0 : (p < 3 ? p - 1 : p - 3);
+            const int ref = 16 * I, g4 = lane >> 2, kq = 2 * (lane & 3);
+            float kk[2][4] = {}, qk[2][4] = {};
+            for (int k0 = 0; k0 < DT; k0 += 16) {
+                // A fragments (rows 16 I + g4, + 8; channels k0 + kq, +1, +8, +9), rescaled by exp(g[row] - g[ref])
+                uint32_t ak[4], aq[4], bk[2][2];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int row = ref + g4 + 8 * (q & 1), c = k0 + kq + 8 * (q >> 1);
+                    const float2 gr = *reinterpret_cast<const float2 *>(gamK + ref * GKLD + c);
+                    const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
+                    const float e0 = __expf(gx.x - gr.x), e1 = __expf(gx.y - gr.y);
+                    const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(S.Ks + ctile_off(row, c, DT)));
+                    const float2 qv = __half22float2(*reinterpret_cast<const __half2 *>(S.Qs + ctile_off(row, c, DT)));
+                    const __half2 hk = __floats2half2_rn(kv.x * e0, kv.y * e1), hq = __floats2half2_rn(qv.x * e0, qv.y * e1);
+                    ak[q] = *reinterpret_cast<const uint32_t *>(&hk);
+                    aq[q] = *reinterpret_cast<const uint32_t *>(&hq);
+                }
+                // B fragments (key rows 16 J + 8 nt + g4; channels k0 + kq, +1 and +8, +9), rescaled by
+                // exp(g[ref] - g[row])
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int row = 16 * J + 8 * nt + g4, c = k0 + kq + 8 * q;
+                        const float2 gr = *reinterpret_cast<const float2 *>(gamK + ref * GKLD + c);
+                        const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
+                        const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(S.Ks + ctile_off(row, c, DT)));
+                        const __half2 hb = __floats2half2_rn(kv.x * __expf(gr.x - gx.x), kv.y * __expf(gr.y - gx.y));
+                        bk[nt][q] = *reinterpret_cast<const uint32_t *>(&hb);
+                    }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    mma16816(kk[nt], ak, bk[nt][0], bk[nt][1]);
+                    mma16816(qk[nt], aq, bk[nt][0], bk[nt][1]);
+                }
+            }
+            // accumulators: rows ref + g4 (+ 8), columns 16 J + 8 nt + kq (+1), each times exp(g[row] - g[ref])
+            // already folded in; write out
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float a2[2] = {kk[nt][2 * h], kk[nt][2 * h + 1]}, q2[2] = {qk[nt][2 * h], qk[nt][2 * h + 1]};
+                    put2(ref + g4 + 8 * h, 16 * J + 8 * nt + kq, a2, q2);
+                }
         }
         for (int e = tid; e < CT * CT / 2; e += K1_THREADS) {  // pairs (i, j0 .. j0 + 1) above the diagonal blocks
             const int i = e / (CT / 2), j0 = 2 * (e % (CT / 2));

@@ -46,9 +46,10 @@ constexpr int NC = 2;  // C x C tiles: 16 x 16 per warp (two n8 tiles)
 // between them (ref = m0, resp. m0 + 16), and exp(g[r] - g[j]) = exp(g[r] - g[ref]) exp(g[ref] - g[j]) with both
 // factors at most 1 (g is non-increasing along the chunk): those terms are one warp MMA over the rescaled
 // X~[j][c] = X[j][c] exp(g[ref][c] - g[j][c]) (built straight into the B fragments), times exp(g[r][c] -
-// g[ref][c]) per output element.  Only the 16 x 16 diagonal block is evaluated term by term; there one pass over
-// the inner index serves all 16 elements of a thread, and terms outside a row's range are dropped by selection,
-// never by a zero factor.
+// g[ref][c]) per output element.  The 16 x 16 diagonal block splits once more at its middle row: its cross 8 x 8
+// quarter the same way, and only the two 8 x 8 triangles term by term, where one pass over the inner index
+// serves all 16 elements of a thread and terms outside a row's range are dropped by selection, never by a zero
+// factor.
 template <bool LOWER, bool INCL>
 __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsigned char *A, const unsigned char *X,
                                             const float *g, int m0, int n0, int lane) {
@@ -99,7 +100,36 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
                 }
             }
     }
-    // ---- the diagonal block, term by term
+    // ---- the diagonal block: its cross quarter (the warp's upper 8 rows against its lower 8 for LOWER, the
+    // reverse otherwise) by the same factorisation around the block's middle row mid = m0 + 8, one k = 8 MMA
+    // with the other half's fragment rows left zero; the two 8 x 8 triangles term by term
+    const int mid = m0 + 8;
+    {
+        const int bn = lane >> 2, bk = 2 * (lane & 3);
+        uint32_t a0 = 0u, a1 = 0u;
+        if (LOWER) a1 = *reinterpret_cast<const uint32_t *>(A + ctile_off(mid + bn, m0 + bk, CT));  // A[r0 + 8][m0 + bk..]
+        else a0 = pack_half2(ctile_get(A, mid + bk, r0, CT), ctile_get(A, mid + bk + 1, r0, CT));  // A[mid + bk..][r0]
+        float off[NK][4];
+#pragma unroll
+        for (int nt = 0; nt < NK; ++nt) {
+            off[nt][0] = off[nt][1] = off[nt][2] = off[nt][3] = 0.f;
+            const int c = n0 + 8 * nt + bn;
+            const float gm = g[mid * DT + c];
+            const int j = LOWER ? m0 + bk : mid + bk;  // k rows of the B fragment
+            const float v0 = ctile_get(X, j, c, DT) * __expf(LOWER ? gm - g[j * DT + c] : g[j * DT + c] - gm);
+            const float v1 = ctile_get(X, j + 1, c, DT) * __expf(LOWER ? gm - g[(j + 1) * DT + c] : g[(j + 1) * DT + c] - gm);
+            mma1688(off[nt], a0, a1, pack_half2(v0, v1));
+        }
+#pragma unroll
+        for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = cq + 8 * nt + h;
+                const float gm = g[mid * DT + c];
+                if (LOWER) acc[0][nt][2 + h] += off[nt][2 + h] * __expf(g[(r0 + 8) * DT + c] - gm);  // rows r0 + 8
+                else acc[0][nt][h] += off[nt][h] * __expf(gm - g[r0 * DT + c]);                    // rows r0
+            }
+    }
     float gr[2][NK][2];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -109,26 +139,28 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
             gr[h][nt][0] = v.x;
             gr[h][nt][1] = v.y;
         }
-    const int lo = LOWER ? m0 : (INCL ? r0 : r0 + 1), hi = LOWER ? (INCL ? r0 + 8 : r0 + 7) : m0 + 15;
-    for (int j = lo; j <= hi; ++j) {
-        // LOWER: row r0 uses j only up to r0 (every j of the loop serves row r0 + 8); else row r0 + 8 uses
-        // i only from r0 + 8 on (every i of the loop serves row r0)
-        const bool v0 = LOWER ? (INCL ? j <= r0 : j < r0) : true;
-        const bool v1 = LOWER ? true : (INCL ? j >= r0 + 8 : j > r0 + 8);
-        const float a0 = LOWER ? ctile_get(A, r0, j, CT) : ctile_get(A, j, r0, CT);
-        const float a1 = LOWER ? ctile_get(A, r0 + 8, j, CT) : ctile_get(A, j, r0 + 8, CT);
+    // row r0 pairs with j (i) = m0 + t, row r0 + 8 with m0 + 8 + t: both inside their own 8-row half
+#pragma unroll 2
+    for (int t = 0; t < 8; ++t) {
+        const int j0 = m0 + t, j1 = mid + t;
+        const bool v0 = LOWER ? (INCL ? j0 <= r0 : j0 < r0) : (INCL ? j0 >= r0 : j0 > r0);
+        const bool v1 = LOWER ? (INCL ? j1 <= r0 + 8 : j1 < r0 + 8) : (INCL ? j1 >= r0 + 8 : j1 > r0 + 8);
+        const float a0 = LOWER ? ctile_get(A, r0, j0, CT) : ctile_get(A, j0, r0, CT);
+        const float a1 = LOWER ? ctile_get(A, r0 + 8, j1, CT) : ctile_get(A, j1, r0 + 8, CT);
 #pragma unroll
         for (int nt = 0; nt < NK; ++nt) {
-            const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(X + ctile_off(j, cq + 8 * nt, DT)));
-            const float2 gj = *reinterpret_cast<const float2 *>(g + j * DT + cq + 8 * nt);
-            const float e00 = __expf(LOWER ? gr[0][nt][0] - gj.x : gj.x - gr[0][nt][0]);
-            const float e01 = __expf(LOWER ? gr[0][nt][1] - gj.y : gj.y - gr[0][nt][1]);
-            const float e10 = __expf(LOWER ? gr[1][nt][0] - gj.x : gj.x - gr[1][nt][0]);
-            const float e11 = __expf(LOWER ? gr[1][nt][1] - gj.y : gj.y - gr[1][nt][1]);
-            acc[0][nt][0] += v0 ? a0 * x.x * e00 : 0.f;
-            acc[0][nt][1] += v0 ? a0 * x.y * e01 : 0.f;
-            acc[0][nt][2] += v1 ? a1 * x.x * e10 : 0.f;
-            acc[0][nt][3] += v1 ? a1 * x.y * e11 : 0.f;
+            const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(X + ctile_off(j0, cq + 8 * nt, DT)));
+            const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(X + ctile_off(j1, cq + 8 * nt, DT)));
+            const float2 g0 = *reinterpret_cast<const float2 *>(g + j0 * DT + cq + 8 * nt);
+            const float2 g1 = *reinterpret_cast<const float2 *>(g + j1 * DT + cq + 8 * nt);
+            const float e00 = __expf(LOWER ? gr[0][nt][0] - g0.x : g0.x - gr[0][nt][0]);
+            const float e01 = __expf(LOWER ? gr[0][nt][1] - g0.y : g0.y - gr[0][nt][1]);
+            const float e10 = __expf(LOWER ? gr[1][nt][0] - g1.x : g1.x - gr[1][nt][0]);
+            const float e11 = __expf(LOWER ? gr[1][nt][1] - g1.y : g1.y - gr[1][nt][1]);
+            acc[0][nt][0] += v0 ? a0 * x0.x * e00 : 0.f;
+            acc[0][nt][1] += v0 ? a0 * x0.y * e01 : 0.f;
+            acc[0][nt][2] += v1 ? a1 * x1.x * e10 : 0.f;
+            acc[0][nt][3] += v1 ? a1 * x1.y * e11 : 0.f;
         }
     }
 }
