@@ -15,9 +15,11 @@
 //    identity tile: one tensor-memory load replaces 16 scattered 2-byte shared-memory reads;
 //  * each buffer is refilled for the CTA's next item as soon as its last reader is done: S_0, dS_next, D,
 //    V_new^T, -dV_new^T after phase 1 and T after phase 4 (bulk copies: one barrier phase per item for the
-//    first group, one on a second barrier for T);
-//    for 16-bit inputs V after phase 1, Q after phase 2 and K after phase 5 (cp.async of the raw rows into
-//    their tile slots, converted to fp16 in place when the item starts).
+//    first group, one on a second barrier for T); for 16-bit inputs V after phase 1, Q after phase 2 and K
+//    after phase 5, each by one TMA tensor load (a 4-D tensor map over [tokens, heads, features] whose box of
+//    8-element rows lands as a column-block-major core-matrix tile: core matrix (r/8, c/8) at
+//    ((c/8) 8 + r/8) 128), converted to fp16 in place when the item starts (rows past the chunk's end and
+//    columns past K or V set to zero).
 //
 // Five MMA phases, each followed by an epilogue that produces the next phase's operands:
 //   1: dk_SC^T = dS^T V_new^T, dW^T = -S0^T dV^T, TdU^T = dV^T T, K^T, P0 = D V_new^T, dT2 = dV V^T,
@@ -27,6 +29,10 @@
 // The WY part of dbeta, sum_k (T^T dW)_jk Gamma_j k_jk + sum_v (T^T dU)_jv v_jv, equals the column sum
 // sum_i T_ij (Gamma_j dT1_ij + dT2_ij) of two chunk x chunk products, so it is taken there.  The epilogues of
 // M = 64 products spread each row's 16 columns over both half-warps.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 #include <type_traits>
 
 #include "gdr_common.cuh"
@@ -68,6 +74,7 @@ struct __align__(1024) K4TSmem {
     float db_wy[2][4][CT], db_a[2][4][CT], dg_q[2][4][CT], last_w[2][16];
     int red_u, red_len, red_tok0, red_hv, red_b;  // the item whose sums are pending (red_u < 0: none), its set
     uint64_t bar, bar2, lbar, tbar;  // MMA groups 1 and 2 of a phase; bulk loads (T on its own barrier)
+    uint64_t kbar, qbar, vbar;       // tensor-map loads of the raw k, q, v rows
     uint32_t tslot;
 };
 
@@ -104,8 +111,12 @@ __device__ __forceinline__ void lds8(const float *p, float (&v)[8]) {
     v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
 }
 
+// Tensor maps of the 16-bit inputs (unused for fp32 inputs): 4-D over (8-element column chunk, token, column
+// block, head), box (8, 64, K/8 or V/8, 1).
 template <typename Tin>
-__global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params P) {
+__global__ void __launch_bounds__(K4T_THREADS, 1)
+    k4_intra_grad_tc(const Params P, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
+                     const __grid_constant__ CUtensorMap tmv) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     K4TSmem &S = *reinterpret_cast<K4TSmem *>(smem_raw);
     if (*P.status & ST_BAD_SEQLENS) return;
@@ -128,6 +139,9 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         tc::mbar_init(&S.bar2, K4T_ISSUERS);
         tc::mbar_init(&S.lbar, 1);
         tc::mbar_init(&S.tbar, 1);
+        tc::mbar_init(&S.kbar, 1);
+        tc::mbar_init(&S.qbar, 1);
+        tc::mbar_init(&S.vbar, 1);
         S.red_u = -1;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -180,33 +194,49 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
             nc = P.K;
         }
     };
-    auto fetch_raw = [&](int it, int which, unsigned char *dst) {  // raw rows into their tile slots
+    // raw rows of an item into their (column-block-major) tile slot: one tensor-map load by the loader thread
+    auto fetch_raw = [&](int it, int which, unsigned char *dst) {
+        ChunkInfo c2;
+        chunk_info(P, it / P.Hv, c2);
+        const int hv2 = it % P.Hv;
+        const int ncb = (which == 2 ? P.V : P.K) >> 3;
+        uint64_t *bar = which == 0 ? &S.kbar : which == 1 ? &S.qbar : &S.vbar;
+        const CUtensorMap *map = which == 0 ? &tmk : which == 1 ? &tmq : &tmv;
+        tc::mbar_expect_tx(bar, (uint32_t)(8 * CT * ncb * 2));
+        tc::tma_load_4d(dst, map, 0, c2.tok0, 0, which == 2 ? hv2 : hv2 / P.G, bar);
+    };
+    // this thread's chunks of a landed tile: 16-bit input -> fp16 in place; rows past len and columns past nc
+    // become zero (the box also covers the next sequence's rows and, for K or V < 128, leaves columns unset)
+    auto convert_raw = [&](unsigned char *dst, int len_, int nc) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = tid + K4T_THREADS * i, cb = e >> 6, r = e & (CT - 1);
+            uint4 *p = reinterpret_cast<uint4 *>(dst + cb * (CT * 16) + r * 16);
+            if (r < len_ && 8 * cb < nc) {
+                if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+                    Raw8<Tin> x;
+                    x.v = *p;
+                    float f[8];
+                    raw_get(x, f);
+                    *p = pack8_half(f);
+                }
+            } else {
+                *p = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    };
+    // fp32 inputs: staged straight into the column-block-major tile (rows past len, columns past nc zero)
+    auto stage_f32 = [&](int it, int which, unsigned char *dst) {
         const Tin *src;
         size_t st;
         int nc, ln;
         input_src(it, which, src, st, nc, ln);
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int c = wid + (K4T_THREADS / 32) * i;
-            const int r = 8 * (c >> 2) + (lane & 7), c8 = 8 * (4 * (c & 3) + (lane >> 3));
-            const bool ok = r < ln && c8 + 8 <= nc;
-            cp_async16_zfill(dst + tc::tile_off(r, c8, DT), ok ? src + (size_t)r * st + c8 : src, ok ? 16 : 0);
-        }
-        cp_async_commit();
-    };
-    auto convert_raw = [&](unsigned char *dst) {  // this thread's chunks: bf16 bits -> fp16 (fp16 stays)
-        if constexpr (kRaw && !std::is_same<Tin, __half>::value) {
-#pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int c = wid + (K4T_THREADS / 32) * i;
-                const int r = 8 * (c >> 2) + (lane & 7), c8 = 8 * (4 * (c & 3) + (lane >> 3));
-                uint4 *p = reinterpret_cast<uint4 *>(dst + tc::tile_off(r, c8, DT));
-                Raw8<Tin> x;
-                x.v = *p;
-                float f[8];
-                raw_get(x, f);
-                *p = pack8_half(f);
-            }
+            const int e = tid + K4T_THREADS * i, cb = e >> 6, r = e & (CT - 1);
+            float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (r < ln && 8 * cb < nc) load8(reinterpret_cast<const float *>(src) + (size_t)r * st + 8 * cb, f);
+            *reinterpret_cast<uint4 *>(dst + cb * (CT * 16) + r * 16) = pack8_half(f);
         }
     };
 
@@ -214,17 +244,18 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         issue_ws1(item);
         issue_ws2(item);
     }
-    if (kRaw) {
+    if (kRaw && tid == 0) {
         fetch_raw(item, 0, S.K);
         fetch_raw(item, 1, S.Q);
         fetch_raw(item, 2, S.V);
     }
-    uint32_t lpar = 0, tpar = 0, mpar = 0, mpar2 = 0;
+    uint32_t lpar = 0, tpar = 0, mpar = 0, mpar2 = 0, kpar = 0, qpar = 0, vpar = 0;
     bool lost = false, okq = true;
     // Barrier phases this thread has not yet seen complete: loads armed and not waited for (the same for every
     // thread: the arming points are passed by all), and MMA commits whose wait gave up.  A wait that gives up
     // leaves its parity unflipped; the exit drains every pending phase before the CTA releases its memory.
     bool l_pend = true, t_pend = true, m_pend = false, m2_pend = false;
+    bool k_pend = kRaw, q_pend = kRaw, v_pend = kRaw;  // tensor-map loads of the raw input rows
     // Each phase: the issuers issue group 1 (committed to bar) and, in phases 1 and 2, group 2 (committed to
     // bar2); every thread waits (bounded) for group 1 itself, and the outcomes of all waits since the last
     // agreement are agreed at the next block-wide barrier (publish_tiles or the end of the item); the
@@ -292,19 +323,17 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         const int pb = ((item - (int)blockIdx.x) / (int)gridDim.x) & 1;
 
         // ---- inputs as fp16 tiles (the workspace tiles are on their way by bulk copy)
-        if constexpr (kRaw) {
-            cp_async_wait<0>();
-            convert_raw(S.K);
-            convert_raw(S.V);  // (Q, first read in phase 2, is converted while phase 1 runs)
+        if constexpr (kRaw) {  // (Q, first read in phase 2, is converted while phase 1 runs)
+            const bool okk = tc::mbar_wait(&S.kbar, kpar, P.spin), okv = tc::mbar_wait(&S.vbar, vpar, P.spin);
+            if (okk) kpar ^= 1u, k_pend = false;
+            if (okv) vpar ^= 1u, v_pend = false;
+            okq &= okk && okv;  // agreed at the barrier below
+            convert_raw(S.K, len, P.K);
+            convert_raw(S.V, len, P.V);
         } else {
-            unsigned char *const dst[3] = {S.K, S.Q, S.V};
-            const Tin *src[3];
-            size_t st[3];
-            int nc[3], ln;
-            for (int w = 0; w < 3; ++w) input_src(item, w, src[w], st[w], nc[w], ln);
-            const Tin *const srcc[3] = {src[0], src[1], src[2]};
-            const float mul[3] = {1.f, 1.f, 1.f};
-            stage_ct_n<Tin, K4T_THREADS, 3>(dst, srcc, st, nc, mul, len, tid);
+            stage_f32(item, 0, S.K);
+            stage_f32(item, 1, S.Q);
+            stage_f32(item, 2, S.V);
         }
         // every thread waits for the workspace tiles itself (the epilogues read some of them directly); the
         // per-token record came with them
@@ -322,14 +351,19 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         // ---------------- phase 1
         if (iss1) {
             if (!fail) {
-                if (slot == 0) tc::gemm(tm + R_KT, sK, DT, true, sI, CT, false, 128, 64, CT, false);
+                if (slot == 0) tc::gemm_ops(tm + R_KT, tc::op_cols(sK, CT, true), tc::op_rows(sI, CT, false), 128, 64, CT, false);
                 else if (slot == 1) tc::gemm(tm + R_DWT, sH, DT, true, sdVn, CT, true, 128, 64, DT, false);
                 else if (slot == 2) tc::gemm(tm + R_DKSC, sdH, DT, true, sVn, CT, true, 128, 64, DT, false);
                 else tc::gemm(tm + R_TDU, sdVn, CT, false, sT, CT, true, 128, 64, CT, false);
             }
             tc::commit(&S.bar);
         }
-        convert_raw(S.Q);  // published to phase 2 by the tile barrier after the first epilogue
+        if constexpr (kRaw) {  // published to phase 2 by the tile barrier after the first epilogue
+            const bool okq2 = tc::mbar_wait(&S.qbar, qpar, P.spin);
+            if (okq2) qpar ^= 1u, q_pend = false;
+            okq &= okq2;
+            convert_raw(S.Q, len, P.K);
+        }
         if (tid < CT) {
             reduce_pending();  // the previous item's sums, while phase 1 runs
             // the record into the arrays the later epilogues read (the first reads it in place; the next
@@ -343,7 +377,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (iss2) {  // group 2 once group 1 is done: it runs during group 1's epilogue
             if (!fail) {
                 if (slot == 0) tc::gemm(tm + C_G1, sD, DT, false, sVn, CT, true, 64, 64, DT, false);
-                else if (slot == 1) tc::gemm(tm + C_DT2, sdVn, CT, true, sV, DT, false, 64, 64, DT, false);
+                else if (slot == 1) tc::gemm_ops(tm + C_DT2, tc::op_rows(sdVn, CT, true), tc::op_cols(sV, CT, false), 64, 64, DT, false);
                 else if (slot == 2) tc::gemm(tm + R_DQI, sH, DT, true, sD, DT, false, 128, 64, DT, false);
             }
             tc::commit(&S.bar2);
@@ -429,8 +463,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 
         // ---------------- phase 2
         if (iss1) {
-            if (slot == 0) tc::gemm(tm + R_QT, sQ, DT, true, sI, CT, false, 128, 64, CT, false);
-            else if (slot == 1) tc::gemm(tm + R_DQA, sK, DT, true, sPm, CT, false, 128, 64, CT, false);
+            if (slot == 0) tc::gemm_ops(tm + R_QT, tc::op_cols(sQ, CT, true), tc::op_rows(sI, CT, false), 128, 64, CT, false);
+            else if (slot == 1) tc::gemm_ops(tm + R_DQA, tc::op_cols(sK, CT, true), tc::op_rows(sPm, CT, false), 128, 64, CT, false);
             tc::commit(&S.bar);
         }
         // S_0, dS_next, D, V_new^T, -dV_new^T and V are not read again in this item (after the MMA issue, so
@@ -438,13 +472,16 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (has_next) {
             if (loader) issue_ws1(next);
             l_pend = true;
-            if (kRaw) fetch_raw(next, 2, S.V);
+            if (kRaw) {
+                if (loader) fetch_raw(next, 2, S.V);
+                v_pend = true;
+            }
         }
         finish_phase(false);
         if (iss2) {
-            if (slot == 0) tc::gemm(tm + R_DKO, sQ, DT, true, sPm, CT, true, 128, 64, CT, false);
+            if (slot == 0) tc::gemm_ops(tm + R_DKO, tc::op_cols(sQ, CT, true), tc::op_rows(sPm, CT, true), 128, 64, CT, false);
             else if (slot == 1) tc::gemm(tm + R_TDW, sdWT, CT, false, sT, CT, true, 128, 64, CT, false);
-            else if (slot == 2) tc::gemm(tm + C_DT1, sdWT, CT, true, sK, DT, false, 64, 64, DT, false);
+            else if (slot == 2) tc::gemm_ops(tm + C_DT1, tc::op_rows(sdWT, CT, true), tc::op_cols(sK, CT, false), 64, 64, DT, false);
             tc::commit(&S.bar2);
         }
         bool ok2;
@@ -530,10 +567,13 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         // ---------------- phase 3: X = dT T^T
         if (iss1) {
             if (slot == 0) tc::gemm(tm + C_X, sdT, CT, false, sT, CT, false, 64, 64, CT, false);
-            else if (slot == 1) tc::gemm(tm + C_KK, sK, DT, false, sK, DT, false, 64, 64, DT, false);
+            else if (slot == 1) tc::gemm_ops(tm + C_KK, tc::op_cols(sK, CT, false), tc::op_cols(sK, CT, false), 64, 64, DT, false);
             tc::commit(&S.bar);
         }
-        if (has_next && kRaw) fetch_raw(next, 1, S.Q);  // Q is not read again in this item
+        if (has_next && kRaw) {  // Q is not read again in this item
+            if (loader) fetch_raw(next, 1, S.Q);
+            q_pend = true;
+        }
         finish_phase(false);
         {
             float a[16];
@@ -586,12 +626,15 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
 
         // ---------------- phase 5: dk_Ar^T = K^T E^T (+), dk_Ac^T = K^T E (-)
         if (iss1) {
-            if (slot == 0) tc::gemm(tm + R_DKAR, sK, DT, true, sE, CT, false, 128, 64, CT, false);
-            else if (slot == 1) tc::gemm(tm + R_DKAC, sK, DT, true, sE, CT, true, 128, 64, CT, false);
+            if (slot == 0) tc::gemm_ops(tm + R_DKAR, tc::op_cols(sK, CT, true), tc::op_rows(sE, CT, false), 128, 64, CT, false);
+            else if (slot == 1) tc::gemm_ops(tm + R_DKAC, tc::op_cols(sK, CT, true), tc::op_rows(sE, CT, true), 128, 64, CT, false);
             tc::commit(&S.bar);
         }
         finish_phase(false);
-        if (has_next && kRaw) fetch_raw(next, 0, S.K);  // K is not read again in this item
+        if (has_next && kRaw) {  // K is not read again in this item
+            if (loader) fetch_raw(next, 0, S.K);
+            k_pend = true;
+        }
         {
             float a[16], b[16];
             tc::ld16x2(tc::taddr(tm, R_DKAR + c0), a, tc::taddr(tm, R_DKAC + c0), b);
@@ -631,8 +674,10 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         if (m2_pend) tc::mbar_wait(&S.bar2, mpar2, DRAIN_LIMIT);
         if (l_pend) tc::mbar_wait(&S.lbar, lpar, DRAIN_LIMIT);
         if (t_pend) tc::mbar_wait(&S.tbar, tpar, DRAIN_LIMIT);
+        if (k_pend) tc::mbar_wait(&S.kbar, kpar, DRAIN_LIMIT);
+        if (q_pend) tc::mbar_wait(&S.qbar, qpar, DRAIN_LIMIT);
+        if (v_pend) tc::mbar_wait(&S.vbar, vpar, DRAIN_LIMIT);
     }
-    cp_async_wait<0>();  // no copy of this thread may still be landing when the CTA exits
     tc::fence_before();
     __syncthreads();
     if (wid == 0) {
@@ -640,6 +685,39 @@ __global__ void __launch_bounds__(K4T_THREADS, 1) k4_intra_grad_tc(const Params 
         tc::tmem_dealloc(tm, K4T_TMEM_COLS);
     }
 }
+
+namespace {
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The 4-D map of a 16-bit input [tokens][heads][cols]: dimensions (8-element chunk, token, column block, head)
+// with byte strides (heads cols 2, 16, cols 2), box (8, 64, cols / 8, 1): one box is a chunk's rows of one
+// head, landing as a column-block-major core-matrix tile.  Rows past the tensor's end read as zero.
+cudaError_t encode_rows_map(CUtensorMap *map, const void *base, int dtype, long long tokens, int heads, int cols) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[4] = {8, (cuuint64_t)tokens, (cuuint64_t)(cols / 8), (cuuint64_t)heads};
+    const cuuint64_t strides[3] = {(cuuint64_t)heads * cols * 2, 16, (cuuint64_t)cols * 2};
+    const cuuint32_t box[4] = {8, (cuuint32_t)CT, (cuuint32_t)(cols / 8), 1};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, dtype == BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                           const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+}  // namespace
 
 template <typename Tin>
 static cudaError_t launch_k4_tc_t(const Params &P, cudaStream_t stream) {
@@ -650,8 +728,18 @@ static cudaError_t launch_k4_tc_t(const Params &P, cudaStream_t stream) {
     if ((e = device_sm_count(&nsm)) != cudaSuccess) return e;
     const long items = (long)P.max_chunks * P.Hv;
     if (items == 0) return cudaSuccess;
+    CUtensorMap mk, mq, mv;
+    memset(&mk, 0, sizeof(mk));
+    memset(&mq, 0, sizeof(mq));
+    memset(&mv, 0, sizeof(mv));
+    if (sizeof(Tin) == 2) {
+        const long long tokens = (long long)P.B * P.T;
+        if ((e = encode_rows_map(&mk, P.k, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
+        if ((e = encode_rows_map(&mq, P.q, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
+        if ((e = encode_rows_map(&mv, P.v, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
+    }
     const int grid = (int)(items < nsm ? items : nsm);  // one persistent CTA per SM
-    k4_intra_grad_tc<Tin><<<grid, K4T_THREADS, smem, stream>>>(P);
+    k4_intra_grad_tc<Tin><<<grid, K4T_THREADS, smem, stream>>>(P, mk, mq, mv);
     return cudaGetLastError();
 }
 

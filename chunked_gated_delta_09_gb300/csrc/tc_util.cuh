@@ -68,6 +68,47 @@ __device__ __forceinline__ void gemm(uint32_t d_tmem, uint32_t a_tile, int a_C, 
             (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// An MMA operand: its descriptor at reduction step 0, the descriptor advance per 16-element reduction step
+// (in the 16-byte units of the start-address field) and whether it is read MN-major.
+struct Operand {
+    uint64_t desc;
+    uint32_t step;
+    bool mn;
+};
+
+// Operand of a row-block-major tile with C columns (core matrix (r/8, c/8) at ((r/8)(C/8) + c/8) * 128; the
+// workspace tiles): as desc_k / desc_mn.
+__device__ __forceinline__ Operand op_rows(uint32_t tile, int C, bool mn) {
+    return mn ? Operand{desc_mn(tile, C, 0), (uint32_t)(2 * (C >> 3) * 128 / 16), true}
+              : Operand{desc_k(tile, C, 0), 256u / 16u, false};
+}
+// Operand of a column-block-major tile with R rows (core matrix (r/8, c/8) at ((c/8)(R/8) + r/8) * 128: the
+// layout a TMA box of 8-element rows lands in).  K-major view: the next core matrix along the reduction (the
+// columns) is (R/8) * 128 bytes on, the next along the rows 128; MN-major view: the reduction runs along the
+// rows (128 bytes per core matrix) and the operand rows along the columns ((R/8) * 128 bytes).
+__device__ __forceinline__ Operand op_cols(uint32_t tile, int R, bool mn) {
+    const uint32_t cb = (uint32_t)(R >> 3) * 128u;
+    return mn ? Operand{smem_desc(tile, 128, cb), 256u / 16u, true} : Operand{smem_desc(tile, cb, 128), 2u * cb / 16u, false};
+}
+
+// D[M x N] (+)= A[M x Kr] B[N x Kr]^T for operands of either tile order.
+__device__ __forceinline__ void gemm_ops(uint32_t d_tmem, Operand a, Operand b, int M, int N, int Kr, bool accumulate) {
+    const uint32_t id = idesc_f16(M, N, a.mn, b.mn);
+    for (int kk = 0; kk < Kr / 16; ++kk)
+        mma(d_tmem, a.desc + (uint64_t)(kk * a.step), b.desc + (uint64_t)(kk * b.step), id,
+            (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// ---- tensor-map (TMA) loads: a 4-D box of the global tensor described by `map` (a kernel parameter) at
+// the given coordinates (innermost first) into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *map, int x0, int x1, int x2, int x3, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x0), "r"(x1), "r"(x2), "r"(x3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
         smem_u32(bar)));
