@@ -29,6 +29,10 @@ SMALL = {
     "k128_v64_gqa4": dict(B=1, T=129, Hk=1, Hv=4, K=128, V=64),
     "strong_decay": dict(B=1, T=256, Hk=1, Hv=2, K=128, V=128, g_shift=-3.0),
     "weak_decay": dict(B=1, T=256, Hk=1, Hv=2, K=128, V=128, g_shift=4.0),
+    # per-channel gate with strong decay: chunk-wide cumulative gates far below the fp32 exponent range, so
+    # any decay factor formed as a ratio of cumulative gates (rather than a difference inside one exp) would
+    # overflow or lose the result
+    "kda_strong_decay": dict(B=1, T=256, Hk=1, Hv=2, K=128, V=128, per_channel=True, g_shift=-3.0),
     "beta_zero": dict(B=1, T=128, Hk=1, Hv=1, K=64, V=64, beta_zero=True),
     "gate_zero": dict(B=1, T=128, Hk=1, Hv=1, K=64, V=64, gate_zero=True),
 }
