@@ -2,6 +2,8 @@
 //   K0 chunk bookkeeping (varlen) -> K1 WY prep -> K2 state recompute -> K3 state-gradient scan
 //   -> K4 per-chunk gradients -> K5 gate reverse cumsum + GQA reduction
 // all queued on the caller's stream.  No device memory is allocated here.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -72,6 +74,38 @@ cudaError_t smem_opt_in(const void *kernel, size_t bytes) {
         g_attr_set[kernel] |= bit;
     }
     return cudaSuccess;
+}
+
+namespace {
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+}  // namespace
+
+// byte strides (heads cols 2, 16, cols 2) for the dimensions (token, column block, head); the innermost
+// dimension is the 8 contiguous elements of a column block
+cudaError_t encode_rows_map(CUtensorMap *map, const void *base, int dtype, long long tokens, int heads, int cols) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[4] = {8, (cuuint64_t)tokens, (cuuint64_t)(cols / 8), (cuuint64_t)heads};
+    const cuuint64_t strides[3] = {(cuuint64_t)heads * cols * 2, 16, (cuuint64_t)cols * 2};
+    const cuuint32_t box[4] = {8, (cuuint32_t)CT, (cuuint32_t)(cols / 8), 1};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, dtype == BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                           const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace gdr

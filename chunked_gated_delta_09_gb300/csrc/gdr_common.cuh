@@ -327,6 +327,16 @@ __device__ __forceinline__ void warp_mma(float (&acc)[MT][NT][4], const __half *
 __device__ __forceinline__ uint32_t ctile_off(int r, int c, int C) {
     return (uint32_t)((r >> 3) * (C >> 3) * 128 + (c >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
 }
+// Byte offset of element (r, c) in a column-block-major core-matrix tile with R rows: block (r/8, c/8) at
+// ((c/8) (R/8) + r/8) 128 (the layout a tensor-map box of 8-element rows lands in).
+__device__ __forceinline__ uint32_t cbtile_off(int r, int c, int R) {
+    return (uint32_t)((c >> 3) * (R >> 3) * 128 + (r >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
+}
+// Either block order: D is the column count of a row-block-major tile (CB = false) or the row count of a
+// column-block-major one (CB = true).
+template <bool CB> __device__ __forceinline__ uint32_t tile_at(int r, int c, int D) {
+    return CB ? cbtile_off(r, c, D) : ctile_off(r, c, D);
+}
 __device__ __forceinline__ float ctile_get(const unsigned char *t, int r, int c, int C) {
     return __half2float(*reinterpret_cast<const __half *>(t + ctile_off(r, c, C)));
 }
@@ -334,12 +344,27 @@ __device__ __forceinline__ void ctile_set(unsigned char *t, int r, int c, int C,
     *reinterpret_cast<__half *>(t + ctile_off(r, c, C)) = __float2half_rn(x);
 }
 
+// m16n8k16 with bf16 operands (BF) or fp16 operands, fp32 accumulators
+template <bool BF>
+__device__ __forceinline__ void mma16816t(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (BF)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        mma16816(c, a, b0, b1);
+}
+
 // warp_mma on core-matrix tiles (each 8 x 8 ldmatrix block is one contiguous core matrix):
-//   A(m, k) = tile element (m, k) of a tile with A_C columns (AT = false) or (k, m) (AT = true);
-//   B(k, n) = tile element (k, n) (BT = false) or (n, k) (BT = true).
-template <int MT, int NT, bool AT, bool BT>
-__device__ __forceinline__ void warp_mma_ct(float (&acc)[MT][NT][4], const unsigned char *A, int A_C,
-                                            const unsigned char *B, int B_C, int m0, int n0, int kdim) {
+//   A(m, k) = tile element (m, k) (AT = false) or (k, m) (AT = true);
+//   B(k, n) = tile element (k, n) (BT = false) or (n, k) (BT = true);
+// ACB / BCB: the tile is column-block-major (A_D / B_D its row count) rather than row-block-major (A_D / B_D
+// its column count); BF: both tiles hold bf16 rather than fp16.
+template <int MT, int NT, bool AT, bool BT, bool ACB = false, bool BCB = false, bool BF = false>
+__device__ __forceinline__ void warp_mma_ct(float (&acc)[MT][NT][4], const unsigned char *A, int A_D,
+                                            const unsigned char *B, int B_D, int m0, int n0, int kdim) {
     const int lane = threadIdx.x & 31;
     const int r8 = lane & 7, mat = lane >> 3;
     for (int k0 = 0; k0 < kdim; k0 += 16) {
@@ -347,19 +372,19 @@ __device__ __forceinline__ void warp_mma_ct(float (&acc)[MT][NT][4], const unsig
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             int mb = m0 + mt * 16;
-            if (!AT) ldsm_x4(a[mt], A + ctile_off(mb + (lane & 15), k0 + (lane >> 4) * 8, A_C));
-            else ldsm_x4_t(a[mt], A + ctile_off(k0 + r8 + (mat >> 1) * 8, mb + (mat & 1) * 8, A_C));
+            if (!AT) ldsm_x4(a[mt], A + tile_at<ACB>(mb + (lane & 15), k0 + (lane >> 4) * 8, A_D));
+            else ldsm_x4_t(a[mt], A + tile_at<ACB>(k0 + r8 + (mat >> 1) * 8, mb + (mat & 1) * 8, A_D));
         }
 #pragma unroll
         for (int nt = 0; nt + 1 < NT; nt += 2) {
             int nb = n0 + nt * 8;
             uint32_t b[4];
-            if (BT) ldsm_x4(b, B + ctile_off(nb + r8 + (mat >> 1) * 8, k0 + (mat & 1) * 8, B_C));
-            else ldsm_x4_t(b, B + ctile_off(k0 + r8 + (mat & 1) * 8, nb + (mat >> 1) * 8, B_C));
+            if (BT) ldsm_x4(b, B + tile_at<BCB>(nb + r8 + (mat >> 1) * 8, k0 + (mat & 1) * 8, B_D));
+            else ldsm_x4_t(b, B + tile_at<BCB>(k0 + r8 + (mat & 1) * 8, nb + (mat >> 1) * 8, B_D));
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                mma16816(acc[mt][nt], a[mt], b[0], b[1]);
-                mma16816(acc[mt][nt + 1], a[mt], b[2], b[3]);
+                mma16816t<BF>(acc[mt][nt], a[mt], b[0], b[1]);
+                mma16816t<BF>(acc[mt][nt + 1], a[mt], b[2], b[3]);
             }
         }
         if (NT & 1) {
@@ -367,10 +392,10 @@ __device__ __forceinline__ void warp_mma_ct(float (&acc)[MT][NT][4], const unsig
             int nb = n0 + nt * 8;
             int m2 = (lane >> 3) & 1;
             uint32_t b[2];
-            if (BT) ldsm_x2(b, B + ctile_off(nb + r8, k0 + m2 * 8, B_C));
-            else ldsm_x2_t(b, B + ctile_off(k0 + r8 + m2 * 8, nb, B_C));
+            if (BT) ldsm_x2(b, B + tile_at<BCB>(nb + r8, k0 + m2 * 8, B_D));
+            else ldsm_x2_t(b, B + tile_at<BCB>(k0 + r8 + m2 * 8, nb, B_D));
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt][nt], a[mt], b[0], b[1]);
+            for (int mt = 0; mt < MT; ++mt) mma16816t<BF>(acc[mt][nt], a[mt], b[0], b[1]);
         }
     }
 }

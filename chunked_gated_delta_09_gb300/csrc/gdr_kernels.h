@@ -1,6 +1,7 @@
 // gdr_kernels.h -- host-side launchers of the backward kernels (internal to libgdrbwd.so).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -13,6 +14,11 @@ struct Params;
 cudaError_t smem_opt_in(const void *kernel, size_t bytes);
 // Streaming-multiprocessor count of the current device (queried once per device).
 cudaError_t device_sm_count(int *out);
+// Tensor map of a 16-bit input [tokens][heads][cols] (dtype BF16 or F16) for loads of a chunk's rows of one
+// head: 4-D over (8-element column chunk, token, column block, head), box (8, 64, cols / 8, 1), so that one
+// box lands as a column-block-major core-matrix tile (core matrix (r/8, c/8) at ((c/8) 8 + r/8) 128 bytes).
+// Rows past the tensor's end read as zero.  cols must be a multiple of 8 and base 16-byte aligned.
+cudaError_t encode_rows_map(CUtensorMap *map, const void *base, int dtype, long long tokens, int heads, int cols);
 
 // K0: varlen chunk bookkeeping (one block).  expect_total_tokens < 0 skips the cu[N] == T check.
 cudaError_t launch_k0(const int32_t *cu, int N, int BT, int max_chunks, int expect_total_tokens, int32_t *chunk_idx,

@@ -11,13 +11,18 @@
 // K~ = K (.) exp(gamma_C - gamma) and Q~ = Q (.) exp(gamma) that the two scans use, and D = scale dO.
 // Per-channel gate: each exp(gamma_a - gamma_b) is taken per key channel inside the K contraction.  For the
 // scalar gate's backward it also writes each unit's per-token record (beta, exp(gamma), exp(gamma_C - gamma),
-// gamma) that the per-chunk gradient kernel fetches whole.  16-bit input rows arrive by bulk copy (one row
-// per thread) and are rearranged in place into the core-matrix tiles.
+// gamma) that the per-chunk gradient kernel fetches whole.  16-bit input rows arrive by tensor-map loads, one
+// per input, as column-block-major core-matrix tiles in their own type: the key Gram and Aqk products take them
+// as they are (bf16 or fp16 operands), and the element-wise pass that forms the decayed copies reads them there.
 //
 // Every matrix output is written in the core-matrix tile layout that the tensor-core kernels read,
 // straight from registers: 8 lanes of an element-wise pass write one contiguous 128-byte core matrix, and
 // a warp's pair stores of an MMA accumulator cover whole core matrices (no store waits at the end of a
 // CTA, so the next CTA on the SM starts at once).  The forward pass runs the same kernel without dO.
+#include <string.h>
+
+#include <type_traits>
+
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
 #include "tc_util.cuh"
@@ -29,10 +34,15 @@ constexpr int GKLD = DT + 4;  // row stride of the per-channel cumulative gate i
                               // apart in bank terms, so a quarter-warp's 16-byte row reads do not collide)
 
 // 8 consecutive fp16 values of a core-matrix tile row segment / 8 fp32 values (16-byte aligned) as floats
-__device__ __forceinline__ void ld8h(const unsigned char *p, float (&x)[8]) {
-    Raw8<__half> r;
+template <typename TT> __device__ __forceinline__ void ld8t(const unsigned char *p, float (&x)[8]) {
+    Raw8<TT> r;
     r.v = *reinterpret_cast<const uint4 *>(p);
     raw_get(r, x);
+}
+// two consecutive 16-bit values as floats
+__device__ __forceinline__ float2 ld2t(const __half *p) { return __half22float2(*reinterpret_cast<const __half2 *>(p)); }
+__device__ __forceinline__ float2 ld2t(const __nv_bfloat16 *p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
 }
 __device__ __forceinline__ void ld8f(const float *p, float (&x)[8]) {
     const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
@@ -40,9 +50,10 @@ __device__ __forceinline__ void ld8f(const float *p, float (&x)[8]) {
 }
 
 struct __align__(1024) K1Smem {
-    // Ks holds K, then (once the decayed copies are written) T as the fp16 operand of the W and U products
-    // and the scratch of the inverse's block products; Qs later holds beta Gamma K, Vs beta V.  AT holds the
-    // raw dO rows on their way to the D tile, then A_kk, then in place its inverse T (fp32).
+    // Ks, Qs, Vs: the chunk's K, Q, V rows as column-block-major core-matrix tiles (bf16 for bf16 inputs, fp16
+    // otherwise).  Ks later holds T as the fp16 operand of the W and U products (row-block-major) and the
+    // scratch of the inverse's block products; Qs later holds beta Gamma K and Vs beta V (fp16, in place).  AT
+    // holds the raw dO rows on their way to the D tile, then A_kk, then in place its inverse T (fp32).
     unsigned char Ks[CT * DT * 2], Qs[CT * DT * 2], Vs[CT * DT * 2];
     float AT[CT][CT + 1];
     float gam[CT];
@@ -91,8 +102,15 @@ __device__ __forceinline__ void inv_level(const float (&A)[CT][CT + 1], float (&
     __syncthreads();
 }
 
+// The tensor maps (16-bit inputs only; unused for fp32) describe k, q (key heads) and v, dO (value heads) as
+// encode_rows_map does.
 template <typename Tin, bool PC>
-__global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Params P) {
+__global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
+    k1_wy_prep(const Params P, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
+               const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo) {
+    // element type of the staged input tiles and of the key Gram / Aqk products
+    using TT = typename std::conditional<std::is_same<Tin, __nv_bfloat16>::value, __nv_bfloat16, __half>::type;
+    constexpr bool kBF = std::is_same<Tin, __nv_bfloat16>::value;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     K1Smem &S = *reinterpret_cast<K1Smem *>(smem_raw);
     float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K1Smem));  // [CT][GKLD], per-channel only
@@ -117,93 +135,74 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
         if (2 * lane < len) gx0 = P.g[(size_t)(ci.tok0 + 2 * lane) * P.Hv + hv];
         if (2 * lane + 1 < len) gx1 = P.g[(size_t)(ci.tok0 + 2 * lane + 1) * P.Hv + hv];
     }
+    const int nin = P.dO ? 4 : 3;
+    unsigned char *const slot[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(&S.AT[0][0])};
+    const int nc[4] = {P.K, P.K, P.V, P.V};
+    bool bad = false;  // an input value that the fp16 operand tiles cannot hold
     if constexpr (sizeof(Tin) == 2) {
-        // The chunk's raw rows, row-major at a 256-byte pitch, by bulk copy into the tile slots (dO into the
-        // A / T buffer, not yet in use): thread t copies row t % 64 of input t / 64, all on one mbarrier that
-        // thread 0 arms with the total before anyone issues.  Each tile is then read row-major and, after a
-        // barrier, written back in place as the fp16 core-matrix tile (dO, scaled, to its workspace tile).
-        const int nin = P.dO ? 4 : 3;
-        unsigned char *const slot[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(&S.AT[0][0])};
-        const Tin *const src[4] = {kp, qp, vp, dop};
-        const size_t st[4] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V, (size_t)P.Hv * P.V};
-        const int nc[4] = {P.K, P.K, P.V, P.V};
+        // one tensor-map load per input (k, q, v, and dO into the A / T buffer, not yet in use), on one mbarrier
         if (tid == 0) {
             tc::mbar_init(&S.rbar, 1);
             asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-            tc::mbar_expect_tx(&S.rbar, (uint32_t)(len * (2 * P.K + (nin - 2) * P.V) * 2));
         }
         __syncthreads();
-        {
-            const int w = tid / CT, r = tid % CT;
-            unsigned char *const dst = w == 0 ? S.Ks : w == 1 ? S.Qs : w == 2 ? S.Vs : slot[3];
-            const Tin *const sp = w == 0 ? kp : w == 1 ? qp : w == 2 ? vp : dop;
-            const size_t sst = w < 2 ? (size_t)P.Hk * P.K : (size_t)P.Hv * P.V;
-            const int snc = w < 2 ? P.K : P.V;
-            if (w < nin && r < len) tc::bulk_g2s(dst + r * DT * 2, sp + (size_t)r * sst, (uint32_t)(snc * 2), &S.rbar);
+        if (tid == 0) {
+            tc::mbar_expect_tx(&S.rbar, (uint32_t)((2 * (P.K >> 3) + (nin - 2) * (P.V >> 3)) * CT * 16));
+            tc::tma_load_4d(S.Ks, &tmk, 0, ci.tok0, 0, hk, &S.rbar);
+            tc::tma_load_4d(S.Qs, &tmq, 0, ci.tok0, 0, hk, &S.rbar);
+            tc::tma_load_4d(S.Vs, &tmv, 0, ci.tok0, 0, hv, &S.rbar);
+            if (P.dO) tc::tma_load_4d(slot[3], &tmo, 0, ci.tok0, 0, hv, &S.rbar);
         }
         const bool landed = tc::mbar_wait(&S.rbar, 0, P.spin);
         if (__syncthreads_or(!landed)) {
             if (tid == 0) {
                 flag_status(P.status, ST_TIMEOUT);
-                tc::mbar_wait(&S.rbar, 0, DRAIN_LIMIT);  // the rows still in flight land before the CTA exits
+                tc::mbar_wait(&S.rbar, 0, DRAIN_LIMIT);  // the tiles still in flight land before the CTA exits
             }
             return;
         }
-        constexpr int PER = CT * (DT / 8) / K1_THREADS;  // 16-byte chunks per thread and tile
-        bool bad = false;  // an input value that fp16 operands cannot hold
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            if (w >= nin) break;
-            // chunk g -> row r, column c8: a quarter-warp takes the 8 rows of one 8-row block at 8 different
-            // column chunks (conflict-free row-major reads and core-matrix writes)
-            uint4 raw[PER];
-#pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int g = tid + K1_THREADS * i, l8 = g & 7;
-                const int r = 8 * (g >> 7) + l8, c8 = 8 * ((((g & 127) >> 3) + l8) & 15);
-                raw[i] = *reinterpret_cast<const uint4 *>(slot[w] + r * DT * 2 + c8 * 2);
-            }
-            if (w < 3) __syncthreads();  // every chunk of this tile read before the in-place writes
-#pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int g = tid + K1_THREADS * i, l8 = g & 7;
-                const int r = 8 * (g >> 7) + l8, c8 = 8 * ((((g & 127) >> 3) + l8) & 15);
-                const uint32_t off = ctile_off(r, c8, DT);
+        // a ragged chunk or narrow features: zero the rows past the chunk (the box also covers the next
+        // sequence's rows) and the column blocks the box left unset
+        if (len < CT || P.K < DT || P.V < DT) {
+            for (int w = 0; w < nin; ++w)
+                for (int e = tid; e < CT * DT / 8; e += K1_THREADS)
+                    if ((e & (CT - 1)) >= len || 8 * (e >> 6) >= nc[w])
+                        *reinterpret_cast<uint4 *>(slot[w] + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+            __syncthreads();
+        }
+        if (P.dO) {  // D = scale dO, straight from the landed tile to its (row-block-major) workspace tile
+            unsigned char *dg = reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT);
+            for (int e = tid; e < CT * DT / 8; e += K1_THREADS) {
+                const int r = e & (CT - 1), c8 = 8 * (e >> 6);
                 float f[8];
-                if (r < len && c8 < nc[w]) {
-                    Raw8<Tin> x;
-                    x.v = raw[i];
-                    raw_get(x, f);
-                } else {
+                ld8t<TT>(slot[3] + e * 16, f);
+                bad |= out_of_f16(f);
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) f[t] = 0.f;
-                }
+                for (int t = 0; t < 8; ++t) f[t] *= P.scale;
+                *reinterpret_cast<uint4 *>(dg + ctile_off(r, c8, DT)) = pack8_half(f);
+            }
+        }
+    } else {
+        // fp32 inputs: each 16-byte fp16 chunk of the column-block-major tiles from 8 input values (rows past
+        // the chunk and columns past K / V zero); D goes straight to its workspace tile
+        const float *const src[4] = {reinterpret_cast<const float *>(kp), reinterpret_cast<const float *>(qp),
+                                     reinterpret_cast<const float *>(vp), reinterpret_cast<const float *>(dop)};
+        const size_t st[4] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V, (size_t)P.Hv * P.V};
+        for (int w = 0; w < nin; ++w)
+            for (int e = tid; e < CT * DT / 8; e += K1_THREADS) {
+                const int r = e & (CT - 1), c8 = 8 * (e >> 6);
+                float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (r < len && c8 < nc[w]) load8(src[w] + (size_t)r * st[w] + c8, f);
+                bad |= out_of_f16(f);
                 if (w == 3) {
 #pragma unroll
                     for (int t = 0; t < 8; ++t) f[t] *= P.scale;
-                    *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT) + off) =
-                        pack8_half(f);
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT) +
+                                               ctile_off(r, c8, DT)) = pack8_half(f);
                 } else {
-                    *reinterpret_cast<uint4 *>(slot[w] + off) = pack8_half(f);
+                    *reinterpret_cast<uint4 *>(slot[w] + e * 16) = pack8_half(f);
                 }
-                bad |= out_of_f16(f);
             }
-        }
-        if (bad) flag_status(P.status, ST_RANGE);
-    } else if (P.dO) {  // backward: also D = scale dO, written straight to its workspace tile
-        unsigned char *const dst[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT)};
-        const Tin *const src[4] = {kp, qp, vp, dop};
-        const size_t st[4] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V, (size_t)P.Hv * P.V};
-        const int nc[4] = {P.K, P.K, P.V, P.V};
-        const float mul[4] = {1.f, 1.f, 1.f, P.scale};
-        stage_ct_n<Tin, K1_THREADS, 4>(dst, src, st, nc, mul, len, tid, P.status);
-    } else {     // forward: no output gradient
-        unsigned char *const dst[3] = {S.Ks, S.Qs, S.Vs};
-        const Tin *const src[3] = {kp, qp, vp};
-        const size_t st[3] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V};
-        const int nc[3] = {P.K, P.K, P.V};
-        const float mul[3] = {1.f, 1.f, 1.f};
-        stage_ct_n<Tin, K1_THREADS, 3>(dst, src, st, nc, mul, len, tid, P.status);
     }
 
     // ---- beta, gate cumsum
@@ -252,8 +251,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
         float kk[1][4][4], qk[1][4][4];
         zero_acc(kk);
         zero_acc(qk);
-        warp_mma_ct<1, 4, false, true>(kk, S.Ks, DT, S.Ks, DT, m0, n0, DT);
-        warp_mma_ct<1, 4, false, true>(qk, S.Qs, DT, S.Ks, DT, m0, n0, DT);
+        warp_mma_ct<1, 4, false, true, true, true, kBF>(kk, S.Ks, CT, S.Ks, CT, m0, n0, DT);
+        warp_mma_ct<1, 4, false, true, true, true, kBF>(qk, S.Qs, CT, S.Ks, CT, m0, n0, DT);
         unsigned char *aqk_g = reinterpret_cast<unsigned char *>(P.Aqk + u * CT * CT);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
@@ -308,9 +307,9 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                     float ki[2][8], qi[2][8], kj[2][8], gi[2][8], gj[2][8];
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        ld8h(S.Ks + ctile_off(i0 + r, c8, DT), ki[r]);
-                        ld8h(S.Qs + ctile_off(i0 + r, c8, DT), qi[r]);
-                        ld8h(S.Ks + ctile_off(j0 + r, c8, DT), kj[r]);
+                        ld8t<TT>(S.Ks + cbtile_off(i0 + r, c8, CT), ki[r]);
+                        ld8t<TT>(S.Qs + cbtile_off(i0 + r, c8, CT), qi[r]);
+                        ld8t<TT>(S.Ks + cbtile_off(j0 + r, c8, CT), kj[r]);
                         ld8f(gamK + (i0 + r) * GKLD + c8, gi[r]);
                         ld8f(gamK + (j0 + r) * GKLD + c8, gj[r]);
                     }
@@ -355,8 +354,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                         const float2 gr = *reinterpret_cast<const float2 *>(gamK + mid * GKLD + c);
                         const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
                         const float e0 = __expf(gx.x - gr.x), e1 = __expf(gx.y - gr.y);
-                        const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(S.Ks + ctile_off(row, c, DT)));
-                        const float2 qv = __half22float2(*reinterpret_cast<const __half2 *>(S.Qs + ctile_off(row, c, DT)));
+                        const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + cbtile_off(row, c, CT)));
+                        const float2 qv = ld2t(reinterpret_cast<const TT *>(S.Qs + cbtile_off(row, c, CT)));
                         ak[q] = pack_half2(kv.x * e0, kv.y * e1);
                         aq[q] = pack_half2(qv.x * e0, qv.y * e1);
                     }
@@ -365,7 +364,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                         const int row = 16 * blk + g4, c = k0 + kq + 8 * q;
                         const float2 gr = *reinterpret_cast<const float2 *>(gamK + mid * GKLD + c);
                         const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
-                        const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(S.Ks + ctile_off(row, c, DT)));
+                        const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + cbtile_off(row, c, CT)));
                         bk[q] = pack_half2(kv.x * __expf(gr.x - gx.x), kv.y * __expf(gr.y - gx.y));
                     }
                     mma16816(kk, ak, bk[0], bk[1]);
@@ -391,8 +390,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                     const float2 gr = *reinterpret_cast<const float2 *>(gamK + ref * GKLD + c);
                     const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
                     const float e0 = __expf(gx.x - gr.x), e1 = __expf(gx.y - gr.y);
-                    const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(S.Ks + ctile_off(row, c, DT)));
-                    const float2 qv = __half22float2(*reinterpret_cast<const __half2 *>(S.Qs + ctile_off(row, c, DT)));
+                    const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + cbtile_off(row, c, CT)));
+                    const float2 qv = ld2t(reinterpret_cast<const TT *>(S.Qs + cbtile_off(row, c, CT)));
                     const __half2 hk = __floats2half2_rn(kv.x * e0, kv.y * e1), hq = __floats2half2_rn(qv.x * e0, qv.y * e1);
                     ak[q] = *reinterpret_cast<const uint32_t *>(&hk);
                     aq[q] = *reinterpret_cast<const uint32_t *>(&hq);
@@ -406,7 +405,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
                         const int row = 16 * J + 8 * nt + g4, c = k0 + kq + 8 * q;
                         const float2 gr = *reinterpret_cast<const float2 *>(gamK + ref * GKLD + c);
                         const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
-                        const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(S.Ks + ctile_off(row, c, DT)));
+                        const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + cbtile_off(row, c, CT)));
                         const __half2 hb = __floats2half2_rn(kv.x * __expf(gr.x - gx.x), kv.y * __expf(gr.y - gx.y));
                         bk[nt][q] = *reinterpret_cast<const uint32_t *>(&hb);
                     }
@@ -444,20 +443,16 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
         unsigned char *Ktg = reinterpret_cast<unsigned char *>(P.Kt + u * CT * DT);
         unsigned char *Qgg = reinterpret_cast<unsigned char *>(P.Qg + u * CT * DT);
         for (int e = tid; e < CT * DT / 8; e += K1_THREADS) {
-            // one 16-byte core-matrix row segment; consecutive lanes walk the 8 rows of a core matrix
-            const int blk = e >> 3, i = 8 * (blk / (DT / 8)) + (e & 7), c8 = 8 * (blk % (DT / 8));
+            // one 16-byte core-matrix row segment (row i, columns c8 .. c8 + 7) at byte 16 e of the
+            // column-block-major tiles; consecutive lanes walk the 8 rows of a core matrix, which are also
+            // one contiguous core matrix of the row-block-major global tiles
+            const int i = e & (CT - 1), c8 = 8 * (e >> 6);
             const uint32_t off = ctile_off(i, c8, DT);
             float kx[8], qx[8], vx[8], o1[8], o2[8], o3[8], o4[8];
-            const __half2 *k2 = reinterpret_cast<const __half2 *>(S.Ks + off);
-            const __half2 *q2 = reinterpret_cast<const __half2 *>(S.Qs + off);
-            const __half2 *v2 = reinterpret_cast<const __half2 *>(S.Vs + off);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                float2 a = __half22float2(k2[t]), b = __half22float2(q2[t]), c = __half22float2(v2[t]);
-                kx[2 * t] = a.x; kx[2 * t + 1] = a.y;
-                qx[2 * t] = b.x; qx[2 * t + 1] = b.y;
-                vx[2 * t] = c.x; vx[2 * t + 1] = c.y;
-            }
+            ld8t<TT>(S.Ks + e * 16, kx);
+            ld8t<TT>(S.Qs + e * 16, qx);
+            ld8t<TT>(S.Vs + e * 16, vx);
+            if constexpr (sizeof(Tin) == 2) bad |= out_of_f16(kx) | out_of_f16(qx) | out_of_f16(vx);
             const float bi = S.beta[i];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
@@ -471,9 +466,10 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
             }
             *reinterpret_cast<uint4 *>(Ktg + off) = pack8_half(o1);
             *reinterpret_cast<uint4 *>(Qgg + off) = pack8_half(o2);
-            tc::st_tile8(S.Qs, i, c8, DT, o3);
-            tc::st_tile8(S.Vs, i, c8, DT, o4);
+            *reinterpret_cast<uint4 *>(S.Qs + e * 16) = pack8_half(o3);  // in place (fp16 from here on)
+            *reinterpret_cast<uint4 *>(S.Vs + e * 16) = pack8_half(o4);
         }
+        if (bad) flag_status(P.status, ST_RANGE);
     }
 
     // ---- T = (I + A_kk)^-1: diagonal 16x16 blocks by per-column forward substitution, then doubling
@@ -521,7 +517,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
         {
             const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 64;
             zero_acc(acc);
-            warp_mma_ct<1, 8, false, false>(acc, oT, CT, S.Qs, DT, m0, n0, CT);
+            warp_mma_ct<1, 8, false, false, false, true>(acc, oT, CT, S.Qs, CT, m0, n0, CT);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -534,7 +530,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3) k1_wy_prep(const Param
         {
             const int m0 = wid * 16;  // 8 warps x 16 value rows, all 64 chunk columns
             zero_acc(acc);
-            warp_mma_ct<1, 8, true, true>(acc, S.Vs, DT, oT, CT, m0, 0, CT);
+            warp_mma_ct<1, 8, true, true, true, false>(acc, S.Vs, CT, oT, CT, m0, 0, CT);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -552,8 +548,20 @@ static cudaError_t launch_k1_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(K1Smem) + (PC ? sizeof(float) * CT * GKLD : 0);
     cudaError_t e = smem_opt_in((const void *)k1_wy_prep<Tin, PC>, smem);
     if (e != cudaSuccess) return e;
+    CUtensorMap mk, mq, mv, mo;
+    memset(&mk, 0, sizeof(mk));
+    memset(&mq, 0, sizeof(mq));
+    memset(&mv, 0, sizeof(mv));
+    memset(&mo, 0, sizeof(mo));
+    if (sizeof(Tin) == 2) {
+        const long long tokens = (long long)P.B * P.T;
+        if ((e = encode_rows_map(&mk, P.k, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
+        if ((e = encode_rows_map(&mq, P.q, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
+        if ((e = encode_rows_map(&mv, P.v, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
+        if (P.dO && (e = encode_rows_map(&mo, P.dO, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
+    }
     dim3 grid(P.max_chunks, P.Hv);
-    k1_wy_prep<Tin, PC><<<grid, K1_THREADS, smem, stream>>>(P);
+    k1_wy_prep<Tin, PC><<<grid, K1_THREADS, smem, stream>>>(P, mk, mq, mv, mo);
     return cudaGetLastError();
 }
 

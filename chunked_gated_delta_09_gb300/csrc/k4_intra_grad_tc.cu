@@ -29,10 +29,6 @@
 // The WY part of dbeta, sum_k (T^T dW)_jk Gamma_j k_jk + sum_v (T^T dU)_jv v_jv, equals the column sum
 // sum_i T_ij (Gamma_j dT1_ij + dT2_ij) of two chunk x chunk products, so it is taken there.  The epilogues of
 // M = 64 products spread each row's 16 columns over both half-warps.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
 #include <type_traits>
 
 #include "gdr_common.cuh"
@@ -686,38 +682,6 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
     }
 }
 
-namespace {
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link against libcuda).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// The 4-D map of a 16-bit input [tokens][heads][cols]: dimensions (8-element chunk, token, column block, head)
-// with byte strides (heads cols 2, 16, cols 2), box (8, 64, cols / 8, 1): one box is a chunk's rows of one
-// head, landing as a column-block-major core-matrix tile.  Rows past the tensor's end read as zero.
-cudaError_t encode_rows_map(CUtensorMap *map, const void *base, int dtype, long long tokens, int heads, int cols) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[4] = {8, (cuuint64_t)tokens, (cuuint64_t)(cols / 8), (cuuint64_t)heads};
-    const cuuint64_t strides[3] = {(cuuint64_t)heads * cols * 2, 16, (cuuint64_t)cols * 2};
-    const cuuint32_t box[4] = {8, (cuuint32_t)CT, (cuuint32_t)(cols / 8), 1};
-    const cuuint32_t estride[4] = {1, 1, 1, 1};
-    const CUresult r = enc(map, dtype == BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
-                           const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-}  // namespace
 
 template <typename Tin>
 static cudaError_t launch_k4_tc_t(const Params &P, cudaStream_t stream) {
