@@ -61,43 +61,83 @@ struct __align__(1024) K1Smem {
     uint64_t rbar;  // 16-bit inputs: the raw rows' bulk copies
 };
 
-// One doubling level of the unit-lower-triangular inverse T = (I + A)^-1 held in fp32 shared memory:
-// for every diagonal pair of B x B blocks (lo, hi = lo + B), T[hi][lo] = -T[hi][hi] (A[hi][lo] T[lo][lo]),
-// with the B x B diagonal blocks of T already final.  2 (64 / (2B)) B^2 / 4 two-by-two output blocks.
-// A and T may be one array (T built in place over A): a level reads A only in the blocks it then overwrites.
-template <int B>
-__device__ __forceinline__ void inv_level(const float (&A)[CT][CT + 1], float (&T)[CT][CT + 1], float (&X)[32][33],
-                                          int tid) {
-    constexpr int NP = CT / (2 * B);        // block pairs
-    constexpr int QB = (B / 2) * (B / 2);   // 2 x 2 blocks per pair
-    constexpr int NQ = NP * QB;             // work items (<= K1_THREADS)
-    static_assert(NQ <= K1_THREADS && NP * B <= 32, "one 2 x 2 block per thread");
-    const bool act = tid < NQ;
-    const int p = tid / QB, m = tid % QB;
-    const int rr = 2 * (m / (B / 2)), cc = 2 * (m % (B / 2));
-    const int lo = 2 * B * p, hi = lo + B;
-    if (act) {  // X = A[hi][lo] T[lo][lo]   (stored at X[p B + r][c])
-        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+// TF32 rounding (round to nearest, ties away) of an fp32 value: the bit pattern the TF32 products take
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+    return r;
+}
+// c (16 x 8, fp32) += A (16 x 8) B (8 x 8) with TF32 operands.  Fragments (g = lane / 4, t = lane % 4):
+// a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4); b0 (t, g), b1 (t + 4, g); c as for m16n8k16.
+__device__ __forceinline__ void mma1688_tf32(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// The same product at about fp32 accuracy by the three-pass TF32 split (Ootomo and Yokota, 2022): each
+// operand x = x_hi + x_lo with x_hi its TF32 rounding and x_lo the TF32 rounding of the remainder, and
+// A B ~ A_lo B_hi + A_hi B_lo + A_hi B_hi (the small terms first; A_lo B_lo is below fp32 rounding).
+__device__ __forceinline__ void mma1688_3xtf32(float (&c)[4], const float (&a)[4], const float (&b)[2]) {
+    uint32_t ah[4], al[4], bh[2], bl[2];
 #pragma unroll
-        for (int k = 0; k < B; ++k) {
-            const float a0 = A[hi + rr][lo + k], a1 = A[hi + rr + 1][lo + k];
-            const float t0 = T[lo + k][lo + cc], t1 = T[lo + k][lo + cc + 1];
-            x00 += a0 * t0; x01 += a0 * t1; x10 += a1 * t0; x11 += a1 * t1;
+    for (int i = 0; i < 4; ++i) {
+        ah[i] = tf32_rna(a[i]);
+        al[i] = tf32_rna(a[i] - __uint_as_float(ah[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        bh[i] = tf32_rna(b[i]);
+        bl[i] = tf32_rna(b[i] - __uint_as_float(bh[i]));
+    }
+    mma1688_tf32(c, al, bh);
+    mma1688_tf32(c, ah, bl);
+    mma1688_tf32(c, ah, bh);
+}
+
+// One doubling level of the unit-lower-triangular inverse T = (I + A)^-1, built in place over A in fp32 shared
+// memory: for every diagonal pair of B x B blocks (lo, hi = lo + B), with the B x B diagonal blocks of T already
+// final, X = A[hi][lo] T[lo][lo] and then T[hi][lo] = -T[hi][hi] X.  Each product is a set of 16 x 8 output
+// tiles, one per warp, as three-pass TF32 warp MMAs over the reduction in steps of 8.  A level reads A only in
+// the blocks it then overwrites, after the barrier between its two products.
+template <int B>
+__device__ __forceinline__ void inv_level_tc(float (&T)[CT][CT + 1], float (&X)[32][33], int wid, int lane) {
+    constexpr int NP = CT / (2 * B);         // block pairs
+    constexpr int PT = (B / 16) * (B / 8);   // 16 x 8 output tiles of one pair's B x B product
+    static_assert(NP * PT <= K1_THREADS / 32 && NP * B <= 32, "one output tile per warp; X holds every pair");
+    const bool act = wid < NP * PT;
+    const int p = wid / PT, tm = (wid % PT) / (B / 8), tn = wid % (B / 8);
+    const int lo = 2 * B * p, hi = lo + B, r0 = 16 * tm, c0 = 8 * tn;
+    const int g = lane >> 2, t = lane & 3;
+    if (act) {  // X[p B + r][c] = sum_k A[hi + r][lo + k] T[lo + k][lo + c]
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k0 = 0; k0 < B; k0 += 8) {
+            const float a[4] = {T[hi + r0 + g][lo + k0 + t], T[hi + r0 + g + 8][lo + k0 + t],
+                                T[hi + r0 + g][lo + k0 + t + 4], T[hi + r0 + g + 8][lo + k0 + t + 4]};
+            const float b[2] = {T[lo + k0 + t][lo + c0 + g], T[lo + k0 + t + 4][lo + c0 + g]};
+            mma1688_3xtf32(c, a, b);
         }
-        X[p * B + rr][cc] = x00; X[p * B + rr][cc + 1] = x01;
-        X[p * B + rr + 1][cc] = x10; X[p * B + rr + 1][cc + 1] = x11;
+        X[p * B + r0 + g][c0 + 2 * t] = c[0];
+        X[p * B + r0 + g][c0 + 2 * t + 1] = c[1];
+        X[p * B + r0 + g + 8][c0 + 2 * t] = c[2];
+        X[p * B + r0 + g + 8][c0 + 2 * t + 1] = c[3];
     }
     __syncthreads();
-    if (act) {  // T[hi][lo] = -T[hi][hi] X
-        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+    if (act) {  // T[hi + r][lo + c] = -sum_k T[hi + r][hi + k] X[p B + k][c]
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < B; ++k) {
-            const float a0 = T[hi + rr][hi + k], a1 = T[hi + rr + 1][hi + k];
-            const float x0 = X[p * B + k][cc], x1 = X[p * B + k][cc + 1];
-            y00 += a0 * x0; y01 += a0 * x1; y10 += a1 * x0; y11 += a1 * x1;
+        for (int k0 = 0; k0 < B; k0 += 8) {
+            const float a[4] = {T[hi + r0 + g][hi + k0 + t], T[hi + r0 + g + 8][hi + k0 + t],
+                                T[hi + r0 + g][hi + k0 + t + 4], T[hi + r0 + g + 8][hi + k0 + t + 4]};
+            const float b[2] = {X[p * B + k0 + t][c0 + g], X[p * B + k0 + t + 4][c0 + g]};
+            mma1688_3xtf32(c, a, b);
         }
-        T[hi + rr][lo + cc] = -y00; T[hi + rr][lo + cc + 1] = -y01;
-        T[hi + rr + 1][lo + cc] = -y10; T[hi + rr + 1][lo + cc + 1] = -y11;
+        T[hi + r0 + g][lo + c0 + 2 * t] = -c[0];
+        T[hi + r0 + g][lo + c0 + 2 * t + 1] = -c[1];
+        T[hi + r0 + g + 8][lo + c0 + 2 * t] = -c[2];
+        T[hi + r0 + g + 8][lo + c0 + 2 * t + 1] = -c[3];
     }
     __syncthreads();
 }
@@ -498,9 +538,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
     float (&X32)[32][33] = *reinterpret_cast<float (*)[32][33]>(S.Ks + CT * CT * 2);
     // off-diagonal blocks by recursive doubling: for a lower block split [[T_11, 0], [X, T_22]] of an inverse,
     // X = -T_22 A_21 T_11.  First the two 32 x 32 diagonal blocks from their 16 x 16 halves, then the whole.
-    // Every thread accumulates a 2 x 2 output block over a fully unrolled inner loop.
-    inv_level<16>(S.AT, S.AT, X32, tid);
-    inv_level<32>(S.AT, S.AT, X32, tid);
+    inv_level_tc<16>(S.AT, X32, wid, lane);
+    inv_level_tc<32>(S.AT, X32, wid, lane);
     for (int e = tid; e < CT * CT / 8; e += K1_THREADS) {
         int i = e / (CT / 8), j8 = (e % (CT / 8)) * 8;
         float x[8];
