@@ -108,6 +108,21 @@ cudaError_t encode_rows_map(CUtensorMap *map, const void *base, int dtype, long 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t encode_rows_map_sw128(CUtensorMap *map, const void *base, int dtype, long long tokens, int heads,
+                                  int cols) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)heads * cols * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)CT};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    const CUresult r = enc(map, dtype == BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                           const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace gdr
 
 namespace {

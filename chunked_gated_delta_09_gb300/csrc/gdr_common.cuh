@@ -332,10 +332,17 @@ __device__ __forceinline__ uint32_t ctile_off(int r, int c, int C) {
 __device__ __forceinline__ uint32_t cbtile_off(int r, int c, int R) {
     return (uint32_t)((c >> 3) * (R >> 3) * 128 + (r >> 3) * 128 + (r & 7) * 16 + (c & 7) * 2);
 }
-// Either block order: D is the column count of a row-block-major tile (CB = false) or the row count of a
-// column-block-major one (CB = true).
-template <bool CB> __device__ __forceinline__ uint32_t tile_at(int r, int c, int D) {
-    return CB ? cbtile_off(r, c, D) : ctile_off(r, c, D);
+// Byte offset of element (r, c) in a 64-row tile of 128-byte-swizzled halves (the layout of two 64-column
+// tensor-map boxes with the 128-byte swizzle, on a 1024-byte-aligned base): columns 64 h .. 64 h + 63 in half h
+// (64 rows of 128 bytes each), the 16-byte chunk j of row r at position j ^ (r % 8).
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+    return (uint32_t)((c >> 6) * (CT * 128) + r * 128 + ((((c >> 3) & 7) ^ (r & 7)) << 4) + (c & 7) * 2);
+}
+// Tile layouts: TL_ROWB row-block-major core-matrix tile (D its column count), TL_COLB column-block-major (D its
+// row count), TL_SW128 the swizzled halves above (D unused).
+constexpr int TL_ROWB = 0, TL_COLB = 1, TL_SW128 = 2;
+template <int L> __device__ __forceinline__ uint32_t tile_at(int r, int c, int D) {
+    return L == TL_SW128 ? sw128_off(r, c) : L == TL_COLB ? cbtile_off(r, c, D) : ctile_off(r, c, D);
 }
 __device__ __forceinline__ float ctile_get(const unsigned char *t, int r, int c, int C) {
     return __half2float(*reinterpret_cast<const __half *>(t + ctile_off(r, c, C)));
@@ -360,9 +367,8 @@ __device__ __forceinline__ void mma16816t(float (&c)[4], const uint32_t (&a)[4],
 // warp_mma on core-matrix tiles (each 8 x 8 ldmatrix block is one contiguous core matrix):
 //   A(m, k) = tile element (m, k) (AT = false) or (k, m) (AT = true);
 //   B(k, n) = tile element (k, n) (BT = false) or (n, k) (BT = true);
-// ACB / BCB: the tile is column-block-major (A_D / B_D its row count) rather than row-block-major (A_D / B_D
-// its column count); BF: both tiles hold bf16 rather than fp16.
-template <int MT, int NT, bool AT, bool BT, bool ACB = false, bool BCB = false, bool BF = false>
+// AL / BL: the tiles' layouts (TL_*; A_D / B_D as tile_at takes them); BF: both tiles hold bf16 rather than fp16.
+template <int MT, int NT, bool AT, bool BT, int AL = TL_ROWB, int BL = TL_ROWB, bool BF = false>
 __device__ __forceinline__ void warp_mma_ct(float (&acc)[MT][NT][4], const unsigned char *A, int A_D,
                                             const unsigned char *B, int B_D, int m0, int n0, int kdim) {
     const int lane = threadIdx.x & 31;
@@ -372,15 +378,15 @@ __device__ __forceinline__ void warp_mma_ct(float (&acc)[MT][NT][4], const unsig
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             int mb = m0 + mt * 16;
-            if (!AT) ldsm_x4(a[mt], A + tile_at<ACB>(mb + (lane & 15), k0 + (lane >> 4) * 8, A_D));
-            else ldsm_x4_t(a[mt], A + tile_at<ACB>(k0 + r8 + (mat >> 1) * 8, mb + (mat & 1) * 8, A_D));
+            if (!AT) ldsm_x4(a[mt], A + tile_at<AL>(mb + (lane & 15), k0 + (lane >> 4) * 8, A_D));
+            else ldsm_x4_t(a[mt], A + tile_at<AL>(k0 + r8 + (mat >> 1) * 8, mb + (mat & 1) * 8, A_D));
         }
 #pragma unroll
         for (int nt = 0; nt + 1 < NT; nt += 2) {
             int nb = n0 + nt * 8;
             uint32_t b[4];
-            if (BT) ldsm_x4(b, B + tile_at<BCB>(nb + r8 + (mat >> 1) * 8, k0 + (mat & 1) * 8, B_D));
-            else ldsm_x4_t(b, B + tile_at<BCB>(k0 + r8 + (mat & 1) * 8, nb + (mat >> 1) * 8, B_D));
+            if (BT) ldsm_x4(b, B + tile_at<BL>(nb + r8 + (mat >> 1) * 8, k0 + (mat & 1) * 8, B_D));
+            else ldsm_x4_t(b, B + tile_at<BL>(k0 + r8 + (mat & 1) * 8, nb + (mat >> 1) * 8, B_D));
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
                 mma16816t<BF>(acc[mt][nt], a[mt], b[0], b[1]);
@@ -392,8 +398,8 @@ __device__ __forceinline__ void warp_mma_ct(float (&acc)[MT][NT][4], const unsig
             int nb = n0 + nt * 8;
             int m2 = (lane >> 3) & 1;
             uint32_t b[2];
-            if (BT) ldsm_x2(b, B + tile_at<BCB>(nb + r8, k0 + m2 * 8, B_D));
-            else ldsm_x2_t(b, B + tile_at<BCB>(k0 + r8 + m2 * 8, nb, B_D));
+            if (BT) ldsm_x2(b, B + tile_at<BL>(nb + r8, k0 + m2 * 8, B_D));
+            else ldsm_x2_t(b, B + tile_at<BL>(k0 + r8 + m2 * 8, nb, B_D));
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) mma16816t<BF>(acc[mt][nt], a[mt], b[0], b[1]);
         }

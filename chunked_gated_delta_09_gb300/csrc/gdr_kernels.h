@@ -19,6 +19,12 @@ cudaError_t device_sm_count(int *out);
 // box lands as a column-block-major core-matrix tile (core matrix (r/8, c/8) at ((c/8) 8 + r/8) 128 bytes).
 // Rows past the tensor's end read as zero.  cols must be a multiple of 8 and base 16-byte aligned.
 cudaError_t encode_rows_map(CUtensorMap *map, const void *base, int dtype, long long tokens, int heads, int cols);
+// The same input for loads of 64-column halves of a chunk's rows with the 128-byte swizzle: 3-D over (column,
+// head, token), box (64, 1, 64), so that one box lands as 64 rows of 128 bytes whose 16-byte chunks are permuted
+// within each row (chunk j of row r at position j ^ (r % 8)); the destination must be 1024-byte aligned.
+// Columns past cols and rows past the tensor's end read as zero.
+cudaError_t encode_rows_map_sw128(CUtensorMap *map, const void *base, int dtype, long long tokens, int heads,
+                                  int cols);
 
 // K0: varlen chunk bookkeeping (one block).  expect_total_tokens < 0 skips the cu[N] == T check.
 cudaError_t launch_k0(const int32_t *cu, int N, int BT, int max_chunks, int expect_total_tokens, int32_t *chunk_idx,

@@ -11,9 +11,10 @@
 // K~ = K (.) exp(gamma_C - gamma) and Q~ = Q (.) exp(gamma) that the two scans use, and D = scale dO.
 // Per-channel gate: each exp(gamma_a - gamma_b) is taken per key channel inside the K contraction.  For the
 // scalar gate's backward it also writes each unit's per-token record (beta, exp(gamma), exp(gamma_C - gamma),
-// gamma) that the per-chunk gradient kernel fetches whole.  16-bit input rows arrive by tensor-map loads, one
-// per input, as column-block-major core-matrix tiles in their own type: the key Gram and Aqk products take them
-// as they are (bf16 or fp16 operands), and the element-wise pass that forms the decayed copies reads them there.
+// gamma) that the per-chunk gradient kernel fetches whole.  16-bit input rows arrive by tensor-map loads (two
+// 64-column boxes per input with the 128-byte swizzle, so that every row segment of 16 bytes can be read without
+// bank conflicts) in their own type: the key Gram and Aqk products take them as they are (bf16 or fp16 operands),
+// and the element-wise pass that forms the decayed copies reads them there.
 //
 // Every matrix output is written in the core-matrix tile layout that the tensor-core kernels read,
 // straight from registers: 8 lanes of an element-wise pass write one contiguous 128-byte core matrix, and
@@ -50,7 +51,7 @@ __device__ __forceinline__ void ld8f(const float *p, float (&x)[8]) {
 }
 
 struct __align__(1024) K1Smem {
-    // Ks, Qs, Vs: the chunk's K, Q, V rows as column-block-major core-matrix tiles (bf16 for bf16 inputs, fp16
+    // Ks, Qs, Vs: the chunk's K, Q, V rows as 128-byte-swizzled halves (sw128_off; bf16 for bf16 inputs, fp16
     // otherwise).  Ks later holds T as the fp16 operand of the W and U products (row-block-major) and the
     // scratch of the inverse's block products; Qs later holds beta Gamma K and Vs beta V (fp16, in place).  AT
     // holds the raw dO rows on their way to the D tile, then A_kk, then in place its inverse T (fp32).
@@ -143,7 +144,7 @@ __device__ __forceinline__ void inv_level_tc(float (&T)[CT][CT + 1], float (&X)[
 }
 
 // The tensor maps (16-bit inputs only; unused for fp32) describe k, q (key heads) and v, dO (value heads) as
-// encode_rows_map does.
+// encode_rows_map_sw128 does.
 template <typename Tin, bool PC>
 __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
     k1_wy_prep(const Params P, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
@@ -152,8 +153,10 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
     using TT = typename std::conditional<std::is_same<Tin, __nv_bfloat16>::value, __nv_bfloat16, __half>::type;
     constexpr bool kBF = std::is_same<Tin, __nv_bfloat16>::value;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    K1Smem &S = *reinterpret_cast<K1Smem *>(smem_raw);
-    float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K1Smem));  // [CT][GKLD], per-channel only
+    // the swizzled tiles need a 1024-byte-aligned base (the launch asks for 1 KB more than the layout)
+    unsigned char *const sbase = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    K1Smem &S = *reinterpret_cast<K1Smem *>(sbase);
+    float *gamK = reinterpret_cast<float *>(sbase + sizeof(K1Smem));  // [CT][GKLD], per-channel only
 
     if (*P.status & ST_BAD_SEQLENS) return;
     const int n = blockIdx.x, hv = blockIdx.y, hk = hv / P.G;
@@ -187,11 +190,16 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
         }
         __syncthreads();
         if (tid == 0) {
-            tc::mbar_expect_tx(&S.rbar, (uint32_t)((2 * (P.K >> 3) + (nin - 2) * (P.V >> 3)) * CT * 16));
-            tc::tma_load_4d(S.Ks, &tmk, 0, ci.tok0, 0, hk, &S.rbar);
-            tc::tma_load_4d(S.Qs, &tmq, 0, ci.tok0, 0, hk, &S.rbar);
-            tc::tma_load_4d(S.Vs, &tmv, 0, ci.tok0, 0, hv, &S.rbar);
-            if (P.dO) tc::tma_load_4d(slot[3], &tmo, 0, ci.tok0, 0, hv, &S.rbar);
+            const int hK = (P.K + 63) >> 6, hV = (P.V + 63) >> 6;  // 64-column boxes per input
+            tc::mbar_expect_tx(&S.rbar, (uint32_t)((2 * hK + (nin - 2) * hV) * CT * 128));
+            for (int h = 0; h < hK; ++h) {
+                tc::tma_load_3d(S.Ks + h * CT * 128, &tmk, 64 * h, hk, ci.tok0, &S.rbar);
+                tc::tma_load_3d(S.Qs + h * CT * 128, &tmq, 64 * h, hk, ci.tok0, &S.rbar);
+            }
+            for (int h = 0; h < hV; ++h) {
+                tc::tma_load_3d(S.Vs + h * CT * 128, &tmv, 64 * h, hv, ci.tok0, &S.rbar);
+                if (P.dO) tc::tma_load_3d(slot[3] + h * CT * 128, &tmo, 64 * h, hv, ci.tok0, &S.rbar);
+            }
         }
         const bool landed = tc::mbar_wait(&S.rbar, 0, P.spin);
         if (__syncthreads_or(!landed)) {
@@ -201,13 +209,15 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
             }
             return;
         }
-        // a ragged chunk or narrow features: zero the rows past the chunk (the box also covers the next
-        // sequence's rows) and the column blocks the box left unset
-        if (len < CT || P.K < DT || P.V < DT) {
+        // a ragged chunk or narrow features: zero the rows past the chunk (the boxes also cover the next
+        // sequence's rows) and a half no box filled (columns past K or V inside a box arrive as zero)
+        if (len < CT || P.K <= 64 || P.V <= 64) {
             for (int w = 0; w < nin; ++w)
-                for (int e = tid; e < CT * DT / 8; e += K1_THREADS)
-                    if ((e & (CT - 1)) >= len || 8 * (e >> 6) >= nc[w])
-                        *reinterpret_cast<uint4 *>(slot[w] + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+                for (int e = tid; e < CT * DT / 8; e += K1_THREADS) {
+                    const int r = e & (CT - 1), c8 = 8 * (e >> 6);
+                    if (r >= len || (c8 >= 64 && nc[w] <= 64))
+                        *reinterpret_cast<uint4 *>(slot[w] + sw128_off(r, c8)) = make_uint4(0u, 0u, 0u, 0u);
+                }
             __syncthreads();
         }
         if (P.dO) {  // D = scale dO, straight from the landed tile to its (row-block-major) workspace tile
@@ -215,7 +225,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
             for (int e = tid; e < CT * DT / 8; e += K1_THREADS) {
                 const int r = e & (CT - 1), c8 = 8 * (e >> 6);
                 float f[8];
-                ld8t<TT>(slot[3] + e * 16, f);
+                ld8t<TT>(slot[3] + sw128_off(r, c8), f);
                 bad |= out_of_f16(f);
 #pragma unroll
                 for (int t = 0; t < 8; ++t) f[t] *= P.scale;
@@ -223,8 +233,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
             }
         }
     } else {
-        // fp32 inputs: each 16-byte fp16 chunk of the column-block-major tiles from 8 input values (rows past
-        // the chunk and columns past K / V zero); D goes straight to its workspace tile
+        // fp32 inputs: each 16-byte fp16 chunk of the swizzled tiles from 8 input values (rows past the chunk
+        // and columns past K / V zero); D goes straight to its workspace tile
         const float *const src[4] = {reinterpret_cast<const float *>(kp), reinterpret_cast<const float *>(qp),
                                      reinterpret_cast<const float *>(vp), reinterpret_cast<const float *>(dop)};
         const size_t st[4] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V, (size_t)P.Hv * P.V};
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
                     *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT) +
                                                ctile_off(r, c8, DT)) = pack8_half(f);
                 } else {
-                    *reinterpret_cast<uint4 *>(slot[w] + e * 16) = pack8_half(f);
+                    *reinterpret_cast<uint4 *>(slot[w] + sw128_off(r, c8)) = pack8_half(f);
                 }
             }
     }
@@ -291,8 +301,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
         float kk[1][4][4], qk[1][4][4];
         zero_acc(kk);
         zero_acc(qk);
-        warp_mma_ct<1, 4, false, true, true, true, kBF>(kk, S.Ks, CT, S.Ks, CT, m0, n0, DT);
-        warp_mma_ct<1, 4, false, true, true, true, kBF>(qk, S.Qs, CT, S.Ks, CT, m0, n0, DT);
+        warp_mma_ct<1, 4, false, true, TL_SW128, TL_SW128, kBF>(kk, S.Ks, 0, S.Ks, 0, m0, n0, DT);
+        warp_mma_ct<1, 4, false, true, TL_SW128, TL_SW128, kBF>(qk, S.Qs, 0, S.Ks, 0, m0, n0, DT);
         unsigned char *aqk_g = reinterpret_cast<unsigned char *>(P.Aqk + u * CT * CT);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
@@ -347,9 +357,9 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
                     float ki[2][8], qi[2][8], kj[2][8], gi[2][8], gj[2][8];
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        ld8t<TT>(S.Ks + cbtile_off(i0 + r, c8, CT), ki[r]);
-                        ld8t<TT>(S.Qs + cbtile_off(i0 + r, c8, CT), qi[r]);
-                        ld8t<TT>(S.Ks + cbtile_off(j0 + r, c8, CT), kj[r]);
+                        ld8t<TT>(S.Ks + sw128_off(i0 + r, c8), ki[r]);
+                        ld8t<TT>(S.Qs + sw128_off(i0 + r, c8), qi[r]);
+                        ld8t<TT>(S.Ks + sw128_off(j0 + r, c8), kj[r]);
                         ld8f(gamK + (i0 + r) * GKLD + c8, gi[r]);
                         ld8f(gamK + (j0 + r) * GKLD + c8, gj[r]);
                     }
@@ -394,8 +404,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
                         const float2 gr = *reinterpret_cast<const float2 *>(gamK + mid * GKLD + c);
                         const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
                         const float e0 = __expf(gx.x - gr.x), e1 = __expf(gx.y - gr.y);
-                        const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + cbtile_off(row, c, CT)));
-                        const float2 qv = ld2t(reinterpret_cast<const TT *>(S.Qs + cbtile_off(row, c, CT)));
+                        const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + sw128_off(row, c)));
+                        const float2 qv = ld2t(reinterpret_cast<const TT *>(S.Qs + sw128_off(row, c)));
                         ak[q] = pack_half2(kv.x * e0, kv.y * e1);
                         aq[q] = pack_half2(qv.x * e0, qv.y * e1);
                     }
@@ -404,7 +414,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
                         const int row = 16 * blk + g4, c = k0 + kq + 8 * q;
                         const float2 gr = *reinterpret_cast<const float2 *>(gamK + mid * GKLD + c);
                         const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
-                        const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + cbtile_off(row, c, CT)));
+                        const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + sw128_off(row, c)));
                         bk[q] = pack_half2(kv.x * __expf(gr.x - gx.x), kv.y * __expf(gr.y - gx.y));
                     }
                     mma16816(kk, ak, bk[0], bk[1]);
@@ -430,8 +440,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
                     const float2 gr = *reinterpret_cast<const float2 *>(gamK + ref * GKLD + c);
                     const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
                     const float e0 = __expf(gx.x - gr.x), e1 = __expf(gx.y - gr.y);
-                    const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + cbtile_off(row, c, CT)));
-                    const float2 qv = ld2t(reinterpret_cast<const TT *>(S.Qs + cbtile_off(row, c, CT)));
+                    const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + sw128_off(row, c)));
+                    const float2 qv = ld2t(reinterpret_cast<const TT *>(S.Qs + sw128_off(row, c)));
                     const __half2 hk = __floats2half2_rn(kv.x * e0, kv.y * e1), hq = __floats2half2_rn(qv.x * e0, qv.y * e1);
                     ak[q] = *reinterpret_cast<const uint32_t *>(&hk);
                     aq[q] = *reinterpret_cast<const uint32_t *>(&hq);
@@ -445,7 +455,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
                         const int row = 16 * J + 8 * nt + g4, c = k0 + kq + 8 * q;
                         const float2 gr = *reinterpret_cast<const float2 *>(gamK + ref * GKLD + c);
                         const float2 gx = *reinterpret_cast<const float2 *>(gamK + row * GKLD + c);
-                        const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + cbtile_off(row, c, CT)));
+                        const float2 kv = ld2t(reinterpret_cast<const TT *>(S.Ks + sw128_off(row, c)));
                         const __half2 hb = __floats2half2_rn(kv.x * __expf(gr.x - gx.x), kv.y * __expf(gr.y - gx.y));
                         bk[nt][q] = *reinterpret_cast<const uint32_t *>(&hb);
                     }
@@ -483,15 +493,15 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
         unsigned char *Ktg = reinterpret_cast<unsigned char *>(P.Kt + u * CT * DT);
         unsigned char *Qgg = reinterpret_cast<unsigned char *>(P.Qg + u * CT * DT);
         for (int e = tid; e < CT * DT / 8; e += K1_THREADS) {
-            // one 16-byte core-matrix row segment (row i, columns c8 .. c8 + 7) at byte 16 e of the
-            // column-block-major tiles; consecutive lanes walk the 8 rows of a core matrix, which are also
-            // one contiguous core matrix of the row-block-major global tiles
+            // one 16-byte row segment (row i, columns c8 .. c8 + 7); consecutive lanes walk 8 rows (distinct
+            // banks in the swizzled tiles), which are one contiguous core matrix of the row-block-major
+            // global tiles
             const int i = e & (CT - 1), c8 = 8 * (e >> 6);
-            const uint32_t off = ctile_off(i, c8, DT);
+            const uint32_t off = ctile_off(i, c8, DT), so = sw128_off(i, c8);
             float kx[8], qx[8], vx[8], o1[8], o2[8], o3[8], o4[8];
-            ld8t<TT>(S.Ks + e * 16, kx);
-            ld8t<TT>(S.Qs + e * 16, qx);
-            ld8t<TT>(S.Vs + e * 16, vx);
+            ld8t<TT>(S.Ks + so, kx);
+            ld8t<TT>(S.Qs + so, qx);
+            ld8t<TT>(S.Vs + so, vx);
             if constexpr (sizeof(Tin) == 2) bad |= out_of_f16(kx) | out_of_f16(qx) | out_of_f16(vx);
             const float bi = S.beta[i];
 #pragma unroll
@@ -506,8 +516,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
             }
             *reinterpret_cast<uint4 *>(Ktg + off) = pack8_half(o1);
             *reinterpret_cast<uint4 *>(Qgg + off) = pack8_half(o2);
-            *reinterpret_cast<uint4 *>(S.Qs + e * 16) = pack8_half(o3);  // in place (fp16 from here on)
-            *reinterpret_cast<uint4 *>(S.Vs + e * 16) = pack8_half(o4);
+            *reinterpret_cast<uint4 *>(S.Qs + so) = pack8_half(o3);  // in place (fp16 from here on)
+            *reinterpret_cast<uint4 *>(S.Vs + so) = pack8_half(o4);
         }
         if (bad) flag_status(P.status, ST_RANGE);
     }
@@ -556,7 +566,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
         {
             const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * 64;
             zero_acc(acc);
-            warp_mma_ct<1, 8, false, false, false, true>(acc, oT, CT, S.Qs, CT, m0, n0, CT);
+            warp_mma_ct<1, 8, false, false, TL_ROWB, TL_SW128>(acc, oT, CT, S.Qs, 0, m0, n0, CT);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -569,7 +579,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
         {
             const int m0 = wid * 16;  // 8 warps x 16 value rows, all 64 chunk columns
             zero_acc(acc);
-            warp_mma_ct<1, 8, true, true, true, false>(acc, S.Vs, CT, oT, CT, m0, 0, CT);
+            warp_mma_ct<1, 8, true, true, TL_SW128, TL_ROWB>(acc, S.Vs, 0, oT, CT, m0, 0, CT);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -584,7 +594,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
 
 template <typename Tin, bool PC>
 static cudaError_t launch_k1_t(const Params &P, cudaStream_t stream) {
-    size_t smem = sizeof(K1Smem) + (PC ? sizeof(float) * CT * GKLD : 0);
+    size_t smem = sizeof(K1Smem) + (PC ? sizeof(float) * CT * GKLD : 0) + 1024;  // (+ alignment slack)
     cudaError_t e = smem_opt_in((const void *)k1_wy_prep<Tin, PC>, smem);
     if (e != cudaSuccess) return e;
     CUtensorMap mk, mq, mv, mo;
@@ -594,10 +604,10 @@ static cudaError_t launch_k1_t(const Params &P, cudaStream_t stream) {
     memset(&mo, 0, sizeof(mo));
     if (sizeof(Tin) == 2) {
         const long long tokens = (long long)P.B * P.T;
-        if ((e = encode_rows_map(&mk, P.k, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
-        if ((e = encode_rows_map(&mq, P.q, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
-        if ((e = encode_rows_map(&mv, P.v, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
-        if (P.dO && (e = encode_rows_map(&mo, P.dO, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
+        if ((e = encode_rows_map_sw128(&mk, P.k, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
+        if ((e = encode_rows_map_sw128(&mq, P.q, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
+        if ((e = encode_rows_map_sw128(&mv, P.v, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
+        if (P.dO && (e = encode_rows_map_sw128(&mo, P.dO, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
     }
     dim3 grid(P.max_chunks, P.Hv);
     k1_wy_prep<Tin, PC><<<grid, K1_THREADS, smem, stream>>>(P, mk, mq, mv, mo);

@@ -109,6 +109,14 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *map, int x0, 
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x0, int x1, int x2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x0), "r"(x1), "r"(x2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
         smem_u32(bar)));
