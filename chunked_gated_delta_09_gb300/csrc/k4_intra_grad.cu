@@ -23,15 +23,8 @@
 // itself) and is taken with the fast hardware exponential (relative error about 1e-6, below the fp16
 // rounding of the operand tiles).
 //
-// All operands live in shared memory as core-matrix tiles; the workspace tiles (row-block-major, ctile_off)
-// and the per-channel gate tile arrive by bulk copy, the 16-bit q, k, v rows by tensor-map loads as
-// column-block-major tiles (cbtile_off), converted to fp16 in place; every copy for the CTA's next item is
-// issued as soon as the current item is done with its buffer.  The workspace holds V_new^T and -dV_new^T
-// (tiles [v][c]).
-#include <string.h>
-
-#include <type_traits>
-
+// All operands live in shared memory as core-matrix tiles (ctile_off); the workspace tiles arrive by
+// bulk copy.  The workspace holds V_new^T and -dV_new^T (tiles [v][c]).
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
 #include "tc_util.cuh"
@@ -57,7 +50,6 @@ constexpr int NC = 2;  // C x C tiles: 16 x 16 per warp (two n8 tiles)
 // quarter the same way, and only the two 8 x 8 triangles term by term, where one pass over the inner index
 // serves all 16 elements of a thread and terms outside a row's range are dropped by selection, never by a zero
 // factor.
-// X is a column-block-major tile (cbtile_off, CT rows), A a row-block-major one.
 template <bool LOWER, bool INCL>
 __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsigned char *A, const unsigned char *X,
                                             const float *g, int m0, int n0, int lane) {
@@ -86,7 +78,7 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int j = k0 + bk + (q & 1) + 8 * (q >> 1);
-                    const float x = __half2float(*reinterpret_cast<const __half *>(X + cbtile_off(j, c, CT)));
+                    const float x = ctile_get(X, j, c, DT);
                     // exponent <= 0 on both sides of the reference row
                     v[q] = x * __expf(LOWER ? gref_b[nt] - g[j * DT + c] : g[j * DT + c] - gref_b[nt]);
                 }
@@ -124,10 +116,8 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
             const int c = n0 + 8 * nt + bn;
             const float gm = g[mid * DT + c];
             const int j = LOWER ? m0 + bk : mid + bk;  // k rows of the B fragment
-            const float x0 = __half2float(*reinterpret_cast<const __half *>(X + cbtile_off(j, c, CT)));
-            const float x1 = __half2float(*reinterpret_cast<const __half *>(X + cbtile_off(j + 1, c, CT)));
-            const float v0 = x0 * __expf(LOWER ? gm - g[j * DT + c] : g[j * DT + c] - gm);
-            const float v1 = x1 * __expf(LOWER ? gm - g[(j + 1) * DT + c] : g[(j + 1) * DT + c] - gm);
+            const float v0 = ctile_get(X, j, c, DT) * __expf(LOWER ? gm - g[j * DT + c] : g[j * DT + c] - gm);
+            const float v1 = ctile_get(X, j + 1, c, DT) * __expf(LOWER ? gm - g[(j + 1) * DT + c] : g[(j + 1) * DT + c] - gm);
             mma1688(off[nt], a0, a1, pack_half2(v0, v1));
         }
 #pragma unroll
@@ -159,8 +149,8 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
         const float a1 = LOWER ? ctile_get(A, r0 + 8, j1, CT) : ctile_get(A, j1, r0 + 8, CT);
 #pragma unroll
         for (int nt = 0; nt < NK; ++nt) {
-            const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(X + cbtile_off(j0, cq + 8 * nt, CT)));
-            const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(X + cbtile_off(j1, cq + 8 * nt, CT)));
+            const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(X + ctile_off(j0, cq + 8 * nt, DT)));
+            const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(X + ctile_off(j1, cq + 8 * nt, DT)));
             const float2 g0 = *reinterpret_cast<const float2 *>(g + j0 * DT + cq + 8 * nt);
             const float2 g1 = *reinterpret_cast<const float2 *>(g + j1 * DT + cq + 8 * nt);
             const float e00 = __expf(LOWER ? gr[0][nt][0] - g0.x : g0.x - gr[0][nt][0]);
@@ -176,8 +166,7 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
 }
 
 struct __align__(1024) K4Smem {
-    unsigned char Qs[CT * DT * 2], Ks[CT * DT * 2], Vs[CT * DT * 2];  // column-block-major (cbtile_off)
-    unsigned char Ds[CT * DT * 2];
+    unsigned char Qs[CT * DT * 2], Ks[CT * DT * 2], Vs[CT * DT * 2], Ds[CT * DT * 2];
     unsigned char VnT[DT * CT * 2], NdVT[DT * CT * 2];  // V_new^T, -dV_new^T  [v][c]
     unsigned char Hs[DT * DT * 2], dHs[DT * DT * 2];    // [v][k]
     unsigned char Ts[CT * CT * 2], Pms[CT * CT * 2];
@@ -211,17 +200,14 @@ __device__ __forceinline__ void store_ck(const float (&a)[1][NT][4], int m0, int
 // chunk_kda_bwd_wy_dqkg_fused): no intra-chunk attention terms (P, dq_intra, dk_O) and no terms through A_kk
 // (E, dk_Ar, dk_Ac, the A part of dbeta); instead dA = strict_lower(-T^T dT T^T) is written out, and the
 // gradient of the cumulative gate goes straight to dg (no reverse cumsum follows).
-// The tensor maps (16-bit inputs only) describe k, q (key heads) and v (value heads) as encode_rows_map does.
 template <typename Tin, bool PC, bool WY>
-__global__ void __launch_bounds__(K4_THREADS, 1)
-    k4_intra_grad(const Params P, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
-                  const __grid_constant__ CUtensorMap tmv) {
+__global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     K4Smem &S = *reinterpret_cast<K4Smem *>(smem_raw);
     float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K4Smem));  // [CT][DT] per-channel only
     // buffers reused once their first owner is done
     unsigned char *dWs = S.Ds;     // dW [r][k]          after dq
-    unsigned char *KGb = S.Qs;     // beta Gamma K       after dk_O (per-channel; row-block-major)
+    unsigned char *KGb = S.Qs;     // beta Gamma K       after dk_O (per-channel)
     unsigned char *dTs = S.Pms;    // dT                 after dk_O
     unsigned char *Xs = S.VnT;     // dT T^T (C x C)     after dk_SC
     unsigned char *Es = S.Pms;     // E                  after X
@@ -237,14 +223,10 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
         while (it < n_items && !chunk_info(P, it / P.Hv, t)) it += gridDim.x;
         return it;
     };
-    constexpr bool kRaw = sizeof(Tin) == 2;  // 16-bit inputs: tensor-map loads; fp32 inputs: staged per item
     constexpr uint32_t kBytesHdH = 2 * DT * DT * 2, kBytesDdV = CT * DT * 2 + DT * CT * 2,
                        kBytesTVn = CT * CT * 2 + DT * CT * 2;
-    // the raw k, q, v tiles (their boxes cover K / 8 or V / 8 column blocks) and the per-channel gate tile
-    const uint32_t kBytesIn =
-        (kRaw ? (uint32_t)(CT * 16 * (2 * (P.K >> 3) + (P.V >> 3))) : 0u) + (PC ? (uint32_t)(CT * DT * 4) : 0u);
     auto issue_HdH = [&](size_t un) {  // expects the whole item's bytes, so it comes first
-        tc::mbar_expect_tx(&S.lbar, kBytesHdH + kBytesDdV + kBytesTVn + kBytesIn);
+        tc::mbar_expect_tx(&S.lbar, kBytesHdH + kBytesDdV + kBytesTVn);
         tc::bulk_g2s(S.Hs, P.h + un * DT * DT, DT * DT * 2, &S.lbar);
         tc::bulk_g2s(S.dHs, P.dh + un * DT * DT, DT * DT * 2, &S.lbar);
     };
@@ -256,20 +238,6 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
         tc::bulk_g2s(S.Ts, P.Tm + un * CT * CT, CT * CT * 2, &S.lbar);
         tc::bulk_g2s(S.VnT, P.Vn + un * DT * CT, DT * CT * 2, &S.lbar);
     };
-    // raw rows of an item's chunk (which: 0 = k, 1 = q, 2 = v) by one tensor-map load into their tile slot
-    auto fetch_in = [&](int it, int which) {
-        if constexpr (kRaw) {
-            ChunkInfo c2;
-            chunk_info(P, it / P.Hv, c2);
-            const int hv2 = it % P.Hv;
-            unsigned char *dst = which == 0 ? S.Ks : which == 1 ? S.Qs : S.Vs;
-            const CUtensorMap *map = which == 0 ? &tmk : which == 1 ? &tmq : &tmv;
-            tc::tma_load_4d(dst, map, 0, c2.tok0, 0, which == 2 ? hv2 : hv2 / P.G, &S.lbar);
-        }
-    };
-    auto fetch_gam = [&](size_t un) {  // the per-channel cumulative gate tile [CT][DT], fp32
-        if constexpr (PC) tc::bulk_g2s(gamK, P.gam + un * CT * DT, CT * DT * 4, &S.lbar);
-    };
     int item = valid_from(blockIdx.x);
     if (item >= n_items) return;
     if (tid == 0) {
@@ -278,10 +246,6 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
         issue_HdH(item);
         issue_DdV(item);
         issue_TVn(item);
-        fetch_in(item, 0);
-        fetch_in(item, 1);
-        fetch_in(item, 2);
-        fetch_gam((size_t)item);
     }
     uint32_t parity = 0;
     while (item < n_items) {
@@ -293,66 +257,36 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
         const int next = valid_from(item + gridDim.x);
         const bool has_next = next < n_items;
 
-        // ---- stage the inputs as fp16 tiles (the workspace tiles, and for 16-bit inputs the raw q, k, v tiles
-        // and the gate tile, are already on their way)
-        if constexpr (!kRaw) {  // fp32 inputs: straight into the column-block-major tiles
-            const Tin *const src[3] = {reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K,
-                                       reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K,
-                                       reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V};
+        // ---- stage the inputs as fp16 tiles (the workspace tiles are already on their way)
+        const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
+        const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
+        const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
+        {
             unsigned char *const dst[3] = {S.Ks, S.Qs, S.Vs};
+            const Tin *const src[3] = {kp, qp, vp};
             const size_t st[3] = {(size_t)P.Hk * P.K, (size_t)P.Hk * P.K, (size_t)P.Hv * P.V};
-            const int ncw[3] = {P.K, P.K, P.V};
-            for (int w = 0; w < 3; ++w)
-                for (int e = tid; e < CT * DT / 8; e += K4_THREADS) {
-                    const int r = e & (CT - 1), c8 = 8 * (e >> 6);
-                    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    if (r < len && c8 < ncw[w]) load8(reinterpret_cast<const float *>(src[w]) + (size_t)r * st[w] + c8, f);
-                    *reinterpret_cast<uint4 *>(dst[w] + e * 16) = pack8_half(f);
-                }
+            const int nc[3] = {P.K, P.K, P.V};
+            const float mul[3] = {1.f, 1.f, 1.f};
+            stage_ct_n<Tin, K4_THREADS, 3>(dst, src, st, nc, mul, len, tid);
         }
         if (tid < CT) {
             S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
             if (!PC) S.gam[tid] = P.gam[u * CT + tid];
         }
-        const bool loaded = tc::mbar_wait(&S.lbar, parity, P.spin);
-        if constexpr (kRaw) {
-            // this thread's 16-byte chunks of the landed tiles: bf16 -> fp16 in place; rows past the chunk and
-            // columns past K or V become zero (a box also covers the next sequence's rows and leaves the column
-            // blocks past K / 8 or V / 8 unset)
-            if (loaded) {
-                unsigned char *const dst[3] = {S.Ks, S.Qs, S.Vs};
-                const int ncw[3] = {P.K, P.K, P.V};
-#pragma unroll
-                for (int w = 0; w < 3; ++w)
-#pragma unroll
-                    for (int i = 0; i < CT * DT / 8 / K4_THREADS; ++i) {
-                        const int e = tid + K4_THREADS * i, r = e & (CT - 1), c8 = 8 * (e >> 6);
-                        uint4 *p = reinterpret_cast<uint4 *>(dst[w] + e * 16);
-                        if (r < len && c8 < ncw[w]) {
-                            if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
-                                Raw8<Tin> x;
-                                x.v = *p;
-                                float f[8];
-                                raw_get(x, f);
-                                *p = pack8_half(f);
-                            }
-                        } else {
-                            *p = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                    }
-                tc::fence_smem_to_async();  // (a later tensor-map load overwrites these chunks)
-            }
+        if (PC)
+            for (int e = tid; e < CT * DT; e += K4_THREADS) gamK[e] = P.gam[u * CT * DT + e];
+        __syncthreads();  // barrier initialised (first item); tiles of the previous item no longer read
+        if (!PC && tid < CT) {
+            S.G[tid] = __expf(S.gam[tid]);
+            S.GC[tid] = __expf(S.gam[len - 1] - S.gam[tid]);
         }
-        if (__syncthreads_or(!loaded)) {  // (also: the staged tiles are complete)
+        const bool loaded = tc::mbar_wait(&S.lbar, parity, P.spin);
+        if (__syncthreads_or(!loaded)) {
             if (tid == 0) {
                 flag_status(P.status, ST_TIMEOUT);
                 tc::mbar_wait(&S.lbar, parity, DRAIN_LIMIT);  // this item's tiles land before the CTA exits
             }
             return;
-        }
-        if (!PC && tid < CT) {  // (first read after the next barrier)
-            S.G[tid] = __expf(S.gam[tid]);
-            S.GC[tid] = __expf(S.gam[len - 1] - S.gam[tid]);
         }
         parity ^= 1u;
 
@@ -361,9 +295,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
         // C x C tiling: rows cm0 .. cm0+15, columns cn0 .. cn0+15
         const int cm0 = (wid & 3) * 16, cn0 = (wid >> 2) * (NC * 8);
         auto G_ = [&](int r, int c) -> float { return PC ? gamK[r * DT + c] : S.gam[r]; };
-        auto Kv = [&](int r, int c) -> float {
-            return __half2float(*reinterpret_cast<const __half *>(S.Ks + cbtile_off(r, c, CT)));
-        };
+        auto Kv = [&](int r, int c) -> float { return ctile_get(S.Ks, r, c, DT); };
         const int rl = len - 1;
         auto row_dbeta = [&](int r) -> float {
             float x = 0.f;
@@ -410,7 +342,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
                     dq[0][nt][e] *= PC ? __expf(G_(acc_row(m0, 0, e), acc_col(n0, nt, e))) : S.G[acc_row(m0, 0, e)];
             if (WY) {
             } else if (!PC) {
-                warp_mma_ct<1, NK, false, false, TL_ROWB, TL_COLB>(dq, S.Pms, CT, S.Ks, CT, m0, n0, CT);
+                warp_mma_ct<1, NK, false, false>(dq, S.Pms, CT, S.Ks, DT, m0, n0, CT);
             } else {
                 decayed_acc<true, true>(dq, S.Pms, S.Ks, gamK, m0, n0, lane);
             }
@@ -419,7 +351,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                    add_dg(nt, e, __half2float(*reinterpret_cast<const __half *>(S.Qs + cbtile_off(r, c, CT))) * dq[0][nt][e]);
+                    add_dg(nt, e, ctile_get(S.Qs, r, c, DT) * dq[0][nt][e]);
                 }
             if (P.G == 1)
                 store_ck(dq, m0, n0, len, P.K, reinterpret_cast<char *>(P.dq) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
@@ -432,7 +364,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
             zero_acc(dk);
             if (WY) {
             } else if (!PC) {
-                warp_mma_ct<1, NK, true, false, TL_ROWB, TL_COLB>(dk, S.Pms, CT, S.Qs, CT, m0, n0, CT);
+                warp_mma_ct<1, NK, true, false>(dk, S.Pms, CT, S.Qs, DT, m0, n0, CT);
             } else {
                 decayed_acc<false, true>(dk, S.Pms, S.Qs, gamK, m0, n0, lane);
             }
@@ -552,9 +484,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
             float a[1][NC][4], b[1][NC][4];
             zero_acc(a);
             zero_acc(b);
-            if (PC) warp_mma_ct<1, NC, false, true>(a, dWs, DT, KGb, DT, cm0, cn0, DT);
-            else warp_mma_ct<1, NC, false, true, TL_ROWB, TL_COLB>(a, dWs, DT, S.Ks, CT, cm0, cn0, DT);
-            warp_mma_ct<1, NC, true, true, TL_ROWB, TL_COLB>(b, S.NdVT, CT, S.Vs, CT, cm0, cn0, DT);  // = -(dV_new V^T)
+            warp_mma_ct<1, NC, false, true>(a, dWs, DT, PC ? KGb : S.Ks, DT, cm0, cn0, DT);
+            warp_mma_ct<1, NC, true, true>(b, S.NdVT, CT, S.Vs, DT, cm0, cn0, DT);  // = -(dV_new V^T)
 #pragma unroll
             for (int nt = 0; nt < NC; ++nt)
 #pragma unroll
@@ -594,18 +525,16 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
                 for (int e = 0; e < 4; ++e) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                     float x = -t[0][nt][e];
-                    rowb[e >> 1] += x * __half2float(*reinterpret_cast<const __half *>(S.Vs + cbtile_off(r, c, CT)));
+                    rowb[e >> 1] += x * ctile_get(S.Vs, r, c, DT);
                     t[0][nt][e] = S.beta[r] * x;
                 }
             store_ck(t, m0, n0, len, P.V, reinterpret_cast<char *>(P.dv) + ((size_t)ci.tok0 * P.Hv + hv) * P.V *
                      (P.dv_dtype == F32 ? 4 : 2), (size_t)P.Hv * P.V, P.dv_dtype);
         }
-        tc::fence_smem_to_async();  // (beta Gamma K was written over Q's tile; the next Q lands there)
-        __syncthreads();  // dTs complete; D (as dW), -dV_new^T, V and beta Gamma K read for the last time
+        __syncthreads();  // dTs complete; D (as dW) and -dV_new^T read for the last time
         if (tid == 0 && has_next) {
+            tc::fence_smem_to_async();
             issue_DdV(next);
-            fetch_in(next, 1);
-            fetch_in(next, 2);
         }
 
         // ---- S9: X = dT T^T -> Xs
@@ -641,7 +570,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
             }
             if (!PC && !WY) {
                 zero_acc(kk);
-                warp_mma_ct<1, NC, false, true, TL_COLB, TL_COLB>(kk, S.Ks, CT, S.Ks, CT, cm0, cn0, DT);
+                warp_mma_ct<1, NC, false, true>(kk, S.Ks, DT, S.Ks, DT, cm0, cn0, DT);
             }
             float rb[2] = {0.f, 0.f};
 #pragma unroll
@@ -688,8 +617,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
             zero_acc(a);
             zero_acc(b);
             if (!PC) {
-                warp_mma_ct<1, NK, false, false, TL_ROWB, TL_COLB>(a, Es, CT, S.Ks, CT, m0, n0, CT);
-                warp_mma_ct<1, NK, true, false, TL_ROWB, TL_COLB>(b, Es, CT, S.Ks, CT, m0, n0, CT);
+                warp_mma_ct<1, NK, false, false>(a, Es, CT, S.Ks, DT, m0, n0, CT);
+                warp_mma_ct<1, NK, true, false>(b, Es, CT, S.Ks, DT, m0, n0, CT);
             } else {
                 decayed_acc<true, false>(a, Es, S.Ks, gamK, m0, n0, lane);
                 decayed_acc<false, false>(b, Es, S.Ks, gamK, m0, n0, lane);
@@ -755,10 +684,6 @@ __global__ void __launch_bounds__(K4_THREADS, 1)
             if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = row_dbeta(tid);
         }
         __syncthreads();  // the next item overwrites the staged inputs and the partial-sum slots
-        if (tid == 0 && has_next) {  // K and the gate tile were read for the last time in this item
-            fetch_in(next, 0);
-            fetch_gam((size_t)next);
-        }
         item = next;
     }
 }
@@ -772,18 +697,8 @@ static cudaError_t launch_k4_t(const Params &P, cudaStream_t stream) {
     if ((e = device_sm_count(&nsm)) != cudaSuccess) return e;
     const long items = (long)P.max_chunks * P.Hv;
     if (items == 0) return cudaSuccess;
-    CUtensorMap mk, mq, mv;
-    memset(&mk, 0, sizeof(mk));
-    memset(&mq, 0, sizeof(mq));
-    memset(&mv, 0, sizeof(mv));
-    if (sizeof(Tin) == 2) {
-        const long long tokens = (long long)P.B * P.T;
-        if ((e = encode_rows_map(&mk, P.k, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
-        if ((e = encode_rows_map(&mq, P.q, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
-        if ((e = encode_rows_map(&mv, P.v, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
-    }
     const int grid = (int)(items < nsm ? items : nsm);  // one persistent CTA per SM
-    k4_intra_grad<Tin, PC, WY><<<grid, K4_THREADS, smem, stream>>>(P, mk, mq, mv);
+    k4_intra_grad<Tin, PC, WY><<<grid, K4_THREADS, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
