@@ -31,6 +31,9 @@
 namespace gdr {
 
 constexpr int K1_THREADS = 256;
+// row strides (floats) of the fp32 A / T array and the doubling scratch: 4 mod 32, so that the 8 rows x 4 columns
+// of a TF32 fragment read fall on 32 distinct banks
+constexpr int ATLD = CT + 4, XLD = 32 + 4;
 constexpr int GKLD = DT + 4;  // row stride of the per-channel cumulative gate in shared memory (rows 16 bytes
                               // apart in bank terms, so a quarter-warp's 16-byte row reads do not collide)
 
@@ -56,7 +59,7 @@ struct __align__(1024) K1Smem {
     // scratch of the inverse's block products; Qs later holds beta Gamma K and Vs beta V (fp16, in place).  AT
     // holds the raw dO rows on their way to the D tile, then A_kk, then in place its inverse T (fp32).
     unsigned char Ks[CT * DT * 2], Qs[CT * DT * 2], Vs[CT * DT * 2];
-    float AT[CT][CT + 1];
+    float AT[CT][ATLD];
     float gam[CT];
     float beta[CT];
     uint64_t rbar;  // 16-bit inputs: the raw rows' bulk copies
@@ -103,7 +106,7 @@ __device__ __forceinline__ void mma1688_3xtf32(float (&c)[4], const float (&a)[4
 // tiles, one per warp, as three-pass TF32 warp MMAs over the reduction in steps of 8.  A level reads A only in
 // the blocks it then overwrites, after the barrier between its two products.
 template <int B>
-__device__ __forceinline__ void inv_level_tc(float (&T)[CT][CT + 1], float (&X)[32][33], int wid, int lane) {
+__device__ __forceinline__ void inv_level_tc(float (&T)[CT][ATLD], float (&X)[32][XLD], int wid, int lane) {
     constexpr int NP = CT / (2 * B);         // block pairs
     constexpr int PT = (B / 16) * (B / 8);   // 16 x 8 output tiles of one pair's B x B product
     static_assert(NP * PT <= K1_THREADS / 32 && NP * B <= 32, "one output tile per warp; X holds every pair");
@@ -545,7 +548,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
     }
     __syncthreads();
     unsigned char *const oT = S.Ks;  // K is no longer needed
-    float (&X32)[32][33] = *reinterpret_cast<float (*)[32][33]>(S.Ks + CT * CT * 2);
+    float (&X32)[32][XLD] = *reinterpret_cast<float (*)[32][XLD]>(S.Ks + CT * CT * 2);
     // off-diagonal blocks by recursive doubling: for a lower block split [[T_11, 0], [X, T_22]] of an inverse,
     // X = -T_22 A_21 T_11.  First the two 32 x 32 diagonal blocks from their 16 x 16 halves, then the whole.
     inv_level_tc<16>(S.AT, X32, wid, lane);
