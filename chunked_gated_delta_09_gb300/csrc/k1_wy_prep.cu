@@ -123,10 +123,8 @@ __device__ __forceinline__ void inv_level_tc(float (&T)[CT][ATLD], float (&X)[32
             const float b[2] = {T[lo + k0 + t][lo + c0 + g], T[lo + k0 + t + 4][lo + c0 + g]};
             mma1688_3xtf32(c, a, b);
         }
-        X[p * B + r0 + g][c0 + 2 * t] = c[0];
-        X[p * B + r0 + g][c0 + 2 * t + 1] = c[1];
-        X[p * B + r0 + g + 8][c0 + 2 * t] = c[2];
-        X[p * B + r0 + g + 8][c0 + 2 * t + 1] = c[3];
+        *reinterpret_cast<float2 *>(&X[p * B + r0 + g][c0 + 2 * t]) = make_float2(c[0], c[1]);
+        *reinterpret_cast<float2 *>(&X[p * B + r0 + g + 8][c0 + 2 * t]) = make_float2(c[2], c[3]);
     }
     __syncthreads();
     if (act) {  // T[hi + r][lo + c] = -sum_k T[hi + r][hi + k] X[p B + k][c]
@@ -138,10 +136,8 @@ __device__ __forceinline__ void inv_level_tc(float (&T)[CT][ATLD], float (&X)[32
             const float b[2] = {X[p * B + k0 + t][c0 + g], X[p * B + k0 + t + 4][c0 + g]};
             mma1688_3xtf32(c, a, b);
         }
-        T[hi + r0 + g][lo + c0 + 2 * t] = -c[0];
-        T[hi + r0 + g][lo + c0 + 2 * t + 1] = -c[1];
-        T[hi + r0 + g + 8][lo + c0 + 2 * t] = -c[2];
-        T[hi + r0 + g + 8][lo + c0 + 2 * t + 1] = -c[3];
+        *reinterpret_cast<float2 *>(&T[hi + r0 + g][lo + c0 + 2 * t]) = make_float2(-c[0], -c[1]);
+        *reinterpret_cast<float2 *>(&T[hi + r0 + g + 8][lo + c0 + 2 * t]) = make_float2(-c[2], -c[3]);
     }
     __syncthreads();
 }
@@ -312,13 +308,14 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
 #pragma unroll
             for (int e = 0; e < 4; e += 2) {
                 const int i = acc_row(m0, 0, e), j = acc_col(n0, nt, e);
-                float aq[2];
+                float aq[2], ak[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const float d = __expf(S.gam[i] - S.gam[j + h]);  // selected only where the argument is <= 0
-                    S.AT[i][j + h] = j + h < i ? S.beta[i] * d * kk[0][nt][e + h] : 0.f;
+                    ak[h] = j + h < i ? S.beta[i] * d * kk[0][nt][e + h] : 0.f;
                     aq[h] = j + h <= i ? d * qk[0][nt][e + h] : 0.f;
                 }
+                *reinterpret_cast<float2 *>(&S.AT[i][j]) = make_float2(ak[0], ak[1]);
                 *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j, CT)) = __floats2half2_rn(aq[0], aq[1]);
             }
     } else {
@@ -341,9 +338,9 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
             for (int bb = 0; bb < 2; ++bb) {
                 const int j = j0 + bb;
                 kd[bb] = (j < i && i < len) ? akk[bb] : 0.f;
-                S.AT[i][j] = S.beta[i] * kd[bb];
                 aq[bb] = (j <= i && i < len) ? aqk[bb] : 0.f;
             }
+            *reinterpret_cast<float2 *>(&S.AT[i][j0]) = make_float2(S.beta[i] * kd[0], S.beta[i] * kd[1]);
             *reinterpret_cast<__half2 *>(aqk_g + ctile_off(i, j0, CT)) = __floats2half2_rn(aq[0], aq[1]);
             if (kd_g) *reinterpret_cast<__half2 *>(kd_g + ctile_off(i, j0, CT)) = __floats2half2_rn(kd[0], kd[1]);
         };
@@ -557,7 +554,10 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
         int i = e / (CT / 8), j8 = (e % (CT / 8)) * 8;
         float x[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = S.AT[i][j8 + t];
+        for (int t = 0; t < 8; t += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(&S.AT[i][j8 + t]);
+            x[t] = v.x, x[t + 1] = v.y, x[t + 2] = v.z, x[t + 3] = v.w;
+        }
         tc::st_tile8(oT, i, j8, CT, x);
         tc::st_tile8(reinterpret_cast<unsigned char *>(P.Tm + u * CT * CT), i, j8, CT, x);
     }
