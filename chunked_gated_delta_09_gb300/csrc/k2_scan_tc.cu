@@ -15,6 +15,9 @@
 // One CTA holds the whole 128 x 128 fp32 state (and Phi) in tensor memory; each step issues two MMA
 // groups: V_new^T = S W^T (M = 128 state rows, N = 64 tokens) and S += V_new^T K~ (N = 128).  Operand
 // tiles arrive by bulk copy one chunk ahead; h_n and V_new^T leave by bulk copy from the operand tiles.
+// The local pass, which stores neither, keeps its fp16 A operands (the state and transition rows, V_new^T and
+// -(Phi W^T)) in tensor memory instead of shared memory: the products then read only their B tiles from
+// shared memory, whose bandwidth bounds the step.
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
 #include "tc_util.cuh"
@@ -26,10 +29,8 @@ constexpr int SC_THREADS = 256;
 template <bool LOCAL>
 struct __align__(1024) FwdSmem {
     unsigned char W[2][CT * DT * 2], Kt[2][CT * DT * 2], U[2][CT * DT * 2];  // U holds U^T tiles [v][c]
-    unsigned char Sa[DT * DT * 2];                // state rows as fp16 (A operand; h_n)
-    unsigned char Vna[DT * CT * 2];               // V_new^T [v][c] (A operand)
-    unsigned char Pa[LOCAL ? DT * DT * 2 : 16];   // transition rows as fp16
-    unsigned char Vpa[LOCAL ? DT * CT * 2 : 16];  // -(Phi W^T)
+    unsigned char Sa[LOCAL ? 16 : DT * DT * 2];   // state rows as fp16 (A operand; h_n): final pass only
+    unsigned char Vna[LOCAL ? 16 : DT * CT * 2];  // V_new^T [v][c] (A operand): final pass only
     float gam[2][DT];                             // gate row block of the chunk (scalar: first CT used)
     uint64_t bar, lbar[2];  // MMA completion, the two tile buffers' loads
     uint32_t tslot;
@@ -91,6 +92,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
     if (tid == 0) issue(c_lo, 0);
     const uint32_t tm = S.tslot;
     constexpr int T_S = 0, T_P = 128, T_VN = LOCAL ? 256 : 128, T_VP = 320;
+    // local pass: the fp16 A operands, packed two per column: state rows (64 columns), then V_new^T over their
+    // first 32 columns once the state's product has completed; the same for the transition rows
+    constexpr int T_SA = 384, T_PA = 448;
 
     // ---- initial state: zero (local pass) or the exact entry state (final pass); transition = I
     {
@@ -118,7 +122,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
         }
         tc::wait_st();
     }
-    const uint32_t sSa = smem_u32(S.Sa), sVna = smem_u32(S.Vna), sPa = smem_u32(S.Pa), sVpa = smem_u32(S.Vpa);
+    const uint32_t sSa = smem_u32(S.Sa), sVna = smem_u32(S.Vna);
     uint32_t parity = 0, lpar0 = 0, lpar1 = 0;
     bool lost = false;
     bool mma_ok = true;  // false: the last MMA commit's phase is still pending (the exit drains it)
@@ -154,14 +158,17 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
 #pragma unroll
         for (int m = 0; m < (LOCAL ? 2 : 1); ++m) {
             const int tcol = m ? T_P : T_S;
-            unsigned char *tile = m ? S.Pa : S.Sa;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int c0 = 64 * half + 32 * h;
                 float v[32];
                 tc::ld32(tc::taddr(tm, tcol + c0), v);
+                if constexpr (LOCAL) {
+                    tc::st32_f16(tc::taddr(tm, (m ? T_PA : T_SA) + c0 / 2), v);
+                } else {
 #pragma unroll
-                for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(tile, row, c0 + j8, DT, v + j8);
+                    for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.Sa, row, c0 + j8, DT, v + j8);
+                }
                 if (PC) {
 #pragma unroll
                     for (int t = 0; t < 32; ++t) v[t] *= expf(S.gam[buf][c0 + t]);
@@ -180,9 +187,14 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
         tc::fence_after();
         // MMA 1: V_new^T (pre) = S W^T   [and  Phi W^T];  h_n leaves by bulk copy
         if (tid == 0) {
-            tc::gemm(tm + T_VN, sSa, DT, false, smem_u32(S.W[buf]), DT, false, 128, 64, DT, false);
-            if (LOCAL) tc::gemm(tm + T_VP, sPa, DT, false, smem_u32(S.W[buf]), DT, false, 128, 64, DT, false);
-            if (!LOCAL) tc::bulk_s2g(P.h + u * DT * DT, S.Sa, DT * DT * 2);
+            if constexpr (LOCAL) {
+                const tc::Operand w = tc::op_rows(smem_u32(S.W[buf]), DT, false);
+                tc::gemm_ta(tm + T_VN, tm + T_SA, w, 64, DT, false);
+                tc::gemm_ta(tm + T_VP, tm + T_PA, w, 64, DT, false);
+            } else {
+                tc::gemm(tm + T_VN, sSa, DT, false, smem_u32(S.W[buf]), DT, false, 128, 64, DT, false);
+                tc::bulk_s2g(P.h + u * DT * DT, S.Sa, DT * DT * 2);
+            }
         }
         mma_done();
         if (lost) break;
@@ -202,14 +214,16 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
                     v[j8 + 2 * t + 1] = f.y - v[j8 + 2 * t + 1];
                 }
             }
-#pragma unroll
-            for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.Vna, row, c0 + j8, CT, v + j8);
-            if (LOCAL) {
+            if constexpr (LOCAL) {
+                tc::st32_f16(tc::taddr(tm, T_SA + c0 / 2), v);
                 tc::ld32(tc::taddr(tm, T_VP + c0), v);
 #pragma unroll
                 for (int t = 0; t < 32; ++t) v[t] = -v[t];
+                tc::st32_f16(tc::taddr(tm, T_PA + c0 / 2), v);
+                tc::wait_st();
+            } else {
 #pragma unroll
-                for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.Vpa, row, c0 + j8, CT, v + j8);
+                for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.Vna, row, c0 + j8, CT, v + j8);
             }
         }
         tc::fence_smem_to_async();
@@ -218,9 +232,12 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
         tc::fence_after();
         // MMA 2: S += V_new^T K~   [Phi += (-(Phi W^T)) K~];  V_new^T leaves by bulk copy
         if (tid == 0) {
-            tc::gemm(tm + T_S, sVna, CT, false, smem_u32(S.Kt[buf]), DT, true, 128, 128, CT, true);
-            if (LOCAL) tc::gemm(tm + T_P, sVpa, CT, false, smem_u32(S.Kt[buf]), DT, true, 128, 128, CT, true);
-            if (!LOCAL) {
+            if constexpr (LOCAL) {
+                const tc::Operand kt = tc::op_rows(smem_u32(S.Kt[buf]), DT, true);
+                tc::gemm_ta(tm + T_S, tm + T_SA, kt, 128, CT, true);
+                tc::gemm_ta(tm + T_P, tm + T_PA, kt, 128, CT, true);
+            } else {
+                tc::gemm(tm + T_S, sVna, CT, false, smem_u32(S.Kt[buf]), DT, true, 128, 128, CT, true);
                 tc::bulk_s2g(P.Vn + u * DT * CT, S.Vna, DT * CT * 2);
                 tc::bulk_commit();
             }

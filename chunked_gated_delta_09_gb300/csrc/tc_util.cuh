@@ -91,6 +91,20 @@ __device__ __forceinline__ Operand op_cols(uint32_t tile, int R, bool mn) {
     return mn ? Operand{smem_desc(tile, 128, cb), 256u / 16u, true} : Operand{smem_desc(tile, cb, 128), 2u * cb / 16u, false};
 }
 
+// D (+)= A B^T with A in tensor memory: M = 128 rows on the lanes, the 16-bit elements of a row packed two per
+// 32-bit column (element 2m in the low half of column m), so a reduction step of 16 is 8 columns on.
+__device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void gemm_ta(uint32_t d_tmem, uint32_t a_tmem, Operand b, int N, int Kr, bool accumulate) {
+    const uint32_t id = idesc_f16(128, N, false, b.mn);
+    for (int kk = 0; kk < Kr / 16; ++kk)
+        mma_ta(d_tmem, a_tmem + 8u * kk, b.desc + (uint64_t)(kk * b.step), id, (accumulate || kk > 0) ? 1u : 0u);
+}
+
 // D[M x N] (+)= A[M x Kr] B[N x Kr]^T for operands of either tile order.
 __device__ __forceinline__ void gemm_ops(uint32_t d_tmem, Operand a, Operand b, int M, int N, int Kr, bool accumulate) {
     const uint32_t id = idesc_f16(M, N, a.mn, b.mn);
@@ -259,6 +273,20 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])));
+}
+// 32 values of this thread's row -> 16 consecutive columns of fp16 pairs (an A operand in tensor memory).
+__device__ __forceinline__ void st32_f16(uint32_t taddr, const float (&v)[32]) {
+    uint32_t p[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const __half2 h = __floats2half2_rn(v[2 * m], v[2 * m + 1]);
+        p[m] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+            taddr),
+        "r"(p[0]), "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]), "r"(p[6]), "r"(p[7]), "r"(p[8]), "r"(p[9]),
+        "r"(p[10]), "r"(p[11]), "r"(p[12]), "r"(p[13]), "r"(p[14]), "r"(p[15]));
 }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
