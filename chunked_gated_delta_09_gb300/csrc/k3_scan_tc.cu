@@ -11,7 +11,8 @@
 //   final pass (LOCAL = false): every segment runs from its exact exit gradient and writes dh_n and
 //     -dV_new^T; segment 0 also writes dh0.
 // One CTA holds the 128 x 128 fp32 dS in tensor memory; each step issues two MMA groups.  Operand tiles
-// arrive by bulk copy one chunk ahead; dh_n and -dV_new^T leave by bulk copy from the operand tiles.
+// arrive by bulk copy one chunk ahead; dh_n and -dV_new^T leave by bulk copy from the operand tiles.  The
+// local pass, which stores neither, keeps its fp16 A operands (dS rows, -dV_new^T) in tensor memory.
 // FACT (local pass only): the factored step of the dh-gradient kernel of section 3 of the same page,
 // dS <- Gamma_C dS + D^T QR - (dS K~^T) W with QR = Q~ - Aqk W formed per chunk by k8_qr.cu, which needs
 // neither Aqk nor dV_new inside the step (selected with GDR_DH_FACTORED=1).
@@ -90,6 +91,9 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
     if (tid == 0) issue(c_hi - 1, (c_hi - 1 - c_lo) & 1);
     const uint32_t tm = S.tslot;
     constexpr int T_S = 0, T_DV = 128;
+    // local pass: dS rows as fp16 pairs (64 columns), then -dV_new^T over their first 32 once the product
+    // that reads dS has completed
+    constexpr int T_SA = 192;
     {
         const float *src = nullptr;
         if (!LOCAL) src = NS > 1 ? P.segdS + su * DT * DT : (P.dht ? P.dht + ((size_t)s * P.Hv + hv) * P.V * P.K : nullptr);
@@ -147,8 +151,12 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
             const int c0 = 64 * half + 32 * h;
             float v[32];
             tc::ld32(tc::taddr(tm, T_S + c0), v);
+            if constexpr (LOCAL) {
+                tc::st32_f16(tc::taddr(tm, T_SA + c0 / 2), v);
+            } else {
 #pragma unroll
-            for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.dSa, row, c0 + j8, DT, v + j8);
+                for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.dSa, row, c0 + j8, DT, v + j8);
+            }
             if (PC) {
 #pragma unroll
                 for (int t = 0; t < 32; ++t) v[t] *= expf(S.gam[buf][c0 + t]);
@@ -168,8 +176,12 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
         if (tid == 0) {  // (FACT: only Y = dS K~^T)
             if (!FACT)
                 tc::gemm(tm + T_DV, smem_u32(S.D[buf]), DT, true, smem_u32(S.Aq[buf]), CT, true, 128, 64, CT, false);
-            tc::gemm(tm + T_DV, sdSa, DT, false, smem_u32(S.Kt[buf]), DT, false, 128, 64, DT, !FACT);
-            if (!LOCAL) tc::bulk_s2g(P.dh + u * DT * DT, S.dSa, DT * DT * 2);
+            if constexpr (LOCAL) {
+                tc::gemm_ta(tm + T_DV, tm + T_SA, tc::op_rows(smem_u32(S.Kt[buf]), DT, false), 64, DT, !FACT);
+            } else {
+                tc::gemm(tm + T_DV, sdSa, DT, false, smem_u32(S.Kt[buf]), DT, false, 128, 64, DT, !FACT);
+                tc::bulk_s2g(P.dh + u * DT * DT, S.dSa, DT * DT * 2);
+            }
         }
         mma_done();
         if (lost) break;
@@ -180,8 +192,13 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
             tc::ld32(tc::taddr(tm, T_DV + c0), v);
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] = -v[t];
+            if constexpr (LOCAL) {
+                tc::st32_f16(tc::taddr(tm, T_SA + c0 / 2), v);
+                tc::wait_st();
+            } else {
 #pragma unroll
-            for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.dVa, row, c0 + j8, CT, v + j8);
+                for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.dVa, row, c0 + j8, CT, v + j8);
+            }
         }
         tc::fence_smem_to_async();
         tc::fence_before();
@@ -190,7 +207,8 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
         // MMA 2: dS += D^T Q~ - dV_new^T W;  -dV_new^T leaves by bulk copy
         if (tid == 0) {
             tc::gemm(tm + T_S, smem_u32(S.D[buf]), DT, true, smem_u32(S.Qg[buf]), DT, true, 128, 128, CT, true);
-            tc::gemm(tm + T_S, sdVa, CT, false, smem_u32(S.W[buf]), DT, true, 128, 128, CT, true);
+            if constexpr (LOCAL) tc::gemm_ta(tm + T_S, tm + T_SA, tc::op_rows(smem_u32(S.W[buf]), DT, true), 128, CT, true);
+            else tc::gemm(tm + T_S, sdVa, CT, false, smem_u32(S.W[buf]), DT, true, 128, 128, CT, true);
             if (!LOCAL) {
                 tc::bulk_s2g(P.dVn + u * DT * CT, S.dVa, DT * CT * 2);
                 tc::bulk_commit();
