@@ -6,7 +6,7 @@
 // transitions (k2_scan_tc.cu writes Phi_s and Phi_s^T, k3_scan_tc.cu writes F_s).  Rows of the state are
 // independent, so a CTA owns CB_ROWS rows of one sequence x head (one wave of CTAs for the usual head
 // counts) and walks the segments serially, prefetching the next segment's transition and summary rows
-// with cp.async while it multiplies by the current ones.  Each thread accumulates four columns of all
+// while it multiplies by the current ones.  Each thread accumulates four columns of all
 // the CTA's rows over one warp's slice of the reduction, so every transition element read from shared
 // memory serves 16 rows; the slices are summed in a fixed order.  The prefetch is two bulk copies (the
 // transition, 64 KB, and the CTA's summary rows, 8 KB, both contiguous) by one thread on the buffer's
