@@ -177,6 +177,24 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
         if (2 * lane < len) gx0 = P.g[(size_t)(ci.tok0 + 2 * lane) * P.Hv + hv];
         if (2 * lane + 1 < len) gx1 = P.g[(size_t)(ci.tok0 + 2 * lane + 1) * P.Hv + hv];
     }
+    if constexpr (PC) {
+        // the chunk's per-channel gate rows, raw, into the gate tile by asynchronous copies (every thread, all in
+        // flight at once; 16 bytes each when the gate tensor is 16-byte aligned, else 4); the cumulative sum below
+        // runs over shared memory
+        if ((reinterpret_cast<uintptr_t>(P.g) & 15u) == 0) {
+            const int c4n = P.K >> 2;
+            for (int e = tid; e < len * c4n; e += K1_THREADS) {
+                const int i = e / c4n, c4 = 4 * (e - i * c4n);
+                cp_async16(gamK + i * GKLD + c4, P.g + ((size_t)(ci.tok0 + i) * P.Hv + hv) * P.K + c4);
+            }
+        } else {
+            for (int e = tid; e < len * P.K; e += K1_THREADS) {
+                const int i = e / P.K, c = e - i * P.K;
+                cp_async4(gamK + i * GKLD + c, P.g + ((size_t)(ci.tok0 + i) * P.Hv + hv) * P.K + c);
+            }
+        }
+        cp_async_commit();
+    }
     const int nin = P.dO ? 4 : 3;
     unsigned char *const slot[4] = {S.Ks, S.Qs, S.Vs, reinterpret_cast<unsigned char *>(&S.AT[0][0])};
     const int nc[4] = {P.K, P.K, P.V, P.V};
@@ -206,6 +224,7 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
                 flag_status(P.status, ST_TIMEOUT);
                 tc::mbar_wait(&S.rbar, 0, DRAIN_LIMIT);  // the tiles still in flight land before the CTA exits
             }
+            if constexpr (PC) cp_async_wait<0>();  // (and this thread's gate-row copies)
             return;
         }
         // a ragged chunk or narrow features: zero the rows past the chunk (the boxes also cover the next
@@ -273,12 +292,14 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
             P.gam[u * CT + r1] = excl + x0 + x1;
         }
     } else {
+        cp_async_wait<0>();
+        __syncthreads();  // the raw gate rows have landed
         if (tid < DT) {
             const int c = tid;
             float run = 0.f;
 #pragma unroll 8
             for (int i = 0; i < CT; ++i) {
-                if (i < len && c < P.K) run += P.g[((size_t)(ci.tok0 + i) * P.Hv + hv) * P.K + c];
+                if (i < len && c < P.K) run += gamK[i * GKLD + c];
                 gamK[i * GKLD + c] = run;
                 P.gam[(u * CT + i) * DT + c] = run;
             }

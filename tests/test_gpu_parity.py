@@ -121,3 +121,26 @@ def test_factored_state_gradient_on_the_t8k_workload(monkeypatch):
     monkeypatch.setenv("GDR_DH_FACTORED", "1")
     prob = workload("gdn_t8k_bf16")
     compare(prob, run_gpu(prob), oracle.problem_backward(prob))
+
+
+@pytest.mark.parametrize("offset", [0, 1], ids=["aligned16", "aligned4"])
+def test_per_channel_gate_tensor_alignment(offset):
+    """The per-channel gate may be only 4-byte aligned (the C ABI's rule for it): the WY preparation then
+    copies its rows 4 bytes at a time instead of 16.  Either way the gradients match the oracle."""
+    from chunked_gated_delta_09_gb300 import ops
+    prob = make_problem("kda_gate_align", B=1, T=200, Hk=1, Hv=2, K=64, V=64, per_channel=True, seed=31)
+    plan = ops.plan_for(prob)
+    dev = ops.problem_to_device(prob, "cuda")
+    g = dev["g"]
+    store = torch.empty(g.numel() + 4, dtype=g.dtype, device="cuda")
+    shifted = store[offset:offset + g.numel()].view_as(g)
+    shifted.copy_(g)
+    assert (shifted.data_ptr() % 16 == 0) == (offset == 0)
+    dev["g"] = shifted
+    out = plan.alloc_outputs("cuda")
+    ws = plan.alloc_workspace("cuda")
+    plan.run(out=out, workspace=ws, **dev)
+    assert plan.get_status(ws) == 0
+    torch.cuda.synchronize()
+    got = {k: v.float().cpu().to(torch.float64).numpy() for k, v in out.items()}
+    compare(prob, got, oracle.problem_backward(prob))
