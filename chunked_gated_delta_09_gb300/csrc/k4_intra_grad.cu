@@ -257,7 +257,12 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         const int next = valid_from(item + gridDim.x);
         const bool has_next = next < n_items;
 
-        // ---- stage the inputs as fp16 tiles (the workspace tiles are already on their way)
+        // ---- stage the inputs as fp16 tiles (the workspace tiles are already on their way); the per-channel gate
+        // tile (workspace, contiguous) by asynchronous 16-byte copies issued first, so that they overlap
+        if (PC) {
+            for (int e = 4 * tid; e < CT * DT; e += 4 * K4_THREADS) cp_async16(gamK + e, P.gam + u * CT * DT + e);
+            cp_async_commit();
+        }
         const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
         const Tin *qp = reinterpret_cast<const Tin *>(P.q) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
         const Tin *vp = reinterpret_cast<const Tin *>(P.v) + ((size_t)ci.tok0 * P.Hv + hv) * P.V;
@@ -273,9 +278,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             S.beta[tid] = tid < len ? load_scalar(P.beta, (size_t)(ci.tok0 + tid) * P.Hv + hv, P.beta_dtype) : 0.f;
             if (!PC) S.gam[tid] = P.gam[u * CT + tid];
         }
-        if (PC)
-            for (int e = tid; e < CT * DT; e += K4_THREADS) gamK[e] = P.gam[u * CT * DT + e];
-        __syncthreads();  // barrier initialised (first item); tiles of the previous item no longer read
+        if (PC) cp_async_wait<0>();
+        __syncthreads();  // barrier initialised (first item); the gate tile landed
         if (!PC && tid < CT) {
             S.G[tid] = __expf(S.gam[tid]);
             S.GC[tid] = __expf(S.gam[len - 1] - S.gam[tid]);
