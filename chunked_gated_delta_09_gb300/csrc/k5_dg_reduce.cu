@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(K5_THREADS) k5_dg_reduce(const Params P) {
     if (!chunk_info(P, n, ci)) return;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int len = ci.len;
+    __shared__ __align__(16) float dgt[PC ? CT : 1][DT];  // per-channel gate: one unit's d(gamma) rows
 
     // reverse cumsum of the gate gradient for each value head of this key head
     for (int hv = hk * P.G; hv < (hk + 1) * P.G; ++hv) {
@@ -55,10 +56,16 @@ __global__ void __launch_bounds__(K5_THREADS) k5_dg_reduce(const Params P) {
                 if (2 * lane + 1 < len) P.dg[(size_t)(ci.tok0 + 2 * lane + 1) * P.Hv + hv] = r1;
             }
         } else {
+            // the unit's d(gamma) tile [CT][DT] (contiguous) into shared memory first, all loads in flight at
+            // once, then one channel per thread walks the rows backwards over shared memory
+            __syncthreads();  // (the previous head's readers are done with the tile)
+            const float4 *src = reinterpret_cast<const float4 *>(P.dgam + u * CT * DT);
+            for (int e = tid; e < len * (DT / 4); e += K5_THREADS) reinterpret_cast<float4 *>(&dgt[0][0])[e] = src[e];
+            __syncthreads();
             for (int c = tid; c < P.K; c += K5_THREADS) {
                 float run = 0.f;
                 for (int r = len - 1; r >= 0; --r) {
-                    run += P.dgam[(u * CT + r) * DT + c];
+                    run += dgt[r][c];
                     P.dg[((size_t)(ci.tok0 + r) * P.Hv + hv) * P.K + c] = run;
                 }
             }
