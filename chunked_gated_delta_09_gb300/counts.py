@@ -115,11 +115,11 @@ def stage_bytes(prob) -> list:
         + (state if prob.h0 is not None else 0) + seg // 2                      # W, U, K~ (+ local pass); h, V_new
     k3 = u * ((tile_cc + 4 * tile_ck) * (2 if ns > 1 else 1) + tile_kk + tile_ck) \
         + (state if prob.dht is not None else 0) + state + seg // 2             # Aqk, D, K~, Q~, W; dh, dV_new; dh0
-    dqdk_out = 2 * C * K * (oq if G == 1 else 4)
+    dqdk_out = 2 * C * K * oq  # (with GQA: per-value-head partials in the output's type)
     scal_in = rec if rec else C * bb + CT * gk * 4  # the record, else beta and gamma
     k4 = u * (2 * tile_kk + 3 * tile_ck + tile_cc + 2 * C * K * ib + C * V * ib + scal_in   # reads
               + dqdk_out + C * V * ov + C * 4 + CT * gk * 4)                               # writes
-    k5 = u * (CT * gk * 4 + C * gk * 4) + (0 if G == 1 else u * 2 * C * K * 4 + (u // G) * 2 * C * K * oq)
+    k5 = u * (CT * gk * 4 + C * gk * 4) + (0 if G == 1 else u * 2 * C * K * oq + (u // G) * 2 * C * K * oq)
     return [float(k0), float(k1), float(k2), float(k3), float(k4), float(k5)]
 
 

@@ -74,7 +74,7 @@ struct Params {
     __half *Vn;          // tile [v][c]   128 x 64   V_new^T
     __half *dVn;         // tile [v][c]   128 x 64   -dV_new^T
     float *dgam;         // [u][CT] or [u][CT][DT]
-    float *dq_h, *dk_h;  // [T][Hv][K] per value head (GQA only)
+    float *dq_h, *dk_h;  // [T][Hv][K] per value head (GQA only), in gqa_part_dtype (workspace sized for fp32)
     // segment-parallel scans: NS segments of Lseg chunks per sequence; per (sequence, head, segment)
     // fp32 [DT][DT] summaries: local end state E, transition product Phi (and its transpose), local
     // start gradient F,
@@ -85,6 +85,13 @@ struct Params {
     // U^T region (dead once the forward scan has run)
     __half *QR;
 };
+
+// Element type of the per-value-head dq / dk partials that the GQA reduction sums: the output's own type
+// (fp32 outputs keep fp32 partials; 16-bit outputs take 16-bit partials, half the bytes to write and read).
+__device__ __forceinline__ int gqa_part_dtype(const Params &P) { return P.dqdk_dtype; }
+__device__ __forceinline__ char *gqa_part(float *base, size_t elem, const Params &P) {
+    return reinterpret_cast<char *>(base) + elem * (P.dqdk_dtype == F32 ? 4 : 2);
+}
 
 // ---------------------------------------------------------------- sequence / chunk bookkeeping
 struct ChunkInfo {

@@ -361,7 +361,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                 store_ck(dq, m0, n0, len, P.K, reinterpret_cast<char *>(P.dq) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
                          (P.dqdk_dtype == F32 ? 4 : 2), (size_t)P.Hk * P.K, P.dqdk_dtype);
             else
-                store_ck(dq, m0, n0, len, P.K, P.dq_h + ((size_t)ci.tok0 * P.Hv + hv) * P.K, (size_t)P.Hv * P.K, F32);
+                store_ck(dq, m0, n0, len, P.K, gqa_part(P.dq_h, ((size_t)ci.tok0 * P.Hv + hv) * P.K, P), (size_t)P.Hv * P.K,
+                         gqa_part_dtype(P));
         }
         // ---- S3: dk_O = P^T Q
         {
@@ -642,7 +643,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             store_ck(dk, m0, n0, len, P.K, reinterpret_cast<char *>(P.dk) + ((size_t)ci.tok0 * P.Hk + hk) * P.K *
                      (P.dqdk_dtype == F32 ? 4 : 2), (size_t)P.Hk * P.K, P.dqdk_dtype);
         else
-            store_ck(dk, m0, n0, len, P.K, P.dk_h + ((size_t)ci.tok0 * P.Hv + hv) * P.K, (size_t)P.Hv * P.K, F32);
+            store_ck(dk, m0, n0, len, P.K, gqa_part(P.dk_h, ((size_t)ci.tok0 * P.Hv + hv) * P.K, P), (size_t)P.Hv * P.K,
+                     gqa_part_dtype(P));
 
         // ---- gate gradient of the cumulative gate
         if (!PC) {

@@ -502,8 +502,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
                                   (((size_t)(ci.tok0 + c0) * P.Hk + hk) * P.K + k) * esize(P.dqdk_dtype),
                               P.dqdk_dtype, (size_t)P.Hk * P.K, nrow, k < P.K, a);
             else
-                store_pairs16(P.dq_h + ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, F32, (size_t)P.Hv * P.K,
-                              nrow, k < P.K, a);
+                store_pairs16(gqa_part(P.dq_h, ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, P), gqa_part_dtype(P),
+                              (size_t)P.Hv * P.K, nrow, k < P.K, a);
             ok2 = wait_group2();
             // dk_O
             tc::ld16x2(tc::taddr(tm, R_DKO + c0), b, tc::taddr(tm, R_TDW + c0), a);
@@ -644,8 +644,8 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
                                   (((size_t)(ci.tok0 + c0) * P.Hk + hk) * P.K + k) * esize(P.dqdk_dtype),
                               P.dqdk_dtype, (size_t)P.Hk * P.K, nrow, k < P.K, dk);
             else
-                store_pairs16(P.dk_h + ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, F32, (size_t)P.Hv * P.K,
-                              nrow, k < P.K, dk);
+                store_pairs16(gqa_part(P.dk_h, ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, P), gqa_part_dtype(P),
+                              (size_t)P.Hv * P.K, nrow, k < P.K, dk);
             // gate gradient: column sums over the feature rows
             const float s = tc::warp_transpose_sum16(dg);
             if (lane < 16) S.dg_q[pb][q][c0 + lane] = s;

@@ -26,6 +26,19 @@ __device__ __forceinline__ void store4(void *p, size_t i, float4 x, int dt) {
     }
 }
 
+// eight consecutive 16-bit values of type dt (one 16-byte load) as floats
+__device__ __forceinline__ void load8_16(const char *p, int dt, float (&o)[8]) {
+    if (dt == BF16) {
+        Raw8<__nv_bfloat16> x;
+        x.v = *reinterpret_cast<const uint4 *>(p);
+        raw_get(x, o);
+    } else {
+        Raw8<__half> x;
+        x.v = *reinterpret_cast<const uint4 *>(p);
+        raw_get(x, o);
+    }
+}
+
 template <bool PC>
 __global__ void __launch_bounds__(K5_THREADS) k5_dg_reduce(const Params P) {
     if (*P.status & ST_BAD_SEQLENS) return;
@@ -72,21 +85,45 @@ __global__ void __launch_bounds__(K5_THREADS) k5_dg_reduce(const Params P) {
         }
     }
     // GQA: dq[t, hk] = sum over the group's value heads (only when Hv > Hk), four channels per thread: the
-    // per-head rows are 16-byte aligned workspace rows (K a multiple of 8), summed in head order
+    // per-head rows are aligned workspace rows (K a multiple of 8) in the output's type (fp32 for fp32
+    // outputs, else the 16-bit type), summed in fp32 in head order
     if (P.G > 1) {
-        const int k4n = P.K / 4;
-        for (int e = tid; e < len * k4n; e += K5_THREADS) {
-            const int r = e / k4n, c = 4 * (e % k4n);
-            const size_t t = (size_t)ci.tok0 + r;
-            float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
-            for (int hv = hk * P.G; hv < (hk + 1) * P.G; ++hv) {
-                const float4 a = *reinterpret_cast<const float4 *>(P.dq_h + (t * P.Hv + hv) * P.K + c);
-                const float4 b = *reinterpret_cast<const float4 *>(P.dk_h + (t * P.Hv + hv) * P.K + c);
-                sq.x += a.x, sq.y += a.y, sq.z += a.z, sq.w += a.w;
-                sk.x += b.x, sk.y += b.y, sk.z += b.z, sk.w += b.w;
+        const int pdt = gqa_part_dtype(P);
+        if (pdt == F32) {  // four channels per thread
+            const int k4n = P.K / 4;
+            for (int e = tid; e < len * k4n; e += K5_THREADS) {
+                const int r = e / k4n, c = 4 * (e % k4n);
+                const size_t t = (size_t)ci.tok0 + r;
+                float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
+                for (int hv = hk * P.G; hv < (hk + 1) * P.G; ++hv) {
+                    const size_t i = (t * P.Hv + hv) * P.K + c;
+                    const float4 a = *reinterpret_cast<const float4 *>(P.dq_h + i);
+                    const float4 b = *reinterpret_cast<const float4 *>(P.dk_h + i);
+                    sq.x += a.x, sq.y += a.y, sq.z += a.z, sq.w += a.w;
+                    sk.x += b.x, sk.y += b.y, sk.z += b.z, sk.w += b.w;
+                }
+                store4(P.dq, (t * P.Hk + hk) * P.K + c, sq, P.dqdk_dtype);
+                store4(P.dk, (t * P.Hk + hk) * P.K + c, sk, P.dqdk_dtype);
             }
-            store4(P.dq, (t * P.Hk + hk) * P.K + c, sq, P.dqdk_dtype);
-            store4(P.dk, (t * P.Hk + hk) * P.K + c, sk, P.dqdk_dtype);
+        } else {  // 16-bit partials: eight channels (16 bytes) per thread
+            const int k8n = P.K / 8;
+            for (int e = tid; e < len * k8n; e += K5_THREADS) {
+                const int r = e / k8n, c = 8 * (e % k8n);
+                const size_t t = (size_t)ci.tok0 + r;
+                float sq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, sk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int hv = hk * P.G; hv < (hk + 1) * P.G; ++hv) {
+                    const size_t i = (t * P.Hv + hv) * P.K + c;
+                    float a[8], b[8];
+                    load8_16(gqa_part(P.dq_h, i, P), pdt, a);
+                    load8_16(gqa_part(P.dk_h, i, P), pdt, b);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) sq[j] += a[j], sk[j] += b[j];
+                }
+                store4(P.dq, (t * P.Hk + hk) * P.K + c, make_float4(sq[0], sq[1], sq[2], sq[3]), P.dqdk_dtype);
+                store4(P.dq, (t * P.Hk + hk) * P.K + c + 4, make_float4(sq[4], sq[5], sq[6], sq[7]), P.dqdk_dtype);
+                store4(P.dk, (t * P.Hk + hk) * P.K + c, make_float4(sk[0], sk[1], sk[2], sk[3]), P.dqdk_dtype);
+                store4(P.dk, (t * P.Hk + hk) * P.K + c + 4, make_float4(sk[4], sk[5], sk[6], sk[7]), P.dqdk_dtype);
+            }
         }
     }
 }
