@@ -154,6 +154,10 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
             else armed1 = true;
         }
         const float gl = PC ? 0.f : S.gam[buf][chunk_len(c) - 1];
+        if (PC) {  // the per-channel chunk decay exp(gamma_C[c]), once per channel, in place of gamma_C
+            if (tid < DT) S.gam[buf][tid] = expf(S.gam[buf][tid]);
+            __syncthreads();
+        }
         // epilogue 0: state rows -> fp16 operand (= h_n), then scale by Gamma_C in place
 #pragma unroll
         for (int m = 0; m < (LOCAL ? 2 : 1); ++m) {
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
                 }
                 if (PC) {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) v[t] *= expf(S.gam[buf][c0 + t]);
+                    for (int t = 0; t < 32; ++t) v[t] *= S.gam[buf][c0 + t];
                 } else {
                     const float G = expf(gl);
 #pragma unroll

@@ -145,6 +145,10 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
             else armed1 = true;
         }
         const float gl = PC ? 0.f : S.gam[buf][chunk_len(c) - 1];
+        if (PC) {  // the per-channel chunk decay exp(gamma_C[c]), once per channel, in place of gamma_C
+            if (tid < DT) S.gam[buf][tid] = expf(S.gam[buf][tid]);
+            __syncthreads();
+        }
         // epilogue 0: dS rows -> fp16 operand (= dh_n), then scale by Gamma_C in place
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
             }
             if (PC) {
 #pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] *= expf(S.gam[buf][c0 + t]);
+                for (int t = 0; t < 32; ++t) v[t] *= S.gam[buf][c0 + t];
             } else {
                 const float G = expf(gl);
 #pragma unroll
