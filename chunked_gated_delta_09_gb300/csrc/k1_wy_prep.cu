@@ -410,12 +410,12 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
                 put2(i0 + 1, j0, akk[1], aqk[1]);
             }
         }
-        // ---- cross quarters of the diagonal blocks: warp 0 blocks 0 and 1, warp 1 blocks 2 and 3; the upper 8
-        // rows sit in the fragments' rows 8..15, rows 0..7 stay zero
-        if (wid < 2) {
+        // ---- cross quarters of the diagonal blocks, on the warps without triangle tasks: warp 5 blocks 0 and 1,
+        // warp 6 block 2, warp 7 block 3; the upper 8 rows sit in the fragments' rows 8..15, rows 0..7 stay zero
+        if (wid >= 5) {
             const int g4 = lane >> 2, kq = 2 * (lane & 3);
-            for (int bi = 0; bi < 2; ++bi) {
-                const int blk = 2 * wid + bi, mid = 16 * blk + 8;
+            for (int bi = 0; bi < (wid == 5 ? 2 : 1); ++bi) {
+                const int blk = wid == 5 ? bi : wid - 4, mid = 16 * blk + 8;
                 float kk[4] = {}, qk[4] = {};
                 for (int k0 = 0; k0 < DT; k0 += 16) {
                     uint32_t ak[4] = {0u, 0u, 0u, 0u}, aq[4] = {0u, 0u, 0u, 0u}, bk[2];
@@ -446,7 +446,6 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
             }
         }
         // ---- blocks below the diagonal: warp 2 + p takes the pair p: (I, J) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-        // (warp 0 summed a second round of diagonal tasks above)
         if (wid >= 2) {
             const int p = wid - 2;
             const int I = p < 1 ? 1 : (p < 3 ? 2 : 3), J = p < 1 ? 0 : (p < 3 ? p - 1 : p - 3);
