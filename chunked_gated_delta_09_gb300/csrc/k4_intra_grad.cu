@@ -35,10 +35,12 @@ constexpr int K4_THREADS = 512;
 // warp tiling: 16 warps, four row blocks of 16 rows x four column blocks
 constexpr int NK = 4;  // C x K tiles: 16 x 32 per warp (four n8 tiles)
 constexpr int NC = 2;  // C x C tiles: 16 x 16 per warp (two n8 tiles)
+constexpr int GKS = DT + 4;  // row stride (floats) of the per-channel gate tile: 4 mod 32, so that the rows a
+                             // fragment's lanes read (several rows, consecutive columns) fall on distinct banks
 
 // Per-channel decayed products on the accumulator layout of a 16 x (8 NK) warp tile (rows r0 = m0 + lane / 4
 // and r0 + 8, column pairs c = n0 + 8 nt + 2 (lane % 4) + {0, 1}), A a C x C and X a C x DT fp16 tile, g the
-// per-channel cumulative gate [CT][DT]:
+// per-channel cumulative gate [CT] rows at stride GKS:
 //   LOWER:  acc[r][c] += sum_{j <= r (INCL) or j < r} A[r][j] X[j][c] exp(g[r][c] - g[j][c])
 //   else:   acc[r][c] += sum_{i >= r (INCL) or i > r} A[i][r] X[i][c] exp(g[i][c] - g[r][c])
 // Sub-chunk factorisation: the warp's rows form one 16-row block of the chunk.  The terms from the other
@@ -64,7 +66,7 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
         const int bk = 2 * (lane & 3);            // B fragment: k rows bk, bk + 1 and bk + 8, bk + 9
         float gref_b[NK];
 #pragma unroll
-        for (int nt = 0; nt < NK; ++nt) gref_b[nt] = g[ref * DT + n0 + 8 * nt + bn];
+        for (int nt = 0; nt < NK; ++nt) gref_b[nt] = g[ref * GKS + n0 + 8 * nt + bn];
         const int r8 = lane & 7, mat = lane >> 3;
         for (int ks = ks_lo; ks < ks_hi; ++ks) {
             const int k0 = 16 * ks;
@@ -80,7 +82,7 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
                     const int j = k0 + bk + (q & 1) + 8 * (q >> 1);
                     const float x = ctile_get(X, j, c, DT);
                     // exponent <= 0 on both sides of the reference row
-                    v[q] = x * __expf(LOWER ? gref_b[nt] - g[j * DT + c] : g[j * DT + c] - gref_b[nt]);
+                    v[q] = x * __expf(LOWER ? gref_b[nt] - g[j * GKS + c] : g[j * GKS + c] - gref_b[nt]);
                 }
                 const __half2 b0 = __floats2half2_rn(v[0], v[1]), b1 = __floats2half2_rn(v[2], v[3]);
                 mma16816(off[0][nt], a, *reinterpret_cast<const uint32_t *>(&b0), *reinterpret_cast<const uint32_t *>(&b1));
@@ -91,11 +93,11 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int c = cq + 8 * nt + h;
-                const float gr = g[ref * DT + c];
+                const float gr = g[ref * GKS + c];
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     const int r = r0 + 8 * rr;
-                    const float gx = g[r * DT + c];
+                    const float gx = g[r * GKS + c];
                     acc[0][nt][2 * rr + h] += off[0][nt][2 * rr + h] * __expf(LOWER ? gx - gr : gr - gx);
                 }
             }
@@ -114,10 +116,10 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
         for (int nt = 0; nt < NK; ++nt) {
             off[nt][0] = off[nt][1] = off[nt][2] = off[nt][3] = 0.f;
             const int c = n0 + 8 * nt + bn;
-            const float gm = g[mid * DT + c];
+            const float gm = g[mid * GKS + c];
             const int j = LOWER ? m0 + bk : mid + bk;  // k rows of the B fragment
-            const float v0 = ctile_get(X, j, c, DT) * __expf(LOWER ? gm - g[j * DT + c] : g[j * DT + c] - gm);
-            const float v1 = ctile_get(X, j + 1, c, DT) * __expf(LOWER ? gm - g[(j + 1) * DT + c] : g[(j + 1) * DT + c] - gm);
+            const float v0 = ctile_get(X, j, c, DT) * __expf(LOWER ? gm - g[j * GKS + c] : g[j * GKS + c] - gm);
+            const float v1 = ctile_get(X, j + 1, c, DT) * __expf(LOWER ? gm - g[(j + 1) * GKS + c] : g[(j + 1) * GKS + c] - gm);
             mma1688(off[nt], a0, a1, pack_half2(v0, v1));
         }
 #pragma unroll
@@ -125,9 +127,9 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int c = cq + 8 * nt + h;
-                const float gm = g[mid * DT + c];
-                if (LOWER) acc[0][nt][2 + h] += off[nt][2 + h] * __expf(g[(r0 + 8) * DT + c] - gm);  // rows r0 + 8
-                else acc[0][nt][h] += off[nt][h] * __expf(gm - g[r0 * DT + c]);                    // rows r0
+                const float gm = g[mid * GKS + c];
+                if (LOWER) acc[0][nt][2 + h] += off[nt][2 + h] * __expf(g[(r0 + 8) * GKS + c] - gm);  // rows r0 + 8
+                else acc[0][nt][h] += off[nt][h] * __expf(gm - g[r0 * GKS + c]);                    // rows r0
             }
     }
     float gr[2][NK][2];
@@ -135,7 +137,7 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
     for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int nt = 0; nt < NK; ++nt) {
-            const float2 v = *reinterpret_cast<const float2 *>(g + (r0 + 8 * h) * DT + cq + 8 * nt);
+            const float2 v = *reinterpret_cast<const float2 *>(g + (r0 + 8 * h) * GKS + cq + 8 * nt);
             gr[h][nt][0] = v.x;
             gr[h][nt][1] = v.y;
         }
@@ -151,8 +153,8 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
         for (int nt = 0; nt < NK; ++nt) {
             const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(X + ctile_off(j0, cq + 8 * nt, DT)));
             const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(X + ctile_off(j1, cq + 8 * nt, DT)));
-            const float2 g0 = *reinterpret_cast<const float2 *>(g + j0 * DT + cq + 8 * nt);
-            const float2 g1 = *reinterpret_cast<const float2 *>(g + j1 * DT + cq + 8 * nt);
+            const float2 g0 = *reinterpret_cast<const float2 *>(g + j0 * GKS + cq + 8 * nt);
+            const float2 g1 = *reinterpret_cast<const float2 *>(g + j1 * GKS + cq + 8 * nt);
             const float e00 = __expf(LOWER ? gr[0][nt][0] - g0.x : g0.x - gr[0][nt][0]);
             const float e01 = __expf(LOWER ? gr[0][nt][1] - g0.y : g0.y - gr[0][nt][1]);
             const float e10 = __expf(LOWER ? gr[1][nt][0] - g1.x : g1.x - gr[1][nt][0]);
@@ -204,7 +206,7 @@ template <typename Tin, bool PC, bool WY>
 __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     K4Smem &S = *reinterpret_cast<K4Smem *>(smem_raw);
-    float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K4Smem));  // [CT][DT] per-channel only
+    float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K4Smem));  // [CT] rows at stride GKS, per-channel only
     // buffers reused once their first owner is done
     unsigned char *dWs = S.Ds;     // dW [r][k]          after dq
     unsigned char *KGb = S.Qs;     // beta Gamma K       after dk_O (per-channel)
@@ -260,7 +262,8 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         // ---- stage the inputs as fp16 tiles (the workspace tiles are already on their way); the per-channel gate
         // tile (workspace, contiguous) by asynchronous 16-byte copies issued first, so that they overlap
         if (PC) {
-            for (int e = 4 * tid; e < CT * DT; e += 4 * K4_THREADS) cp_async16(gamK + e, P.gam + u * CT * DT + e);
+            for (int e = 4 * tid; e < CT * DT; e += 4 * K4_THREADS)
+                cp_async16(gamK + (e / DT) * GKS + e % DT, P.gam + u * CT * DT + e);
             cp_async_commit();
         }
         const Tin *kp = reinterpret_cast<const Tin *>(P.k) + ((size_t)ci.tok0 * P.Hk + hk) * P.K;
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         const int m0 = (wid & 3) * 16, n0 = (wid >> 2) * (NK * 8);
         // C x C tiling: rows cm0 .. cm0+15, columns cn0 .. cn0+15
         const int cm0 = (wid & 3) * 16, cn0 = (wid >> 2) * (NC * 8);
-        auto G_ = [&](int r, int c) -> float { return PC ? gamK[r * DT + c] : S.gam[r]; };
+        auto G_ = [&](int r, int c) -> float { return PC ? gamK[r * GKS + c] : S.gam[r]; };
         auto Kv = [&](int r, int c) -> float { return ctile_get(S.Ks, r, c, DT); };
         const int rl = len - 1;
         auto row_dbeta = [&](int r) -> float {
@@ -474,7 +477,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             if (PC) {
                 for (int e = tid; e < CT * DT; e += K4_THREADS) {
                     int r = e / DT, c = e % DT;
-                    ctile_set(KGb, r, c, DT, S.beta[r] * __expf(gamK[e]) * Kv(r, c));
+                    ctile_set(KGb, r, c, DT, S.beta[r] * __expf(gamK[r * GKS + c]) * Kv(r, c));
                 }
             }
         }
@@ -696,7 +699,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 
 template <typename Tin, bool PC, bool WY = false>
 static cudaError_t launch_k4_t(const Params &P, cudaStream_t stream) {
-    size_t smem = sizeof(K4Smem) + (PC ? sizeof(float) * CT * DT : 0);
+    size_t smem = sizeof(K4Smem) + (PC ? sizeof(float) * CT * GKS : 0);
     cudaError_t e = smem_opt_in((const void *)k4_intra_grad<Tin, PC, WY>, smem);
     if (e != cudaSuccess) return e;
     int nsm = 0;
