@@ -142,7 +142,7 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
             gr[h][nt][1] = v.y;
         }
     // row r0 pairs with j (i) = m0 + t, row r0 + 8 with m0 + 8 + t: both inside their own 8-row half
-#pragma unroll 2
+#pragma unroll 1  // (rolled: fewer live registers, fewer spills)
     for (int t = 0; t < 8; ++t) {
         const int j0 = m0 + t, j1 = mid + t;
         const bool v0 = LOWER ? (INCL ? j0 <= r0 : j0 < r0) : (INCL ? j0 >= r0 : j0 > r0);
