@@ -86,12 +86,18 @@ NUM_SMS = 152
 
 
 def scan_segments(prob) -> int:
+    """The segment count the library's plan picks (the same estimate of the scans' time in chunk steps)."""
     units = prob.N * prob.Hv
     maxnc = (prob.T + prob.BT - 1) // prob.BT if prob.cu_seqlens is None else \
         (prob.B * prob.T + prob.BT - 1) // prob.BT
-    ns = NUM_SMS // units if units > 0 else 1
-    ns = min(ns, (maxnc + 3) // 4)
-    return max(ns, 1)
+    maxns = NUM_SMS // units if units > 0 else 1
+    maxns = min(maxns, (maxnc + 3) // 4)
+    ns, best = 1, float(maxnc)
+    for k in range(2, maxns + 1):
+        c = 2.0 * ((maxnc + k - 1) // k) + 12.0 + 3.5 * (k - 1)
+        if c < best:
+            ns, best = k, c
+    return ns
 
 
 def stage_bytes(prob) -> list:

@@ -229,11 +229,21 @@ gdr_status gdr_bwd_create(const gdr_bwd_desc *desc, gdr_bwd_plan **out) {
     }
     p->max_chunks = (int)mc;
     {
-        // segments: enough (sequence x head x segment) CTAs to give every SM one, at least 4 chunks each
+        // segments: at most one wave of (sequence x head x segment) CTAs, at least 4 chunks each; among those,
+        // the count that minimises the scans' estimated time in chunk steps (measured on GB300): one segment
+        // walks all chunks once; ns > 1 segments walk 2 ceil(chunks / ns) steps (local and final passes), plus
+        // about 12 steps of fixed cost (two more launches, the segment summaries written and read) and 3.5 per
+        // serial combine step
         long long units = (long long)p->N * d.Hv;
         long long maxnc = p->dense ? p->nts : ((long long)d.T + d.BT - 1) / d.BT;
-        long long ns = units > 0 ? plan_sm_count() / units : 1;
-        ns = ns < (maxnc + 3) / 4 ? ns : (maxnc + 3) / 4;
+        long long maxns = units > 0 ? plan_sm_count() / units : 1;
+        maxns = maxns < (maxnc + 3) / 4 ? maxns : (maxnc + 3) / 4;
+        long long ns = 1;
+        double best = (double)maxnc;
+        for (long long k = 2; k <= maxns; ++k) {
+            const double c = 2.0 * (double)((maxnc + k - 1) / k) + 12.0 + 3.5 * (double)(k - 1);
+            if (c < best) best = c, ns = k;
+        }
         const char *env = getenv("GDR_NSEG");
         if (env && atoi(env) > 0) ns = atoi(env);
         if (ns < 1) ns = 1;
