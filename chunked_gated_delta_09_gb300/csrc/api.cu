@@ -375,6 +375,11 @@ static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *work
     const bool any_chunks = plan->max_chunks > 0;
     if (any_chunks && (e = launch_k1(P, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     if (!mark(2)) return GDR_ERR_CUDA;
+    if (any_chunks && plan->NS == 1) {
+        // one segment: both scans in one launch (timed as the forward-scan stage; the next stage is empty)
+        if ((e = launch_k23_scan_pair(P, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+        if (!mark(3) || !mark(4)) return GDR_ERR_CUDA;
+    } else {
     if (any_chunks && plan->NS > 1) {
         if ((e = launch_k2_scan(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
         if ((e = launch_k23_combine(P, true, stream)) != cudaSuccess) return GDR_ERR_CUDA;
@@ -392,6 +397,7 @@ static gdr_status run_impl(gdr_bwd_plan *plan, const gdr_bwd_args *a, void *work
     }
     if ((e = launch_k3_scan(P, false, stream)) != cudaSuccess) return GDR_ERR_CUDA;
     if (!mark(4)) return GDR_ERR_CUDA;
+    }
     if (any_chunks && (e = (plan->k4_tc ? launch_k4_tc(P, stream) : launch_k4(P, stream))) != cudaSuccess)
         return GDR_ERR_CUDA;
     if (!mark(5)) return GDR_ERR_CUDA;
@@ -415,10 +421,10 @@ gdr_status gdr_bwd_run_profiled(gdr_bwd_plan *plan, const gdr_bwd_args *a, void 
 int gdr_bwd_launch_count(const gdr_bwd_plan *plan) {
     if (!plan) return 0;
     int n = plan->dense ? 0 : 1;  // K0
-    n += 1;                       // the final state-gradient scan always runs (it also writes dh0)
-    if (plan->max_chunks > 0) n += 4;  // K1, forward scan, K4, K5
-    if (plan->max_chunks > 0 && plan->NS > 1) n += 4 + (plan->dh_factored ? 1 : 0);  // local scans, combines (QR)
-    return n;
+    if (plan->max_chunks == 0) return n + 1;  // the state-gradient scan alone (it writes dh0)
+    if (plan->NS == 1) return n + 4;          // K1, both scans in one launch, K4, K5
+    // K1, the two final scans, K4, K5; the local scans and combines (and QR)
+    return n + 5 + 4 + (plan->dh_factored ? 1 : 0);
 }
 
 gdr_status gdr_fwd_run(gdr_bwd_plan *plan, const gdr_fwd_args *a, void *workspace, size_t ws_bytes, void *stream_) {

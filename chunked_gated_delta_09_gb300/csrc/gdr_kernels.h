@@ -35,6 +35,8 @@ cudaError_t launch_k1(const Params &P, cudaStream_t stream);
 // the tensor cores: local (zero-start) pass or final (exact-start) pass.
 cudaError_t launch_k2_scan(const Params &P, bool local, cudaStream_t stream);
 cudaError_t launch_k3_scan(const Params &P, bool local, cudaStream_t stream);
+// With one segment per sequence: both scans' single passes as one grid (forward CTAs first).
+cudaError_t launch_k23_scan_pair(const Params &P, cudaStream_t stream);
 // Exact fp32 combination of segment summaries (forward entry states / backward exit gradients).
 cudaError_t launch_k23_combine(const Params &P, bool fwd, cudaStream_t stream);
 // K4: per-chunk gradients dq, dk, dv, dbeta and the cumulative-gate gradient.

@@ -18,6 +18,7 @@
 // neither Aqk nor dV_new inside the step (selected with GDR_DH_FACTORED=1).
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
+#include "k2_scan_body.cuh"
 #include "tc_util.cuh"
 
 namespace gdr {
@@ -33,13 +34,14 @@ struct __align__(1024) BwdSmem {
     uint32_t tslot;
 };
 
+// The whole kernel for one CTA: bid is its (sequence x head x segment) index.
 template <bool PC, bool LOCAL, bool FACT = false>
-__global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
+__device__ __forceinline__ void k3_scan_body(const Params &P, const int bid) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     BwdSmem &S = *reinterpret_cast<BwdSmem *>(smem_raw);
     if (*P.status & ST_BAD_SEQLENS) return;
     const int NS = P.NS;
-    const int seg = blockIdx.x % NS, hv = (blockIdx.x / NS) % P.Hv, s = blockIdx.x / (NS * P.Hv);
+    const int seg = bid % NS, hv = (bid / NS) % P.Hv, s = bid / (NS * P.Hv);
     int bos, eos;
     seq_range(P, s, bos, eos);
     const int nc = (eos - bos + P.BT - 1) / P.BT;
@@ -258,6 +260,22 @@ __global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
 }
 
 template <bool PC, bool LOCAL, bool FACT = false>
+__global__ void __launch_bounds__(SB_THREADS, 1) k3_scan_tc(const Params P) {
+    k3_scan_body<PC, LOCAL, FACT>(P, (int)blockIdx.x);
+}
+
+// One segment per sequence: the forward state recompute and the state-gradient scan do not depend on each
+// other (both read only the WY preparation's tiles), so their single passes run as one grid, the first N Hv
+// CTAs walking the forward recurrence and the rest the reverse one; with few sequences x heads each scan alone
+// would leave most SMs idle.
+template <bool PC>
+__global__ void __launch_bounds__(SB_THREADS, 1) k23_scan_pair(const Params P) {
+    const int n = P.N * P.Hv;
+    if ((int)blockIdx.x < n) k2_scan_body<PC, false>(P, (int)blockIdx.x);
+    else k3_scan_body<PC, false>(P, (int)blockIdx.x - n);
+}
+
+template <bool PC, bool LOCAL, bool FACT = false>
 static cudaError_t launch_bwd_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(BwdSmem);
     cudaError_t e =
@@ -265,6 +283,21 @@ static cudaError_t launch_bwd_t(const Params &P, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     k3_scan_tc<PC, LOCAL, FACT><<<P.N * P.Hv * P.NS, SB_THREADS, smem, stream>>>(P);
     return cudaGetLastError();
+}
+
+template <bool PC>
+static cudaError_t launch_pair_t(const Params &P, cudaStream_t stream) {
+    const size_t smem = sizeof(BwdSmem) > sizeof(FwdSmem<false>) ? sizeof(BwdSmem) : sizeof(FwdSmem<false>);
+    cudaError_t e = smem_opt_in((const void *)k23_scan_pair<PC>, smem);
+    if (e != cudaSuccess) return e;
+    k23_scan_pair<PC><<<2 * P.N * P.Hv, SB_THREADS, smem, stream>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_k23_scan_pair(const Params &P, cudaStream_t stream) {
+    if (P.NS != 1) return cudaErrorInvalidValue;
+    static_assert(SB_THREADS == SC_THREADS, "one block shape for both scans");
+    return P.per_channel ? launch_pair_t<true>(P, stream) : launch_pair_t<false>(P, stream);
 }
 
 cudaError_t launch_k3_scan(const Params &P, bool local, cudaStream_t stream) {

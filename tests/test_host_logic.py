@@ -86,3 +86,15 @@ def test_factored_scan_adds_one_launch(monkeypatch):
     base = ops.GdrBwdPlan(**kw).launch_count
     monkeypatch.setenv("GDR_DH_FACTORED", "1")
     assert ops.GdrBwdPlan(**kw).launch_count == base + 1
+
+
+def test_single_segment_runs_both_scans_in_one_launch():
+    """A short sequence (32 chunks per head here) is scanned as one segment, and then the forward and the
+    state-gradient scans share one launch: K1, the scan pair, K4, K5 (host-only plan creation)."""
+    from chunked_gated_delta_09_gb300 import counts, ops
+    from chunked_gated_delta_09_gb300.inputs import workload
+    assert counts.scan_segments(workload("kda_t2k_fp16")) == 1
+    assert ops.GdrBwdPlan(B=1, T=2048, Hk=32, Hv=32, K=128, V=128, per_channel=True).launch_count == 4
+    # a long one is segmented: K1, two local scans, two combines, two final scans, K4, K5
+    assert counts.scan_segments(workload("gdn_t32k_bf16")) == 9
+    assert ops.GdrBwdPlan(B=1, T=32768, Hk=16, Hv=16, K=128, V=128).launch_count == 9
