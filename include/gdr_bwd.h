@@ -118,7 +118,9 @@ gdr_status gdr_bwd_run(gdr_bwd_plan *plan, const gdr_bwd_args *args, void *works
 /* Same as gdr_bwd_run, and records events[0] before the first stage and events[i + 1] after stage i
  * (events: GDR_BWD_NUM_STAGES + 1 cudaEvent_t handles created by the caller, all on `stream`'s device).
  * A stage that has nothing to do (stage 0 for dense input) records its event right after the previous
- * one.  Used to time each kernel on the stream it runs on.  NULL events -> GDR_ERR_INVALID_ARG. */
+ * one.  When the plan scans every sequence as one segment, stages 2 and 3 run as one launch, timed as
+ * stage 2 (stage 3 then records its event right after).  Used to time each kernel on the stream it runs
+ * on.  NULL events -> GDR_ERR_INVALID_ARG. */
 gdr_status gdr_bwd_run_profiled(gdr_bwd_plan *plan, const gdr_bwd_args *args, void *workspace, size_t ws_bytes,
                                 void *stream, void *const *events);
 
