@@ -132,39 +132,57 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
                 else acc[0][nt][h] += off[nt][h] * __expf(gm - g[r0 * GKS + c]);                    // rows r0
             }
     }
-    float gr[2][NK][2];
+    // The two 8 x 8 triangles, term by term.  Row r0 = m0 + g (and r0 + 8 in the other half, with the same
+    // terms) has own_n terms, t in order k = 0, 1, .. (t = k below the diagonal, t = 7 - k above it); the lane
+    // of row 7 - g in the same column quad (lane ^ 28) has the complement, NPAIR in all.  The two share them
+    // evenly: a lane with more than NH terms keeps its first NH and its partner takes the rest (into pacc,
+    // returned by one shuffle per accumulator), so every lane runs NH iterations instead of 8.
+    constexpr int NPAIR = INCL ? 9 : 7, NH = (NPAIR + 1) / 2;
+    const int gq = lane >> 2;
+    const int own_n = LOWER ? (INCL ? gq + 1 : gq) : (INCL ? 8 - gq : 7 - gq);
+    const int par_n = NPAIR - own_n, own_cap = own_n < NH ? own_n : NH;
+    float pacc[NK][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int nt = 0; nt < NK; ++nt) {
-            const float2 v = *reinterpret_cast<const float2 *>(g + (r0 + 8 * h) * GKS + cq + 8 * nt);
-            gr[h][nt][0] = v.x;
-            gr[h][nt][1] = v.y;
-        }
-    // row r0 pairs with j (i) = m0 + t, row r0 + 8 with m0 + 8 + t: both inside their own 8-row half
+    for (int nt = 0; nt < NK; ++nt) pacc[nt][0] = pacc[nt][1] = pacc[nt][2] = pacc[nt][3] = 0.f;
 #pragma unroll 1  // (rolled: fewer live registers, fewer spills)
-    for (int t = 0; t < 8; ++t) {
+    for (int i = 0; i < NH; ++i) {
+        const bool mine = i < own_cap;
+        const int k = mine ? i : NH + (i - own_n);
+        const bool valid = mine || k < par_n;
+        const int row = m0 + (mine ? gq : 7 - gq);  // this term's row in the first half (second: row + 8)
+        const int t = valid ? (LOWER ? k : 7 - k) : 0;  // (k reaches 8 on a spare iteration: keep rows in the tile)
         const int j0 = m0 + t, j1 = mid + t;
-        const bool v0 = LOWER ? (INCL ? j0 <= r0 : j0 < r0) : (INCL ? j0 >= r0 : j0 > r0);
-        const bool v1 = LOWER ? (INCL ? j1 <= r0 + 8 : j1 < r0 + 8) : (INCL ? j1 >= r0 + 8 : j1 > r0 + 8);
-        const float a0 = LOWER ? ctile_get(A, r0, j0, CT) : ctile_get(A, j0, r0, CT);
-        const float a1 = LOWER ? ctile_get(A, r0 + 8, j1, CT) : ctile_get(A, j1, r0 + 8, CT);
+        const float a0 = valid ? (LOWER ? ctile_get(A, row, j0, CT) : ctile_get(A, j0, row, CT)) : 0.f;
+        const float a1 = valid ? (LOWER ? ctile_get(A, row + 8, j1, CT) : ctile_get(A, j1, row + 8, CT)) : 0.f;
 #pragma unroll
         for (int nt = 0; nt < NK; ++nt) {
             const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(X + ctile_off(j0, cq + 8 * nt, DT)));
             const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(X + ctile_off(j1, cq + 8 * nt, DT)));
             const float2 g0 = *reinterpret_cast<const float2 *>(g + j0 * GKS + cq + 8 * nt);
             const float2 g1 = *reinterpret_cast<const float2 *>(g + j1 * GKS + cq + 8 * nt);
-            const float e00 = __expf(LOWER ? gr[0][nt][0] - g0.x : g0.x - gr[0][nt][0]);
-            const float e01 = __expf(LOWER ? gr[0][nt][1] - g0.y : g0.y - gr[0][nt][1]);
-            const float e10 = __expf(LOWER ? gr[1][nt][0] - g1.x : g1.x - gr[1][nt][0]);
-            const float e11 = __expf(LOWER ? gr[1][nt][1] - g1.y : g1.y - gr[1][nt][1]);
-            acc[0][nt][0] += v0 ? a0 * x0.x * e00 : 0.f;
-            acc[0][nt][1] += v0 ? a0 * x0.y * e01 : 0.f;
-            acc[0][nt][2] += v1 ? a1 * x1.x * e10 : 0.f;
-            acc[0][nt][3] += v1 ? a1 * x1.y * e11 : 0.f;
+            const float2 r0g = *reinterpret_cast<const float2 *>(g + row * GKS + cq + 8 * nt);
+            const float2 r1g = *reinterpret_cast<const float2 *>(g + (row + 8) * GKS + cq + 8 * nt);
+            // (an invalid term has a = 0 and its exponent may be positive: it is selected away, never multiplied)
+            const float e00 = __expf(LOWER ? r0g.x - g0.x : g0.x - r0g.x);
+            const float e01 = __expf(LOWER ? r0g.y - g0.y : g0.y - r0g.y);
+            const float e10 = __expf(LOWER ? r1g.x - g1.x : g1.x - r1g.x);
+            const float e11 = __expf(LOWER ? r1g.y - g1.y : g1.y - r1g.y);
+            const float y0 = valid ? a0 * x0.x * e00 : 0.f, y1 = valid ? a0 * x0.y * e01 : 0.f;
+            const float y2 = valid ? a1 * x1.x * e10 : 0.f, y3 = valid ? a1 * x1.y * e11 : 0.f;
+            acc[0][nt][0] += mine ? y0 : 0.f;
+            acc[0][nt][1] += mine ? y1 : 0.f;
+            acc[0][nt][2] += mine ? y2 : 0.f;
+            acc[0][nt][3] += mine ? y3 : 0.f;
+            pacc[nt][0] += mine ? 0.f : y0;
+            pacc[nt][1] += mine ? 0.f : y1;
+            pacc[nt][2] += mine ? 0.f : y2;
+            pacc[nt][3] += mine ? 0.f : y3;
         }
     }
+#pragma unroll
+    for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[0][nt][e] += __shfl_xor_sync(0xffffffffu, pacc[nt][e], 28);
 }
 
 struct __align__(1024) K4Smem {
