@@ -149,6 +149,7 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
         const bool mine = i < own_cap;
         const int k = mine ? i : NH + (i - own_n);
         const bool valid = mine || k < par_n;
+        const float wm = mine ? 1.f : 0.f, wp = 1.f - wm;
         const int row = m0 + (mine ? gq : 7 - gq);  // this term's row in the first half (second: row + 8)
         const int t = valid ? (LOWER ? k : 7 - k) : 0;  // (k reaches 8 on a spare iteration: keep rows in the tile)
         const int j0 = m0 + t, j1 = mid + t;
@@ -169,14 +170,15 @@ __device__ __forceinline__ void decayed_acc(float (&acc)[1][NK][4], const unsign
             const float e11 = __expf(LOWER ? r1g.y - g1.y : g1.y - r1g.y);
             const float y0 = valid ? a0 * x0.x * e00 : 0.f, y1 = valid ? a0 * x0.y * e01 : 0.f;
             const float y2 = valid ? a1 * x1.x * e10 : 0.f, y3 = valid ? a1 * x1.y * e11 : 0.f;
-            acc[0][nt][0] += mine ? y0 : 0.f;
-            acc[0][nt][1] += mine ? y1 : 0.f;
-            acc[0][nt][2] += mine ? y2 : 0.f;
-            acc[0][nt][3] += mine ? y3 : 0.f;
-            pacc[nt][0] += mine ? 0.f : y0;
-            pacc[nt][1] += mine ? 0.f : y1;
-            pacc[nt][2] += mine ? 0.f : y2;
-            pacc[nt][3] += mine ? 0.f : y3;
+            // (y finite: a 0 / 1 weight routes it to this lane's sums or the partner's)
+            acc[0][nt][0] = fmaf(wm, y0, acc[0][nt][0]);
+            acc[0][nt][1] = fmaf(wm, y1, acc[0][nt][1]);
+            acc[0][nt][2] = fmaf(wm, y2, acc[0][nt][2]);
+            acc[0][nt][3] = fmaf(wm, y3, acc[0][nt][3]);
+            pacc[nt][0] = fmaf(wp, y0, pacc[nt][0]);
+            pacc[nt][1] = fmaf(wp, y1, pacc[nt][1]);
+            pacc[nt][2] = fmaf(wp, y2, pacc[nt][2]);
+            pacc[nt][3] = fmaf(wp, y3, pacc[nt][3]);
         }
     }
 #pragma unroll
@@ -225,6 +227,9 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     K4Smem &S = *reinterpret_cast<K4Smem *>(smem_raw);
     float *gamK = reinterpret_cast<float *>(smem_raw + sizeof(K4Smem));  // [CT] rows at stride GKS, per-channel only
+    // per-channel gate: the decayed key Gram tile (from the WY preparation), fetched with the item's other tiles
+    unsigned char *Kds = reinterpret_cast<unsigned char *>(gamK + CT * GKS);
+    constexpr bool kKd = PC && !WY;
     // buffers reused once their first owner is done
     unsigned char *dWs = S.Ds;     // dW [r][k]          after dq
     unsigned char *KGb = S.Qs;     // beta Gamma K       after dk_O (per-channel)
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
         return it;
     };
     constexpr uint32_t kBytesHdH = 2 * DT * DT * 2, kBytesDdV = CT * DT * 2 + DT * CT * 2,
-                       kBytesTVn = CT * CT * 2 + DT * CT * 2;
+                       kBytesTVn = CT * CT * 2 + DT * CT * 2 + (kKd ? CT * CT * 2 : 0);
     auto issue_HdH = [&](size_t un) {  // expects the whole item's bytes, so it comes first
         tc::mbar_expect_tx(&S.lbar, kBytesHdH + kBytesDdV + kBytesTVn);
         tc::bulk_g2s(S.Hs, P.h + un * DT * DT, DT * DT * 2, &S.lbar);
@@ -257,6 +262,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
     auto issue_TVn = [&](size_t un) {
         tc::bulk_g2s(S.Ts, P.Tm + un * CT * CT, CT * CT * 2, &S.lbar);
         tc::bulk_g2s(S.VnT, P.Vn + un * DT * CT, DT * CT * 2, &S.lbar);
+        if (kKd) tc::bulk_g2s(Kds, P.Kd + un * CT * CT, CT * CT * 2, &S.lbar);
     };
     int item = valid_from(blockIdx.x);
     if (item >= n_items) return;
@@ -492,10 +498,23 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                     int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
                     *reinterpret_cast<__half2 *>(dWs + ctile_off(r, c, DT)) = __floats2half2_rn(t[0][nt][e], t[0][nt][e + 1]);
                 }
-            if (PC) {
-                for (int e = tid; e < CT * DT; e += K4_THREADS) {
-                    int r = e / DT, c = e % DT;
-                    ctile_set(KGb, r, c, DT, S.beta[r] * __expf(gamK[r * GKS + c]) * Kv(r, c));
+            if (PC) {  // 8 columns of one row per step; the 8 lanes of a quarter-warp take the 8 rows of a core matrix
+                for (int e = tid; e < CT * DT / 8; e += K4_THREADS) {
+                    const int r = e & (CT - 1), c8 = 8 * (e >> 6);
+                    const uint4 kv = *reinterpret_cast<const uint4 *>(S.Ks + ctile_off(r, c8, DT));
+                    const float4 ga = *reinterpret_cast<const float4 *>(gamK + r * GKS + c8);
+                    const float4 gb = *reinterpret_cast<const float4 *>(gamK + r * GKS + c8 + 4);
+                    const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                    const __half2 *k2 = reinterpret_cast<const __half2 *>(&kv);
+                    const float b = S.beta[r];
+                    float f[8];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float2 kf = __half22float2(k2[t]);
+                        f[2 * t] = b * __expf(gv[2 * t]) * kf.x;
+                        f[2 * t + 1] = b * __expf(gv[2 * t + 1]) * kf.y;
+                    }
+                    *reinterpret_cast<uint4 *>(KGb + ctile_off(r, c8, DT)) = pack8_half(f);
                 }
             }
         }
@@ -611,7 +630,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
                             L = __expf(S.gam[i] - S.gam[j]);
                             kkd = L * kk[0][nt][e];
                         } else {  // the decayed key Gram, formed by the WY preparation
-                            kkd = ctile_get(reinterpret_cast<const unsigned char *>(P.Kd + u * CT * CT), i, j, CT);
+                            kkd = ctile_get(Kds, i, j, CT);
                         }
                     }
                     rb[e >> 1] += dA * kkd;
@@ -633,7 +652,7 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
             if ((lane & 3) == 0) S.dbp[4 + (wid >> 2)][m0 + (lane >> 2) + 8 * h] = s;
         }
         __syncthreads();
-        if (tid == 0 && has_next) {  // T and V_new^T (as X) read for the last time in S10
+        if (tid == 0 && has_next) {  // T, V_new^T (as X) and the decayed key Gram read for the last time in S10
             tc::fence_smem_to_async();
             issue_TVn(next);
         }
@@ -693,19 +712,25 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 #pragma unroll
             for (int nt = 0; nt < NK; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
-                    float x = dgam[0][PC ? nt : 0][e];
+                for (int e = 0; e < 4; e += 2) {  // column pairs c, c + 1 (c even)
+                    const int r = acc_row(m0, 0, e), c = acc_col(n0, nt, e);
+                    float x[2] = {dgam[0][PC ? nt : 0][e], dgam[0][PC ? nt : 0][e + 1]};
                     if (r == rl) {
-                        float l = 0.f;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) l += S.lrp[i][c];
-                        x += l;
+                        for (int h = 0; h < 2; ++h) {
+                            float l = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) l += S.lrp[i][c + h];
+                            x[h] += l;
+                        }
                     }
                     if (WY) {  // gradient of the cumulative gate, straight to the output
-                        if (r < len && c < P.K) P.dg[((size_t)(ci.tok0 + r) * P.Hv + hv) * P.K + c] = x;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if (r < len && c + h < P.K) P.dg[((size_t)(ci.tok0 + r) * P.Hv + hv) * P.K + c + h] = x[h];
                     } else {
-                        P.dgam[(u * CT + r) * DT + c] = r < len ? x : 0.f;
+                        *reinterpret_cast<float2 *>(P.dgam + (u * CT + r) * DT + c) =
+                            r < len ? make_float2(x[0], x[1]) : make_float2(0.f, 0.f);
                     }
                 }
             if (tid < len) P.dbeta[(size_t)(ci.tok0 + tid) * P.Hv + hv] = row_dbeta(tid);
@@ -717,7 +742,9 @@ __global__ void __launch_bounds__(K4_THREADS, 1) k4_intra_grad(const Params P) {
 
 template <typename Tin, bool PC, bool WY = false>
 static cudaError_t launch_k4_t(const Params &P, cudaStream_t stream) {
-    size_t smem = sizeof(K4Smem) + (PC ? sizeof(float) * CT * GKS : 0);
+    static_assert(sizeof(K4Smem) + sizeof(float) * CT * GKS + CT * CT * 2 <= 227 * 1024,
+                  "the per-channel kernel's shared memory exceeds the 227 KB a CTA can have");
+    size_t smem = sizeof(K4Smem) + (PC ? sizeof(float) * CT * GKS : 0) + (PC && !WY ? CT * CT * 2 : 0);
     cudaError_t e = smem_opt_in((const void *)k4_intra_grad<Tin, PC, WY>, smem);
     if (e != cudaSuccess) return e;
     int nsm = 0;
