@@ -121,11 +121,14 @@ def stage_bytes(prob) -> list:
         + (state if prob.h0 is not None else 0) + seg // 2                      # W, U, K~ (+ local pass); h, V_new
     k3 = u * ((tile_cc + 4 * tile_ck) * (2 if ns > 1 else 1) + tile_kk + tile_ck) \
         + (state if prob.dht is not None else 0) + state + seg // 2             # Aqk, D, K~, Q~, W; dh, dV_new; dh0
-    dqdk_out = 2 * C * K * oq  # (with GQA: per-value-head partials in the output's type)
+    dqdk_out = 2 * C * K * oq  # (with GQA: each value head's rows, added in place or per-head partials)
     scal_in = rec if rec else C * bb + CT * gk * 4  # the record, else beta and gamma
     k4 = u * (2 * tile_kk + 3 * tile_ck + tile_cc + 2 * C * K * ib + C * V * ib + scal_in   # reads
               + dqdk_out + C * V * ov + C * 4 + CT * gk * 4)                               # writes
-    k5 = u * (CT * gk * 4 + C * gk * 4) + (0 if G == 1 else u * 2 * C * K * oq + (u // G) * 2 * C * K * oq)
+    # GQA group sum in the closing kernel: only after the per-channel (mma.sync) gradient kernel, which writes
+    # per-value-head partials; the scalar gate's tcgen05 kernel sums each group in place
+    gsum = G > 1 and prob.per_channel
+    k5 = u * (CT * gk * 4 + C * gk * 4) + (u * 2 * C * K * oq + (u // G) * 2 * C * K * oq if gsum else 0)
     return [float(k0), float(k1), float(k2), float(k3), float(k4), float(k5)]
 
 

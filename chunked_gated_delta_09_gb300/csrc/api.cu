@@ -168,7 +168,9 @@ void layout(gdr_bwd_plan &p) {
     p.o_Vn = take(sizeof(__half) * units * CT * DT);
     p.o_dVn = take(sizeof(__half) * units * CT * DT);
     p.o_dgam = take(sizeof(float) * units * CT * gw);
-    size_t per_head = p.G > 1 ? sizeof(float) * (size_t)p.tokens * d.Hv * d.K : 0;
+    // per-value-head dq / dk for the group sum in the closing kernel: only the mma.sync gradient kernel
+    // writes them (the tcgen05 one sums each key head's group in place)
+    size_t per_head = p.G > 1 && !p.k4_tc ? sizeof(float) * (size_t)p.tokens * d.Hv * d.K : 0;
     p.o_dqh = take(per_head);
     p.o_dkh = take(per_head);
     size_t seg_units = p.NS > 1 ? (size_t)p.N * d.Hv * p.NS : 0;
@@ -309,8 +311,8 @@ static void fill_common(const gdr_bwd_plan *plan, char *ws, Params &P) {
     P.Vn = reinterpret_cast<__half *>(ws + plan->o_Vn);
     P.dVn = reinterpret_cast<__half *>(ws + plan->o_dVn);
     P.dgam = reinterpret_cast<float *>(ws + plan->o_dgam);
-    P.dq_h = plan->G > 1 ? reinterpret_cast<float *>(ws + plan->o_dqh) : nullptr;
-    P.dk_h = plan->G > 1 ? reinterpret_cast<float *>(ws + plan->o_dkh) : nullptr;
+    P.dq_h = plan->G > 1 && !plan->k4_tc ? reinterpret_cast<float *>(ws + plan->o_dqh) : nullptr;
+    P.dk_h = plan->G > 1 && !plan->k4_tc ? reinterpret_cast<float *>(ws + plan->o_dkh) : nullptr;
     P.NS = plan->NS;
     P.Lseg = plan->Lseg;
     if (plan->NS > 1) {

@@ -74,7 +74,8 @@ struct Params {
     __half *Vn;          // tile [v][c]   128 x 64   V_new^T
     __half *dVn;         // tile [v][c]   128 x 64   -dV_new^T
     float *dgam;         // [u][CT] or [u][CT][DT]
-    float *dq_h, *dk_h;  // [T][Hv][K] per value head (GQA only), in gqa_part_dtype (workspace sized for fp32)
+    float *dq_h, *dk_h;  // [T][Hv][K] per value head (GQA with the mma.sync gradient kernel; else null), in
+                         // gqa_part_dtype (workspace sized for fp32)
     // segment-parallel scans: NS segments of Lseg chunks per sequence; per (sequence, head, segment)
     // fp32 [DT][DT] summaries: local end state E, transition product Phi (and its transpose), local
     // start gradient F,

@@ -7,8 +7,9 @@
 // tcgen05.ld.
 //
 // Layout of the work:
-//  * persistent CTAs (one per SM, 16 warps) take the items (chunk n, value head hv), item = n Hv + hv,
-//    round-robin;
+//  * persistent CTAs (one per SM, 16 warps) take the items (chunk n, value head hv), item = n Hv + hv, by
+//    key-head group: the value heads that share a key head run on one CTA one after the other (groups
+//    round-robin), the first storing the key head's dq / dk rows and the others adding to them;
 //  * products with a chunk x feature result are computed transposed (feature x chunk, M = 128), so each
 //    epilogue thread owns one feature row and 16 chunk columns; chunk x chunk products use M = 64;
 //  * the feature-major copies K^T, V^T, Q^T that those epilogues need come from products with a 64 x 64
@@ -81,24 +82,51 @@ __device__ __forceinline__ void st2(__half *p, float lo, float hi) {
     *reinterpret_cast<__half2 *>(p) = __floats2half2_rn(lo, hi);
 }
 __device__ __forceinline__ void st2(float *p, float lo, float hi) { *reinterpret_cast<float2 *>(p) = make_float2(lo, hi); }
-template <typename To>
+// add a pair to memory (a reduction in the element's own type; no value is returned)
+__device__ __forceinline__ void red2(__nv_bfloat16 *p, float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    asm volatile("red.global.add.noftz.bf16x2 [%0], %1;\n" ::"l"(p), "r"(*reinterpret_cast<const uint32_t *>(&v))
+                 : "memory");
+}
+__device__ __forceinline__ void red2(__half *p, float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    asm volatile("red.global.add.noftz.f16x2 [%0], %1;\n" ::"l"(p), "r"(*reinterpret_cast<const uint32_t *>(&v))
+                 : "memory");
+}
+__device__ __forceinline__ void red2(float *p, float lo, float hi) {
+    asm volatile("red.global.add.f32 [%0], %1;\n" ::"l"(p), "f"(lo) : "memory");
+    asm volatile("red.global.add.f32 [%0], %1;\n" ::"l"(p + 1), "f"(hi) : "memory");
+}
+template <bool ADD, typename To>
 __device__ __forceinline__ void pairs16_t(To *p, size_t rs, int n, bool act, const float (&x)[16]) {
     const bool odd = (threadIdx.x & 1) != 0;
     To *q = odd ? p - 1 + rs : p;  // the pair's even column, on the first row this lane writes
 #pragma unroll
     for (int t = 0; t < 16; t += 2) {
         const float recv = __shfl_xor_sync(0xffffffffu, odd ? x[t] : x[t + 1], 1);
-        if (act && t + (odd ? 1 : 0) < n) st2(q + (size_t)t * rs, odd ? recv : x[t], odd ? x[t + 1] : recv);
+        if (act && t + (odd ? 1 : 0) < n) {
+            if (ADD) red2(q + (size_t)t * rs, odd ? recv : x[t], odd ? x[t + 1] : recv);
+            else st2(q + (size_t)t * rs, odd ? recv : x[t], odd ? x[t + 1] : recv);
+        }
     }
 }
 // x[t] -> element (t, 0) of a row-major output with row stride rs (elements), for the first n rows.  Lanes
 // 2m and 2m + 1 hold adjacent columns; the even lane writes rows 0, 2, .. and the odd lane rows 1, 3, .. of
 // both columns with one 2-element store each.  Every lane of the warp calls it (shuffles); act says whether
 // this lane's column exists (the same for both lanes of a pair: the feature sizes are even).
+// ADD: added to what is there instead (same lanes, same addresses).
+template <bool ADD = false>
 __device__ __forceinline__ void store_pairs16(void *p, int dt, size_t rs, int n, bool act, const float (&x)[16]) {
-    if (dt == BF16) pairs16_t(reinterpret_cast<__nv_bfloat16 *>(p), rs, n, act, x);
-    else if (dt == F16) pairs16_t(reinterpret_cast<__half *>(p), rs, n, act, x);
-    else pairs16_t(reinterpret_cast<float *>(p), rs, n, act, x);
+    if (dt == BF16) pairs16_t<ADD>(reinterpret_cast<__nv_bfloat16 *>(p), rs, n, act, x);
+    else if (dt == F16) pairs16_t<ADD>(reinterpret_cast<__half *>(p), rs, n, act, x);
+    else pairs16_t<ADD>(reinterpret_cast<float *>(p), rs, n, act, x);
+}
+// A key head's dq / dk row block: the group's first value head stores it, the others add to it.  One CTA
+// runs a group's items in head order and a given element is always written by the same thread, so the
+// additions follow the stores in program order and the sum's order is fixed (run-to-run identical).
+__device__ __forceinline__ void put_pairs16(bool add, void *p, int dt, size_t rs, int n, bool act, const float (&x)[16]) {
+    if (add) store_pairs16<true>(p, dt, rs, n, act, x);
+    else store_pairs16<false>(p, dt, rs, n, act, x);
 }
 __device__ __forceinline__ size_t esize(int dt) { return dt == F32 ? 4 : 2; }
 // 8 consecutive floats of a 16-byte aligned shared array as two vector loads
@@ -109,7 +137,8 @@ __device__ __forceinline__ void lds8(const float *p, float (&v)[8]) {
 
 // Tensor maps of the 16-bit inputs (unused for fp32 inputs): 4-D over (8-element column chunk, token, column
 // block, head), box (8, 64, K/8 or V/8, 1).
-template <typename Tin>
+// GRP: grouped-query attention (several value heads per key head), whose groups are summed in place.
+template <typename Tin, bool GRP>
 __global__ void __launch_bounds__(K4T_THREADS, 1)
     k4_intra_grad_tc(const Params P, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmv) {
@@ -117,13 +146,19 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
     K4TSmem &S = *reinterpret_cast<K4TSmem *>(smem_raw);
     if (*P.status & ST_BAD_SEQLENS) return;
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
-    const int n_items = P.max_chunks * P.Hv;
-    auto valid_from = [&](int it) -> int {
+    // Items go out by key-head group: the G value heads that read one key head are consecutive items (item =
+    // n Hv + hv, hv = hk G + i), and a CTA runs a whole group in head order before its next group (groups
+    // round-robin over the CTAs), so the group's dq / dk are summed in place in the outputs.
+    const int n_items = P.max_chunks * P.Hv, G = GRP ? P.G : 1;
+    auto valid_from = [&](int it) -> int {  // it: the first item of a group
         ChunkInfo t;
-        while (it < n_items && !chunk_info(P, it / P.Hv, t)) it += gridDim.x;
+        while (it < n_items && !chunk_info(P, it / P.Hv, t)) it += (int)gridDim.x * G;
         return it;
     };
-    int item = valid_from(blockIdx.x);
+    auto next_item = [&](int it) -> int {
+        return (it + 1) % G != 0 ? it + 1 : valid_from(it + 1 + ((int)gridDim.x - 1) * G);
+    };
+    int item = valid_from((int)blockIdx.x * G);
     if (item >= n_items) return;
     // 16-bit inputs are fetched raw ahead of time and converted in place; fp32 inputs are staged directly
     constexpr bool kRaw = sizeof(Tin) == 2;
@@ -312,11 +347,12 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
         chunk_info(P, n, ci);
         const size_t u = (size_t)item;  // = n Hv + hv
         const int len = ci.len, rl = len - 1;
-        const int next = valid_from(item + gridDim.x);
+        const int next = next_item(item);
         const bool has_next = next < n_items;
         const int nrow = len - c0 < 0 ? 0 : (len - c0 > 16 ? 16 : len - c0);  // valid rows among c0 .. c0+15
-        // partial-sum set of this item: its position in the CTA's sequence (invalid items only trail the list)
-        const int pb = ((item - (int)blockIdx.x) / (int)gridDim.x) & 1;
+        // partial-sum set of this item: the parity of its place in the CTA's sequence (invalid items only trail
+        // the list)
+        const int pb = ((item / G - (int)blockIdx.x) / (int)gridDim.x * G + item % G) & 1;
 
         // ---- inputs as fp16 tiles (the workspace tiles are on their way by bulk copy)
         if constexpr (kRaw) {  // (Q, first read in phase 2, is converted while phase 1 runs)
@@ -497,13 +533,9 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
                     dg[t] += qreg[t] * a[t];
                 }
             }
-            if (P.G == 1)
-                store_pairs16(reinterpret_cast<char *>(P.dq) +
-                                  (((size_t)(ci.tok0 + c0) * P.Hk + hk) * P.K + k) * esize(P.dqdk_dtype),
-                              P.dqdk_dtype, (size_t)P.Hk * P.K, nrow, k < P.K, a);
-            else
-                store_pairs16(gqa_part(P.dq_h, ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, P), gqa_part_dtype(P),
-                              (size_t)P.Hv * P.K, nrow, k < P.K, a);
+            put_pairs16(GRP && hv % G != 0,
+                        reinterpret_cast<char *>(P.dq) + (((size_t)(ci.tok0 + c0) * P.Hk + hk) * P.K + k) * esize(P.dqdk_dtype),
+                        P.dqdk_dtype, (size_t)P.Hk * P.K, nrow, k < P.K, a);
             ok2 = wait_group2();
             // dk_O
             tc::ld16x2(tc::taddr(tm, R_DKO + c0), b, tc::taddr(tm, R_TDW + c0), a);
@@ -639,13 +671,9 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
                 dk[t] += a[t] + b[t];
                 dg[t] += kreg[t] * (a[t] - b[t]);
             }
-            if (P.G == 1)
-                store_pairs16(reinterpret_cast<char *>(P.dk) +
-                                  (((size_t)(ci.tok0 + c0) * P.Hk + hk) * P.K + k) * esize(P.dqdk_dtype),
-                              P.dqdk_dtype, (size_t)P.Hk * P.K, nrow, k < P.K, dk);
-            else
-                store_pairs16(gqa_part(P.dk_h, ((size_t)(ci.tok0 + c0) * P.Hv + hv) * P.K + k, P), gqa_part_dtype(P),
-                              (size_t)P.Hv * P.K, nrow, k < P.K, dk);
+            put_pairs16(GRP && hv % G != 0,
+                        reinterpret_cast<char *>(P.dk) + (((size_t)(ci.tok0 + c0) * P.Hk + hk) * P.K + k) * esize(P.dqdk_dtype),
+                        P.dqdk_dtype, (size_t)P.Hk * P.K, nrow, k < P.K, dk);
             // gate gradient: column sums over the feature rows
             const float s = tc::warp_transpose_sum16(dg);
             if (lane < 16) S.dg_q[pb][q][c0 + lane] = s;
@@ -683,15 +711,15 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
 }
 
 
-template <typename Tin>
+template <typename Tin, bool GRP>
 static cudaError_t launch_k4_tc_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(K4TSmem);
-    cudaError_t e = smem_opt_in((const void *)k4_intra_grad_tc<Tin>, smem);
+    cudaError_t e = smem_opt_in((const void *)k4_intra_grad_tc<Tin, GRP>, smem);
     if (e != cudaSuccess) return e;
     int nsm = 0;
     if ((e = device_sm_count(&nsm)) != cudaSuccess) return e;
-    const long items = (long)P.max_chunks * P.Hv;
-    if (items == 0) return cudaSuccess;
+    const long groups = (long)P.max_chunks * P.Hk;  // the G items of a key-head group run on one CTA
+    if (groups == 0) return cudaSuccess;
     CUtensorMap mk, mq, mv;
     memset(&mk, 0, sizeof(mk));
     memset(&mq, 0, sizeof(mq));
@@ -702,15 +730,20 @@ static cudaError_t launch_k4_tc_t(const Params &P, cudaStream_t stream) {
         if ((e = encode_rows_map(&mq, P.q, P.qkv_dtype, tokens, P.Hk, P.K)) != cudaSuccess) return e;
         if ((e = encode_rows_map(&mv, P.v, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
     }
-    const int grid = (int)(items < nsm ? items : nsm);  // one persistent CTA per SM
-    k4_intra_grad_tc<Tin><<<grid, K4T_THREADS, smem, stream>>>(P, mk, mq, mv);
+    const int grid = (int)(groups < nsm ? groups : nsm);  // one persistent CTA per SM
+    k4_intra_grad_tc<Tin, GRP><<<grid, K4T_THREADS, smem, stream>>>(P, mk, mq, mv);
     return cudaGetLastError();
 }
 
+template <bool GRP>
+static cudaError_t launch_k4_tc_g(const Params &P, cudaStream_t stream) {
+    if (P.qkv_dtype == F32) return launch_k4_tc_t<float, GRP>(P, stream);
+    if (P.qkv_dtype == BF16) return launch_k4_tc_t<__nv_bfloat16, GRP>(P, stream);
+    return launch_k4_tc_t<__half, GRP>(P, stream);
+}
+
 cudaError_t launch_k4_tc(const Params &P, cudaStream_t stream) {
-    if (P.qkv_dtype == F32) return launch_k4_tc_t<float>(P, stream);
-    if (P.qkv_dtype == BF16) return launch_k4_tc_t<__nv_bfloat16>(P, stream);
-    return launch_k4_tc_t<__half>(P, stream);
+    return P.G > 1 ? launch_k4_tc_g<true>(P, stream) : launch_k4_tc_g<false>(P, stream);
 }
 
 }  // namespace gdr

@@ -84,10 +84,11 @@ __global__ void __launch_bounds__(K5_THREADS) k5_dg_reduce(const Params P) {
             }
         }
     }
-    // GQA: dq[t, hk] = sum over the group's value heads (only when Hv > Hk), four channels per thread: the
-    // per-head rows are aligned workspace rows (K a multiple of 8) in the output's type (fp32 for fp32
-    // outputs, else the 16-bit type), summed in fp32 in head order
-    if (P.G > 1) {
+    // GQA: dq[t, hk] = sum over the group's value heads (when Hv > Hk and the gradient kernel wrote
+    // per-value-head rows; the tcgen05 one sums in place), four channels per thread: the per-head rows are
+    // aligned workspace rows (K a multiple of 8) in the output's type (fp32 for fp32 outputs, else the 16-bit
+    // type), summed in fp32 in head order
+    if (P.G > 1 && P.dq_h) {
         const int pdt = gqa_part_dtype(P);
         if (pdt == F32) {  // four channels per thread
             const int k4n = P.K / 4;

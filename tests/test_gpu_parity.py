@@ -27,6 +27,8 @@ SMALL = {
     "no_h0_no_dht": dict(B=1, T=130, Hk=1, Hv=1, K=128, V=128, has_h0=False, has_dht=False),
     "k64_v32": dict(B=1, T=100, Hk=1, Hv=1, K=64, V=32),
     "k128_v64_gqa4": dict(B=1, T=129, Hk=1, Hv=4, K=128, V=64),
+    # three value heads per key head, fp16 throughout: the group's dq / dk summed in place in fp16
+    "fp16_gqa3": dict(B=1, T=200, Hk=2, Hv=6, K=64, V=64, qkv_dtype=torch.float16),
     "strong_decay": dict(B=1, T=256, Hk=1, Hv=2, K=128, V=128, g_shift=-3.0),
     "weak_decay": dict(B=1, T=256, Hk=1, Hv=2, K=128, V=128, g_shift=4.0),
     # per-channel gate with strong decay: chunk-wide cumulative gates far below the fp32 exponent range, so
