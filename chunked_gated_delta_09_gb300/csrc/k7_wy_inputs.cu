@@ -3,7 +3,9 @@
 // The stage (MindSpeed-Ops chunk_kda_bwd.md: chunk_kda_bwd_wy_dqkg_fused) receives the chunk quantities
 // that the full backward computes itself: the chunk-local cumulative gate g [T, H, K], the triangular matrix
 // A [T, H, BT], the chunk states h and their gradients dh [NT, H, K, V] (fp32), V_new and its gradient dv
-// [T, H, V], and dO.  One CTA per chunk x head writes them in the layout of the per-chunk gradient kernel:
+// [T, H, V], and dO.  Four CTAs per chunk x head (grid z: the gate, T and D; S_0; dS_next; V_new^T and
+// -dV_new^T, about 60-100 KB of reads each, so that more reads are in flight per SM than one CTA's serial
+// stages allow) write them in the layout of the per-chunk gradient kernel:
 // gamma [CT][DT] fp32 (rows past the chunk end repeat its last row, so in-chunk decays stay at most 1),
 // T = A as a [r][i] tile, D = scale dO as a [r][v] tile, S_0 and dS_next as [v][k] tiles (transposed through
 // registers), V_new^T and -dV_new^T as [v][c] tiles.  Padding is zero.  No shared memory: every transposed
@@ -89,41 +91,46 @@ __global__ void __launch_bounds__(K7_THREADS) k7_wy_inputs(const Params P, const
     if (!chunk_info(P, n, ci)) return;
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31, len = ci.len;
     const size_t u = (size_t)n * P.Hv + hv;
+    const int part = blockIdx.z;
 
-    // cumulative gate, rows past the end repeat the last row (g is only 4-byte aligned: scalar loads,
-    // consecutive threads on consecutive channels; 16-byte stores into the workspace)
-    for (int e = tid; e < CT * DT / 4; e += K7_THREADS) {
-        const int r = e / (DT / 4), c4 = (e % (DT / 4)) * 4, rr = r < len ? r : len - 1;
-        const float *src = P.g + ((size_t)(ci.tok0 + rr) * P.Hv + hv) * P.K;
-        float4 o;
-        o.x = c4 < P.K ? src[c4] : 0.f;
-        o.y = c4 + 1 < P.K ? src[c4 + 1] : 0.f;
-        o.z = c4 + 2 < P.K ? src[c4 + 2] : 0.f;
-        o.w = c4 + 3 < P.K ? src[c4 + 3] : 0.f;
-        reinterpret_cast<float4 *>(P.gam + u * CT * DT)[e] = o;
+    if (part == 0) {
+        // cumulative gate, rows past the end repeat the last row (g is only 4-byte aligned: scalar loads,
+        // consecutive threads on consecutive channels; 16-byte stores into the workspace)
+        for (int e = tid; e < CT * DT / 4; e += K7_THREADS) {
+            const int r = e / (DT / 4), c4 = (e % (DT / 4)) * 4, rr = r < len ? r : len - 1;
+            const float *src = P.g + ((size_t)(ci.tok0 + rr) * P.Hv + hv) * P.K;
+            float4 o;
+            o.x = c4 < P.K ? src[c4] : 0.f;
+            o.y = c4 + 1 < P.K ? src[c4 + 1] : 0.f;
+            o.z = c4 + 2 < P.K ? src[c4 + 2] : 0.f;
+            o.w = c4 + 3 < P.K ? src[c4 + 3] : 0.f;
+            reinterpret_cast<float4 *>(P.gam + u * CT * DT)[e] = o;
+        }
+        // T = A (the chunk's valid columns only) and D = scale dO
+        rows_to_tile(reinterpret_cast<unsigned char *>(P.Tm + u * CT * CT), CT,
+                     A + ((size_t)ci.tok0 * P.Hv + hv) * P.BT, (size_t)P.Hv * P.BT, len, len < P.BT ? len : P.BT, 1.f,
+                     tid);
+        rows_to_tile(reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT), DT,
+                     reinterpret_cast<const Tin *>(P.dO) + ((size_t)ci.tok0 * P.Hv + hv) * P.V, (size_t)P.Hv * P.V,
+                     len, P.V, P.scale, tid);
+    } else if (part == 1) {  // S_0: [K][V] fp32 per chunk -> a [v][k] tile
+        transpose_to_tile(reinterpret_cast<unsigned char *>(P.h + u * DT * DT), DT, h + u * P.K * P.V, (size_t)P.V,
+                          P.K, P.V, 1.f, wid, lane);
+    } else if (part == 2) {  // dS_next, the same way
+        transpose_to_tile(reinterpret_cast<unsigned char *>(P.dh + u * DT * DT), DT, dh + u * P.K * P.V, (size_t)P.V,
+                          P.K, P.V, 1.f, wid, lane);
+    } else {  // V_new^T and -dV_new^T: [c][v] rows -> [v][c] tiles
+        transpose_to_tile(reinterpret_cast<unsigned char *>(P.Vn + u * DT * CT), CT,
+                          vnew + ((size_t)ci.tok0 * P.Hv + hv) * P.V, (size_t)P.Hv * P.V, len, P.V, 1.f, wid, lane);
+        transpose_to_tile(reinterpret_cast<unsigned char *>(P.dVn + u * DT * CT), CT,
+                          dvin + ((size_t)ci.tok0 * P.Hv + hv) * P.V, (size_t)P.Hv * P.V, len, P.V, -1.f, wid, lane);
     }
-    // T = A (the chunk's valid columns only) and D = scale dO
-    rows_to_tile(reinterpret_cast<unsigned char *>(P.Tm + u * CT * CT), CT, A + ((size_t)ci.tok0 * P.Hv + hv) * P.BT,
-                 (size_t)P.Hv * P.BT, len, len < P.BT ? len : P.BT, 1.f, tid);
-    rows_to_tile(reinterpret_cast<unsigned char *>(P.Dt + u * CT * DT), DT,
-                 reinterpret_cast<const Tin *>(P.dO) + ((size_t)ci.tok0 * P.Hv + hv) * P.V, (size_t)P.Hv * P.V, len,
-                 P.V, P.scale, tid);
-    // S_0 and dS_next: [K][V] fp32 per chunk -> [v][k] tiles
-    transpose_to_tile(reinterpret_cast<unsigned char *>(P.h + u * DT * DT), DT, h + u * P.K * P.V, (size_t)P.V, P.K,
-                      P.V, 1.f, wid, lane);
-    transpose_to_tile(reinterpret_cast<unsigned char *>(P.dh + u * DT * DT), DT, dh + u * P.K * P.V, (size_t)P.V,
-                      P.K, P.V, 1.f, wid, lane);
-    // V_new^T and -dV_new^T: [c][v] rows -> [v][c] tiles
-    transpose_to_tile(reinterpret_cast<unsigned char *>(P.Vn + u * DT * CT), CT,
-                      vnew + ((size_t)ci.tok0 * P.Hv + hv) * P.V, (size_t)P.Hv * P.V, len, P.V, 1.f, wid, lane);
-    transpose_to_tile(reinterpret_cast<unsigned char *>(P.dVn + u * DT * CT), CT,
-                      dvin + ((size_t)ci.tok0 * P.Hv + hv) * P.V, (size_t)P.Hv * P.V, len, P.V, -1.f, wid, lane);
 }
 
 template <typename Tin>
 static cudaError_t launch_k7_t(const Params &P, const void *A, const void *vnew, const void *dvin, const float *h,
                                const float *dh, cudaStream_t stream) {
-    dim3 grid(P.max_chunks, P.Hv);
+    dim3 grid(P.max_chunks, P.Hv, 4);  // the four parts of a chunk x head (see the kernel)
     k7_wy_inputs<Tin><<<grid, K7_THREADS, 0, stream>>>(P, reinterpret_cast<const Tin *>(A),
                                                        reinterpret_cast<const Tin *>(vnew),
                                                        reinterpret_cast<const Tin *>(dvin), h, dh);
