@@ -5,8 +5,10 @@
 //     V_new = U - W S^T,      S <- Gamma_C S + V_new^T K~        (K~ = K (.) exp(gamma_C - gamma))
 // i.e. S <- S M_n + U^T K~ with the transition M_n = Gamma_C I - W^T K~ (K x K).  A sequence is cut into
 // segments of Lseg chunks so that sequences x heads x segments CTAs fill the GPU:
-//   local pass (LOCAL = true): every segment runs from a zero state (-> E_s) and, alongside, the rows
-//     of the transition product Phi_s = prod M_n run from the identity (the same update without U);
+//   local pass (LOCAL = true): every segment runs from a zero state (-> E_s) and, in a second CTA, the
+//     rows of the transition product Phi_s = prod M_n run from the identity (the same update without U);
+//     the two chains are independent and their CTAs share an SM (half the tensor memory each), so each
+//     one's products run while the other's epilogues do;
 //   combine (k23_combine.cu): S_entry(s+1) = S_entry(s) Phi_s + E_s, exactly, in fp32;
 //   final pass (LOCAL = false): every segment runs from its exact entry state and writes h_n and V_new.
 // This is the state-passing correction that the page's context-parallel path applies across devices
@@ -15,9 +17,9 @@
 // One CTA holds the whole 128 x 128 fp32 state (and Phi) in tensor memory; each step issues two MMA
 // groups: V_new^T = S W^T (M = 128 state rows, N = 64 tokens) and S += V_new^T K~ (N = 128).  Operand
 // tiles arrive by bulk copy one chunk ahead; h_n and V_new^T leave by bulk copy from the operand tiles.
-// The local pass, which stores neither, keeps its fp16 A operands (the state and transition rows, V_new^T and
+// The local pass, which stores neither, keeps its fp16 A operands (the state or transition rows, V_new^T or
 // -(Phi W^T)) in tensor memory instead of shared memory: the products then read only their B tiles from
-// shared memory, whose bandwidth bounds the step.
+// shared memory.
 #pragma once
 
 #include "gdr_common.cuh"
@@ -39,9 +41,10 @@ struct __align__(1024) FwdSmem {
 };
 
 // The whole kernel for one CTA: bid is its (sequence x head x segment) index (the launch that pairs the two
-// final passes runs it with the CTA index of its first half).
+// final passes runs it with the CTA index of its first half); local pass: phi selects the transition chain
+// (else the state chain).
 template <bool PC, bool LOCAL>
-__device__ __forceinline__ void k2_scan_body(const Params &P, const int bid) {
+__device__ __forceinline__ void k2_scan_body(const Params &P, const int bid, const bool phi = false) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     FwdSmem<LOCAL> &S = *reinterpret_cast<FwdSmem<LOCAL> *>(smem_raw);
     if (*P.status & ST_BAD_SEQLENS) return;
@@ -66,7 +69,7 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid) {
     const int q = wid & 3, half = wid >> 2;
     const int row = 32 * q + lane;  // state row (v) / transition row (k') owned in the epilogues
 
-    if (wid == 0) tc::tmem_alloc(&S.tslot, LOCAL ? 512 : 256);
+    if (wid == 0) tc::tmem_alloc(&S.tslot, 256);
     if (tid == 0) {
         tc::mbar_init(&S.bar, 1);
         tc::mbar_init(&S.lbar[0], 1);
@@ -82,10 +85,10 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid) {
         const size_t u = (size_t)(base + c) * P.Hv + hv;
         const uint32_t gbytes = PC ? DT * 4 : CT * 4;
         const float *gsrc = PC ? P.gam + (u * CT + chunk_len(c) - 1) * DT : P.gam + u * CT;
-        tc::mbar_expect_tx(&S.lbar[buf], 3 * CT * DT * 2 + gbytes);
+        tc::mbar_expect_tx(&S.lbar[buf], (phi ? 2 : 3) * CT * DT * 2 + gbytes);
         tc::bulk_g2s(S.W[buf], P.W + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
         tc::bulk_g2s(S.Kt[buf], P.Kt + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
-        tc::bulk_g2s(S.U[buf], P.U + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
+        if (!phi) tc::bulk_g2s(S.U[buf], P.U + u * CT * DT, CT * DT * 2, &S.lbar[buf]);  // (the transition: no U)
         tc::bulk_g2s(S.gam[buf], gsrc, gbytes, &S.lbar[buf]);
     };
     tc::fence_before();
@@ -95,12 +98,13 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid) {
     bool armed0 = true, armed1 = false;
     if (tid == 0) issue(c_lo, 0);
     const uint32_t tm = S.tslot;
-    constexpr int T_S = 0, T_P = 128, T_VN = LOCAL ? 256 : 128, T_VP = 320;
-    // local pass: the fp16 A operands, packed two per column: state rows (64 columns), then V_new^T over their
-    // first 32 columns once the state's product has completed; the same for the transition rows
-    constexpr int T_SA = 384, T_PA = 448;
+    // the chain's rows (state, or transition in the local pass's second CTA), then V_new^T (resp. Phi W^T)
+    constexpr int T_S = 0, T_VN = 128;
+    // local pass: the fp16 A operands, packed two per column: the chain's rows (64 columns), then V_new^T (resp.
+    // -(Phi W^T)) over their first 32 columns once the first product has completed
+    constexpr int T_SA = 192;
 
-    // ---- initial state: zero (local pass) or the exact entry state (final pass); transition = I
+    // ---- initial rows: zero state or identity transition (local pass), the exact entry state (final pass)
     {
         const float *src = nullptr;
         if (!LOCAL) src = NS > 1 ? P.segSin + su * DT * DT : (P.h0 ? P.h0 + ((size_t)s * P.Hv + hv) * P.V * P.K : nullptr);
@@ -114,15 +118,12 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid) {
                 if (src) {
                     if (NS > 1) x = src[(size_t)row * DT + col];
                     else if (row < P.V && col < P.K) x = src[(size_t)row * P.K + col];
+                } else if (LOCAL && phi) {
+                    x = col == row ? 1.f : 0.f;
                 }
                 v[t] = x;
             }
             tc::st32(tc::taddr(tm, T_S + 64 * half + 32 * h), v);
-            if (LOCAL) {
-#pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] = (64 * half + 32 * h + t == row) ? 1.f : 0.f;
-                tc::st32(tc::taddr(tm, T_P + 64 * half + 32 * h), v);
-            }
         }
         tc::wait_st();
     }
@@ -162,43 +163,37 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid) {
             if (tid < DT) S.gam[buf][tid] = expf(S.gam[buf][tid]);
             __syncthreads();
         }
-        // epilogue 0: state rows -> fp16 operand (= h_n), then scale by Gamma_C in place
+        // epilogue 0: the chain's rows -> fp16 operand (= h_n), then scale by Gamma_C in place
 #pragma unroll
-        for (int m = 0; m < (LOCAL ? 2 : 1); ++m) {
-            const int tcol = m ? T_P : T_S;
+        for (int h = 0; h < 2; ++h) {
+            const int c0 = 64 * half + 32 * h;
+            float v[32];
+            tc::ld32(tc::taddr(tm, T_S + c0), v);
+            if constexpr (LOCAL) {
+                tc::st32_f16(tc::taddr(tm, T_SA + c0 / 2), v);
+            } else {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c0 = 64 * half + 32 * h;
-                float v[32];
-                tc::ld32(tc::taddr(tm, tcol + c0), v);
-                if constexpr (LOCAL) {
-                    tc::st32_f16(tc::taddr(tm, (m ? T_PA : T_SA) + c0 / 2), v);
-                } else {
-#pragma unroll
-                    for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.Sa, row, c0 + j8, DT, v + j8);
-                }
-                if (PC) {
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) v[t] *= S.gam[buf][c0 + t];
-                } else {
-                    const float G = expf(gl);
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) v[t] *= G;
-                }
-                tc::st32(tc::taddr(tm, tcol + c0), v);
+                for (int j8 = 0; j8 < 32; j8 += 8) tc::st_tile8(S.Sa, row, c0 + j8, DT, v + j8);
             }
+            if (PC) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t) v[t] *= S.gam[buf][c0 + t];
+            } else {
+                const float G = expf(gl);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) v[t] *= G;
+            }
+            tc::st32(tc::taddr(tm, T_S + c0), v);
         }
         tc::wait_st();
         tc::fence_smem_to_async();
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
-        // MMA 1: V_new^T (pre) = S W^T   [and  Phi W^T];  h_n leaves by bulk copy
+        // MMA 1: V_new^T (pre) = S W^T   [transition: Phi W^T];  h_n leaves by bulk copy
         if (tid == 0) {
             if constexpr (LOCAL) {
-                const tc::Operand w = tc::op_rows(smem_u32(S.W[buf]), DT, false);
-                tc::gemm_ta(tm + T_VN, tm + T_SA, w, 64, DT, false);
-                tc::gemm_ta(tm + T_VP, tm + T_PA, w, 64, DT, false);
+                tc::gemm_ta(tm + T_VN, tm + T_SA, tc::op_rows(smem_u32(S.W[buf]), DT, false), 64, DT, false);
             } else {
                 tc::gemm(tm + T_VN, sSa, DT, false, smem_u32(S.W[buf]), DT, false, 128, 64, DT, false);
                 tc::bulk_s2g(P.h + u * DT * DT, S.Sa, DT * DT * 2);
@@ -211,23 +206,24 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid) {
             const int c0 = 32 * half;
             float v[32];
             tc::ld32(tc::taddr(tm, T_VN + c0), v);
+            if (LOCAL && phi) {
 #pragma unroll
-            for (int j8 = 0; j8 < 32; j8 += 8) {  // U^T row segment: 16-byte reads of the [v][c] tile
-                const __half2 *u2 =
-                    reinterpret_cast<const __half2 *>(S.U[buf] + tc::tile_off(row, c0 + j8, CT));
+                for (int t = 0; t < 32; ++t) v[t] = -v[t];
+            } else {
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float2 f = __half22float2(u2[t]);
-                    v[j8 + 2 * t] = f.x - v[j8 + 2 * t];
-                    v[j8 + 2 * t + 1] = f.y - v[j8 + 2 * t + 1];
+                for (int j8 = 0; j8 < 32; j8 += 8) {  // U^T row segment: 16-byte reads of the [v][c] tile
+                    const __half2 *u2 =
+                        reinterpret_cast<const __half2 *>(S.U[buf] + tc::tile_off(row, c0 + j8, CT));
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float2 f = __half22float2(u2[t]);
+                        v[j8 + 2 * t] = f.x - v[j8 + 2 * t];
+                        v[j8 + 2 * t + 1] = f.y - v[j8 + 2 * t + 1];
+                    }
                 }
             }
             if constexpr (LOCAL) {
                 tc::st32_f16(tc::taddr(tm, T_SA + c0 / 2), v);
-                tc::ld32(tc::taddr(tm, T_VP + c0), v);
-#pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] = -v[t];
-                tc::st32_f16(tc::taddr(tm, T_PA + c0 / 2), v);
                 tc::wait_st();
             } else {
 #pragma unroll
@@ -238,12 +234,10 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid) {
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
-        // MMA 2: S += V_new^T K~   [Phi += (-(Phi W^T)) K~];  V_new^T leaves by bulk copy
+        // MMA 2: S += V_new^T K~   [transition: Phi += (-(Phi W^T)) K~];  V_new^T leaves by bulk copy
         if (tid == 0) {
             if constexpr (LOCAL) {
-                const tc::Operand kt = tc::op_rows(smem_u32(S.Kt[buf]), DT, true);
-                tc::gemm_ta(tm + T_S, tm + T_SA, kt, 128, CT, true);
-                tc::gemm_ta(tm + T_P, tm + T_PA, kt, 128, CT, true);
+                tc::gemm_ta(tm + T_S, tm + T_SA, tc::op_rows(smem_u32(S.Kt[buf]), DT, true), 128, CT, true);
             } else {
                 tc::gemm(tm + T_S, sVna, CT, false, smem_u32(S.Kt[buf]), DT, true, 128, 128, CT, true);
                 tc::bulk_s2g(P.Vn + u * DT * CT, S.Vna, DT * CT * 2);
@@ -252,24 +246,21 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid) {
         }
         mma_done();
     }
-    // ---- local pass: segment summaries E_s (state), Phi_s and Phi_s^T (transition rows), fp32
+    // ---- local pass: segment summaries E_s (state CTA), Phi_s and Phi_s^T (transition CTA), fp32
     if (LOCAL && !lost) {
+        float *dst = (phi ? P.segPhi : P.segE) + su * DT * DT + (size_t)row * DT;
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            float *dst = (m ? P.segPhi : P.segE) + su * DT * DT + (size_t)row * DT;
+        for (int h = 0; h < 2; ++h) {
+            const int c0 = 64 * half + 32 * h;
+            float v[32];
+            tc::ld32(tc::taddr(tm, T_S + c0), v);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c0 = 64 * half + 32 * h;
-                float v[32];
-                tc::ld32(tc::taddr(tm, (m ? T_P : T_S) + c0), v);
+            for (int t = 0; t < 32; t += 4)
+                *reinterpret_cast<float4 *>(dst + c0 + t) = make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]);
+            if (phi) {  // Phi^T, so that the backward combine also reads rows
+                float *dT = P.segPhiT + su * DT * DT + row;
 #pragma unroll
-                for (int t = 0; t < 32; t += 4)
-                    *reinterpret_cast<float4 *>(dst + c0 + t) = make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]);
-                if (m) {  // Phi^T, so that the backward combine also reads rows
-                    float *dT = P.segPhiT + su * DT * DT + row;
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) dT[(size_t)(c0 + t) * DT] = v[t];
-                }
+                for (int t = 0; t < 32; ++t) dT[(size_t)(c0 + t) * DT] = v[t];
             }
         }
     }
@@ -300,7 +291,7 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid) {
     __syncthreads();
     if (wid == 0) {
         tc::fence_after();
-        tc::tmem_dealloc(tm, LOCAL ? 512 : 256);
+        tc::tmem_dealloc(tm, 256);
     }
 }
 

@@ -3,9 +3,12 @@
 
 namespace gdr {
 
+// Local pass: two CTAs per (sequence x head x segment), the state chain (even) and the transition chain
+// (odd), two per SM.
 template <bool PC, bool LOCAL>
-__global__ void __launch_bounds__(SC_THREADS, 1) k2_scan_tc(const Params P) {
-    k2_scan_body<PC, LOCAL>(P, (int)blockIdx.x);
+__global__ void __launch_bounds__(SC_THREADS, LOCAL ? 2 : 1) k2_scan_tc(const Params P) {
+    if (LOCAL) k2_scan_body<PC, LOCAL>(P, (int)blockIdx.x >> 1, (blockIdx.x & 1) != 0);
+    else k2_scan_body<PC, LOCAL>(P, (int)blockIdx.x);
 }
 
 template <bool PC, bool LOCAL>
@@ -13,7 +16,7 @@ static cudaError_t launch_fwd_t(const Params &P, cudaStream_t stream) {
     size_t smem = sizeof(FwdSmem<LOCAL>);
     cudaError_t e = smem_opt_in((const void *)k2_scan_tc<PC, LOCAL>, smem);
     if (e != cudaSuccess) return e;
-    k2_scan_tc<PC, LOCAL><<<P.N * P.Hv * P.NS, SC_THREADS, smem, stream>>>(P);
+    k2_scan_tc<PC, LOCAL><<<P.N * P.Hv * P.NS * (LOCAL ? 2 : 1), SC_THREADS, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
