@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libgdrbwd.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "k0_chunk_indices.cu", "k1_wy_prep.cu", "k2_scan_tc.cu", "k3_scan_tc.cu", "k23_combine.cu",
-           "k4_intra_grad.cu", "k4_intra_grad_tc.cu", "k5_dg_reduce.cu", "k6_fwd_output.cu", "k7_wy_inputs.cu", "k8_qr.cu",
+           "k4_intra_grad.cu", "k4_intra_grad_tc.cu", "k5_dg_reduce.cu", "k7_wy_inputs.cu", "k8_qr.cu",
            "noalloc.cu"]
 
 

@@ -456,8 +456,8 @@ gdr_status gdr_fwd_run(gdr_bwd_plan *plan, const gdr_fwd_args *a, void *workspac
     P.o = a->o;
     P.ht = a->ht;
     P.Kd = nullptr;  // the decayed key Gram serves only the backward's dbeta
-    // the forward: chunk bookkeeping, WY preparation without dO, the state recompute (which also writes
-    // the final state), then the per-chunk output
+    // the forward: chunk bookkeeping, WY preparation without dO, the state recompute, whose final pass also
+    // writes each chunk's output and the final state
     if (cudaMemsetAsync(P.status, 0, sizeof(int), stream) != cudaSuccess) return GDR_ERR_CUDA;
     if (!plan->dense &&
         launch_k0(a->cu_seqlens, plan->N, d.BT, plan->max_chunks, d.T, P.chunk_idx, P.chunk_off, P.status, stream) !=
@@ -469,8 +469,7 @@ gdr_status gdr_fwd_run(gdr_bwd_plan *plan, const gdr_fwd_args *a, void *workspac
         if (launch_k2_scan(P, true, stream) != cudaSuccess) return GDR_ERR_CUDA;
         if (launch_k23_combine(P, true, stream) != cudaSuccess) return GDR_ERR_CUDA;
     }
-    if ((any_chunks || P.ht) && launch_k2_scan(P, false, stream) != cudaSuccess) return GDR_ERR_CUDA;
-    if (any_chunks && launch_k6_fwd_output(P, stream) != cudaSuccess) return GDR_ERR_CUDA;
+    if ((any_chunks || P.ht) && launch_k2_scan_out(P, stream) != cudaSuccess) return GDR_ERR_CUDA;
     return GDR_OK;
 }
 
@@ -524,8 +523,8 @@ gdr_status gdr_wy_bwd_run(gdr_bwd_plan *plan, const gdr_wy_args *a, void *worksp
 int gdr_fwd_launch_count(const gdr_bwd_plan *plan) {
     if (!plan) return 0;
     int n = plan->dense ? 0 : 1;                             // K0
-    n += 1;                                                  // the final state scan (final state)
-    if (plan->max_chunks > 0) n += 2;                        // K1, output
+    n += 1;                                                  // the final scan pass (output, final state)
+    if (plan->max_chunks > 0) n += 1;                        // K1
     if (plan->max_chunks > 0 && plan->NS > 1) n += 2;        // local scan and combine
     return n;
 }

@@ -34,6 +34,8 @@ cudaError_t launch_k1(const Params &P, cudaStream_t stream);
 // K2 / K3: forward state recompute (fused_gdr_h) and reverse state-gradient scan, segment-parallel on
 // the tensor cores: local (zero-start) pass or final (exact-start) pass.
 cudaError_t launch_k2_scan(const Params &P, bool local, cudaStream_t stream);
+// The forward's final pass with the output fused in (writes o and ht; no h_n, V_new).
+cudaError_t launch_k2_scan_out(const Params &P, cudaStream_t stream);
 cudaError_t launch_k3_scan(const Params &P, bool local, cudaStream_t stream);
 // With one segment per sequence: both scans' single passes as one grid (forward CTAs first).
 cudaError_t launch_k23_scan_pair(const Params &P, cudaStream_t stream);
@@ -45,8 +47,6 @@ cudaError_t launch_k4(const Params &P, cudaStream_t stream);
 cudaError_t launch_k4_tc(const Params &P, cudaStream_t stream);
 // K5: reverse cumsum of the gate gradient and GQA reduction of dq / dk.
 cudaError_t launch_k5(const Params &P, cudaStream_t stream);
-// forward output o = scale (diag(Gamma) Q S_0^T + (M (.) Q K^T) V_new) per chunk
-cudaError_t launch_k6_fwd_output(const Params &P, cudaStream_t stream);
 // the WY-gradient stage taken alone: its inputs as workspace tiles, then the per-chunk kernel in that mode
 cudaError_t launch_k7_wy_inputs(const Params &P, const void *A, const void *v_new, const void *dv_in, const float *h,
                                 const float *dh, cudaStream_t stream);

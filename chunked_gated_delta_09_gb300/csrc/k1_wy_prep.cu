@@ -579,7 +579,8 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
             x[t] = v.x, x[t + 1] = v.y, x[t + 2] = v.z, x[t + 3] = v.w;
         }
         tc::st_tile8(oT, i, j8, CT, x);
-        tc::st_tile8(reinterpret_cast<unsigned char *>(P.Tm + u * CT * CT), i, j8, CT, x);
+        // (the forward, which runs without dO, needs T only for W and U)
+        if (P.dO) tc::st_tile8(reinterpret_cast<unsigned char *>(P.Tm + u * CT * CT), i, j8, CT, x);
     }
     __syncthreads();
 

@@ -10,7 +10,8 @@
 //     the two chains are independent and their CTAs share an SM (half the tensor memory each), so each
 //     one's products run while the other's epilogues do;
 //   combine (k23_combine.cu): S_entry(s+1) = S_entry(s) Phi_s + E_s, exactly, in fp32;
-//   final pass (LOCAL = false): every segment runs from its exact entry state and writes h_n and V_new.
+//   final pass (LOCAL = false): every segment runs from its exact entry state and writes h_n and V_new
+//     (in the forward pass, OUT = true, it writes the chunk outputs o instead; see k2_scan_body).
 // This is the state-passing correction that the page's context-parallel path applies across devices
 // (section 3: partition states corrected with an all-gather), done inside one GPU.
 //
@@ -30,11 +31,13 @@ namespace gdr {
 
 constexpr int SC_THREADS = 256;
 
-template <bool LOCAL>
+// OUT (the forward's final pass): W[buf] holds the W tile and then the Q~ tile, and Aq the Aqk tiles.
+template <bool LOCAL, bool OUT = false>
 struct __align__(1024) FwdSmem {
-    unsigned char W[2][CT * DT * 2], Kt[2][CT * DT * 2], U[2][CT * DT * 2];  // U holds U^T tiles [v][c]
+    unsigned char W[2][(OUT ? 2 : 1) * CT * DT * 2], Kt[2][CT * DT * 2], U[2][CT * DT * 2];  // U^T tiles [v][c]
     unsigned char Sa[LOCAL ? 16 : DT * DT * 2];   // state rows as fp16 (A operand; h_n): final pass only
     unsigned char Vna[LOCAL ? 16 : DT * CT * 2];  // V_new^T [v][c] (A operand): final pass only
+    unsigned char Aq[OUT ? 2 : 1][OUT ? CT * CT * 2 : 16];
     float gam[2][DT];                             // gate row block of the chunk (scalar: first CT used)
     uint64_t bar, lbar[2];  // MMA completion, the two tile buffers' loads
     uint32_t tslot;
@@ -42,11 +45,15 @@ struct __align__(1024) FwdSmem {
 
 // The whole kernel for one CTA: bid is its (sequence x head x segment) index (the launch that pairs the two
 // final passes runs it with the CTA index of its first half); local pass: phi selects the transition chain
-// (else the state chain).
-template <bool PC, bool LOCAL>
+// (else the state chain).  OUT (final pass of the forward): the chunk's output
+// o^T = scale (S_0 Q~^T + V_new^T Aqk^T) is formed in the same steps (S_0 Q~^T in the product that takes
+// S_0 W^T, as its second 64 columns; V_new^T Aqk^T after S += V_new^T K~) and written, while h_n and V_new,
+// which only the backward reads, are not.
+template <bool PC, bool LOCAL, bool OUT = false>
 __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid, const bool phi = false) {
+    static_assert(!(LOCAL && OUT), "the output comes from the final pass");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    FwdSmem<LOCAL> &S = *reinterpret_cast<FwdSmem<LOCAL> *>(smem_raw);
+    FwdSmem<LOCAL, OUT> &S = *reinterpret_cast<FwdSmem<LOCAL, OUT> *>(smem_raw);
     if (*P.status & ST_BAD_SEQLENS) return;
     const int NS = P.NS;
     const int seg = bid % NS, hv = (bid / NS) % P.Hv, s = bid / (NS * P.Hv);
@@ -85,10 +92,14 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid, con
         const size_t u = (size_t)(base + c) * P.Hv + hv;
         const uint32_t gbytes = PC ? DT * 4 : CT * 4;
         const float *gsrc = PC ? P.gam + (u * CT + chunk_len(c) - 1) * DT : P.gam + u * CT;
-        tc::mbar_expect_tx(&S.lbar[buf], (phi ? 2 : 3) * CT * DT * 2 + gbytes);
+        tc::mbar_expect_tx(&S.lbar[buf], (phi ? 2 : 3) * CT * DT * 2 + gbytes + (OUT ? CT * DT * 2 + CT * CT * 2 : 0));
         tc::bulk_g2s(S.W[buf], P.W + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
         tc::bulk_g2s(S.Kt[buf], P.Kt + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
         if (!phi) tc::bulk_g2s(S.U[buf], P.U + u * CT * DT, CT * DT * 2, &S.lbar[buf]);  // (the transition: no U)
+        if (OUT) {  // Q~ right after W (one 128-row B operand), and Aqk
+            tc::bulk_g2s(S.W[buf] + CT * DT * 2, P.Qg + u * CT * DT, CT * DT * 2, &S.lbar[buf]);
+            tc::bulk_g2s(S.Aq[buf], P.Aqk + u * CT * CT, CT * CT * 2, &S.lbar[buf]);
+        }
         tc::bulk_g2s(S.gam[buf], gsrc, gbytes, &S.lbar[buf]);
     };
     tc::fence_before();
@@ -99,7 +110,7 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid, con
     if (tid == 0) issue(c_lo, 0);
     const uint32_t tm = S.tslot;
     // the chain's rows (state, or transition in the local pass's second CTA), then V_new^T (resp. Phi W^T)
-    constexpr int T_S = 0, T_VN = 128;
+    constexpr int T_S = 0, T_VN = 128, T_O = 192;  // (T_O: the output o^T, OUT only)
     // local pass: the fp16 A operands, packed two per column: the chain's rows (64 columns), then V_new^T (resp.
     // -(Phi W^T)) over their first 32 columns once the first product has completed
     constexpr int T_SA = 192;
@@ -194,9 +205,9 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid, con
         if (tid == 0) {
             if constexpr (LOCAL) {
                 tc::gemm_ta(tm + T_VN, tm + T_SA, tc::op_rows(smem_u32(S.W[buf]), DT, false), 64, DT, false);
-            } else {
-                tc::gemm(tm + T_VN, sSa, DT, false, smem_u32(S.W[buf]), DT, false, 128, 64, DT, false);
-                tc::bulk_s2g(P.h + u * DT * DT, S.Sa, DT * DT * 2);
+            } else {  // (OUT: N = 128 over [W ; Q~], the second half = S_0 Q~^T at T_O)
+                tc::gemm(tm + T_VN, sSa, DT, false, smem_u32(S.W[buf]), DT, false, 128, OUT ? 128 : 64, DT, false);
+                if (!OUT) tc::bulk_s2g(P.h + u * DT * DT, S.Sa, DT * DT * 2);
             }
         }
         mma_done();
@@ -240,11 +251,33 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid, con
                 tc::gemm_ta(tm + T_S, tm + T_SA, tc::op_rows(smem_u32(S.Kt[buf]), DT, true), 128, CT, true);
             } else {
                 tc::gemm(tm + T_S, sVna, CT, false, smem_u32(S.Kt[buf]), DT, true, 128, 128, CT, true);
-                tc::bulk_s2g(P.Vn + u * DT * CT, S.Vna, DT * CT * 2);
-                tc::bulk_commit();
+                if (OUT) {
+                    tc::gemm(tm + T_O, sVna, CT, false, smem_u32(S.Aq[buf]), CT, false, 128, 64, CT, true);
+                } else {
+                    tc::bulk_s2g(P.Vn + u * DT * CT, S.Vna, DT * CT * 2);
+                    tc::bulk_commit();
+                }
             }
         }
         mma_done();
+        if constexpr (OUT) {  // o rows of this chunk: each thread one value row, 32 chunk rows (coalesced)
+            if (lost) break;
+            const int c0 = 32 * half, len = chunk_len(c);
+            float v[32];
+            tc::ld32(tc::taddr(tm, T_O + c0), v);
+            if (row < P.V) {
+                const size_t rs = (size_t)P.Hv * P.V, o0 = ((size_t)(bos + c * P.BT) * P.Hv + hv) * P.V + row;
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    if (c0 + t < len) {
+                        const size_t oi = o0 + (size_t)(c0 + t) * rs;
+                        const float x = P.scale * v[t];
+                        if (P.qkv_dtype == BF16) reinterpret_cast<__nv_bfloat16 *>(P.o)[oi] = __float2bfloat16_rn(x);
+                        else if (P.qkv_dtype == F16) reinterpret_cast<__half *>(P.o)[oi] = __float2half_rn(x);
+                        else reinterpret_cast<float *>(P.o)[oi] = x;
+                    }
+            }
+        }
     }
     // ---- local pass: segment summaries E_s (state CTA), Phi_s and Phi_s^T (transition CTA), fp32
     if (LOCAL && !lost) {

@@ -156,7 +156,7 @@ gdr_status gdr_bwd_get_status_noalloc(gdr_bwd_plan *plan, void *stream);
 /* ---- Forward pass (the output and final state that the backward above differentiates).
  * Per sequence and value head, S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T and
  * o_t = scale S_t q_t, computed chunkwise: the WY preparation and the state recompute of the backward,
- * then per chunk o = scale (diag(Gamma) Q S_0^T + (M (.) Q K^T) V_new) ("FlashQLA backward explained",
+ * whose final pass also forms per chunk o = scale (diag(Gamma) Q S_0^T + (M (.) Q K^T) V_new) ("FlashQLA backward explained",
  * section 1: the forward whose saved state the backward recomputes; MindSpeed-Ops chunk_kda_bwd.md, input
  * table: the chunk states h and v_new).  The per-channel gate acts on the K index as in the backward.
  * Uses the backward's plan and workspace (gdr_bwd_workspace_bytes); dO, dht and the gradient fields of
