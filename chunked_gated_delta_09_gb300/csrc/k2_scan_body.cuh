@@ -260,22 +260,31 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid, con
             }
         }
         mma_done();
-        if constexpr (OUT) {  // o rows of this chunk: each thread one value row, 32 chunk rows (coalesced)
+        if constexpr (OUT) {
+            // o rows of this chunk: each thread holds one value row and 32 chunk rows; lanes 2m and 2m + 1
+            // (value rows v, v + 1) swap halves so that the even lane writes the even chunk rows and the odd
+            // lane the odd ones, each as one store of the pair (v, v + 1) (V is even)
             if (lost) break;
             const int c0 = 32 * half, len = chunk_len(c);
+            const bool odd = (lane & 1) != 0;
             float v[32];
             tc::ld32(tc::taddr(tm, T_O + c0), v);
-            if (row < P.V) {
-                const size_t rs = (size_t)P.Hv * P.V, o0 = ((size_t)(bos + c * P.BT) * P.Hv + hv) * P.V + row;
+            const size_t rs = (size_t)P.Hv * P.V;
+            const size_t o0 = ((size_t)(bos + c * P.BT) * P.Hv + hv) * P.V + (row & ~1);
 #pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    if (c0 + t < len) {
-                        const size_t oi = o0 + (size_t)(c0 + t) * rs;
-                        const float x = P.scale * v[t];
-                        if (P.qkv_dtype == BF16) reinterpret_cast<__nv_bfloat16 *>(P.o)[oi] = __float2bfloat16_rn(x);
-                        else if (P.qkv_dtype == F16) reinterpret_cast<__half *>(P.o)[oi] = __float2half_rn(x);
-                        else reinterpret_cast<float *>(P.o)[oi] = x;
-                    }
+            for (int t = 0; t < 32; t += 2) {
+                const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[t] : v[t + 1], 1);
+                const int r = c0 + t + (odd ? 1 : 0);
+                const float a = P.scale * (odd ? recv : v[t]), b = P.scale * (odd ? v[t + 1] : recv);
+                if (r < len && row < P.V) {
+                    const size_t oi = o0 + (size_t)r * rs;
+                    if (P.qkv_dtype == BF16)
+                        *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(P.o) + oi) = __floats2bfloat162_rn(a, b);
+                    else if (P.qkv_dtype == F16)
+                        *reinterpret_cast<__half2 *>(reinterpret_cast<__half *>(P.o) + oi) = __floats2half2_rn(a, b);
+                    else
+                        *reinterpret_cast<float2 *>(reinterpret_cast<float *>(P.o) + oi) = make_float2(a, b);
+                }
             }
         }
     }
