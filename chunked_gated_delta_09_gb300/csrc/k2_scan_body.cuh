@@ -261,29 +261,45 @@ __device__ __forceinline__ void k2_scan_body(const Params &P, const int bid, con
         }
         mma_done();
         if constexpr (OUT) {
-            // o rows of this chunk: each thread holds one value row and 32 chunk rows; lanes 2m and 2m + 1
-            // (value rows v, v + 1) swap halves so that the even lane writes the even chunk rows and the odd
-            // lane the odd ones, each as one store of the pair (v, v + 1) (V is even)
+            // o rows of this chunk: each thread holds one value row and 32 chunk rows.  The four lanes of a quad
+            // (value rows 4g .. 4g + 3) transpose each block of 4 chunk rows among themselves (two swap rounds),
+            // so that lane j writes chunk row 4b + j of the four value rows with one 8-byte store (V is a
+            // multiple of 8)
             if (lost) break;
-            const int c0 = 32 * half, len = chunk_len(c);
-            const bool odd = (lane & 1) != 0;
+            const int c0 = 32 * half, len = chunk_len(c), j = lane & 3;
             float v[32];
             tc::ld32(tc::taddr(tm, T_O + c0), v);
             const size_t rs = (size_t)P.Hv * P.V;
-            const size_t o0 = ((size_t)(bos + c * P.BT) * P.Hv + hv) * P.V + (row & ~1);
+            const size_t o0 = ((size_t)(bos + c * P.BT) * P.Hv + hv) * P.V + (row & ~3);
 #pragma unroll
-            for (int t = 0; t < 32; t += 2) {
-                const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[t] : v[t + 1], 1);
-                const int r = c0 + t + (odd ? 1 : 0);
-                const float a = P.scale * (odd ? recv : v[t]), b = P.scale * (odd ? v[t + 1] : recv);
+            for (int b = 0; b < 32; b += 4) {
+#pragma unroll
+                for (int sw = 2; sw >= 1; sw >>= 1) {
+                    const bool up = (j & sw) != 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (i & sw) continue;
+                        const float recv = __shfl_xor_sync(0xffffffffu, up ? v[b + i] : v[b + i + sw], sw);
+                        if (up) v[b + i] = recv;
+                        else v[b + i + sw] = recv;
+                    }
+                }
+                const int r = c0 + b + j;  // v[b .. b + 3]: value rows (row & ~3) .. + 3 at chunk row r
                 if (r < len && row < P.V) {
                     const size_t oi = o0 + (size_t)r * rs;
-                    if (P.qkv_dtype == BF16)
-                        *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(P.o) + oi) = __floats2bfloat162_rn(a, b);
-                    else if (P.qkv_dtype == F16)
-                        *reinterpret_cast<__half2 *>(reinterpret_cast<__half *>(P.o) + oi) = __floats2half2_rn(a, b);
-                    else
-                        *reinterpret_cast<float2 *>(reinterpret_cast<float *>(P.o) + oi) = make_float2(a, b);
+                    const float x0 = P.scale * v[b], x1 = P.scale * v[b + 1], x2 = P.scale * v[b + 2],
+                                x3 = P.scale * v[b + 3];
+                    if (P.qkv_dtype == BF16) {
+                        const __nv_bfloat162 p0 = __floats2bfloat162_rn(x0, x1), p1 = __floats2bfloat162_rn(x2, x3);
+                        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(P.o) + oi) =
+                            make_uint2(*reinterpret_cast<const uint32_t *>(&p0), *reinterpret_cast<const uint32_t *>(&p1));
+                    } else if (P.qkv_dtype == F16) {
+                        const __half2 p0 = __floats2half2_rn(x0, x1), p1 = __floats2half2_rn(x2, x3);
+                        *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(P.o) + oi) =
+                            make_uint2(*reinterpret_cast<const uint32_t *>(&p0), *reinterpret_cast<const uint32_t *>(&p1));
+                    } else {
+                        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(P.o) + oi) = make_float4(x0, x1, x2, x3);
+                    }
                 }
             }
         }
