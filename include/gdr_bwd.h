@@ -111,8 +111,9 @@ gdr_status gdr_bwd_run(gdr_bwd_plan *plan, const gdr_bwd_args *args, void *works
                        void *stream);
 
 /* Number of stages and the kernels behind them: 0 varlen chunk bookkeeping, 1 WY preparation,
- * 2 forward state recompute, 3 state-gradient scan, 4 per-chunk gradients, 5 gate reverse cumsum and
- * GQA reduction. */
+ * 2 forward state recompute, 3 state-gradient scan, 4 per-chunk gradients (with GQA, the tcgen05 kernel of
+ * the scalar gate also sums each key head's group of value heads), 5 gate reverse cumsum and, after the
+ * per-channel gate's kernel, the GQA reduction. */
 #define GDR_BWD_NUM_STAGES 6
 
 /* Same as gdr_bwd_run, and records events[0] before the first stage and events[i + 1] after stage i
