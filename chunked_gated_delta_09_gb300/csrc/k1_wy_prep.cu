@@ -158,7 +158,9 @@ __global__ void __launch_bounds__(K1_THREADS, PC ? 2 : 3)
     float *gamK = reinterpret_cast<float *>(sbase + sizeof(K1Smem));  // [CT][GKLD], per-channel only
 
     if (*P.status & ST_BAD_SEQLENS) return;
-    const int n = blockIdx.x, hv = blockIdx.y, hk = hv / P.G;
+    // heads fastest: CTAs that run at the same time read the same tokens' rows of all heads (whole rows of the
+    // [token][head][feature] inputs) rather than one head's rows of many tokens
+    const int n = (int)(blockIdx.x / (unsigned)P.Hv), hv = (int)(blockIdx.x % (unsigned)P.Hv), hk = hv / P.G;
     ChunkInfo ci;
     if (!chunk_info(P, n, ci)) return;
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
@@ -633,7 +635,8 @@ static cudaError_t launch_k1_t(const Params &P, cudaStream_t stream) {
         if ((e = encode_rows_map_sw128(&mv, P.v, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
         if (P.dO && (e = encode_rows_map_sw128(&mo, P.dO, P.qkv_dtype, tokens, P.Hv, P.V)) != cudaSuccess) return e;
     }
-    dim3 grid(P.max_chunks, P.Hv);
+    if ((long long)P.max_chunks * P.Hv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    dim3 grid((unsigned)P.max_chunks * (unsigned)P.Hv);  // CTA n Hv + hv
     k1_wy_prep<Tin, PC><<<grid, K1_THREADS, smem, stream>>>(P, mk, mq, mv, mo);
     return cudaGetLastError();
 }
